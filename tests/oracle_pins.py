@@ -1,0 +1,347 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with:
+
+* a library routine computing the same thing another way (numpy's float16,
+  torch's bfloat16, numpy/scipy softmax attention on contiguous K/V),
+* the pages' printed worked example of a block table,
+* an invariant of the definition (block-id permutation, shared vs private
+  prefix blocks, split-context identity),
+* a closed-form special case (one token, identical keys, empty context).
+
+The same functions run against deliberately broken builds of the oracle in
+``test_oracle_mutants.py``; every mutant must trip at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+STORAGE_NP = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+NAN_BITS_BF16 = 0x7FC0
+
+
+# ---------------------------------------------------------------------------
+# Helpers that build small paged inputs (no oracle code involved).
+# ---------------------------------------------------------------------------
+
+def to_storage(x, dtype):
+    """fp64/fp32 array -> stored elements (bf16 as uint16 bit patterns)."""
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32))
+    if dtype == "f32":
+        return t.numpy().astype(np.float32)
+    if dtype == "f16":
+        return t.to(torch.float16).numpy()
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def widen_lib(a, dtype):
+    """Stored elements -> float64 by the libraries' own conversions."""
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    return a.astype(np.float64)
+
+
+def poison(shape, dtype):
+    if dtype == "bf16":
+        return np.full(shape, NAN_BITS_BF16, dtype=np.uint16)
+    return np.full(shape, np.nan, dtype=STORAGE_NP[dtype])
+
+
+def paged_case(seed, lens, B, Hq, Hkv, D, dtype, spare_blocks=3):
+    """Random per-sequence contiguous K/V placed block by block in a shuffled pool.
+
+    Block j of sequence s holds that sequence's tokens jB .. jB+B-1 (the
+    pages' picture of a block: B consecutive tokens' keys and values).
+    Returns the stored arrays and the contiguous fp64 copies.
+    """
+    rng = np.random.default_rng(seed)
+    S = len(lens)
+    need = [-(-L // B) for L in lens]
+    NB = sum(need) + spare_blocks
+    perm = rng.permutation(NB)
+    MB = max(max(need), 1)
+    bt = np.full((S, MB), -1, dtype=np.int32)
+    k = 0
+    for s in range(S):
+        for j in range(need[s]):
+            bt[s, j] = perm[k]
+            k += 1
+    kpool = poison((NB, B, Hkv, D), dtype)
+    vpool = poison((NB, B, Hkv, D), dtype)
+    Kc, Vc = [], []
+    for s, L in enumerate(lens):
+        Ks = to_storage(rng.standard_normal((L, Hkv, D)), dtype)
+        Vs = to_storage(rng.standard_normal((L, Hkv, D)), dtype)
+        for j in range(need[s]):
+            n = min(B, L - j * B)
+            kpool[bt[s, j], :n] = Ks[j * B:j * B + n]
+            vpool[bt[s, j], :n] = Vs[j * B:j * B + n]
+        Kc.append(widen_lib(Ks, dtype))
+        Vc.append(widen_lib(Vs, dtype))
+    q = to_storage(rng.standard_normal((S, Hq, D)), dtype)
+    return dict(q=q, k=kpool, v=vpool, bt=bt, lens=np.asarray(lens, np.int32), Kc=Kc, Vc=Vc,
+                qc=widen_lib(q, dtype), B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, NB=NB,
+                scale=1.0 / math.sqrt(D))
+
+
+def brute_force(case):
+    """Contiguous softmax attention with numpy/scipy (query head h -> kv head h // g)."""
+    S, Hq, D = case["q"].shape
+    g = Hq // case["Hkv"]
+    out = np.zeros((S, Hq, D))
+    for s in range(S):
+        if case["lens"][s] == 0:
+            continue
+        for h in range(Hq):
+            K = case["Kc"][s][:, h // g, :]
+            V = case["Vc"][s][:, h // g, :]
+            z = case["scale"] * (K @ case["qc"][s, h])
+            out[s, h] = scipy.special.softmax(z) @ V
+    return out
+
+
+def run_decode(orc, case, **kw):
+    return orc.decode(case["q"], case["k"], case["v"], case["bt"], case["lens"], case["scale"],
+                      case["dtype"], **kw)
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# Element decoding.
+# ---------------------------------------------------------------------------
+
+def pin_f16_decoding(orc):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.f16_to_double(b) for b in bits.tolist()])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), f"fp16 decoding differs at {np.nonzero(~same)[0][:5]}"
+
+
+def pin_bf16_decoding(orc):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = widen_lib(bits, "bf16")
+    got = np.array([orc.bf16_to_double(b) for b in bits.tolist()])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), f"bf16 decoding differs at {np.nonzero(~same)[0][:5]}"
+
+
+# ---------------------------------------------------------------------------
+# Address translation.
+# ---------------------------------------------------------------------------
+
+def pin_block_table_example(orc):
+    """The pages' printed 10-token, B = 4 sequence in blocks [5, 2, 9], grown to 13."""
+    rows = read_golden("block_table_b4.txt")
+    B = int(rows[0][1])
+    n0, nblocks, waste = int(rows[1][1]), int(rows[1][3]), int(rows[1][5])
+    table = [int(x) for x in rows[1][7:]]
+    assert len(table) == nblocks
+    bt = np.array([table], dtype=np.int32)
+    held = [orc.slot(bt, 0, i, B) // B for i in range(n0)]
+    assert held == sorted(held, key=table.index), "tokens leave logical block order"
+    assert sorted(set(held), key=table.index) == table, "tokens not spread over the table"
+    assert nblocks * B - n0 == waste
+    for row in rows[2:]:
+        n_tokens = int(row[2])
+        grown = [int(x) for x in row[4:row.index("wrote")]]
+        bt = np.array([grown], dtype=np.int32)
+        pos = n_tokens - 1
+        slot = orc.slot(bt, 0, pos, B)
+        if row[-1] == "current":
+            assert slot // B == table[-1] and slot % B != 0, (row, slot)
+        else:
+            assert slot // B == grown[-1] and slot % B == 0, (row, slot)
+        table = grown
+
+
+def pin_slot_bijection(orc):
+    """Disjoint tables: every (seq, pos) gets its own slot, each block holds
+    at most B consecutive positions, blocks are used in table order."""
+    case = paged_case(11, [1, 5, 8, 13, 31], 8, 2, 1, 8, "f32")
+    B, bt, lens = case["B"], case["bt"], case["lens"]
+    seen = set()
+    for s, L in enumerate(lens):
+        slots = [orc.slot(bt, s, i, B) for i in range(L)]
+        assert all(0 <= x < case["NB"] * B for x in slots)
+        seen.update(slots)
+        blocks = [x // B for x in slots]
+        offs = [x % B for x in slots]
+        assert offs == [i % B for i in range(L)]
+        assert blocks == [int(bt[s, i // B]) for i in range(L)]
+        assert len(set(blocks)) == -(-L // B)
+    assert len(seen) == int(lens.sum())
+    # the mapping entry point agrees with the single-slot function and pads with -1
+    ts = np.array([0, 3, 4, 4, 2], np.int32)
+    tp = np.array([0, 12, 30, -1, 7], np.int32)
+    sm = orc.slot_mapping(bt, ts, tp, B)
+    assert sm.tolist() == [orc.slot(bt, 0, 0, B), orc.slot(bt, 3, 12, B),
+                           orc.slot(bt, 4, 30, B), -1, orc.slot(bt, 2, 7, B)]
+
+
+def pin_append_scatter(orc):
+    """Append writes each token row at its slot and leaves everything else alone."""
+    rng = np.random.default_rng(5)
+    NB, B, Hkv, D = 6, 4, 2, 8
+    for dtype in ("f32", "f16", "bf16"):
+        kpool = poison((NB, B, Hkv, D), dtype)
+        vpool = poison((NB, B, Hkv, D), dtype)
+        T = 9
+        k = to_storage(rng.standard_normal((T, Hkv, D)), dtype)
+        v = to_storage(rng.standard_normal((T, Hkv, D)), dtype)
+        slots = rng.permutation(NB * B)[:T].astype(np.int64)
+        slots[3] = -1
+        slots[7] = NB * B + 2
+        ek, ev = kpool.copy(), vpool.copy()
+        keep = (slots >= 0) & (slots < NB * B)
+        ek.reshape(NB * B, Hkv, D)[slots[keep]] = k[keep]
+        ev.reshape(NB * B, Hkv, D)[slots[keep]] = v[keep]
+        bad = orc.append(k, v, slots, kpool, vpool)
+        assert bad == 1
+        assert kpool.tobytes() == ek.tobytes() and vpool.tobytes() == ev.tobytes()
+
+
+def pin_gather_order(orc):
+    """Tokens appended through the slot mapping come back from the gather in
+    logical order (row i of the gather holds the value written for position i)."""
+    B, Hkv, D = 4, 2, 8
+    case = paged_case(3, [1, 4, 5, 14], B, 2, Hkv, D, "f32")
+    kpool = poison((case["NB"], B, Hkv, D), "f32")
+    vpool = poison((case["NB"], B, Hkv, D), "f32")
+    for s, L in enumerate(case["lens"]):
+        pos = np.arange(L, dtype=np.int32)
+        seq = np.full(L, s, np.int32)
+        sm = orc.slot_mapping(case["bt"], seq, pos, B)
+        rows = np.zeros((L, Hkv, D), np.float32)
+        rows[:, :, 0] = pos[:, None] + 1000 * s
+        rows[:, :, 1] = np.arange(Hkv)[None, :]
+        orc.append(rows, rows, sm, kpool, vpool)
+    for s, L in enumerate(case["lens"]):
+        for h in range(Hkv):
+            G = orc.gather(kpool, case["bt"], s, L, h, "f32")
+            assert G[:, 0].tolist() == [i + 1000 * s for i in range(L)]
+            assert (G[:, 1] == h).all()
+
+
+# ---------------------------------------------------------------------------
+# Decode attention.
+# ---------------------------------------------------------------------------
+
+def pin_decode_bruteforce(orc):
+    """Equal to contiguous numpy/scipy attention on tiny inputs, all element types."""
+    shapes = [([1, 3, 4, 5, 17], 4, 1, 1, 8),
+              ([2, 7, 8, 9, 33], 8, 4, 2, 16),
+              ([16, 1, 25], 16, 8, 1, 8),
+              ([5, 12], 4, 6, 3, 4)]
+    for i, (lens, B, Hq, Hkv, D) in enumerate(shapes):
+        for dtype in ("f32", "f16", "bf16"):
+            case = paged_case(100 + i, lens, B, Hq, Hkv, D, dtype)
+            got = run_decode(orc, case)
+            ref = brute_force(case)
+            err = np.abs(got - ref).max()
+            assert err < 1e-12, (lens, B, Hq, Hkv, D, dtype, err)
+
+
+def pin_block_permutation_invariance(orc):
+    """Renumbering physical blocks (data moved with them) changes nothing."""
+    case = paged_case(21, [3, 17, 40, 9], 8, 4, 2, 16, "bf16")
+    base = run_decode(orc, case)
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(case["NB"])
+    k2 = np.empty_like(case["k"])
+    v2 = np.empty_like(case["v"])
+    k2[perm] = case["k"]
+    v2[perm] = case["v"]
+    bt2 = np.where(case["bt"] >= 0, perm[np.maximum(case["bt"], 0)], -1).astype(np.int32)
+    moved = dict(case, k=k2, v=v2, bt=bt2)
+    assert np.array_equal(run_decode(orc, moved), base)
+
+
+def pin_shared_prefix(orc):
+    """Sequences that share prefix blocks (refcount > 1) give the same result
+    as the same sequences holding private copies of those blocks."""
+    B, Hkv, D, dtype = 4, 2, 8, "f16"
+    case = paged_case(31, [13, 13, 13], B, 4, Hkv, D, dtype, spare_blocks=8)
+    k, v, bt = case["k"].copy(), case["v"].copy(), case["bt"].copy()
+    # make seqs 1 and 2 start with seq 0's first two blocks (8 tokens) as private copies
+    spare = sorted(set(range(case["NB"])) - set(bt[bt >= 0].tolist()))
+    for s in (1, 2):
+        for j in range(2):
+            k[bt[s, j]] = k[bt[0, j]]
+            v[bt[s, j]] = v[bt[0, j]]
+    private = dict(case, k=k, v=v, bt=bt)
+    shared_bt = bt.copy()
+    shared_bt[1:, :2] = bt[0, :2]
+    shared = dict(case, k=k, v=v, bt=shared_bt)
+    refs = np.bincount(shared_bt[shared_bt >= 0].ravel(), minlength=case["NB"])
+    assert refs[bt[0, 0]] == 3 and spare
+    assert np.array_equal(run_decode(orc, private), run_decode(orc, shared))
+
+
+def pin_special_cases(orc):
+    # one token: softmax weight 1, the output is that token's value exactly
+    case = paged_case(41, [1, 1], 4, 2, 1, 8, "bf16")
+    got = run_decode(orc, case)
+    for s in range(2):
+        for h in range(2):
+            assert np.array_equal(got[s, h], case["Vc"][s][0, 0])
+    # identical keys: uniform weights, the output is the mean of the values
+    case = paged_case(42, [11], 4, 1, 1, 8, "f32")
+    K = case["k"].copy()
+    ids = case["bt"][0][case["bt"][0] >= 0]
+    K[ids] = K[ids[0], 0]
+    got = run_decode(orc, dict(case, k=K))
+    assert np.abs(got[0, 0] - case["Vc"][0][:, 0].mean(axis=0)).max() < 1e-14
+    # empty context: zeros, no NaN
+    case = paged_case(43, [0, 5], 4, 2, 2, 8, "f32")
+    got = run_decode(orc, case)
+    assert (got[0] == 0).all() and np.isfinite(got[1]).all()
+    # a query of zeros: uniform weights again
+    case = paged_case(44, [7], 4, 1, 1, 8, "f32")
+    q0 = np.zeros_like(case["q"])
+    got = run_decode(orc, dict(case, q=q0))
+    assert np.abs(got[0, 0] - case["Vc"][0][:, 0].mean(axis=0)).max() < 1e-14
+
+
+def pin_partition_merge(orc):
+    """Splitting the context and merging partition states is an identity."""
+    case = paged_case(51, [45, 9], 4, 4, 2, 8, "f16")
+    full = run_decode(orc, case)
+    args = (case["q"], case["k"], case["v"], case["bt"], case["scale"], case["dtype"])
+    for s, L in enumerate(case["lens"]):
+        for qh in range(case["Hq"]):
+            for P in (4, 8, 12, 64):
+                cuts = list(range(0, L, P)) + [L]
+                parts = [orc.decode_partition(*args, s, qh, a, b) for a, b in zip(cuts, cuts[1:])]
+                o = np.array([p[0] for p in parts])
+                m = np.array([p[1] for p in parts])
+                l = np.array([p[2] for p in parts])
+                merged = orc.lse_merge(m, l, o)
+                assert np.abs(merged - full[s, qh]).max() < 1e-12, (s, qh, P)
+            o1, m1, l1 = orc.decode_partition(*args, s, qh, 0, L)
+            assert np.abs(o1 / l1 - full[s, qh]).max() < 1e-12
+            oe, me, le = orc.decode_partition(*args, s, qh, 3, 3)
+            assert me == -math.inf and le == 0 and (oe == 0).all()
+            mixed = orc.lse_merge(np.array([me, m1]), np.array([le, l1]), np.stack([oe, o1]))
+            assert np.abs(mixed - full[s, qh]).max() < 1e-12
+
+
+ALL_PINS = [pin_f16_decoding, pin_bf16_decoding, pin_block_table_example, pin_slot_bijection,
+            pin_append_scatter, pin_gather_order, pin_decode_bruteforce,
+            pin_block_permutation_invariance, pin_shared_prefix, pin_special_cases,
+            pin_partition_merge]
