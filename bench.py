@@ -1,0 +1,545 @@
+"""Benchmark: one decode step of one layer over a block-paged KV cache.
+
+A step is the whole hot path over one batch: address translation of the
+step's new tokens (paged_kv_slot_mapping), their K/V append
+(paged_kv_append) and the fused paged-attention decode of every sequence
+(paged_attention_decode, split-K partitions + merge where configured).
+
+Default workload: the Llama-2-7B-shaped MHA layer (64 sequences, 32 heads,
+head_dim 128, fp16, block size 16, lengths uniform in [128, 2048], physical
+blocks shuffled over a pool 1.25x the need), synthetic seeded inputs.
+
+Prints one JSON line (rank 0). `value` is whole-job paged-decode GB/s: the
+step's algorithmic bytes (unique KV bytes + q + out + block-table + length
+bytes) over the device-timed step; `--impl reference` times the fp64 CPU
+oracle instead on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+if REPO not in sys.path:
+    sys.path.insert(0, REPO)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import materialize, new_pools, preset  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu", "api.cu",
+                  "decode_instances.cuh"]
+
+# partition size (tokens) used for each workload's decode; 0 = no split
+PARTITION = {"tiny": 0, "mha7b": 256, "gqa8b_prefix": 256, "longctx_splitk": 512}
+
+DESCRIPTION = {
+    "tiny": "tiny: 4 seqs, lens {2,18,34,65}, B16, 4q/2kv heads, D64, fp32",
+    "mha7b": "mha7b: Llama-2-7B-shaped MHA layer, 64 seqs, lens U[128,2048], 32q=32kv heads, "
+             "D128, fp16, B16, shuffled pool 1.25x need",
+    "gqa8b_prefix": "gqa8b_prefix: Llama-3-8B-shaped GQA layer, 256 seqs, lognormal lens "
+                    "(median 1024, sigma 0.75, clip [513,8192]), 32q/8kv heads, D128, bf16, B16, "
+                    "groups of 16 share a 512-token prefix",
+    "longctx_splitk": "longctx_splitk: 8 seqs, lens U[32768,131072], 64q/8kv heads, D128, bf16, "
+                      "B16, 512-token partitions + LSE merge",
+}
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting (algorithmic: what the method must move at minimum)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(wl):
+    """(algorithmic bytes per decode, logical-KV bytes per decode, KV-unique bytes)."""
+    B, elt = wl.block_size, wl.element_bytes
+    row = wl.n_kv_heads * wl.head_dim * elt          # one token's K (or V) for all kv heads
+    used = {}
+    nblk_total = 0
+    for s in range(wl.num_seqs):
+        L = int(wl.context_lens[s])
+        nb = -(-L // B)
+        nblk_total += nb
+        for j in range(nb):
+            b = int(wl.block_tables[s, j])
+            n = min(B, L - j * B)
+            if used.get(b, 0) < n:
+                used[b] = n
+    kv_unique = 2 * row * sum(used.values())
+    kv_logical = 2 * row * int(wl.context_lens.sum())
+    other = 2 * wl.num_seqs * wl.n_q_heads * wl.head_dim * elt + 4 * nblk_total + 4 * wl.num_seqs
+    return kv_unique + other, kv_logical + other, kv_unique
+
+
+def append_bytes(wl, tokens):
+    return 2 * 2 * tokens * wl.row_bytes + 8 * tokens
+
+
+def measured_peak():
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(REPO, "paged_kv_cache_233_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, partition):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(REPO, "profiles", f"decode_{workload}_traffic.txt")
+    try:
+        kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line)
+    except OSError:
+        return None
+    if kv.get("source_digest") != kernel_source_digest() or int(kv.get("partition", -1)) != partition:
+        return None
+    try:
+        return float(kv["dram_bytes_per_decode"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# The step
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device-resident inputs and the three calls of one decode step."""
+
+    def __init__(self, wl, device, partition):
+        import paged_kv_cache_233_gb300 as pk
+        self.pk = pk
+        self.wl = wl
+        self.partition = partition
+        self.t = materialize(wl, device)
+        self.kc, self.vc = new_pools(wl, device, fill=0.0)
+        self.bt = torch.from_numpy(wl.block_tables).to(device)
+        self.lens = torch.from_numpy(wl.context_lens).to(device)
+        self.step_seq = torch.from_numpy(wl.step_seq).to(device)
+        self.step_pos = torch.from_numpy(wl.step_pos).to(device)
+        self.slots = torch.empty(len(wl.step_seq), dtype=torch.int64, device=device)
+        self.out = torch.empty_like(self.t["q"])
+        self.ws = pk.new_workspace(self.t["q"], self.bt, wl.block_size, partition)
+        # bulk fill of the history (timed separately: append GB/s over the whole context)
+        fill_seq = torch.from_numpy(wl.fill_seq).to(device)
+        fill_pos = torch.from_numpy(wl.fill_pos).to(device)
+        fill_slots = torch.empty(len(wl.fill_seq), dtype=torch.int64, device=device)
+        pk.paged_kv_slot_mapping(self.bt, fill_seq, fill_pos, fill_slots, wl.num_blocks,
+                                 wl.block_size)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pk.paged_kv_append(self.t["k_fill"], self.t["v_fill"], fill_slots, self.kc, self.vc)
+        e1.record()
+        torch.cuda.synchronize()
+        self.fill_ms = e0.elapsed_time(e1)
+        self.fill_tokens = len(wl.fill_seq)
+        del fill_seq, fill_pos, fill_slots
+        self.launches_per_step = 3 + (1 if partition > 0 else 0)
+
+    def run(self, ev=None):
+        pk, wl = self.pk, self.wl
+        pk.paged_kv_slot_mapping(self.bt, self.step_seq, self.step_pos, self.slots,
+                                 wl.num_blocks, wl.block_size)
+        pk.paged_kv_append(self.t["k_step"], self.t["v_step"], self.slots, self.kc, self.vc)
+        if ev is not None:
+            ev[0].record()
+        pk.paged_attention_decode(self.t["q"], self.kc, self.vc, self.bt, self.lens, wl.scale,
+                                  self.out, self.partition, self.ws)
+        if ev is not None:
+            ev[1].record()
+
+
+def time_steps(step, steps, dist_ctx):
+    """Device time of exactly `steps` steps (max over ranks), plus decode-only time."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        step.run(pairs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    total_ms = dist_ctx.max(start.elapsed_time(stop))
+    decode_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
+    return total_ms, decode_ms
+
+
+def time_e2e(step, steps):
+    """Same step through the public API with host inputs: pinned host -> device
+    copies of the step's inputs and a device -> host read of its output."""
+    wl, t = step.wl, step.t
+    host = {name: x.cpu().pin_memory() for name, x in (
+        ("q", t["q"]), ("k", t["k_step"]), ("v", t["v_step"]), ("bt", step.bt),
+        ("lens", step.lens), ("seq", step.step_seq), ("pos", step.step_pos))}
+    dev = {"q": t["q"], "k": t["k_step"], "v": t["v_step"], "bt": step.bt, "lens": step.lens,
+           "seq": step.step_seq, "pos": step.step_pos}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        for name, x in host.items():
+            dev[name].copy_(x, non_blocking=True)
+        step.run()
+        out_host.copy_(step.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def host_storage(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_pools(orc, wl, tensors):
+    shape = (wl.num_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim)
+    np_dtype = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[wl.dtype]
+    kc = np.zeros(shape, dtype=np_dtype)
+    vc = np.zeros(shape, dtype=np_dtype)
+    for seq, pos, k, v in ((wl.fill_seq, wl.fill_pos, tensors["k_fill"], tensors["v_fill"]),
+                           (wl.step_seq, wl.step_pos, tensors["k_step"], tensors["v_step"])):
+        sm = orc.slot_mapping(wl.block_tables, seq, pos, wl.block_size)
+        orc.append(host_storage(k), host_storage(v), sm, kc, vc)
+    return kc, vc
+
+
+def oracle_rate(orc, wl, q, kc, vc, budget_s, start_unit=0):
+    """Time the oracle's decode over consecutive (seq, kv head) units until the
+    budget is spent. Returns (bytes, seconds, units, threads)."""
+    units = [(s, h) for s in range(wl.num_seqs) for h in range(wl.n_kv_heads)]
+    threads = orc.max_threads()
+    row = wl.head_dim * wl.element_bytes
+    done_bytes, elapsed, n = 0, 0.0, 0
+    i = start_unit % len(units)
+    chunk = max(1, threads)
+    while elapsed < budget_s and n < len(units):
+        batch = [units[(i + k) % len(units)] for k in range(min(chunk, len(units) - n))]
+        t0 = time.perf_counter()
+        orc.decode(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, units=batch,
+                   threads=threads)
+        elapsed += time.perf_counter() - t0
+        for s, _ in batch:
+            L = int(wl.context_lens[s])
+            done_bytes += 2 * L * row + 2 * wl.group * wl.head_dim * wl.element_bytes
+        n += len(batch)
+        i += len(batch)
+    return done_bytes, elapsed, n, threads
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; replicas of the workload)
+# ---------------------------------------------------------------------------
+
+class DistCtx:
+    def __init__(self, connect=True):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1 and connect:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x):
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x):
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def workload_for(name, rank):
+    wl = preset(name)
+    if rank:
+        wl = preset(name, seed=wl.seed + 1000 * rank)
+    return wl
+
+
+# ---------------------------------------------------------------------------
+# Arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, ctx):
+    """The fp64 CPU oracle, as it stands, on bounded samples of the workload."""
+    if ctx.rank != 0:
+        return None
+    import oracle
+    orc = oracle.get()
+    wl = preset(args.config)
+    tensors = materialize(wl, "cpu")
+    kc, vc = oracle_pools(orc, wl, tensors)
+    q = host_storage(tensors["q"])
+    per_step = max(0.05, min(20.0, args.reference_budget / max(1, args.steps + args.warmup)))
+    for w in range(args.warmup):
+        oracle_rate(orc, wl, q, kc, vc, per_step, start_unit=w)
+    total_bytes, total_s, total_units, threads = 0, 0.0, 0, 1
+    for k in range(args.steps):
+        b, s, n, threads = oracle_rate(orc, wl, q, kc, vc, per_step, start_unit=k * 7)
+        total_bytes += b
+        total_s += s
+        total_units += n
+    value = total_bytes / total_s / 1e9
+    sample = (f"{total_units} (sequence, kv head) units over {args.steps} steps, "
+              f"~{per_step:.2f} s of oracle work per step, of {wl.num_seqs * wl.n_kv_heads} units")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": ctx.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": DESCRIPTION[args.config]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def measure_gate(name, args, device):
+    """Decode-only roofline fraction of one workload (for the stated targets)."""
+    import paged_kv_cache_233_gb300 as pk
+    wl = preset(name)
+    P = PARTITION[name]
+    step = Step(wl, device, P)
+    for _ in range(args.warmup):
+        step.run()
+    reps = args.gate_reps
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        pairs[i][0].record()
+        pk.paged_attention_decode(step.t["q"], step.kc, step.vc, step.bt, step.lens, wl.scale,
+                                  step.out, P, step.ws)
+        pairs[i][1].record()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in pairs]
+    algo, logical, kv_unique = decode_bytes(wl)
+    peak, _ = measured_peak()
+    med = statistics.median(ms)
+    res = {"decode_ms_median": med, "achieved_gbs": algo / med / 1e6,
+           "frac": algo / med / 1e6 / peak, "logical_gbs": logical / med / 1e6,
+           "algorithmic_bytes": algo, "kv_unique_bytes": kv_unique, "partition_tokens": P,
+           "decode_path": pk.last_decode_path(), "reps": reps}
+    del step
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, ctx):
+    import paged_kv_cache_233_gb300 as pk
+    from paged_kv_cache_233_gb300 import build as pk_build
+    if ctx.rank == 0:
+        pk_build.build()
+    ctx.barrier()
+    pk_build.build()
+    pk.load()
+    torch.cuda.set_device(ctx.local_rank)
+    device = torch.device("cuda", ctx.local_rank)
+    if args.path is not None:
+        pk.set_option(pk.OPT_DECODE_PATH, args.path)
+    if args.ctas is not None:
+        pk.set_option(pk.OPT_CTAS_PER_SM, args.ctas)
+    wl = workload_for(args.config, ctx.rank)
+    P = PARTITION[args.config] if args.partition is None else args.partition
+    step = Step(wl, device, P)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if pk.device_errors():
+        raise RuntimeError("device error flags set during warm-up")
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        total_ms, decode_ms = time_steps(step, args.steps, ctx)
+    clocks = clk.summary()
+    ms_per_step = total_ms / args.steps
+    algo, logical, kv_unique = decode_bytes(wl)
+    all_bytes = ctx.sum(algo)
+    value = all_bytes / ms_per_step / 1e6                      # GB/s, whole job
+    seq_decodes = ctx.sum(wl.num_seqs) / (ms_per_step * 1e-3)
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e2e_ms, h2d, d2h = time_e2e(step, e2e_steps)
+    e2e_ms = ctx.max(e2e_ms)
+    peak, peak_kind = measured_peak()
+    achieved = algo / decode_ms / 1e6
+    result = None
+    if ctx.rank == 0:
+        result = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ctx.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic",
+            "config": {"workload": DESCRIPTION[args.config], "partition_tokens": P,
+                       "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
+                       "l2": f"inputs larger than L2: KV pool {2 * wl.num_blocks * wl.block_size * wl.row_bytes / 1e9:.2f} GB",
+                       "parallelism": f"replicas x{ctx.world} (one workload per GPU)"},
+            "seq_decodes_per_s_per_layer": seq_decodes,
+            "kv_logical_gbs": ctx.sum(logical) / ms_per_step / 1e6,
+            "append_bulk_gbs": append_bytes(wl, step.fill_tokens) / step.fill_ms / 1e6,
+            "clocks": clocks,
+            "e2e": {"value": all_bytes / e2e_ms / 1e6, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "gpu_launches": step.launches_per_step * args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(args.config, P),
+                         "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)",
+                         "kernel": "paged_decode_kernel + lse_merge_kernel (one decode call)",
+                         "decode_ms": decode_ms, "algorithmic_bytes_per_launch": algo},
+        }
+    del step
+    torch.cuda.empty_cache()
+    if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
+        result["gates"] = {name: measure_gate(name, args, device)
+                           for name in ("gqa8b_prefix", "longctx_splitk")}
+    if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
+        import oracle
+        orc = oracle.get()
+        wl0 = preset(args.config)
+        tensors = materialize(wl0, "cpu")
+        kc, vc = oracle_pools(orc, wl0, tensors)
+        b, s, n, threads = oracle_rate(orc, wl0, host_storage(tensors["q"]), kc, vc,
+                                       args.cpu_budget)
+        result["cpu_baseline"] = {
+            "value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {wl0.num_seqs * wl0.n_kv_heads} (sequence, kv head) units "
+                      f"of the same workload, {s:.1f} s of fp64 oracle decode"}
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="mha7b", choices=sorted(DESCRIPTION))
+    ap.add_argument("--partition", type=int, default=None)
+    ap.add_argument("--path", type=int, default=None, help="1 CUDA-core, 2 tensor-core decode")
+    ap.add_argument("--ctas", type=int, default=None, help="persistent decode CTAs per SM")
+    ap.add_argument("--e2e-steps", type=int, default=400)
+    ap.add_argument("--gate-reps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--reference-budget", type=float, default=90.0)
+    ap.add_argument("--no-gates", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    ctx = DistCtx(connect=args.impl == "ours")
+    try:
+        result = run_reference(args, ctx) if args.impl == "reference" else run_ours(args, ctx)
+    finally:
+        ctx.close()
+    if result is not None:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

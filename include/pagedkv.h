@@ -1,0 +1,208 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: attention over a block-paged KV cache on
+ * one GB300 (sm_103a).
+ *
+ * The cache of one layer is a pool of fixed-size blocks, one K pool and one V
+ * pool, each laid out
+ *
+ *     [num_blocks][block_size][n_kv_heads][head_dim]      (row-major, dense)
+ *
+ * and indexed by physical block, not by sequence (page "Paged-KV + Continuous
+ * Batching From Scratch", section 1 "Paging is really about not reserving").
+ * A sequence owns a block table: the list of its physical blocks in logical
+ * order. Token i of sequence s lives in slot
+ *
+ *     slot(s, i) = block_table[s][i / block_size] * block_size + i % block_size
+ *
+ * (page "How a serving engine actually works", section "The one formula").
+ *
+ * Conventions shared by every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller. The
+ *     library allocates no memory, frees nothing and keeps no pointer after a
+ *     call returns. Arrays are dense, row-major, 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls only enqueue work on it and return without
+ *     synchronising; results are ready when the stream reaches them.
+ *   - `dtype` is a pagedkv_dtype. q, k, v, the pools and out share it.
+ *   - Argument and shape checks run on the host before anything is enqueued;
+ *     a failed check returns a negative pagedkv_status and enqueues nothing.
+ *   - Out-of-range values found on the device (a block id outside the pool,
+ *     a slot past the pool, a context length longer than the block table) are
+ *     never dereferenced: the kernel skips or clamps the access and sets a bit
+ *     in a sticky device error word that pagedkv_device_errors() returns.
+ *   - Kernels never trap. Every wait inside a kernel is bounded in time; a
+ *     wait that gives up sets PAGEDKV_DEVERR_TIMEOUT and the kernel returns.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAGEDKV_ABI_VERSION 1
+
+typedef enum {
+    PAGEDKV_F32 = 0,   /* IEEE binary32 */
+    PAGEDKV_F16 = 1,   /* IEEE binary16 */
+    PAGEDKV_BF16 = 2   /* bfloat16 */
+} pagedkv_dtype;
+
+typedef enum {
+    PAGEDKV_OK = 0,
+    PAGEDKV_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer */
+    PAGEDKV_ERR_UNSUPPORTED = -2,  /* valid but not built: e.g. head_dim 96 */
+    PAGEDKV_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+    PAGEDKV_ERR_BOUNDS = -4,       /* pagedkv_device_errors() found a set bit */
+    PAGEDKV_ERR_WORKSPACE = -5     /* split-K workspace missing or too small */
+} pagedkv_status;
+
+/* Bits of the sticky device error word. */
+#define PAGEDKV_DEVERR_SLOT_RANGE   0x01u  /* append: slot >= num_blocks*block_size */
+#define PAGEDKV_DEVERR_BLOCK_ID     0x02u  /* a block table entry outside [0, num_blocks) */
+#define PAGEDKV_DEVERR_CONTEXT_LEN  0x04u  /* context_len < 0 or > max_blocks_per_seq*block_size */
+#define PAGEDKV_DEVERR_POSITION     0x08u  /* slot mapping: position past the block table */
+#define PAGEDKV_DEVERR_SEQ_INDEX    0x10u  /* slot mapping: token_seq outside [0, num_seqs) */
+#define PAGEDKV_DEVERR_TIMEOUT      0x20u  /* a bounded in-kernel wait gave up */
+
+/*
+ * paged_kv_slot_mapping -- address translation for a batch of new tokens.
+ *
+ * Implements "The one formula" (page "How a serving engine actually works"):
+ * token t belongs to sequence token_seq[t] at logical position token_pos[t];
+ *
+ *     slot_mapping[t] = block_tables[seq][pos / block_size] * block_size
+ *                       + pos % block_size.
+ *
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq], device
+ *   token_seq     int32 [num_tokens], device
+ *   token_pos     int32 [num_tokens], device; a negative position is padding
+ *   slot_mapping  int64 [num_tokens], device, written
+ *
+ * Padding maps to -1. A position past the table, a sequence index outside
+ * [0, num_seqs) or a block id outside [0, num_blocks) also maps to -1 and sets
+ * the matching device error bit. num_tokens == 0 enqueues nothing.
+ */
+int paged_kv_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
+                          const int32_t *token_pos, int64_t *slot_mapping, int num_tokens,
+                          int num_seqs, int max_blocks_per_seq, int block_size, int num_blocks,
+                          void *stream);
+
+/*
+ * paged_kv_append -- scatter new tokens' K and V rows into their pool slots.
+ *
+ * The write half of the paged cache (page "Paged-KV + Continuous Batching From
+ * Scratch", section "What's deliberately still missing": the append is plain
+ * indexing into the pool):
+ *
+ *     k_cache[slot / block_size][slot % block_size][:][:] = k[t][:][:]
+ *     v_cache[slot / block_size][slot % block_size][:][:] = v[t][:][:]
+ *
+ * with slot = slot_mapping[t]. A bit copy: the pools end up bit-identical to
+ * what plain indexing produces.
+ *
+ *   k, v          [num_tokens][n_kv_heads][head_dim] of dtype, device
+ *   slot_mapping  int64 [num_tokens], device; slot < 0 is padding (skipped)
+ *   k_cache,
+ *   v_cache       [num_blocks][block_size][n_kv_heads][head_dim] of dtype,
+ *                 device, updated in place
+ *
+ * A slot >= num_blocks*block_size is skipped and sets PAGEDKV_DEVERR_SLOT_RANGE.
+ * Two tokens with the same slot race; the caller must not do that.
+ * Requires n_kv_heads*head_dim*sizeof(dtype) to be a multiple of 16 bytes.
+ */
+int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache,
+                    void *v_cache, int num_tokens, int num_blocks, int block_size,
+                    int n_kv_heads, int head_dim, int dtype, void *stream);
+
+/*
+ * paged_attention_decode -- fused paged-attention decode.
+ *
+ * The kernel the pages name as the next step and never build (page "Paged-KV +
+ * Continuous Batching From Scratch", section "What's deliberately still
+ * missing"; page "Paged Attention and the Block Manager", section "The
+ * measurement"): attention over each sequence's cache, reading K and V
+ * through the block table inside the kernel instead of gathering them into a
+ * contiguous copy first. The mathematics is unchanged softmax attention:
+ *
+ *     for each sequence s and query head h (kv head h / (n_q_heads/n_kv_heads)):
+ *         z_i   = scale * q[s][h] . K_s[i]          for i < context_lens[s]
+ *         out[s][h] = sum_i softmax(z)_i V_s[i]
+ *
+ * with K_s[i] = k_cache at slot(s, i). Scores, the running max and sum and the
+ * output accumulator are fp32; out is rounded once to dtype (round to nearest
+ * even). A context length of 0 gives a zero row.
+ *
+ *   q             [num_seqs][n_q_heads][head_dim] of dtype, device
+ *   k_cache,
+ *   v_cache       [num_blocks][block_size][n_kv_heads][head_dim] of dtype, device
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq], device; entries past a
+ *                 sequence's ceil(context_len / block_size) blocks are never read
+ *   context_lens  int32 [num_seqs], device
+ *   out           [num_seqs][n_q_heads][head_dim] of dtype, device, written
+ *
+ * partition_tokens == 0: each (sequence, kv head) is processed whole.
+ * partition_tokens > 0 (a multiple of 16): split-K. Each sequence's context is
+ *   cut into partitions of that many tokens; each (sequence, kv head,
+ *   partition) produces an unnormalised state per query head
+ *       m_p = max z_i,  l_p = sum e^(z_i - m_p),  o_p = sum e^(z_i - m_p) V_i
+ *   over its tokens, and a merge kernel combines them:
+ *       M = max_p m_p,  out = sum_p e^(m_p - M) o_p / sum_p e^(m_p - M) l_p.
+ *   Sequences that fit in one partition skip the merge. The states live in
+ *   the caller's workspace (see paged_attention_workspace_bytes), as fp32
+ *       o [num_seqs][n_q_heads][P][head_dim], then m [num_seqs][n_q_heads][P],
+ *       then l [num_seqs][n_q_heads][P],
+ *   P = ceil(max_blocks_per_seq*block_size / partition_tokens), each array
+ *   starting on a 256-byte boundary; m is in natural-log units. Entries of
+ *   partitions a sequence does not have are left untouched.
+ *
+ * Supported: head_dim 64 or 128; block_size 8, 16 or 32; n_q_heads a multiple
+ * of n_kv_heads with n_q_heads / n_kv_heads <= 8; num_seqs <= 4096.
+ * workspace may be NULL when partition_tokens == 0.
+ */
+int paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           float scale, void *out, int num_seqs, int n_q_heads, int n_kv_heads,
+                           int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                           int partition_tokens, void *workspace, size_t workspace_bytes,
+                           int dtype, void *stream);
+
+/* Workspace bytes paged_attention_decode needs for these sizes (0 when
+ * partition_tokens == 0). Returns 0 for invalid sizes as well. */
+size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,
+                                       int max_blocks_per_seq, int block_size,
+                                       int partition_tokens);
+
+/*
+ * pagedkv_device_errors -- read (and optionally clear) the sticky device
+ * error word of the current device. Synchronises the device first, so it
+ * sees every kernel enqueued before the call. *flags receives the PAGEDKV_DEVERR_*
+ * bits. Returns PAGEDKV_OK when no bit is set, PAGEDKV_ERR_BOUNDS when one is,
+ * PAGEDKV_ERR_CUDA when the read fails.
+ */
+int pagedkv_device_errors(unsigned int *flags, int reset);
+
+/* Tuning knobs, process-wide and not thread-safe; for tests and benchmarks. */
+#define PAGEDKV_OPT_DECODE_PATH    1  /* 0 auto, 1 CUDA-core (SIMT) path, 2 tensor-core (mma) path */
+#define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */
+#define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
+int pagedkv_set_option(int option, int value);
+int pagedkv_get_option(int option);
+
+/* Library path of the last decode call, for tests: 1 SIMT, 2 mma. */
+int pagedkv_last_decode_path(void);
+
+/* Human-readable name of a pagedkv_status. Never NULL. */
+const char *pagedkv_status_string(int status);
+
+/* PAGEDKV_ABI_VERSION of the built library. */
+int pagedkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,211 @@
+"""GB300-native paged KV cache: append and fused paged-attention decode.
+
+A thin ctypes binding over ``libpagedkv.so`` (C ABI in ``include/pagedkv.h``).
+It only marshals torch tensors into pointers and sizes: every step of the
+path runs in the library's CUDA kernels, and there is no CPU fallback. If the
+library has not been built, the first call raises ``PagedKVError`` (build it
+with ``python -m paged_kv_cache_233_gb300.build``).
+
+The entry points keep the C names:
+
+    paged_kv_slot_mapping(block_tables, token_seq, token_pos, slot_mapping, num_blocks, block_size)
+    paged_kv_append(k, v, slot_mapping, k_cache, v_cache)
+    paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                           partition_tokens=0, workspace=None)
+    paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq,
+                                    block_size, partition_tokens)
+
+All tensors live on the current CUDA device; work is enqueued on the current
+torch stream (or the stream passed) and the calls return without waiting.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PagedKVError", "paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
+    "paged_attention_workspace_bytes", "new_workspace", "device_errors", "set_option",
+    "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
+    "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP = 1, 2, 3
+EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
+           "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
+           "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
+           "pagedkv_abi_version")
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load():
+    """Load libpagedkv.so (once). Raises PagedKVError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise PagedKVError(
+            f"{_LIB_PATH} is not built: run `python -m paged_kv_cache_233_gb300.build` "
+            "(the paged-KV path has no fallback)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.paged_kv_slot_mapping.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.paged_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32,
+                                           i32, i32, i32, i32, i32, vp, sz, i32, vp]
+    lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_workspace_bytes.restype = sz
+    lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+    lib.pagedkv_set_option.argtypes = [i32, i32]
+    lib.pagedkv_get_option.argtypes = [i32]
+    lib.pagedkv_status_string.argtypes = [i32]
+    lib.pagedkv_status_string.restype = ctypes.c_char_p
+    for name in ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
+                 "pagedkv_device_errors", "pagedkv_set_option", "pagedkv_get_option",
+                 "pagedkv_last_decode_path", "pagedkv_abi_version"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().pagedkv_status_string(int(status)).decode()
+
+
+def abi_version():
+    return load().pagedkv_abi_version()
+
+
+def _check(status, what):
+    if status != 0:
+        raise PagedKVError(f"{what}: {status_string(status)} ({status})")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise PagedKVError(f"{name} must be a CUDA tensor (the paged-KV path has no CPU fallback)")
+    if not t.is_contiguous():
+        raise PagedKVError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PagedKVError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _code(t):
+    try:
+        return DTYPE_CODES[t.dtype]
+    except KeyError:
+        raise PagedKVError(f"unsupported element type {t.dtype}") from None
+
+
+def paged_kv_slot_mapping(block_tables, token_seq, token_pos, slot_mapping, num_blocks, block_size,
+                          stream=None):
+    """slot_mapping[t] = block_tables[seq][pos // B] * B + pos % B (int64; -1 for padding)."""
+    n = token_seq.numel()
+    if token_pos.numel() != n or slot_mapping.numel() != n:
+        raise PagedKVError("token_seq, token_pos and slot_mapping differ in length")
+    st = load().paged_kv_slot_mapping(
+        _dev(block_tables, "block_tables", torch.int32), _dev(token_seq, "token_seq", torch.int32),
+        _dev(token_pos, "token_pos", torch.int32), _dev(slot_mapping, "slot_mapping", torch.int64),
+        n, block_tables.shape[0], block_tables.shape[1], int(block_size), int(num_blocks),
+        _stream(stream))
+    _check(st, "paged_kv_slot_mapping")
+
+
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """Scatter k/v [T][Hkv][D] into the pools [NB][B][Hkv][D] at slot_mapping[T]."""
+    if k.dim() != 3 or k.shape != v.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise PagedKVError("expected k, v [T][Hkv][D] and pools [NB][B][Hkv][D]")
+    if k.dtype != k_cache.dtype or v.dtype != k.dtype or v_cache.dtype != k.dtype:
+        raise PagedKVError("k, v and the pools must share one element type")
+    if tuple(k.shape[1:]) != tuple(k_cache.shape[2:]):
+        raise PagedKVError("token rows do not match the pool's [Hkv][D]")
+    if slot_mapping.numel() != k.shape[0]:
+        raise PagedKVError("slot_mapping length differs from the number of tokens")
+    NB, B, Hkv, D = k_cache.shape
+    st = load().paged_kv_append(
+        _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), k.shape[0], NB, B, Hkv, D, _code(k),
+        _stream(stream))
+    _check(st, "paged_kv_append")
+
+
+def paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq, block_size,
+                                    partition_tokens):
+    return load().paged_attention_workspace_bytes(int(num_seqs), int(n_q_heads), int(head_dim),
+                                                  int(max_blocks_per_seq), int(block_size),
+                                                  int(partition_tokens))
+
+
+def new_workspace(q, block_tables, block_size, partition_tokens):
+    """A device buffer large enough for split-K decode with these shapes (None if not split)."""
+    n = paged_attention_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], block_tables.shape[1],
+                                        block_size, partition_tokens)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                           partition_tokens=0, workspace=None, stream=None):
+    """out[s][h] = softmax(scale * q[s][h] . K_s) V_s with K_s, V_s read through block_tables."""
+    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
+    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
+        raise PagedKVError("q, out and the pools must share one element type")
+    S, Hq, D = q.shape
+    NB, B, Hkv, Dk = k_cache.shape
+    if Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise PagedKVError("shape mismatch between q, the pools, block_tables and context_lens")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().paged_attention_decode(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S, Hq, Hkv,
+        D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr, ws_bytes, _code(q),
+        _stream(stream))
+    _check(st, "paged_attention_decode")
+
+
+def device_errors(reset=True):
+    """The sticky device error bits (synchronises the device); 0 when clean."""
+    flags = ctypes.c_uint(0)
+    st = load().pagedkv_device_errors(ctypes.byref(flags), 1 if reset else 0)
+    if st not in (0, -4):
+        _check(st, "pagedkv_device_errors")
+    return flags.value
+
+
+def set_option(option, value):
+    _check(load().pagedkv_set_option(int(option), int(value)), "pagedkv_set_option")
+
+
+def get_option(option):
+    return load().pagedkv_get_option(int(option))
+
+
+def last_decode_path():
+    return load().pagedkv_last_decode_path()

@@ -1,0 +1,348 @@
+// api.cu -- the C ABI of libpagedkv (declared in include/pagedkv.h).
+//
+// Host-side argument checks, the per-device error word, TMA descriptor
+// encoding for the K/V pools, decode-path selection and the launches. No
+// memory is allocated here; every buffer belongs to the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "decode_launch.h"
+
+namespace pkv {
+cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
+                                const int32_t *token_pos, int64_t *slot_mapping, int num_tokens,
+                                int num_seqs, int max_blocks, int block_size, int num_blocks,
+                                unsigned int *err, cudaStream_t st);
+cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache,
+                          void *v_cache, int num_tokens, long long row_bytes, long long num_slots,
+                          int num_sms, unsigned int *err, cudaStream_t st);
+}  // namespace pkv
+
+// Sticky error word, one per device that loads the library.
+__device__ unsigned int g_pagedkv_errors = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSeqs = 4096;
+
+std::mutex g_mu;
+unsigned int *g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+int g_opt_path = pkv::kPathAuto;
+int g_opt_ctas_per_sm = 0;
+int g_opt_mma_min_group = 4;
+int g_last_path = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int elem_bytes(int dtype) { return dtype == PAGEDKV_F32 ? 4 : 2; }
+
+bool valid_dtype(int dtype) {
+    return dtype == PAGEDKV_F32 || dtype == PAGEDKV_F16 || dtype == PAGEDKV_BF16;
+}
+
+// Error-word address and SM count of the current device (looked up once per device).
+int device_state(unsigned int **err, int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PAGEDKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pagedkv_errors) != cudaSuccess || !p) return PAGEDKV_ERR_CUDA;
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            return PAGEDKV_ERR_CUDA;
+        g_num_sms[dev] = n;
+        g_err_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *err = g_err_ptr[dev];
+    *sms = g_num_sms[dev];
+    return PAGEDKV_OK;
+}
+
+int encoder(EncodeTiledFn *fn) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return PAGEDKV_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return PAGEDKV_OK;
+}
+
+// TMA view of one pool: (head_dim, n_kv_heads, num_slots) with a box of one
+// 128-byte column slab x one head x min(block_size, 16) tokens, 128-byte swizzle.
+int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim, int n_kv_heads,
+                    long long num_slots, int block_size) {
+    EncodeTiledFn fn = nullptr;
+    int st = encoder(&fn);
+    if (st != PAGEDKV_OK) return st;
+    const int eb = elem_bytes(dtype);
+    const CUtensorMapDataType dt = dtype == PAGEDKV_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == PAGEDKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(n_kv_heads), cuuint64_t(num_slots)};
+    const cuuint64_t strides[2] = {cuuint64_t(head_dim) * eb, cuuint64_t(n_kv_heads) * head_dim * eb};
+    const cuuint32_t box[3] = {cuuint32_t(128 / eb), 1u, cuuint32_t(block_size < 16 ? block_size : 16)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map, dt, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+long long max_parts_for(int max_blocks, int block_size, int part_tokens) {
+    const long long cap = (long long)max_blocks * block_size;
+    return (cap + part_tokens - 1) / part_tokens;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pagedkv_abi_version(void) { return PAGEDKV_ABI_VERSION; }
+
+const char *pagedkv_status_string(int status) {
+    switch (status) {
+        case PAGEDKV_OK: return "ok";
+        case PAGEDKV_ERR_INVALID_ARG: return "invalid argument";
+        case PAGEDKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PAGEDKV_ERR_CUDA: return "CUDA error";
+        case PAGEDKV_ERR_BOUNDS: return "device reported an out-of-range value";
+        case PAGEDKV_ERR_WORKSPACE: return "split-K workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int pagedkv_set_option(int option, int value) {
+    switch (option) {
+        case PAGEDKV_OPT_DECODE_PATH:
+            if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_path = value;
+            return PAGEDKV_OK;
+        case PAGEDKV_OPT_CTAS_PER_SM:
+            if (value < 0 || value > 8) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_ctas_per_sm = value;
+            return PAGEDKV_OK;
+        case PAGEDKV_OPT_MMA_MIN_GROUP:
+            if (value < 1 || value > 9) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_mma_min_group = value;
+            return PAGEDKV_OK;
+        default:
+            return PAGEDKV_ERR_INVALID_ARG;
+    }
+}
+
+int pagedkv_get_option(int option) {
+    switch (option) {
+        case PAGEDKV_OPT_DECODE_PATH: return g_opt_path;
+        case PAGEDKV_OPT_CTAS_PER_SM: return g_opt_ctas_per_sm;
+        case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
+        default: return PAGEDKV_ERR_INVALID_ARG;
+    }
+}
+
+int pagedkv_last_decode_path(void) { return g_last_path; }
+
+int pagedkv_device_errors(unsigned int *flags, int reset) {
+    if (!flags) return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    unsigned int h = 0;
+    if (cudaMemcpy(&h, err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    if (reset && cudaMemset(err, 0, sizeof h) != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    *flags = h;
+    return h ? PAGEDKV_ERR_BOUNDS : PAGEDKV_OK;
+}
+
+int paged_kv_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
+                          const int32_t *token_pos, int64_t *slot_mapping, int num_tokens,
+                          int num_seqs, int max_blocks_per_seq, int block_size, int num_blocks,
+                          void *stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 1 || block_size < 1 ||
+        num_blocks < 1)
+        return PAGEDKV_ERR_INVALID_ARG;
+    if ((long long)num_blocks * block_size > (1ll << 62)) return PAGEDKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PAGEDKV_OK;
+    if (!block_tables || !token_seq || !token_pos || !slot_mapping) return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(block_tables, 4) || !aligned(token_seq, 4) || !aligned(token_pos, 4) ||
+        !aligned(slot_mapping, 8))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    const cudaError_t e = pkv::launch_slot_mapping(block_tables, token_seq, token_pos, slot_mapping,
+                                                   num_tokens, num_seqs, max_blocks_per_seq,
+                                                   block_size, num_blocks, err,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache,
+                    void *v_cache, int num_tokens, int num_blocks, int block_size, int n_kv_heads,
+                    int head_dim, int dtype, void *stream) {
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || n_kv_heads < 1 || head_dim < 1 ||
+        !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    const long long row_bytes = (long long)n_kv_heads * head_dim * elem_bytes(dtype);
+    if (row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return PAGEDKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PAGEDKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    const cudaError_t e = pkv::launch_append(k, v, slot_mapping, k_cache, v_cache, num_tokens,
+                                             row_bytes, (long long)num_blocks * block_size, sms,
+                                             err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,
+                                       int max_blocks_per_seq, int block_size,
+                                       int partition_tokens) {
+    if (partition_tokens <= 0 || num_seqs < 0 || n_q_heads < 1 || head_dim < 1 ||
+        max_blocks_per_seq < 1 || block_size < 1)
+        return 0;
+    const size_t rows = size_t(num_seqs) * n_q_heads *
+                        size_t(max_parts_for(max_blocks_per_seq, block_size, partition_tokens));
+    return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
+}
+
+int paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, float scale,
+                           void *out, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int partition_tokens, void *workspace, size_t workspace_bytes,
+                           int dtype, void *stream) {
+    // ---- shapes
+    if (num_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1 || num_blocks < 1 ||
+        block_size < 1 || max_blocks_per_seq < 1 || partition_tokens < 0 || !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PAGEDKV_ERR_INVALID_ARG;
+    if (partition_tokens % pkv::kTile != 0) return PAGEDKV_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PAGEDKV_ERR_INVALID_ARG;
+    const int group = n_q_heads / n_kv_heads;
+    if (head_dim != 64 && head_dim != 128) return PAGEDKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PAGEDKV_ERR_UNSUPPORTED;
+    if (group > 8 || num_seqs > kMaxSeqs) return PAGEDKV_ERR_UNSUPPORTED;
+    const long long num_slots = (long long)num_blocks * block_size;
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    if (num_slots > INT_MAX || cap > INT_MAX / 2) return PAGEDKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PAGEDKV_OK;
+    // ---- pointers
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PAGEDKV_ERR_INVALID_ARG;
+    // ---- path
+    int path = g_opt_path;
+    if (path == pkv::kPathAuto)
+        path = (dtype != PAGEDKV_F32 && group >= g_opt_mma_min_group) ? pkv::kPathMma
+                                                                       : pkv::kPathSimt;
+    if (path == pkv::kPathMma && dtype == PAGEDKV_F32) return PAGEDKV_ERR_UNSUPPORTED;
+    int gmax = 8;
+    if (path == pkv::kPathSimt) gmax = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : 8;
+    // ---- split-K
+    const bool split = partition_tokens > 0;
+    const int P = split ? partition_tokens : int((cap + pkv::kTile - 1) / pkv::kTile * pkv::kTile);
+    const long long max_parts = split ? max_parts_for(max_blocks_per_seq, block_size, P) : 1;
+    float *ws_o = nullptr, *ws_m = nullptr, *ws_l = nullptr;
+    if (split) {
+        const size_t need = paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim,
+                                                            max_blocks_per_seq, block_size, P);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+            return PAGEDKV_ERR_WORKSPACE;
+        const size_t rows = size_t(num_seqs) * n_q_heads * size_t(max_parts);
+        uint8_t *w = static_cast<uint8_t *>(workspace);
+        ws_o = reinterpret_cast<float *>(w);
+        ws_m = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)));
+        ws_l = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)) +
+                                         round256(rows * sizeof(float)));
+    }
+    // ---- device
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    pkv::DecodeLaunch a;
+    st = encode_pool_map(&a.kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+    if (st != PAGEDKV_OK) return st;
+    st = encode_pool_map(&a.vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+    if (st != PAGEDKV_OK) return st;
+    int log2_block = 0;
+    while ((1 << log2_block) < block_size) ++log2_block;
+    pkv::DecodeParams &p = a.p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.ws_o = ws_o;
+    p.ws_m = ws_m;
+    p.ws_l = ws_l;
+    p.err = err;
+    p.scale_log2 = scale * pkv::kLog2e;
+    p.num_seqs = num_seqs;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = group;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.log2_block = log2_block;
+    p.max_blocks = max_blocks_per_seq;
+    p.part_tokens = P;
+    p.max_parts = int(max_parts);
+    p.split = split ? 1 : 0;
+    p.log2_stages = pkv::decode_log2_stages(elem_bytes(dtype), head_dim);
+    a.head_dim = head_dim;
+    a.path = path;
+    a.gmax = gmax;
+    a.ctas_per_sm = g_opt_ctas_per_sm;
+    a.num_sms = sms;
+    a.max_units = (long long)num_seqs * n_kv_heads * max_parts;
+    a.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (dtype) {
+        case PAGEDKV_F32: e = pkv::launch_decode_f32(a); break;
+        case PAGEDKV_F16: e = pkv::launch_decode_f16(a); break;
+        default: e = pkv::launch_decode_bf16(a); break;
+    }
+    if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    if (split) {
+        e = pkv::launch_lse_merge(dtype, head_dim, ws_o, ws_m, ws_l, context_lens, out, num_seqs,
+                                  n_q_heads, P, int(max_parts), int(cap), err, a.stream);
+        if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    }
+    g_last_path = path;
+    return PAGEDKV_OK;
+}
+
+}  // extern "C"

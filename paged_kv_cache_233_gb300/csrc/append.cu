@@ -1,0 +1,101 @@
+// append.cu -- address translation and the paged KV append.
+//
+// slot_mapping: "How a serving engine actually works", section "The one
+// formula": slot = block_table[seq][pos / B] * B + pos % B.
+// append: "Paged-KV + Continuous Batching From Scratch", section 1 (one pool
+// per layer laid out [num_blocks][block_size][n_kv_heads][head_dim]): each
+// new token's K and V rows are copied, 16 bytes per thread and instruction,
+// to row `slot` of the pools.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+__global__ void __launch_bounds__(256)
+slot_mapping_kernel(const int32_t *__restrict__ block_tables, const int32_t *__restrict__ token_seq,
+                    const int32_t *__restrict__ token_pos, int64_t *__restrict__ slot_mapping,
+                    int num_tokens, int num_seqs, int max_blocks, int block_size, int num_blocks,
+                    unsigned int *err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= num_tokens) return;
+    const int pos = token_pos[t];
+    const int seq = token_seq[t];
+    int64_t slot = -1;
+    if (pos >= 0) {
+        const int j = pos / block_size;
+        if (seq < 0 || seq >= num_seqs) {
+            atomicOr(err, PAGEDKV_DEVERR_SEQ_INDEX);
+        } else if (j >= max_blocks) {
+            atomicOr(err, PAGEDKV_DEVERR_POSITION);
+        } else {
+            const int pb = block_tables[int64_t(seq) * max_blocks + j];
+            if (pb < 0 || pb >= num_blocks)
+                atomicOr(err, PAGEDKV_DEVERR_BLOCK_ID);
+            else
+                slot = int64_t(pb) * block_size + (pos - j * block_size);
+        }
+    }
+    slot_mapping[t] = slot;
+}
+
+// `tpr` threads copy one row; a CTA works on blockDim.x / tpr rows at a time.
+__global__ void __launch_bounds__(256)
+append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+              const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache,
+              uint4 *__restrict__ v_cache, int num_tokens, int vec_per_row, int tpr,
+              long long num_slots, unsigned int *err) {
+    const int rows_per_cta = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;
+    const int c0 = threadIdx.x - sub * tpr;
+    for (long long t = (long long)blockIdx.x * rows_per_cta + sub; t < num_tokens;
+         t += (long long)gridDim.x * rows_per_cta) {
+        const long long slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (c0 == 0) atomicOr(err, PAGEDKV_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const uint4 *ks = k + t * vec_per_row;
+        const uint4 *vs = v + t * vec_per_row;
+        uint4 *kd = k_cache + slot * vec_per_row;
+        uint4 *vd = v_cache + slot * vec_per_row;
+        for (int c = c0; c < vec_per_row; c += tpr) {
+            const uint4 a = __ldcs(ks + c);
+            const uint4 b = __ldcs(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
+                                const int32_t *token_pos, int64_t *slot_mapping, int num_tokens,
+                                int num_seqs, int max_blocks, int block_size, int num_blocks,
+                                unsigned int *err, cudaStream_t st) {
+    const int blocks = (num_tokens + 255) / 256;
+    slot_mapping_kernel<<<blocks, 256, 0, st>>>(block_tables, token_seq, token_pos, slot_mapping,
+                                                num_tokens, num_seqs, max_blocks, block_size,
+                                                num_blocks, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache,
+                          void *v_cache, int num_tokens, long long row_bytes, long long num_slots,
+                          int num_sms, unsigned int *err, cudaStream_t st) {
+    const int vec_per_row = int(row_bytes / 16);
+    int tpr = 32;
+    while (tpr < vec_per_row && tpr < 256) tpr <<= 1;
+    const int rows_per_cta = 256 / tpr;
+    long long blocks = (num_tokens + rows_per_cta - 1) / rows_per_cta;
+    const long long cap = (long long)num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    append_kernel<<<unsigned(blocks), 256, 0, st>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_tokens, vec_per_row,
+        tpr, num_slots, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,22 @@
+// decode_bf16.cu -- bf16 instantiations of the paged decode kernel (CUDA-core and
+// tensor-core paths).
+#include "decode_instances.cuh"
+
+namespace pkv {
+
+cudaError_t launch_decode_bf16(const DecodeLaunch &a) {
+    if (a.path == kPathMma) {
+        switch (a.head_dim) {
+            case 64: return launch_decode_instance<__nv_bfloat16, 64, 8, true>(a);
+            case 128: return launch_decode_instance<__nv_bfloat16, 128, 8, true>(a);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (a.head_dim) {
+        case 64: return launch_simt_by_group<__nv_bfloat16, 64>(a);
+        case 128: return launch_simt_by_group<__nv_bfloat16, 128>(a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

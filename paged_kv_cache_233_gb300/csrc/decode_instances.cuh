@@ -1,0 +1,49 @@
+// decode_instances.cuh -- launch helper shared by the per-element-type
+// translation units (each includes this once with its own element type).
+#pragma once
+
+#include "decode_kernel.cuh"
+#include "decode_launch.h"
+
+namespace pkv {
+
+template <typename T, int D, int GM, bool kMma>
+static cudaError_t launch_decode_instance(const DecodeLaunch &a) {
+    using Geo = StageGeometry<T, D>;
+    auto kernel = paged_decode_kernel<T, D, GM, kMma>;
+    const DecodeSmem lay{Geo::kStageBytes, 1 << a.p.log2_stages, a.p.num_seqs, D, GM};
+    const int smem = lay.request();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // per-device record of the dynamic shared memory this kernel was opened up to
+    static int opened[64] = {0};
+    if (dev < 64 && opened[dev] < smem) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        opened[dev] = smem;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecodeThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int want = a.ctas_per_sm > 0 ? a.ctas_per_sm : 2;
+    long long grid = (long long)(want < per_sm ? want : per_sm) * a.num_sms;
+    if (grid > a.max_units) grid = a.max_units;
+    if (grid < 1) grid = 1;
+    kernel<<<dim3((unsigned)grid), dim3(kDecodeThreads), smem, a.stream>>>(a.kmap, a.vmap, a.p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_simt_by_group(const DecodeLaunch &a) {
+    switch (a.gmax) {
+        case 1: return launch_decode_instance<T, D, 1, false>(a);
+        case 2: return launch_decode_instance<T, D, 2, false>(a);
+        case 4: return launch_decode_instance<T, D, 4, false>(a);
+        case 8: return launch_decode_instance<T, D, 8, false>(a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,64 @@
+// decode_params.h -- parameters and shared-memory layout of the paged decode
+// kernel, visible to host launch code and device code alike.
+#pragma once
+
+#include <stdint.h>
+
+#ifndef __CUDACC__
+#define __host__
+#define __device__
+#endif
+
+namespace pkv {
+
+constexpr int kTile = 16;                 // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
+constexpr int kSlabBytes = kTile * 128;   // one 128-byte-wide column slab of a stage
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+    const void *q;
+    void *out;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *ws_o;
+    float *ws_m;
+    float *ws_l;
+    unsigned int *err;
+    float scale_log2;     // softmax scale * log2(e): scores are kept in base-2 units
+    int num_seqs;
+    int n_q_heads;
+    int n_kv_heads;
+    int group;            // n_q_heads / n_kv_heads
+    int num_blocks;
+    int block_size;
+    int log2_block;
+    int max_blocks;       // block table row length
+    int part_tokens;      // tokens per partition (multiple of kTile)
+    int max_parts;        // partitions per (seq, q head) in the workspace
+    int split;            // 1: multi-partition sequences write partition states
+    int log2_stages;      // ring of 1 << log2_stages stages
+};
+
+// Byte layout of the dynamic shared memory (host and device agree on it).
+struct DecodeSmem {
+    int stage_bytes, stages, seqs, head_dim, gmax;
+    __host__ __device__ int ring() const { return stages * stage_bytes; }
+    __host__ __device__ int bars() const { return ring(); }                        // full, empty
+    __host__ __device__ int flag() const { return bars() + 16 * stages; }
+    __host__ __device__ int seq_base() const { return flag() + 16; }               // seqs + 1 ints
+    __host__ __device__ int seq_len() const { return seq_base() + 4 * (seqs + 1); }
+    __host__ __device__ int merge_o() const { return (seq_len() + 4 * seqs + 15) & ~15; }
+    __host__ __device__ int row_stride() const { return head_dim + 4; }            // floats
+    __host__ __device__ int merge_m() const {
+        return merge_o() + 4 * kConsumerWarps * gmax * row_stride();
+    }
+    __host__ __device__ int merge_l() const { return merge_m() + 4 * kConsumerWarps * gmax; }
+    __host__ __device__ int total() const { return merge_l() + 4 * kConsumerWarps * gmax; }
+    // bytes to request: layout plus slack to align the ring to 1024 B
+    __host__ __device__ int request() const { return total() + 1024; }
+};
+
+}  // namespace pkv

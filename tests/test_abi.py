@@ -1,0 +1,121 @@
+"""The C ABI library loads and exports what include/pagedkv.h declares (CPU only).
+
+No call here reaches the GPU: only host-side argument checks, which return
+before anything is enqueued, and pure size arithmetic.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_233_gb300 as pk
+from paged_kv_cache_233_gb300 import build as pk_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pagedkv.h")
+
+INVALID, UNSUPPORTED, WORKSPACE = -1, -2, -5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pk_build.build()
+    return pk.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*([a-z_0-9]+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for name in ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
+                 "paged_attention_workspace_bytes", "pagedkv_status_string"):
+        assert name in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(pk.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in pagedkv.h but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert pk.abi_version() == 1
+    assert pk.status_string(0) == "ok"
+    for st in (-1, -2, -3, -4, -5):
+        assert pk.status_string(st) and pk.status_string(st) != "unknown status"
+    assert pk.status_string(12345) == "unknown status"
+
+
+def _decode(lib, **kw):
+    args = dict(q=1 << 12, k=1 << 12, v=1 << 12, bt=1 << 12, lens=1 << 12, scale=0.125, out=1 << 12,
+                S=4, Hq=4, Hkv=2, D=64, NB=32, B=16, MB=5, P=0, ws=None, ws_bytes=0, dtype=0)
+    args.update(kw)
+    return lib.paged_attention_decode(
+        ctypes.c_void_p(args["q"]), ctypes.c_void_p(args["k"]), ctypes.c_void_p(args["v"]),
+        ctypes.c_void_p(args["bt"]), ctypes.c_void_p(args["lens"]), args["scale"],
+        ctypes.c_void_p(args["out"]), args["S"], args["Hq"], args["Hkv"], args["D"], args["NB"],
+        args["B"], args["MB"], args["P"], ctypes.c_void_p(args["ws"]), args["ws_bytes"],
+        args["dtype"], None)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    assert _decode(lib, Hq=3, Hkv=2) == INVALID
+    assert _decode(lib, D=96) == UNSUPPORTED
+    assert _decode(lib, B=12) == UNSUPPORTED
+    assert _decode(lib, Hq=32, Hkv=2) == UNSUPPORTED        # group of 16
+    assert _decode(lib, P=100) == INVALID                    # not a multiple of 16
+    assert _decode(lib, dtype=7) == INVALID
+    assert _decode(lib, scale=float("nan")) == INVALID
+    assert _decode(lib, q=(1 << 12) + 8) == INVALID          # misaligned
+    assert _decode(lib, out=0) == INVALID                    # null
+    assert _decode(lib, P=16, ws=None) == WORKSPACE
+    assert _decode(lib, P=16, ws=1 << 12, ws_bytes=64) == WORKSPACE
+    assert _decode(lib, S=0) == 0                            # nothing to do, nothing enqueued
+    assert _decode(lib, S=5000) == UNSUPPORTED
+
+
+def test_append_and_slot_mapping_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    # row of 3 heads x 2 fp16 = 12 bytes is not a multiple of 16
+    assert lib.paged_kv_append(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 8, 16, 3, 2, 1, None) == INVALID
+    assert lib.paged_kv_append(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 8, 16, 2, 64, 9, None) == INVALID
+    assert lib.paged_kv_append(vp(0), vp(0), vp(0), vp(0), vp(0), 0, 8, 16, 2, 64, 1, None) == 0
+    assert lib.paged_kv_append(vp(0), vp(16), vp(16), vp(16), vp(16), 4, 8, 16, 2, 64, 1, None) == INVALID
+    assert lib.paged_kv_slot_mapping(vp(16), vp(16), vp(16), vp(16), 4, 2, 0, 16, 8, None) == INVALID
+    assert lib.paged_kv_slot_mapping(vp(0), vp(0), vp(0), vp(0), 0, 2, 4, 16, 8, None) == 0
+
+
+def test_workspace_size_follows_the_documented_layout(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for S, Hq, D, MB, B, P in [(8, 64, 128, 8192, 16, 512), (4, 4, 64, 5, 16, 16), (3, 2, 64, 7, 8, 48)]:
+        parts = -(-(MB * B) // P)
+        rows = S * Hq * parts
+        want = r256(rows * D * 4) + 2 * r256(rows * 4)
+        assert pk.paged_attention_workspace_bytes(S, Hq, D, MB, B, P) == want
+    assert pk.paged_attention_workspace_bytes(8, 64, 128, 100, 16, 0) == 0
+
+
+def test_options_round_trip(lib):
+    old = pk.get_option(pk.OPT_MMA_MIN_GROUP)
+    pk.set_option(pk.OPT_MMA_MIN_GROUP, 2)
+    assert pk.get_option(pk.OPT_MMA_MIN_GROUP) == 2
+    pk.set_option(pk.OPT_MMA_MIN_GROUP, old)
+    with pytest.raises(pk.PagedKVError):
+        pk.set_option(pk.OPT_DECODE_PATH, 9)
+    with pytest.raises(pk.PagedKVError):
+        pk.set_option(99, 0)
+
+
+def test_tensors_must_be_on_the_gpu(lib):
+    import torch
+    x = torch.zeros(4, 2, 64)
+    with pytest.raises(pk.PagedKVError, match="CUDA"):
+        pk.paged_kv_append(x, x, torch.zeros(4, dtype=torch.int64), torch.zeros(8, 16, 2, 64),
+                           torch.zeros(8, 16, 2, 64))

@@ -1,0 +1,218 @@
+"""CUDA path against the fp64 oracle, element by element (needs a GPU).
+
+Append and slot mapping must be bit-exact; decode must be within max-abs
+2e-3 (fp16), 1.5e-2 (bf16) or 1e-5 (fp32) of the oracle.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_233_gb300 as pk
+from paged_support import (TOL, assert_close, gpu_decode, gpu_fill, oracle_decode, oracle_fill,
+                           to_f64, to_np, units_to_rows)
+from workloads import make_workload, materialize, preset
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"auto": 0, "simt": 1, "mma": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pk.load()
+    torch.cuda.set_device(0)
+    yield
+    pk.set_option(pk.OPT_DECODE_PATH, 0)
+
+
+@pytest.fixture(autouse=True)
+def clean_error_word():
+    pk.device_errors(reset=True)
+    yield
+    pk.set_option(pk.OPT_DECODE_PATH, 0)
+
+
+def run_both(orc, wl, partition_tokens=0, path="auto"):
+    t = materialize(wl, "cuda")
+    kc, vc, bt, slots = gpu_fill(wl, t)
+    pk.set_option(pk.OPT_DECODE_PATH, PATHS[path])
+    out, ws = gpu_decode(wl, t["q"], kc, vc, bt, partition_tokens)
+    okc, ovc, oslots = oracle_fill(orc, wl, t)
+    ref = oracle_decode(orc, wl, t["q"], okc, ovc)
+    return dict(t=t, kc=kc, vc=vc, bt=bt, slots=slots, out=out, ws=ws, okc=okc, ovc=ovc,
+                oslots=oslots, ref=ref)
+
+
+# ---------------------------------------------------------------------------
+# The tiny workload, end to end
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("partition_tokens", [0, 16, 32])
+def test_tiny_workload(orc, partition_tokens):
+    wl = preset("tiny")
+    r = run_both(orc, wl, partition_tokens)
+    for tag in ("fill", "step"):
+        assert np.array_equal(r["slots"][tag].cpu().numpy(), r["oslots"][tag])
+    assert to_np(r["kc"]).tobytes() == r["okc"].tobytes()
+    assert to_np(r["vc"]).tobytes() == r["ovc"].tobytes()
+    assert_close(r["out"], r["ref"], "f32", what="tiny")
+    assert pk.device_errors() == 0
+
+
+def test_tiny_workload_lengths_before_the_append(orc):
+    """The other reading of the tiny workload's lengths: decode over the tokens
+    held before the step's append (the new token is in the pool but unread)."""
+    wl = preset("tiny")
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    wl.context_lens = wl.context_lens - 1
+    out, _ = gpu_decode(wl, t["q"], kc, vc, bt)
+    assert_close(out, oracle_decode(orc, wl, t["q"], okc, ovc), "f32", what="tiny-before")
+
+
+# ---------------------------------------------------------------------------
+# Sweeps over the supported shapes, both decode paths, split and not
+# ---------------------------------------------------------------------------
+
+SWEEP_LENS = [1, 2, 7, 8, 9, 15, 16, 17, 31, 33, 49, 64, 67, 100, 203, 517]
+
+
+def sweep_cases():
+    for dtype in ("f32", "f16", "bf16"):
+        for D in (64, 128):
+            for B in (8, 16, 32):
+                for g in (1, 2, 4, 8):
+                    paths = ["simt"] if dtype == "f32" else ["simt", "mma"]
+                    for path in paths:
+                        for P in (0, 48):
+                            yield pytest.param(dtype, D, B, g, path, P,
+                                               id=f"{dtype}-D{D}-B{B}-g{g}-{path}-P{P}")
+
+
+@pytest.mark.parametrize("dtype,D,B,g,path,P", list(sweep_cases()))
+def test_decode_sweep(orc, dtype, D, B, g, path, P):
+    Hkv = 2
+    seed = zlib.crc32(f"{dtype}-{D}-{B}-{g}".encode()) % 10000
+    wl = make_workload("sweep", dtype, SWEEP_LENS, Hkv * g, Hkv, D, B, seed, pool_factor=1.5)
+    r = run_both(orc, wl, P, path)
+    assert pk.last_decode_path() == PATHS[path]
+    assert to_np(r["kc"]).tobytes() == r["okc"].tobytes()
+    assert to_np(r["vc"]).tobytes() == r["ovc"].tobytes()
+    assert_close(r["out"], r["ref"], dtype, what=f"{dtype} D{D} B{B} g{g} {path} P{P}")
+    assert pk.device_errors() == 0
+
+
+@pytest.mark.parametrize("dtype,path", [("bf16", "mma"), ("f16", "simt"), ("f32", "simt")])
+def test_split_partition_states(orc, dtype, path):
+    """The split-K partition states in the workspace match the oracle's
+    per-partition (m, l, o) for every (sequence, head, partition)."""
+    P, D, Hkv, g = 32, 64, 2, 4
+    wl = make_workload("parts", dtype, [5, 32, 33, 97, 130], Hkv * g, Hkv, D, 16, 77)
+    r = run_both(orc, wl, P, path)
+    S, Hq = wl.num_seqs, wl.n_q_heads
+    max_parts = -(-(wl.max_blocks_per_seq * wl.block_size) // P)
+    rows = S * Hq * max_parts
+    r256 = lambda x: (x + 255) // 256 * 256
+    ws = r["ws"].cpu().numpy().view(np.float32)
+    o_all = ws[:rows * D].reshape(S, Hq, max_parts, D)
+    m_all = ws[r256(rows * D * 4) // 4:][:rows].reshape(S, Hq, max_parts)
+    l_all = ws[(r256(rows * D * 4) + r256(rows * 4)) // 4:][:rows].reshape(S, Hq, max_parts)
+    q = to_np(r["t"]["q"])
+    checked = 0
+    for s, L in enumerate(wl.context_lens):
+        nparts = -(-int(L) // P)
+        if nparts < 2:
+            continue
+        for qh in range(Hq):
+            for p_ in range(nparts):
+                o, m, l = orc.decode_partition(q, r["okc"], r["ovc"], wl.block_tables, wl.scale,
+                                               dtype, s, qh, p_ * P, min(int(L), (p_ + 1) * P))
+                gm, gl, go = float(m_all[s, qh, p_]), float(l_all[s, qh, p_]), o_all[s, qh, p_]
+                assert abs(gm - m) < 1e-4, (s, qh, p_, gm, m)
+                assert abs(gl / math.exp(m - gm) - l) / l < 1e-4
+                assert np.abs(go / gl - o / l).max() < TOL[dtype]
+                checked += 1
+    assert checked > 0
+    assert_close(r["out"], r["ref"], dtype, what="split")
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+
+def test_empty_and_single_token_contexts(orc):
+    wl = make_workload("edge", "bf16", [1, 1, 16, 1], 8, 2, 128, 16, 5)
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    wl.context_lens = np.array([0, 1, 16, 0], dtype=np.int32)
+    for path in ("simt", "mma"):
+        pk.set_option(pk.OPT_DECODE_PATH, PATHS[path])
+        for P in (0, 16):
+            out, _ = gpu_decode(wl, t["q"], kc, vc, bt, P)
+            o = to_f64(out)
+            assert (o[0] == 0).all() and (o[3] == 0).all()
+            assert_close(out, oracle_decode(orc, wl, t["q"], okc, ovc), "bf16", what="edge")
+    assert pk.device_errors() == 0
+
+
+def test_empty_batch_is_a_no_op():
+    q = torch.empty(0, 4, 64, device="cuda", dtype=torch.float16)
+    kc = torch.zeros(4, 16, 2, 64, device="cuda", dtype=torch.float16)
+    bt = torch.zeros(0, 2, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(0, dtype=torch.int32, device="cuda")
+    pk.paged_attention_decode(q, kc, kc, bt, lens, 0.125, q.clone())
+    torch.cuda.synchronize()
+
+
+def test_bad_block_ids_and_lengths_are_flagged_not_dereferenced():
+    wl = make_workload("bad", "f16", [40, 40], 4, 2, 64, 16, 3)
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    assert pk.device_errors() == 0
+    bad = bt.clone()
+    bad[0, 1] = wl.num_blocks + 1000          # past the pool
+    bad[1, 0] = -7
+    out, _ = gpu_decode(wl, t["q"], kc, vc, bad)
+    assert pk.device_errors() & 0x02
+    lens = torch.tensor([40, 10 ** 6], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(t["q"])
+    pk.paged_attention_decode(t["q"], kc, vc, bt, lens, wl.scale, out)
+    assert pk.device_errors() & 0x04
+
+
+def test_slot_mapping_padding_and_errors(orc):
+    wl = make_workload("slots", "f32", [20, 3], 2, 2, 64, 8, 9)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    seq = torch.tensor([0, 0, 1, 1, 5, 0], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([0, 19, 2, -1, 0, 10 ** 5], dtype=torch.int32, device="cuda")
+    sm = torch.empty(6, dtype=torch.int64, device="cuda")
+    pk.paged_kv_slot_mapping(bt, seq, pos, sm, wl.num_blocks, wl.block_size)
+    got = sm.cpu().numpy()
+    assert got[3] == -1 and got[4] == -1 and got[5] == -1
+    ref = orc.slot_mapping(wl.block_tables, [0, 0, 1], [0, 19, 2], wl.block_size)
+    assert got[:3].tolist() == ref.tolist()
+    flags = pk.device_errors()
+    assert flags & 0x10 and flags & 0x08
+
+
+def test_append_skips_padding_and_flags_out_of_range_slots(orc):
+    NB, B, Hkv, D = 4, 8, 2, 64
+    kc = torch.full((NB, B, Hkv, D), float("nan"), device="cuda")
+    vc = kc.clone()
+    k = torch.randn(5, Hkv, D, device="cuda")
+    v = torch.randn(5, Hkv, D, device="cuda")
+    slots = torch.tensor([3, -1, NB * B, 31, 0], dtype=torch.int64, device="cuda")
+    pk.paged_kv_append(k, v, slots, kc, vc)
+    assert pk.device_errors() & 0x01
+    okc = np.full((NB, B, Hkv, D), np.nan, np.float32)
+    ovc = okc.copy()
+    bad = orc.append(to_np(k), to_np(v), slots.cpu().numpy(), okc, ovc)
+    assert bad == 1
+    assert to_np(kc).tobytes() == okc.tobytes() and to_np(vc).tobytes() == ovc.tobytes()
