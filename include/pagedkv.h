@@ -189,6 +189,7 @@ int pagedkv_device_errors(unsigned int *flags, int reset);
 #define PAGEDKV_OPT_DECODE_PATH    1  /* 0 auto, 1 CUDA-core (SIMT) path, 2 tensor-core (mma) path */
 #define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */
 #define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
+#define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16); 0 = library default */
 int pagedkv_set_option(int option, int value);
 int pagedkv_get_option(int option);
 

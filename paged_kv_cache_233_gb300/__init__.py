@@ -27,14 +27,14 @@ __all__ = [
     "PagedKVError", "paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
     "paged_attention_workspace_bytes", "new_workspace", "device_errors", "set_option",
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
-    "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP",
+    "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP = 1, 2, 3
+OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP, OPT_STAGES = 1, 2, 3, 4
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",

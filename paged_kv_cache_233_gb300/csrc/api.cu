@@ -38,6 +38,7 @@ int g_num_sms[kMaxDevices] = {};
 int g_opt_path = pkv::kPathAuto;
 int g_opt_ctas_per_sm = 0;
 int g_opt_mma_min_group = 4;
+int g_opt_stages = 0;
 int g_last_path = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -88,22 +89,30 @@ int encoder(EncodeTiledFn *fn) {
     return PAGEDKV_OK;
 }
 
-// TMA view of one pool: (head_dim, n_kv_heads, num_slots) with a box of one
-// 128-byte column slab x one head x min(block_size, 16) tokens, 128-byte swizzle.
+// TMA view of one pool as a 4-D tensor (x: 128-byte column slab elements,
+// token slot, slab, kv head) so that one box holds [heads][slabs][tokens][128 B]
+// in shared memory; strides in bytes: token n_kv_heads*head_dim*eb, slab 128,
+// head head_dim*eb. The box is every slab of `heads` heads x 16 tokens, or for
+// 8-token blocks one slab of one head x 8 tokens. 128-byte swizzle.
 int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim, int n_kv_heads,
-                    long long num_slots, int block_size) {
+                    long long num_slots, int block_size, int heads) {
     EncodeTiledFn fn = nullptr;
     int st = encoder(&fn);
     if (st != PAGEDKV_OK) return st;
     const int eb = elem_bytes(dtype);
+    const int slabs = head_dim * eb / 128;
     const CUtensorMapDataType dt = dtype == PAGEDKV_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dtype == PAGEDKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(n_kv_heads), cuuint64_t(num_slots)};
-    const cuuint64_t strides[2] = {cuuint64_t(head_dim) * eb, cuuint64_t(n_kv_heads) * head_dim * eb};
-    const cuuint32_t box[3] = {cuuint32_t(128 / eb), 1u, cuuint32_t(block_size < 16 ? block_size : 16)};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = fn(map, dt, 3, const_cast<void *>(pool), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {cuuint64_t(128 / eb), cuuint64_t(num_slots), cuuint64_t(slabs),
+                                cuuint64_t(n_kv_heads)};
+    const cuuint64_t strides[3] = {cuuint64_t(n_kv_heads) * head_dim * eb, 128u,
+                                   cuuint64_t(head_dim) * eb};
+    const bool whole = block_size >= pkv::kTile;
+    const cuuint32_t box[4] = {cuuint32_t(128 / eb), cuuint32_t(whole ? pkv::kTile : block_size),
+                               cuuint32_t(whole ? slabs : 1), cuuint32_t(whole ? heads : 1)};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
@@ -148,6 +157,10 @@ int pagedkv_set_option(int option, int value) {
             if (value < 1 || value > 9) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_mma_min_group = value;
             return PAGEDKV_OK;
+        case PAGEDKV_OPT_STAGES:
+            if (value < 0 || value == 1 || value > 16) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_stages = value;
+            return PAGEDKV_OK;
         default:
             return PAGEDKV_ERR_INVALID_ARG;
     }
@@ -158,6 +171,7 @@ int pagedkv_get_option(int option) {
         case PAGEDKV_OPT_DECODE_PATH: return g_opt_path;
         case PAGEDKV_OPT_CTAS_PER_SM: return g_opt_ctas_per_sm;
         case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
+        case PAGEDKV_OPT_STAGES: return g_opt_stages;
         default: return PAGEDKV_ERR_INVALID_ARG;
     }
 }
@@ -293,10 +307,12 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     int sms = 0;
     int st = device_state(&err, &sms);
     if (st != PAGEDKV_OK) return st;
+    // kv heads per unit: one consumer warp per head when n_kv_heads allows
+    const int hpu = n_kv_heads % 4 == 0 ? 4 : (n_kv_heads % 2 == 0 ? 2 : 1);
     pkv::DecodeLaunch a;
-    st = encode_pool_map(&a.kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+    st = encode_pool_map(&a.kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, hpu);
     if (st != PAGEDKV_OK) return st;
-    st = encode_pool_map(&a.vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+    st = encode_pool_map(&a.vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, hpu);
     if (st != PAGEDKV_OK) return st;
     int log2_block = 0;
     while ((1 << log2_block) < block_size) ++log2_block;
@@ -321,13 +337,16 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     p.part_tokens = P;
     p.max_parts = int(max_parts);
     p.split = split ? 1 : 0;
-    p.log2_stages = pkv::decode_log2_stages(elem_bytes(dtype), head_dim);
+    p.stages = g_opt_stages ? g_opt_stages : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu);
+    p.heads_per_unit = hpu;
+    p.log2_hpu = hpu == 4 ? 2 : (hpu == 2 ? 1 : 0);
+    p.rows_per_box = block_size < pkv::kTile ? block_size : pkv::kTile;
     a.head_dim = head_dim;
     a.path = path;
     a.gmax = gmax;
     a.ctas_per_sm = g_opt_ctas_per_sm;
     a.num_sms = sms;
-    a.max_units = (long long)num_seqs * n_kv_heads * max_parts;
+    a.max_units = (long long)num_seqs * (n_kv_heads / hpu) * max_parts;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (dtype) {

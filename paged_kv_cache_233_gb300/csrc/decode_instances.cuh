@@ -9,9 +9,10 @@ namespace pkv {
 
 template <typename T, int D, int GM, bool kMma>
 static cudaError_t launch_decode_instance(const DecodeLaunch &a) {
-    using Geo = StageGeometry<T, D>;
     auto kernel = paged_decode_kernel<T, D, GM, kMma>;
-    const DecodeSmem lay{Geo::kStageBytes, 1 << a.p.log2_stages, a.p.num_seqs, D, GM};
+    const int stage_bytes = decode_stage_bytes(int(sizeof(T)), D, a.p.heads_per_unit);
+    const int merge = a.p.heads_per_unit < kConsumerWarps ? 1 : 0;
+    const DecodeSmem lay{stage_bytes, a.p.stages, a.p.num_seqs, D, GM, merge};
     const int smem = lay.request();
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -8,29 +8,34 @@
 // gathered into a contiguous copy first ("Paged Attention and the Block
 // Manager", section "The measurement").
 //
-// Work decomposition. A unit is (sequence s, kv head h, partition p): the
-// tokens [p*P, min((p+1)*P, L_s)) of one kv head, for all g = n_q_heads /
-// n_kv_heads query heads that read it (so each K/V byte is fetched once per kv
-// head). Without split-K, P covers the whole context and p = 0. Units are
-// numbered sequence-major and dealt round-robin to a persistent grid of CTAs.
+// Work decomposition. A unit is (sequence s, group of H kv heads, partition
+// p): tokens [p*P, min((p+1)*P, L_s)) of H consecutive kv heads, for all the
+// query heads that read them (each K/V byte is fetched once per kv head).
+// H is 4 when n_kv_heads allows, else 2 or 1. Without split-K, P covers the
+// whole context and p = 0. Units are numbered sequence-major and dealt
+// round-robin to a persistent grid of CTAs.
 //
 // Inside a CTA (5 warps):
 //   warp 0      producer. Its lanes hold a window of the block table row and
-//               hand each block id to lane 0 by shuffle; lane 0 issues one TMA
-//               tile load per 128-byte column slab of K and of V for every
-//               16-token tile into a ring of shared-memory stages
-//               (mbarrier transaction counts signal arrival).
-//   warps 1..4  consumers. Tile i of a unit goes to consumer i mod 4; each
-//               keeps an fp32 online-softmax state (running max m, running sum
-//               l, accumulator o) per query head. At the end of a unit the four
-//               states are combined through shared memory and written either
-//               as the normalised output or as the unnormalised partition state
-//               (split-K), which a merge kernel combines.
+//               hand each block id to lane 0 by shuffle; lane 0 issues, per
+//               16-token tile, one 4-D TMA load of K and one of V covering all
+//               H heads and all 128-byte column slabs of those tokens, into a
+//               ring of shared-memory stages (mbarrier transaction counts
+//               signal arrival; all four consumers release a stage).
+//   warps 1..4  consumers. Warp w owns kv head (w mod H) of the unit and, when
+//               H < 4, every (4/H)-th tile of it. Each keeps an fp32
+//               online-softmax state (running max m, running sum l,
+//               accumulator o) per query head of its kv head and writes its
+//               result straight to the output (or, under split-K, its
+//               unnormalised partition state to the workspace). Only when
+//               H < 4 do warps sharing a head combine states through shared
+//               memory at the end of a unit. Every consumer waits on every
+//               stage in ring order, so a stage's parity is never ambiguous.
 //
-// Stage layout: for each of K and V, kSlabs column slabs of 16 rows x 128 B,
-// written by TMA with the 128-byte swizzle (16-byte chunk c of row r lands at
-// chunk c ^ (r & 7)), so that both row-wise vector loads and the 8x8 matrix
-// loads of the tensor-core path are free of bank conflicts.
+// Stage layout, for each of K and V: [head][slab][16 rows][128 B], written by
+// TMA with the 128-byte swizzle (16-byte chunk c of row r lands at chunk
+// c ^ (r & 7)), so row-wise vector loads and the 8x8 matrix loads of the
+// tensor-core path are both free of bank conflicts.
 //
 // Two consumer flavours:
 //   SIMT  CUDA-core FMAs. Lanes own 16-byte column chunks of rows; per tile a
@@ -55,16 +60,18 @@ constexpr uint32_t kFull = 0xffffffffu;
 template <typename T, int D>
 struct StageGeometry {
     static constexpr int kRowBytes = D * int(sizeof(T));
-    static constexpr int kSlabs = kRowBytes / 128;
-    static constexpr int kHalf = kSlabs * kSlabBytes;  // K (or V) part of a stage
-    static constexpr int kStageBytes = 2 * kHalf;
-    static constexpr int kBoxElems = 128 / int(sizeof(T));
-    static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
+    static constexpr int kSlabs = kRowBytes / kRowBytes128;
+    static constexpr int kSlabBytes = kTile * kRowBytes128;   // 16 rows of one slab, one head
+    static constexpr int kHeadBytes = kSlabs * kSlabBytes;    // all slabs of one head
+    static_assert(kRowBytes % kRowBytes128 == 0, "rows must be whole 128-byte slabs");
 };
 
-// Shared-memory byte offset of 16-byte chunk `chunk` (0 .. kSlabs*8-1) of row `row`.
+// Shared-memory byte offset, within one head's part of a stage, of 16-byte
+// chunk `chunk` (0 .. slabs*8-1) of row `row`.
+template <int kSlabBytes>
 __device__ __forceinline__ uint32_t swz(int chunk, int row) {
-    return uint32_t((chunk >> 3) * kSlabBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    return uint32_t((chunk >> 3) * kSlabBytes + row * kRowBytes128 +
+                    (((chunk & 7) ^ (row & 7)) << 4));
 }
 
 // Butterfly transpose-reduction: N partial sums per lane across the low
@@ -105,6 +112,24 @@ __device__ __forceinline__ void unpack16(const uint4 &w, float *f) {
     }
 }
 
+// floats -> 16 bytes of elements
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float *f) {
+    uint4 w;
+    if constexpr (sizeof(T) == 4) {
+        w.x = __float_as_uint(f[0]);
+        w.y = __float_as_uint(f[1]);
+        w.z = __float_as_uint(f[2]);
+        w.w = __float_as_uint(f[3]);
+    } else {
+        w.x = Elem<T>::pack2(f[0], f[1]);
+        w.y = Elem<T>::pack2(f[2], f[3]);
+        w.z = Elem<T>::pack2(f[4], f[5]);
+        w.w = Elem<T>::pack2(f[6], f[7]);
+    }
+    return w;
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -116,6 +141,15 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ void sts128_zero(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
+
+// Where a unit's result goes: the output rows (normalised) or, under split-K,
+// the partition-state rows of the workspace.
+struct UnitSink {
+    bool partial;
+    size_t out_row0;   // row (s * n_q_heads + qh0) of out, qh0 = this warp's first q head
+    size_t ws_row0;    // workspace row of (s, qh0, part); q head qh0 + j adds j * max_parts
+    int max_parts;
+};
 
 // ---------------------------------------------------------------------------
 // CUDA-core consumer
@@ -135,29 +169,32 @@ struct SimtConsumer {
     float o[GM][EPL];
     float m[GM];
     float l[GM];
-    int r;   // row group of this lane
-    int i;   // 16-byte chunk of the row owned by this lane
+    uint4 qn[GM];   // next unit's query rows, prefetched
+    int r;          // row group of this lane
+    int i;          // 16-byte chunk of the row owned by this lane
 
     __device__ void init(int lane) {
         r = lane / LPR;
         i = lane % LPR;
     }
 
-    __device__ void begin_unit(const T *qrow0, int g, float scale_log2) {
+    __device__ void prefetch_q(const T *qrow0, int g) {
+#pragma unroll
+        for (int j = 0; j < GM; ++j)
+            qn[j] = j < g ? __ldg(reinterpret_cast<const uint4 *>(qrow0 + j * D) + i)
+                          : make_uint4(0, 0, 0, 0);
+    }
+
+    __device__ void begin_unit(float scale_log2) {
 #pragma unroll
         for (int j = 0; j < GM; ++j) {
             m[j] = -INFINITY;
             l[j] = 0.f;
+            unpack16<T>(qn[j], q[j]);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[j][e] = 0.f;
-            if (j < g) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4 *>(qrow0 + j * D) + i);
-                unpack16<T>(w, q[j]);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) q[j][e] *= scale_log2;
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) q[j][e] = 0.f;
+            for (int e = 0; e < EPL; ++e) {
+                o[j][e] = 0.f;
+                q[j][e] *= scale_log2;
             }
         }
     }
@@ -167,7 +204,7 @@ struct SimtConsumer {
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const int t = k * TPW + r;
-            unpack16<T>(lds128(kaddr + swz(i, t)), x[k]);
+            unpack16<T>(lds128(kaddr + swz<G::kSlabBytes>(i, t)), x[k]);
         }
         const int my_tok = (i >> (LOG_LPR - LOG_NT)) * TPW + r;
         float p[GM], alpha[GM];
@@ -200,7 +237,7 @@ struct SimtConsumer {
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const int t = k * TPW + r;
-            unpack16<T>(lds128(vaddr + swz(i, t)), x[k]);
+            unpack16<T>(lds128(vaddr + swz<G::kSlabBytes>(i, t)), x[k]);
             if (t >= nvalid) {
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) x[k][e] = 0.f;
@@ -221,8 +258,9 @@ struct SimtConsumer {
         }
     }
 
-    // Fold the lane-distributed state into the merge buffer row of this warp.
-    __device__ void end_unit(float *mo, float *mm, float *ml, int g, int lane, int stride) {
+    // Sum the lane-distributed state: afterwards lanes of row group 0 hold o
+    // and every lane holds the full l.
+    __device__ void reduce(int g) {
 #pragma unroll
         for (int j = 0; j < GM; ++j) {
             if (j < g) {
@@ -231,16 +269,55 @@ struct SimtConsumer {
 #pragma unroll
                     for (int e = 0; e < EPL; ++e)
                         o[j][e] += __shfl_xor_sync(kFull, o[j][e], mask);
-                float lj = l[j];
 #pragma unroll
-                for (int mask = 16; mask >= 1; mask >>= 1) lj += __shfl_xor_sync(kFull, lj, mask);
+                for (int mask = 16; mask >= 1; mask >>= 1)
+                    l[j] += __shfl_xor_sync(kFull, l[j], mask);
+            }
+        }
+    }
+
+    // Write the whole result of this warp's kv head (after reduce()).
+    __device__ void store(const UnitSink &sink, T *out, float *ws_o, float *ws_m, float *ws_l,
+                          int g, int lane) {
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+            if (j < g) {
+                if (sink.partial) {
+                    const size_t row = sink.ws_row0 + size_t(j) * sink.max_parts;
+                    if (r == 0) {
+                        float *dst = ws_o + row * D + i * EPL;
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 4)
+                            *reinterpret_cast<float4 *>(dst + e) =
+                                make_float4(o[j][e], o[j][e + 1], o[j][e + 2], o[j][e + 3]);
+                    }
+                    if (lane == 0) {
+                        ws_m[row] = m[j] * kLn2;
+                        ws_l[row] = l[j];
+                    }
+                } else if (r == 0) {
+                    const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
+                    float v[EPL];
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) v[e] = o[j][e] * inv;
+                    *reinterpret_cast<uint4 *>(out + (sink.out_row0 + j) * D + i * EPL) = pack16<T>(v);
+                }
+            }
+        }
+    }
+
+    // Stage this warp's state for a cross-warp merge (after reduce()).
+    __device__ void stash(float *mo, float *mm, float *ml, int g, int lane, int stride) {
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+            if (j < g) {
                 if (r == 0) {
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) mo[j * stride + i * EPL + e] = o[j][e];
                 }
                 if (lane == 0) {
                     mm[j] = m[j];
-                    ml[j] = lj;
+                    ml[j] = l[j];
                 }
             }
         }
@@ -252,11 +329,13 @@ struct SimtConsumer {
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 struct MmaConsumer {
+    using G = StageGeometry<T, D>;
     static constexpr int KS = D / 16;   // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;   // m-tiles of O^T = V^T P^T
     static constexpr bool kBf16 = Elem<T>::kBf16;
 
     uint32_t qb[KS][2];
+    uint32_t qn[KS][2];   // next unit's fragments, prefetched
     float o[MT][4];
     float m[2];     // running max (base 2) of heads 2c, 2c+1
     float lp[2];    // this lane's part of the running sums
@@ -270,19 +349,27 @@ struct MmaConsumer {
         r8 = lane & 7;
     }
 
-    __device__ void begin_unit(const T *qrow0, int g) {
+    __device__ void prefetch_q(const T *qrow0, int g) {
+        const bool live = grp < g;
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(qrow0 + grp * D);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qn[kk][0] = live ? __ldg(row + kk * 8 + c) : 0u;
+            qn[kk][1] = live ? __ldg(row + kk * 8 + 4 + c) : 0u;
+        }
+    }
+
+    __device__ void begin_unit() {
         m[0] = m[1] = -INFINITY;
         lp[0] = lp[1] = 0.f;
 #pragma unroll
         for (int t = 0; t < MT; ++t)
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[t][e] = 0.f;
-        const bool live = grp < g;
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(qrow0 + grp * D);
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-            qb[kk][0] = live ? __ldg(row + kk * 8 + c) : 0u;
-            qb[kk][1] = live ? __ldg(row + kk * 8 + 4 + c) : 0u;
+            qb[kk][0] = qn[kk][0];
+            qb[kk][1] = qn[kk][1];
         }
     }
 
@@ -293,7 +380,7 @@ struct MmaConsumer {
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 uint32_t a[4];
-                ldmatrix_x4(kaddr + swz(2 * kk + (mi >> 1), tok), a);
+                ldmatrix_x4(kaddr + swz<G::kSlabBytes>(2 * kk + (mi >> 1), tok), a);
                 mma_m16n8k16<kBf16>(s, a, qb[kk][0], qb[kk][1]);
             }
         }
@@ -329,18 +416,51 @@ struct MmaConsumer {
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
             uint32_t a[4];
-            ldmatrix_x4_trans(vaddr + swz(2 * t + (mi & 1), tok), a);
+            ldmatrix_x4_trans(vaddr + swz<G::kSlabBytes>(2 * t + (mi & 1), tok), a);
             mma_m16n8k16<kBf16>(o[t], a, b0, b1);
         }
     }
 
-    __device__ void end_unit(float *mo, float *mm, float *ml, int g, int stride) {
-        float l0 = lp[0], l1 = lp[1];
+    // Full row sums of this lane's two heads (lanes with the same c agree).
+    __device__ void reduce() {
 #pragma unroll
         for (int mask = 4; mask <= 16; mask <<= 1) {
-            l0 += __shfl_xor_sync(kFull, l0, mask);
-            l1 += __shfl_xor_sync(kFull, l1, mask);
+            lp[0] += __shfl_xor_sync(kFull, lp[0], mask);
+            lp[1] += __shfl_xor_sync(kFull, lp[1], mask);
         }
+    }
+
+    __device__ void store(const UnitSink &sink, T *out, float *ws_o, float *ws_m, float *ws_l,
+                          int g) {
+#pragma unroll
+        for (int hsel = 0; hsel < 2; ++hsel) {
+            const int h = 2 * c + hsel;
+            if (h >= g) continue;
+            if (sink.partial) {
+                const size_t row = sink.ws_row0 + size_t(h) * sink.max_parts;
+                float *dst = ws_o + row * D;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    dst[t * 16 + grp] = o[t][hsel];
+                    dst[t * 16 + grp + 8] = o[t][2 + hsel];
+                }
+                if (grp == 0) {
+                    ws_m[row] = m[hsel] * kLn2;
+                    ws_l[row] = lp[hsel];
+                }
+            } else {
+                const float inv = lp[hsel] > 0.f ? 1.f / lp[hsel] : 0.f;
+                T *dst = out + (sink.out_row0 + h) * D;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    dst[t * 16 + grp] = Elem<T>::from_float(o[t][hsel] * inv);
+                    dst[t * 16 + grp + 8] = Elem<T>::from_float(o[t][2 + hsel] * inv);
+                }
+            }
+        }
+    }
+
+    __device__ void stash(float *mo, float *mm, float *ml, int g, int stride) {
         const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
@@ -355,11 +475,35 @@ struct MmaConsumer {
             }
         }
         if (grp == 0) {
-            if (h0 < g) { mm[h0] = m[0]; ml[h0] = l0; }
-            if (h1 < g) { mm[h1] = m[1]; ml[h1] = l1; }
+            if (h0 < g) { mm[h0] = m[0]; ml[h0] = lp[0]; }
+            if (h1 < g) { mm[h1] = m[1]; ml[h1] = lp[1]; }
         }
     }
 };
+
+// ---------------------------------------------------------------------------
+// Unit walk shared by the producer and the consumers
+// ---------------------------------------------------------------------------
+struct Unit {
+    int s, hg, part, L, t0, t1, ntiles;
+};
+
+// Unit u; `s` is a cursor into the sequence prefix sums (units are visited in
+// increasing order, so it only moves forward).
+__device__ __forceinline__ Unit unit_at(int u, int &s, const int *seq_base, const int *seq_len,
+                                        int groups, int P) {
+    while (seq_base[s + 1] <= u) ++s;
+    Unit x;
+    const int rr = u - seq_base[s];
+    x.s = s;
+    x.part = rr / groups;
+    x.hg = rr - x.part * groups;
+    x.L = seq_len[s];
+    x.t0 = x.part * P;
+    x.t1 = min(x.L, x.t0 + P);
+    x.ntiles = (x.t1 - x.t0 + kTile - 1) / kTile;
+    return x;
+}
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -373,29 +517,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const sm = smem_raw + (base - raw);
-    const int NS = 1 << p.log2_stages;
+    const int NS = p.stages;
     const int S = p.num_seqs;
-    DecodeSmem lay{G::kStageBytes, NS, S, D, GM};
+    const int H = p.heads_per_unit;
+    const int TL = kConsumerWarps >> p.log2_hpu;          // consumer warps per kv head
+    const int half_bytes = H * G::kHeadBytes;            // K (or V) part of a stage
+    const int stage_bytes = 2 * half_bytes;
+    const DecodeSmem lay{stage_bytes, NS, S, D, GM, TL > 1 ? 1 : 0};
     const uint32_t full0 = base + lay.bars();
     const uint32_t empty0 = full0 + 8 * NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + lay.flag());
     int *seq_base = reinterpret_cast<int *>(sm + lay.seq_base());
     int *seq_len = reinterpret_cast<int *>(sm + lay.seq_len());
-    float *merge_o = reinterpret_cast<float *>(sm + lay.merge_o());
-    float *merge_m = reinterpret_cast<float *>(sm + lay.merge_m());
-    float *merge_l = reinterpret_cast<float *>(sm + lay.merge_l());
-    const int stride = lay.row_stride();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int B = p.block_size;
-    const int Hkv = p.n_kv_heads;
+    const int groups = p.n_kv_heads >> p.log2_hpu;       // head groups per sequence
     const int P = p.part_tokens;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -405,7 +549,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             tma_prefetch_descriptor(&kmap);
             tma_prefetch_descriptor(&vmap);
         }
-        // units of each sequence: max(1, ceil(L / P)) partitions x n_kv_heads, prefix-summed
+        // units of each sequence: max(1, ceil(L / P)) partitions x head groups, prefix-summed
         const int cap = p.max_blocks * B;
         int carry = 0;
         if (lane == 0) seq_base[0] = 0;
@@ -417,7 +561,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int Lc = min(max(L, 0), cap);
                 if (Lc != L) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
                 seq_len[s] = Lc;
-                cnt = (Lc > 0 ? (Lc + P - 1) / P : 1) * Hkv;
+                cnt = (Lc > 0 ? (Lc + P - 1) / P : 1) * groups;
             }
             int x = cnt;
 #pragma unroll
@@ -431,39 +575,48 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     __syncthreads();
     const int total_units = seq_base[S];
+    if (int(blockIdx.x) >= total_units) return;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        uint32_t gt = 0;      // tiles armed so far by this CTA
+        uint32_t armed = 0;   // tiles armed so far by this CTA
+        int stage = 0;
+        uint32_t phase = 0;
         bool ok = true;
         int s = 0;
+        // lane-parallel window of 32 block-table entries starting at block j0
+        auto load_window = [&](const Unit &x, int j0) {
+            const int nblk = (x.L + B - 1) >> p.log2_block;
+            const int j = j0 + lane;
+            return j < nblk ? __ldg(p.block_tables + size_t(x.s) * p.max_blocks + j) : -1;
+        };
+        Unit cur = unit_at(blockIdx.x, s, seq_base, seq_len, groups, P);
+        int nxt_base = cur.t0 >> p.log2_block;
+        int nxt_val = load_window(cur, nxt_base);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            while (seq_base[s + 1] <= u) ++s;
-            const int rr = u - seq_base[s];
-            const int part = rr / Hkv;
-            const int h = rr - part * Hkv;
-            const int L = seq_len[s];
-            const int t0 = part * P;
-            const int t1 = min(L, t0 + P);
-            const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-            const int nblk = (L + B - 1) >> p.log2_block;    // blocks this sequence holds
-            const int32_t *bt_row = p.block_tables + size_t(s) * p.max_blocks;
-            int win_base = -64, win_val = -1;
-            for (int i = 0; i < ntiles; ++i) {
-                const int tok = t0 + i * kTile;
+            int win_base = nxt_base, win_val = nxt_val;
+            const bool has_next = u + int(gridDim.x) < total_units;
+            int s_next = s;
+            Unit nx = cur;
+            if (has_next) {
+                // prefetch the first window of this CTA's next unit
+                nx = unit_at(u + gridDim.x, s_next, seq_base, seq_len, groups, P);
+                nxt_base = nx.t0 >> p.log2_block;
+                nxt_val = load_window(nx, nxt_base);
+            }
+            const int h0 = cur.hg << p.log2_hpu;
+            for (int i = 0; i < cur.ntiles; ++i) {
+                const int tok = cur.t0 + i * kTile;
                 const int j0 = tok >> p.log2_block;
-                const bool two = (B < kTile) && (tok + B < t1);
+                const bool two = (B < kTile) && (tok + B < cur.t1);
                 if (j0 < win_base || j0 + 1 >= win_base + 32) {
                     win_base = j0;
-                    const int j = j0 + lane;
-                    win_val = j < nblk ? __ldg(bt_row + j) : -1;
+                    win_val = load_window(cur, j0);
                 }
                 int pb0 = __shfl_sync(kFull, win_val, j0 - win_base);
                 int pb1 = __shfl_sync(kFull, win_val, (j0 + 1 - win_base) & 31);
                 if (lane == 0) {
-                    const uint32_t stage = gt & uint32_t(NS - 1);
-                    const uint32_t parity = ((gt >> p.log2_stages) & 1u) ^ 1u;
-                    if (*abort_flag || !mbar_wait(empty0 + 8 * stage, parity, p.err)) {
+                    if (*abort_flag || !mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.err)) {
                         ok = false;
                     } else {
                         if (pb0 < 0 || pb0 >= p.num_blocks) {
@@ -474,140 +627,172 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
                             pb1 = 0;
                         }
-                        const uint32_t box = B >= kTile ? kSlabBytes : kSlabBytes / 2;
-                        const uint32_t bytes = 2u * G::kSlabs * (two ? 2u * box : box);
                         const uint32_t fb = full0 + 8 * stage;
-                        mbar_arrive_expect_tx(fb, bytes);
-                        const uint32_t kdst = base + stage * G::kStageBytes;
-                        const uint32_t vdst = kdst + G::kHalf;
-                        const int z0 = pb0 * B + (tok & (B - 1));
-#pragma unroll
-                        for (int sl = 0; sl < G::kSlabs; ++sl) {
-                            tma_load_3d(kdst + sl * kSlabBytes, &kmap, sl * G::kBoxElems, h, z0, fb);
-                            tma_load_3d(vdst + sl * kSlabBytes, &vmap, sl * G::kBoxElems, h, z0, fb);
-                        }
-                        if (two) {
-                            const int z1 = pb1 * B;
-#pragma unroll
-                            for (int sl = 0; sl < G::kSlabs; ++sl) {
-                                tma_load_3d(kdst + sl * kSlabBytes + box, &kmap, sl * G::kBoxElems, h, z1, fb);
-                                tma_load_3d(vdst + sl * kSlabBytes + box, &vmap, sl * G::kBoxElems, h, z1, fb);
+                        const uint32_t kdst = base + stage * stage_bytes;
+                        const uint32_t vdst = kdst + half_bytes;
+                        if (B >= kTile) {
+                            // one box per operand: every slab of H heads x 16 tokens
+                            const int z0 = pb0 * B + (tok & (B - 1));
+                            mbar_arrive_expect_tx(fb, uint32_t(stage_bytes));
+                            tma_load_4d(kdst, &kmap, 0, z0, 0, h0, fb);
+                            tma_load_4d(vdst, &vmap, 0, z0, 0, h0, fb);
+                        } else {
+                            // 8-token blocks: one box per (block, head, slab)
+                            const int nb = two ? 2 : 1;
+                            mbar_arrive_expect_tx(fb, uint32_t(stage_bytes / 2 * nb));
+                            for (int b = 0; b < nb; ++b) {
+                                const int z = (b ? pb1 : pb0) * B;
+                                for (int hh = 0; hh < H; ++hh)
+                                    for (int sl = 0; sl < G::kSlabs; ++sl) {
+                                        const uint32_t off = hh * G::kHeadBytes + sl * G::kSlabBytes +
+                                                             b * (G::kSlabBytes / 2);
+                                        tma_load_4d(kdst + off, &kmap, 0, z, sl, h0 + hh, fb);
+                                        tma_load_4d(vdst + off, &vmap, 0, z, sl, h0 + hh, fb);
+                                    }
                             }
                         }
-                        ++gt;
+                        ++armed;
                     }
                 }
                 ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+            cur = nx;
+            s = s_next;
         }
         if (!ok && lane == 0) {
             // Stop everyone, then wait (bounded) for this CTA's copies still in flight.
             *abort_flag = 1;
-            const uint32_t first = gt > uint32_t(NS) ? gt - NS : 0u;
-            for (uint32_t k = first; k < gt; ++k)
-                mbar_wait(full0 + 8 * (k & uint32_t(NS - 1)), (k >> p.log2_stages) & 1u, p.err);
+            const uint32_t first = armed > uint32_t(NS) ? armed - NS : 0u;
+            for (uint32_t k = first; k < armed; ++k)
+                mbar_wait(full0 + 8 * (k % uint32_t(NS)), (k / uint32_t(NS)) & 1u, p.err);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp - 1;
+    const int hh = cw & (H - 1);          // kv head of the unit this warp owns
+    const int tw = cw >> p.log2_hpu;      // which of the TL warps sharing that head
     const int g = p.group;
-    const int tid_c = threadIdx.x - 32;
-    constexpr int kConsumerThreads = 32 * kConsumerWarps;
     using Simt = SimtConsumer<T, D, GM>;
     using Mma = MmaConsumer<T, D>;
     typename std::conditional<kMma, Mma, Simt>::type st;
     st.init(lane);
-    float *my_o = merge_o + cw * GM * stride;
-    float *my_m = merge_m + cw * GM;
-    float *my_l = merge_l + cw * GM;
 
-    uint32_t gt_base = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     int s = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-        while (seq_base[s + 1] <= u) ++s;
-        const int rr = u - seq_base[s];
-        const int part = rr / Hkv;
-        const int h = rr - part * Hkv;
-        const int L = seq_len[s];
-        const int t0 = part * P;
-        const int t1 = min(L, t0 + P);
-        const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-        const int nparts = L > 0 ? (L + P - 1) / P : 1;
-        const T *qrow0 = reinterpret_cast<const T *>(p.q) + (size_t(s) * p.n_q_heads + h * g) * D;
-        if constexpr (kMma) st.begin_unit(qrow0, g);
-        else st.begin_unit(qrow0, g, p.scale_log2);
-
-        for (int i = cw; i < ntiles; i += kConsumerWarps) {
-            const uint32_t gt = gt_base + uint32_t(i);
-            const uint32_t stage = gt & uint32_t(NS - 1);
+    int unit_count = 0;
+    const T *qbase = reinterpret_cast<const T *>(p.q);
+    Unit cur = unit_at(blockIdx.x, s, seq_base, seq_len, groups, P);
+    st.prefetch_q(qbase + (size_t(cur.s) * p.n_q_heads + ((cur.hg << p.log2_hpu) + hh) * g) * D, g);
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++unit_count) {
+        const int qh0 = ((cur.hg << p.log2_hpu) + hh) * g;   // first q head of this warp
+        if constexpr (kMma) st.begin_unit();
+        else st.begin_unit(p.scale_log2);
+        const bool has_next = u + int(gridDim.x) < total_units;
+        int s_next = s;
+        Unit nx = cur;
+        if (has_next) {
+            nx = unit_at(u + gridDim.x, s_next, seq_base, seq_len, groups, P);
+            st.prefetch_q(qbase + (size_t(nx.s) * p.n_q_heads + ((nx.hg << p.log2_hpu) + hh) * g) * D, g);
+        }
+        for (int i = 0; i < cur.ntiles; ++i) {
             int good = !*abort_flag;
-            if (good) good = mbar_wait(full0 + 8 * stage, (gt >> p.log2_stages) & 1u, p.err);
+            if (good) good = mbar_wait(full0 + 8 * stage, phase, p.err);
             if (!__all_sync(kFull, good)) {
                 *abort_flag = 1;
-                continue;
-            }
-            const int nvalid = min(kTile, t1 - (t0 + i * kTile));
-            const uint32_t kaddr = base + stage * G::kStageBytes;
-            const uint32_t vaddr = kaddr + G::kHalf;
-            if constexpr (kMma) {
-                if (nvalid < kTile) {
-                    // rows past the context may hold anything (even NaN): zero the V rows
-                    const int n16 = (kTile - nvalid) * G::kSlabs * 8;
-                    for (int x = lane; x < n16; x += 32) {
-                        const int row = nvalid + x / (G::kSlabs * 8);
-                        const int rem = x % (G::kSlabs * 8);
-                        sts128_zero(vaddr + (rem >> 3) * kSlabBytes + row * 128 + (rem & 7) * 16);
+            } else if ((i & (TL - 1)) == tw) {
+                const int nvalid = min(kTile, cur.t1 - (cur.t0 + i * kTile));
+                const uint32_t kaddr = base + stage * stage_bytes + hh * G::kHeadBytes;
+                const uint32_t vaddr = kaddr + half_bytes;
+                if constexpr (kMma) {
+                    if (nvalid < kTile) {
+                        // rows past the context may hold anything (even NaN): zero this head's V rows
+                        const int n16 = (kTile - nvalid) * G::kSlabs * 8;
+                        for (int x = lane; x < n16; x += 32) {
+                            const int row = nvalid + x / (G::kSlabs * 8);
+                            const int rem = x % (G::kSlabs * 8);
+                            sts128_zero(vaddr + (rem >> 3) * G::kSlabBytes + row * kRowBytes128 + (rem & 7) * 16);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                    st.tile(kaddr, vaddr, nvalid, p.scale_log2);
+                } else {
+                    st.tile(kaddr, vaddr, nvalid, g);
                 }
-                st.tile(kaddr, vaddr, nvalid, p.scale_log2);
-            } else {
-                st.tile(kaddr, vaddr, nvalid, g);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
-        gt_base += uint32_t(ntiles);
 
-        // ---- combine the four consumer states of this unit
-        if constexpr (kMma) st.end_unit(my_o, my_m, my_l, g, stride);
-        else st.end_unit(my_o, my_m, my_l, g, lane, stride);
-        named_barrier(1, kConsumerThreads);
-        const bool write_partial = p.split && nparts > 1;
-        for (int idx = tid_c; idx < g * D; idx += kConsumerThreads) {
-            const int j = idx / D;
-            const int d = idx - j * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * GM + j]);
-            float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float f = fast_exp2(merge_m[w * GM + j] - M);
-                    num = fmaf(f, merge_o[(w * GM + j) * stride + d], num);
-                    den = fmaf(f, merge_l[w * GM + j], den);
+        // ---- result of this unit
+        const int nparts = cur.L > 0 ? (cur.L + P - 1) / P : 1;
+        UnitSink sink;
+        sink.partial = p.split && nparts > 1;
+        sink.out_row0 = size_t(cur.s) * p.n_q_heads + qh0;
+        sink.max_parts = p.max_parts;
+        sink.ws_row0 = (size_t(cur.s) * p.n_q_heads + qh0) * p.max_parts + cur.part;
+        if constexpr (kMma) st.reduce();
+        else st.reduce(g);
+        if (TL == 1) {
+            if constexpr (kMma) st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g);
+            else st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g, lane);
+        } else {
+            // warps sharing a kv head combine their states (double-buffered slots,
+            // so one barrier per unit suffices)
+            const int stride = lay.row_stride();
+            const int slot = unit_count & 1;
+            float *mo0 = reinterpret_cast<float *>(sm + lay.merge_o()) + slot * kConsumerWarps * GM * stride;
+            float *mm0 = reinterpret_cast<float *>(sm + lay.merge_m()) + slot * kConsumerWarps * GM;
+            float *ml0 = reinterpret_cast<float *>(sm + lay.merge_l()) + slot * kConsumerWarps * GM;
+            if constexpr (kMma) st.stash(mo0 + cw * GM * stride, mm0 + cw * GM, ml0 + cw * GM, g, stride);
+            else st.stash(mo0 + cw * GM * stride, mm0 + cw * GM, ml0 + cw * GM, g, lane, stride);
+            named_barrier(1, 32 * kConsumerWarps);
+            const int qu0 = (cur.hg << p.log2_hpu) * g;      // first q head of the unit
+            for (int idx = threadIdx.x - 32; idx < H * g * D; idx += 32 * kConsumerWarps) {
+                const int h = idx / (g * D);
+                const int rem = idx - h * g * D;
+                const int j = rem / D;
+                const int d = rem - j * D;
+                float M = -INFINITY;
+                for (int t = 0; t < TL; ++t) M = fmaxf(M, mm0[(t * H + h) * GM + j]);
+                float num = 0.f, den = 0.f;
+                if (M != -INFINITY) {
+                    for (int t = 0; t < TL; ++t) {
+                        const int w = t * H + h;
+                        const float f = fast_exp2(mm0[w * GM + j] - M);
+                        num = fmaf(f, mo0[(w * GM + j) * stride + d], num);
+                        den = fmaf(f, ml0[w * GM + j], den);
+                    }
                 }
-            }
-            const int qh = h * g + j;
-            if (write_partial) {
-                const size_t row = (size_t(s) * p.n_q_heads + qh) * p.max_parts + part;
-                p.ws_o[row * D + d] = num;
-                if (d == 0) {
-                    p.ws_m[row] = M * kLn2;
-                    p.ws_l[row] = den;
+                const int qh = qu0 + h * g + j;
+                if (sink.partial) {
+                    const size_t row = (size_t(cur.s) * p.n_q_heads + qh) * p.max_parts + cur.part;
+                    p.ws_o[row * D + d] = num;
+                    if (d == 0) {
+                        p.ws_m[row] = M * kLn2;
+                        p.ws_l[row] = den;
+                    }
+                } else {
+                    const float v = den > 0.f ? num / den : 0.f;
+                    reinterpret_cast<T *>(p.out)[(size_t(cur.s) * p.n_q_heads + qh) * D + d] =
+                        Elem<T>::from_float(v);
                 }
-            } else {
-                const float v = den > 0.f ? num / den : 0.f;
-                reinterpret_cast<T *>(p.out)[(size_t(s) * p.n_q_heads + qh) * D + d] =
-                    Elem<T>::from_float(v);
             }
         }
-        named_barrier(1, kConsumerThreads);
+        cur = nx;
+        s = s_next;
     }
 }
 

@@ -35,7 +35,7 @@ cudaError_t launch_lse_merge(int dtype, int head_dim, const float *ws_o, const f
                              int num_seqs, int n_q_heads, int part_tokens, int max_parts,
                              int max_context, unsigned int *err, cudaStream_t stream);
 
-// Stage-ring size for an element size and head_dim (power of two).
-int decode_log2_stages(int elem_bytes, int head_dim);
+// Stage-ring size for an element size, head_dim and kv heads per unit.
+int decode_stages(int elem_bytes, int head_dim, int heads_per_unit);
 
 }  // namespace pkv

@@ -12,9 +12,9 @@
 namespace pkv {
 
 constexpr int kTile = 16;                 // tokens per pipeline stage
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 4;         // also the largest kv-head group of a unit
 constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
-constexpr int kSlabBytes = kTile * 128;   // one 128-byte-wide column slab of a stage
+constexpr int kRowBytes128 = 128;         // width of one swizzled column slab
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -39,12 +39,16 @@ struct DecodeParams {
     int part_tokens;      // tokens per partition (multiple of kTile)
     int max_parts;        // partitions per (seq, q head) in the workspace
     int split;            // 1: multi-partition sequences write partition states
-    int log2_stages;      // ring of 1 << log2_stages stages
+    int stages;           // ring size (>= 2)
+    int heads_per_unit;   // kv heads per unit: 1, 2 or 4 (one consumer warp per head)
+    int log2_hpu;
+    int rows_per_box;     // tokens per TMA box: min(block_size, kTile)
 };
 
 // Byte layout of the dynamic shared memory (host and device agree on it).
+// merge == 0 when every consumer warp owns a whole head (no cross-warp merge).
 struct DecodeSmem {
-    int stage_bytes, stages, seqs, head_dim, gmax;
+    int stage_bytes, stages, seqs, head_dim, gmax, merge;
     __host__ __device__ int ring() const { return stages * stage_bytes; }
     __host__ __device__ int bars() const { return ring(); }                        // full, empty
     __host__ __device__ int flag() const { return bars() + 16 * stages; }
@@ -52,13 +56,18 @@ struct DecodeSmem {
     __host__ __device__ int seq_len() const { return seq_base() + 4 * (seqs + 1); }
     __host__ __device__ int merge_o() const { return (seq_len() + 4 * seqs + 15) & ~15; }
     __host__ __device__ int row_stride() const { return head_dim + 4; }            // floats
-    __host__ __device__ int merge_m() const {
-        return merge_o() + 4 * kConsumerWarps * gmax * row_stride();
-    }
-    __host__ __device__ int merge_l() const { return merge_m() + 4 * kConsumerWarps * gmax; }
-    __host__ __device__ int total() const { return merge_l() + 4 * kConsumerWarps * gmax; }
+    // two slots (double buffer) x consumer warps x gmax heads
+    __host__ __device__ int merge_rows() const { return merge ? 2 * kConsumerWarps * gmax : 0; }
+    __host__ __device__ int merge_m() const { return merge_o() + 4 * merge_rows() * row_stride(); }
+    __host__ __device__ int merge_l() const { return merge_m() + 4 * merge_rows(); }
+    __host__ __device__ int total() const { return merge_l() + 4 * merge_rows(); }
     // bytes to request: layout plus slack to align the ring to 1024 B
     __host__ __device__ int request() const { return total() + 1024; }
 };
+
+// Bytes of one stage: K and V for kTile tokens of `heads` kv heads.
+__host__ __device__ inline int decode_stage_bytes(int elem_bytes, int head_dim, int heads) {
+    return 2 * heads * head_dim * elem_bytes * kTile;
+}
 
 }  // namespace pkv

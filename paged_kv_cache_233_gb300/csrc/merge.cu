@@ -94,12 +94,11 @@ cudaError_t launch_lse_merge(int dtype, int head_dim, const float *ws_o, const f
     }
 }
 
-int decode_log2_stages(int elem_bytes, int head_dim) {
-    // about 64 KB of K/V stages per CTA, two CTAs per SM
-    const int stage = 2 * head_dim * elem_bytes / 128 * kSlabBytes;
-    int lg = 0;
-    while ((2 << lg) * stage <= 64 * 1024 && lg < 4) ++lg;
-    return lg < 1 ? 1 : lg;
+int decode_stages(int elem_bytes, int head_dim, int heads_per_unit) {
+    // about 96 KB of K/V stages per CTA (two CTAs per SM), at least double buffered
+    const int stage = decode_stage_bytes(elem_bytes, head_dim, heads_per_unit);
+    int n = (96 * 1024) / stage;
+    return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
 }  // namespace pkv

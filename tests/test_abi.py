@@ -111,6 +111,11 @@ def test_options_round_trip(lib):
         pk.set_option(pk.OPT_DECODE_PATH, 9)
     with pytest.raises(pk.PagedKVError):
         pk.set_option(99, 0)
+    with pytest.raises(pk.PagedKVError):
+        pk.set_option(pk.OPT_STAGES, 1)
+    pk.set_option(pk.OPT_STAGES, 3)
+    assert pk.get_option(pk.OPT_STAGES) == 3
+    pk.set_option(pk.OPT_STAGES, 0)
 
 
 def test_tensors_must_be_on_the_gpu(lib):
