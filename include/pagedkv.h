@@ -177,6 +177,40 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
                                        int partition_tokens);
 
 /*
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that
+ * must not allocate device memory on their call path and so cannot provide a
+ * split-K workspace: a serving loop with a fixed per-step latency budget
+ * (cudaMalloc may synchronise the device and take milliseconds), a plug-in
+ * whose host application owns all device memory through its own pool, or a
+ * process that has already handed the free memory to another allocator.
+ * The pages have no counterpart to this entry point.
+ *
+ * Same arguments and results as paged_attention_decode, without workspace
+ * and workspace_bytes: the partition states live in one library-owned device
+ * array of PAGEDKV_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
+ * library keeps until the process exits. The call allocates nothing.
+ *   - A split whose paged_attention_workspace_bytes() exceeds
+ *     PAGEDKV_NOALLOC_SCRATCH_BYTES is rejected with PAGEDKV_ERR_WORKSPACE
+ *     before anything is enqueued. partition_tokens == 0 needs no scratch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents. Nothing in it needs to start at zero: each call writes
+ *     every partition state it later reads. Calls whose work overlaps on the
+ *     GPU (for example on two streams without an ordering between them) race
+ *     on the array and give wrong results; order them on one stream.
+ */
+#define PAGEDKV_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int paged_attention_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   float scale, void *out, int num_seqs, int n_q_heads,
+                                   int n_kv_heads, int head_dim, int num_blocks, int block_size,
+                                   int max_blocks_per_seq, int partition_tokens, int dtype,
+                                   void *stream);
+
+
+/*
  * pagedkv_device_errors -- read (and optionally clear) the sticky device
  * error word of the current device. Synchronises the device first, so it
  * sees every kernel enqueued before the call. *flags receives the PAGEDKV_DEVERR_*

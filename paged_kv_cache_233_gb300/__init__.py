@@ -28,6 +28,7 @@ __all__ = [
     "paged_attention_workspace_bytes", "new_workspace", "device_errors", "set_option",
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
+    "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,10 +36,11 @@ _LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP, OPT_STAGES = 1, 2, 3, 4
+NOALLOC_SCRATCH_BYTES = 64 << 20   # PAGEDKV_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
-           "pagedkv_abi_version")
+           "pagedkv_abi_version", "paged_attention_decode_noalloc")
 
 
 class PagedKVError(RuntimeError):
@@ -67,6 +69,9 @@ def load():
     lib.paged_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32,
                                            i32, i32, i32, i32, i32, vp, sz, i32, vp]
+    lib.paged_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32,
+                                                   i32, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.paged_attention_decode_noalloc.restype = i32
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -188,6 +193,31 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr, ws_bytes, _code(q),
         _stream(stream))
     _check(st, "paged_attention_decode")
+
+
+def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                   partition_tokens=0, stream=None):
+    """paged_attention_decode without a workspace argument, for callers that must
+    not allocate device memory on their call path (a serving loop with a fixed
+    latency budget, a plug-in whose host owns all device memory, a process whose
+    free memory belongs to another allocator). Split-K partition states go to a
+    fixed library-owned device array of NOALLOC_SCRATCH_BYTES shared by every
+    call on the device: order such calls on one stream. A split that needs more
+    than that raises PagedKVError (status -5)."""
+    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
+    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
+        raise PagedKVError("q, out and the pools must share one element type")
+    S, Hq, D = q.shape
+    NB, B, Hkv, Dk = k_cache.shape
+    if Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise PagedKVError("shape mismatch between q, the pools, block_tables and context_lens")
+    st = load().paged_attention_decode_noalloc(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S, Hq, Hkv,
+        D, NB, B, block_tables.shape[1], int(partition_tokens), _code(q), _stream(stream))
+    _check(st, "paged_attention_decode_noalloc")
 
 
 def device_errors(reset=True):
