@@ -294,16 +294,17 @@ def oracle_pools(orc, wl, tensors):
 
 
 def oracle_rate(orc, wl, q, kc, vc, budget_s, start_unit=0):
-    """Time the oracle's decode over consecutive (seq, kv head) units until the
-    budget is spent. Returns (bytes, seconds, units, threads)."""
+    """Time the oracle's decode over consecutive (seq, kv head) units, cycling
+    through the workload, until the budget is spent. Returns (bytes, seconds,
+    units, threads)."""
     units = [(s, h) for s in range(wl.num_seqs) for h in range(wl.n_kv_heads)]
     threads = orc.max_threads()
     row = wl.head_dim * wl.element_bytes
     done_bytes, elapsed, n = 0, 0.0, 0
     i = start_unit % len(units)
     chunk = max(1, threads)
-    while elapsed < budget_s and n < len(units):
-        batch = [units[(i + k) % len(units)] for k in range(min(chunk, len(units) - n))]
+    while elapsed < budget_s:
+        batch = [units[(i + k) % len(units)] for k in range(chunk)]
         t0 = time.perf_counter()
         orc.decode(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, units=batch,
                    threads=threads)
@@ -433,6 +434,60 @@ def measure_gate(name, args, device):
     return res
 
 
+def measure_trace(block_size, device, partition=256):
+    """The continuous-batching workload (64 requests, up to 64 slots, 65,536-slot
+    pool, LIFO recompute preemption) through the hot path, step by step. Step
+    inputs are gathered on the device beforehand; each step's three calls are
+    timed with CUDA events."""
+    import paged_kv_cache_233_gb300 as pk
+    from types import SimpleNamespace
+    from workloads import cb_trace, step_inputs, trace_tensors
+    tw = cb_trace(block_size=block_size, slots=64)
+    tensors = trace_tensors(tw, device)
+    shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
+    kc = torch.zeros(shape, dtype=tw.torch_dtype, device=device)
+    vc = torch.zeros_like(kc)
+    steps = []
+    for plan in tw.plans:
+        x = step_inputs(tw, plan, tensors, device)
+        x["slots"] = torch.empty(len(plan.token_row), dtype=torch.int64, device=device)
+        x["out"] = torch.empty_like(x["q"])
+        x["ws"] = pk.new_workspace(x["q"], x["block_tables"], tw.block_size, partition)
+        steps.append((plan, x))
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in steps]
+    for (plan, x), (a, b) in zip(steps, ev):
+        a.record()
+        pk.paged_kv_slot_mapping(x["block_tables"], x["token_row"], x["token_pos"], x["slots"],
+                                 tw.num_blocks, tw.block_size)
+        pk.paged_kv_append(x["k"], x["v"], x["slots"], kc, vc)
+        pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"], tw.scale,
+                                  x["out"], partition, x["ws"])
+        b.record()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(ms)
+    dec_bytes = 0
+    app_bytes = 0
+    decodes = 0
+    row = tw.n_kv_heads * tw.head_dim * tw.element_bytes
+    for plan, _ in steps:
+        view = SimpleNamespace(block_size=tw.block_size, element_bytes=tw.element_bytes,
+                               n_kv_heads=tw.n_kv_heads, head_dim=tw.head_dim,
+                               n_q_heads=tw.n_q_heads, num_seqs=len(plan.rids),
+                               context_lens=plan.context_lens, block_tables=plan.block_tables)
+        dec_bytes += decode_bytes(view)[0]
+        app_bytes += 4 * len(plan.token_row) * row + 8 * len(plan.token_row)
+        decodes += len(plan.rids)
+    return {"steps": len(steps), "preemptions": tw.preemptions,
+            "max_running": max(len(p.rids) for p, _ in steps),
+            "total_ms": total_ms, "decode_gbs": dec_bytes / total_ms / 1e6,
+            "seq_decodes_per_s": decodes / (total_ms * 1e-3),
+            "append_gbs_in_step": app_bytes / total_ms / 1e6,
+            "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition}
+
+
 def run_ours(args, ctx):
     import paged_kv_cache_233_gb300 as pk
     from paged_kv_cache_233_gb300 import build as pk_build
@@ -498,6 +553,9 @@ def run_ours(args, ctx):
     if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
         result["gates"] = {name: measure_gate(name, args, device)
                            for name in ("gqa8b_prefix", "longctx_splitk")}
+    if ctx.rank == 0 and not args.no_trace and ctx.world == 1:
+        result["trace"] = {f"B{b}": measure_trace(b, device) for b in (8, 16, 32)}
+        torch.cuda.empty_cache()
     if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
         import oracle
         orc = oracle.get()
@@ -508,8 +566,9 @@ def run_ours(args, ctx):
                                        args.cpu_budget)
         result["cpu_baseline"] = {
             "value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {wl0.num_seqs * wl0.n_kv_heads} (sequence, kv head) units "
-                      f"of the same workload, {s:.1f} s of fp64 oracle decode"}
+            "sample": f"{n} (sequence, kv head) units taken in order, cycling over the "
+                      f"{wl0.num_seqs * wl0.n_kv_heads} units of the same workload; {s:.1f} s of "
+                      f"fp64 oracle decode on {threads} threads"}
     return result
 
 
@@ -529,6 +588,7 @@ def main(argv=None):
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-gates", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-trace", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

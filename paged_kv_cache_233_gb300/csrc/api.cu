@@ -337,7 +337,7 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     p.part_tokens = P;
     p.max_parts = int(max_parts);
     p.split = split ? 1 : 0;
-    p.stages = g_opt_stages ? g_opt_stages : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu);
+    p.stages = g_opt_stages ? g_opt_stages : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu, P);
     p.heads_per_unit = hpu;
     p.log2_hpu = hpu == 4 ? 2 : (hpu == 2 ? 1 : 0);
     p.rows_per_box = block_size < pkv::kTile ? block_size : pkv::kTile;

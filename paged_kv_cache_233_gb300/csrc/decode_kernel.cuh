@@ -576,6 +576,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncthreads();
     const int total_units = seq_base[S];
     if (int(blockIdx.x) >= total_units) return;
+    // a dependent merge launch may start once every CTA got here or exited;
+    // it waits on this grid's completion before reading the partition states
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

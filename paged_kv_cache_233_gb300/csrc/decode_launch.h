@@ -36,6 +36,6 @@ cudaError_t launch_lse_merge(int dtype, int head_dim, const float *ws_o, const f
                              int max_context, unsigned int *err, cudaStream_t stream);
 
 // Stage-ring size for an element size, head_dim and kv heads per unit.
-int decode_stages(int elem_bytes, int head_dim, int heads_per_unit);
+int decode_stages(int elem_bytes, int head_dim, int heads_per_unit, int part_tokens);
 
 }  // namespace pkv

@@ -8,6 +8,7 @@ sequence owns. It never computes a slot, a gather or an attention value.
 """
 from .synth import (PagedWorkload, TORCH_DTYPES, make_workload, materialize, new_pools,
                     preset, PRESETS)
+from .trace import TraceWorkload, cb_trace, step_inputs, trace_tensors
 
 __all__ = ["PagedWorkload", "TORCH_DTYPES", "make_workload", "materialize", "new_pools",
-           "preset", "PRESETS"]
+           "preset", "PRESETS", "TraceWorkload", "cb_trace", "step_inputs", "trace_tensors"]
