@@ -39,7 +39,7 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu",
                   "decode_instances.cuh"]
 
 # partition size (tokens) used for each workload's decode; 0 = no split
-PARTITION = {"tiny": 0, "mha7b": 256, "gqa8b_prefix": 256, "longctx_splitk": 512}
+PARTITION = {"tiny": 0, "mha7b": 320, "gqa8b_prefix": 320, "longctx_splitk": 512}
 
 DESCRIPTION = {
     "tiny": "tiny: 4 seqs, lens {2,18,34,65}, B16, 4q/2kv heads, D64, fp32",

@@ -68,6 +68,9 @@ typedef enum {
 #define PAGEDKV_DEVERR_SEQ_INDEX    0x10u  /* slot mapping: token_seq outside [0, num_seqs) */
 #define PAGEDKV_DEVERR_TIMEOUT      0x20u  /* a bounded in-kernel wait gave up */
 
+/* partition_tokens value of paged_attention_decode selecting the balanced split. */
+#define PAGEDKV_PARTITION_BALANCED  (-1)
+
 /*
  * paged_kv_slot_mapping -- address translation for a batch of new tokens.
  *
@@ -145,6 +148,16 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
  *   out           [num_seqs][n_q_heads][head_dim] of dtype, device, written
  *
  * partition_tokens == 0: each (sequence, kv head) is processed whole.
+ * partition_tokens == PAGEDKV_PARTITION_BALANCED (-1): balanced split. The
+ *   list of all 16-token tiles, ordered [sequence][kv head group][tile], is
+ *   cut into equal contiguous shares, one per CTA of the (persistent) grid, so
+ *   every CTA streams the same number of bytes whatever the length mix. A
+ *   (sequence, kv head) that falls inside one share is written directly; one
+ *   that spans shares leaves one unnormalised state per share (at most two
+ *   per CTA) in the workspace, which a merge kernel combines as below. The
+ *   workspace layout of this mode is internal; size it with
+ *   paged_attention_workspace_bytes(..., PAGEDKV_PARTITION_BALANCED), which
+ *   depends on the current device's SM count.
  * partition_tokens > 0 (a multiple of 16): split-K. Each sequence's context is
  *   cut into partitions of that many tokens; each (sequence, kv head,
  *   partition) produces an unnormalised state per query head
@@ -171,7 +184,8 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
                            int dtype, void *stream);
 
 /* Workspace bytes paged_attention_decode needs for these sizes (0 when
- * partition_tokens == 0). Returns 0 for invalid sizes as well. */
+ * partition_tokens == 0). Returns 0 for invalid sizes as well, and for the
+ * balanced split when no CUDA device is current. */
 size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,
                                        int max_blocks_per_seq, int block_size,
                                        int partition_tokens);
@@ -191,7 +205,8 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
  * library keeps until the process exits. The call allocates nothing.
  *   - A split whose paged_attention_workspace_bytes() exceeds
  *     PAGEDKV_NOALLOC_SCRATCH_BYTES is rejected with PAGEDKV_ERR_WORKSPACE
- *     before anything is enqueued. partition_tokens == 0 needs no scratch.
+ *     before anything is enqueued. partition_tokens == 0 needs no scratch;
+ *     PAGEDKV_PARTITION_BALANCED uses it like any split.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

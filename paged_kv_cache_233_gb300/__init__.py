@@ -28,7 +28,7 @@ __all__ = [
     "paged_attention_workspace_bytes", "new_workspace", "device_errors", "set_option",
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
-    "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,7 @@ _LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP, OPT_STAGES = 1, 2, 3, 4
 NOALLOC_SCRATCH_BYTES = 64 << 20   # PAGEDKV_NOALLOC_SCRATCH_BYTES
+PARTITION_BALANCED = -1            # PAGEDKV_PARTITION_BALANCED
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
@@ -174,7 +175,11 @@ def new_workspace(q, block_tables, block_size, partition_tokens):
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                            partition_tokens=0, workspace=None, stream=None):
-    """out[s][h] = softmax(scale * q[s][h] . K_s) V_s with K_s, V_s read through block_tables."""
+    """out[s][h] = softmax(scale * q[s][h] . K_s) V_s with K_s, V_s read through block_tables.
+
+    partition_tokens: 0 = no split, > 0 = split-K in partitions of that many
+    tokens, PARTITION_BALANCED = equal tile shares per CTA; splits need a
+    workspace (new_workspace)."""
     if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
         raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
     if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:

@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSeqs = 4096;
+constexpr int kMaxCtasPerSm = 8;
 
 std::mutex g_mu;
 unsigned int *g_err_ptr[kMaxDevices] = {};
@@ -120,6 +121,23 @@ int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim,
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// SM count of the current device (no error word lookup).
+int current_sm_count(int *sms) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return PAGEDKV_ERR_CUDA;
+    *sms = n;
+    return PAGEDKV_OK;
+}
+
+// Piece rows of the balanced split: two slots per CTA of the largest grid the
+// CTAs-per-SM option allows, each with up to 4 kv heads x 8 query heads.
+size_t balanced_rows(int sms, int n_q_heads) {
+    const size_t rows_per_piece = size_t(n_q_heads < 32 ? n_q_heads : 32);
+    return 2 * size_t(kMaxCtasPerSm) * size_t(sms) * rows_per_piece;
+}
+
 long long max_parts_for(int max_blocks, int block_size, int part_tokens) {
     const long long cap = (long long)max_blocks * block_size;
     return (cap + part_tokens - 1) / part_tokens;
@@ -150,7 +168,7 @@ int pagedkv_set_option(int option, int value) {
             g_opt_path = value;
             return PAGEDKV_OK;
         case PAGEDKV_OPT_CTAS_PER_SM:
-            if (value < 0 || value > 8) return PAGEDKV_ERR_INVALID_ARG;
+            if (value < 0 || value > kMaxCtasPerSm) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_ctas_per_sm = value;
             return PAGEDKV_OK;
         case PAGEDKV_OPT_MMA_MIN_GROUP:
@@ -242,11 +260,19 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
 size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,
                                        int max_blocks_per_seq, int block_size,
                                        int partition_tokens) {
-    if (partition_tokens <= 0 || num_seqs < 0 || n_q_heads < 1 || head_dim < 1 ||
-        max_blocks_per_seq < 1 || block_size < 1)
+    if (num_seqs < 0 || n_q_heads < 1 || head_dim < 1 || max_blocks_per_seq < 1 || block_size < 1)
         return 0;
-    const size_t rows = size_t(num_seqs) * n_q_heads *
-                        size_t(max_parts_for(max_blocks_per_seq, block_size, partition_tokens));
+    size_t rows = 0;
+    if (partition_tokens == PAGEDKV_PARTITION_BALANCED) {
+        int sms = 0;
+        if (current_sm_count(&sms) != PAGEDKV_OK) return 0;
+        rows = balanced_rows(sms, n_q_heads);
+    } else if (partition_tokens > 0) {
+        rows = size_t(num_seqs) * n_q_heads *
+               size_t(max_parts_for(max_blocks_per_seq, block_size, partition_tokens));
+    } else {
+        return 0;
+    }
     return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
 }
 
@@ -258,10 +284,12 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
                            int dtype, void *stream) {
     // ---- shapes
     if (num_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1 || num_blocks < 1 ||
-        block_size < 1 || max_blocks_per_seq < 1 || partition_tokens < 0 || !valid_dtype(dtype))
+        block_size < 1 || max_blocks_per_seq < 1 || !valid_dtype(dtype) ||
+        (partition_tokens < 0 && partition_tokens != PAGEDKV_PARTITION_BALANCED))
         return PAGEDKV_ERR_INVALID_ARG;
     if (n_q_heads % n_kv_heads != 0) return PAGEDKV_ERR_INVALID_ARG;
-    if (partition_tokens % pkv::kTile != 0) return PAGEDKV_ERR_INVALID_ARG;
+    const bool balanced = partition_tokens == PAGEDKV_PARTITION_BALANCED;
+    if (!balanced && partition_tokens % pkv::kTile != 0) return PAGEDKV_ERR_INVALID_ARG;
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PAGEDKV_ERR_INVALID_ARG;
     const int group = n_q_heads / n_kv_heads;
     if (head_dim != 64 && head_dim != 128) return PAGEDKV_ERR_UNSUPPORTED;
@@ -286,16 +314,26 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     int gmax = 8;
     if (path == pkv::kPathSimt) gmax = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : 8;
     // ---- split-K
-    const bool split = partition_tokens > 0;
-    const int P = split ? partition_tokens : int((cap + pkv::kTile - 1) / pkv::kTile * pkv::kTile);
-    const long long max_parts = split ? max_parts_for(max_blocks_per_seq, block_size, P) : 1;
+    const bool split = partition_tokens != 0;
+    const int P = partition_tokens > 0 ? partition_tokens
+                                       : int((cap + pkv::kTile - 1) / pkv::kTile * pkv::kTile);
+    const long long max_parts =
+        partition_tokens > 0 ? max_parts_for(max_blocks_per_seq, block_size, P) : 1;
     float *ws_o = nullptr, *ws_m = nullptr, *ws_l = nullptr;
     if (split) {
         const size_t need = paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim,
-                                                            max_blocks_per_seq, block_size, P);
-        if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+                                                            max_blocks_per_seq, block_size,
+                                                            partition_tokens);
+        if (need == 0 || !workspace || workspace_bytes < need || !aligned(workspace, 256))
             return PAGEDKV_ERR_WORKSPACE;
-        const size_t rows = size_t(num_seqs) * n_q_heads * size_t(max_parts);
+        size_t rows;
+        if (balanced) {
+            int sms = 0;
+            if (current_sm_count(&sms) != PAGEDKV_OK) return PAGEDKV_ERR_CUDA;
+            rows = balanced_rows(sms, n_q_heads);
+        } else {
+            rows = size_t(num_seqs) * n_q_heads * size_t(max_parts);
+        }
         uint8_t *w = static_cast<uint8_t *>(workspace);
         ws_o = reinterpret_cast<float *>(w);
         ws_m = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)));
@@ -337,6 +375,7 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     p.part_tokens = P;
     p.max_parts = int(max_parts);
     p.split = split ? 1 : 0;
+    p.balanced = balanced ? 1 : 0;
     p.stages = g_opt_stages ? g_opt_stages : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu, P);
     p.heads_per_unit = hpu;
     p.log2_hpu = hpu == 4 ? 2 : (hpu == 2 ? 1 : 0);
@@ -346,7 +385,9 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     a.gmax = gmax;
     a.ctas_per_sm = g_opt_ctas_per_sm;
     a.num_sms = sms;
-    a.max_units = (long long)num_seqs * (n_kv_heads / hpu) * max_parts;
+    a.max_units = balanced ? (long long)num_seqs * (n_kv_heads / hpu) * ((cap + pkv::kTile - 1) / pkv::kTile)
+                           : (long long)num_seqs * (n_kv_heads / hpu) * max_parts;
+    a.grid_used = 0;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (dtype) {
@@ -355,7 +396,12 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
         default: e = pkv::launch_decode_bf16(a); break;
     }
     if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
-    if (split) {
+    if (balanced) {
+        e = pkv::launch_piece_merge(dtype, head_dim, ws_o, ws_m, ws_l, context_lens, out, num_seqs,
+                                    n_q_heads, n_kv_heads / hpu, hpu * group, a.grid_used,
+                                    int(cap), a.stream);
+        if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
+    } else if (split) {
         e = pkv::launch_lse_merge(dtype, head_dim, ws_o, ws_m, ws_l, context_lens, out, num_seqs,
                                   n_q_heads, P, int(max_parts), int(cap), err, a.stream);
         if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;

@@ -4,7 +4,7 @@
 
 namespace pkv {
 
-cudaError_t launch_decode_bf16(const DecodeLaunch &a) {
+cudaError_t launch_decode_bf16(DecodeLaunch &a) {
     if (a.path == kPathMma) {
         switch (a.head_dim) {
             case 64: return launch_decode_instance<__nv_bfloat16, 64, 8, true>(a);

@@ -4,7 +4,7 @@
 
 namespace pkv {
 
-cudaError_t launch_decode_f16(const DecodeLaunch &a) {
+cudaError_t launch_decode_f16(DecodeLaunch &a) {
     if (a.path == kPathMma) {
         switch (a.head_dim) {
             case 64: return launch_decode_instance<__half, 64, 8, true>(a);

@@ -3,7 +3,7 @@
 
 namespace pkv {
 
-cudaError_t launch_decode_f32(const DecodeLaunch &a) {
+cudaError_t launch_decode_f32(DecodeLaunch &a) {
     if (a.path != kPathSimt) return cudaErrorInvalidValue;
     switch (a.head_dim) {
         case 64: return launch_simt_by_group<float, 64>(a);

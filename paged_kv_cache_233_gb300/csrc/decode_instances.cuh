@@ -8,7 +8,7 @@
 namespace pkv {
 
 template <typename T, int D, int GM, bool kMma>
-static cudaError_t launch_decode_instance(const DecodeLaunch &a) {
+static cudaError_t launch_decode_instance(DecodeLaunch &a) {
     auto kernel = paged_decode_kernel<T, D, GM, kMma>;
     const int stage_bytes = decode_stage_bytes(int(sizeof(T)), D, a.p.heads_per_unit);
     const int merge = a.p.heads_per_unit < kConsumerWarps ? 1 : 0;
@@ -32,12 +32,13 @@ static cudaError_t launch_decode_instance(const DecodeLaunch &a) {
     long long grid = (long long)(want < per_sm ? want : per_sm) * a.num_sms;
     if (grid > a.max_units) grid = a.max_units;
     if (grid < 1) grid = 1;
+    a.grid_used = int(grid);
     kernel<<<dim3((unsigned)grid), dim3(kDecodeThreads), smem, a.stream>>>(a.kmap, a.vmap, a.p);
     return cudaGetLastError();
 }
 
 template <typename T, int D>
-static cudaError_t launch_simt_by_group(const DecodeLaunch &a) {
+static cudaError_t launch_simt_by_group(DecodeLaunch &a) {
     switch (a.gmax) {
         case 1: return launch_decode_instance<T, D, 1, false>(a);
         case 2: return launch_decode_instance<T, D, 2, false>(a);

@@ -147,8 +147,8 @@ __device__ __forceinline__ void sts128_zero(uint32_t addr) {
 struct UnitSink {
     bool partial;
     size_t out_row0;   // row (s * n_q_heads + qh0) of out, qh0 = this warp's first q head
-    size_t ws_row0;    // workspace row of (s, qh0, part); q head qh0 + j adds j * max_parts
-    int max_parts;
+    size_t ws_row0;    // workspace row of q head qh0 of this unit's state
+    int j_stride;      // rows between consecutive q heads of the group
 };
 
 // ---------------------------------------------------------------------------
@@ -283,7 +283,7 @@ struct SimtConsumer {
         for (int j = 0; j < GM; ++j) {
             if (j < g) {
                 if (sink.partial) {
-                    const size_t row = sink.ws_row0 + size_t(j) * sink.max_parts;
+                    const size_t row = sink.ws_row0 + size_t(j) * sink.j_stride;
                     if (r == 0) {
                         float *dst = ws_o + row * D + i * EPL;
 #pragma unroll
@@ -437,7 +437,7 @@ struct MmaConsumer {
             const int h = 2 * c + hsel;
             if (h >= g) continue;
             if (sink.partial) {
-                const size_t row = sink.ws_row0 + size_t(h) * sink.max_parts;
+                const size_t row = sink.ws_row0 + size_t(h) * sink.j_stride;
                 float *dst = ws_o + row * D;
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
@@ -485,25 +485,83 @@ struct MmaConsumer {
 // Unit walk shared by the producer and the consumers
 // ---------------------------------------------------------------------------
 struct Unit {
-    int s, hg, part, L, t0, t1, ntiles;
+    int s, hg, L, t0, t1, ntiles;
+    int part;       // fixed partitions: partition index within the sequence
+    bool partial;   // the result is a partition state, not the final row
+    int slot;       // balanced split: which of this CTA's two piece slots
 };
 
-// Unit u; `s` is a cursor into the sequence prefix sums (units are visited in
-// increasing order, so it only moves forward).
-__device__ __forceinline__ Unit unit_at(int u, int &s, const int *seq_base, const int *seq_len,
-                                        int groups, int P) {
-    while (seq_base[s + 1] <= u) ++s;
-    Unit x;
-    const int rr = u - seq_base[s];
-    x.s = s;
-    x.part = rr / groups;
-    x.hg = rr - x.part * groups;
-    x.L = seq_len[s];
-    x.t0 = x.part * P;
-    x.t1 = min(x.L, x.t0 + P);
-    x.ntiles = (x.t1 - x.t0 + kTile - 1) / kTile;
-    return x;
-}
+// This CTA's units, in order (producer and consumers walk identical copies).
+//  Fixed mode: units blockIdx.x + k * gridDim.x of the sequence-major list
+//    [sequence][partition][head group]; a unit is partial when split-K is on
+//    and its sequence has more than one partition.
+//  Balanced mode: the CTA's equal, contiguous share of the global list of
+//    16-token tiles [sequence][head group][tile]; a unit is the part of one
+//    (sequence, head group) inside that share, partial unless it is the whole
+//    sequence. Only a share's first and last units can be partial; they go to
+//    piece slots 0 and 1 of the CTA.
+struct Walk {
+    const int *seq_base;   // per-sequence prefix sums of units (fixed) or tiles (balanced)
+    const int *seq_len;
+    int groups, P, split, balanced;
+    int s, pos, end, stride, count;
+
+    __device__ void init(const int *base, const int *len, int S, int groups_, int P_, int split_,
+                         int balanced_) {
+        seq_base = base;
+        seq_len = len;
+        groups = groups_;
+        P = P_;
+        split = split_;
+        balanced = balanced_;
+        s = 0;
+        count = 0;
+        const long long total = base[S];
+        if (balanced) {
+            pos = int(total * blockIdx.x / gridDim.x);
+            end = int(total * (blockIdx.x + 1) / gridDim.x);
+            stride = 0;
+        } else {
+            pos = blockIdx.x;
+            end = int(total);
+            stride = gridDim.x;
+        }
+    }
+
+    __device__ bool has_work() const { return pos < end; }
+
+    __device__ bool next(Unit &x) {
+        if (pos >= end) return false;
+        while (seq_base[s + 1] <= pos) ++s;
+        x.s = s;
+        x.L = seq_len[s];
+        const int rr = pos - seq_base[s];
+        if (balanced) {
+            const int nt = (x.L + kTile - 1) / kTile;     // tiles per head group (> 0 here)
+            x.hg = rr / nt;
+            const int tf = rr - x.hg * nt;
+            const int tl = min(nt, tf + (end - pos));
+            x.part = 0;
+            x.t0 = tf * kTile;
+            x.t1 = min(x.L, tl * kTile);
+            x.ntiles = tl - tf;
+            x.partial = !(tf == 0 && tl == nt);
+            x.slot = count == 0 ? 0 : 1;
+            pos += tl - tf;
+        } else {
+            x.part = rr / groups;
+            x.hg = rr - x.part * groups;
+            x.t0 = x.part * P;
+            x.t1 = min(x.L, x.t0 + P);
+            x.ntiles = (x.t1 - x.t0 + kTile - 1) / kTile;
+            x.partial = split && x.L > P;
+            x.slot = 0;
+            pos += stride;
+        }
+        ++count;
+        return true;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -549,7 +607,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             tma_prefetch_descriptor(&kmap);
             tma_prefetch_descriptor(&vmap);
         }
-        // units of each sequence: max(1, ceil(L / P)) partitions x head groups, prefix-summed
+        // per sequence, prefix-summed: units = max(1, ceil(L / P)) partitions x head
+        // groups (fixed mode), or 16-token tiles x head groups (balanced mode)
         const int cap = p.max_blocks * B;
         int carry = 0;
         if (lane == 0) seq_base[0] = 0;
@@ -561,7 +620,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int Lc = min(max(L, 0), cap);
                 if (Lc != L) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
                 seq_len[s] = Lc;
-                cnt = (Lc > 0 ? (Lc + P - 1) / P : 1) * groups;
+                cnt = (p.balanced ? (Lc + kTile - 1) / kTile : (Lc > 0 ? (Lc + P - 1) / P : 1)) * groups;
             }
             int x = cnt;
 #pragma unroll
@@ -574,8 +633,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
     }
     __syncthreads();
-    const int total_units = seq_base[S];
-    if (int(blockIdx.x) >= total_units) return;
+    Walk walk;
+    walk.init(seq_base, seq_len, S, groups, P, p.split, p.balanced);
+    if (!walk.has_work()) return;
     // a dependent merge launch may start once every CTA got here or exited;
     // it waits on this grid's completion before reading the partition states
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -586,24 +646,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        int s = 0;
         // lane-parallel window of 32 block-table entries starting at block j0
         auto load_window = [&](const Unit &x, int j0) {
             const int nblk = (x.L + B - 1) >> p.log2_block;
             const int j = j0 + lane;
             return j < nblk ? __ldg(p.block_tables + size_t(x.s) * p.max_blocks + j) : -1;
         };
-        Unit cur = unit_at(blockIdx.x, s, seq_base, seq_len, groups, P);
+        Unit cur;
+        walk.next(cur);
         int nxt_base = cur.t0 >> p.log2_block;
         int nxt_val = load_window(cur, nxt_base);
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        while (ok) {
             int win_base = nxt_base, win_val = nxt_val;
-            const bool has_next = u + int(gridDim.x) < total_units;
-            int s_next = s;
-            Unit nx = cur;
+            Unit nx;
+            const bool has_next = walk.next(nx);
             if (has_next) {
                 // prefetch the first window of this CTA's next unit
-                nx = unit_at(u + gridDim.x, s_next, seq_base, seq_len, groups, P);
                 nxt_base = nx.t0 >> p.log2_block;
                 nxt_val = load_window(nx, nxt_base);
             }
@@ -664,8 +722,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     phase ^= 1u;
                 }
             }
+            if (!has_next) break;
             cur = nx;
-            s = s_next;
         }
         if (!ok && lane == 0) {
             // Stop everyone, then wait (bounded) for this CTA's copies still in flight.
@@ -689,22 +747,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
     int stage = 0;
     uint32_t phase = 0;
-    int s = 0;
     int unit_count = 0;
     const T *qbase = reinterpret_cast<const T *>(p.q);
-    Unit cur = unit_at(blockIdx.x, s, seq_base, seq_len, groups, P);
+    Unit cur;
+    walk.next(cur);
     st.prefetch_q(qbase + (size_t(cur.s) * p.n_q_heads + ((cur.hg << p.log2_hpu) + hh) * g) * D, g);
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++unit_count) {
+    for (;; ++unit_count) {
         const int qh0 = ((cur.hg << p.log2_hpu) + hh) * g;   // first q head of this warp
         if constexpr (kMma) st.begin_unit();
         else st.begin_unit(p.scale_log2);
-        const bool has_next = u + int(gridDim.x) < total_units;
-        int s_next = s;
-        Unit nx = cur;
-        if (has_next) {
-            nx = unit_at(u + gridDim.x, s_next, seq_base, seq_len, groups, P);
+        Unit nx;
+        const bool has_next = walk.next(nx);
+        if (has_next)
             st.prefetch_q(qbase + (size_t(nx.s) * p.n_q_heads + ((nx.hg << p.log2_hpu) + hh) * g) * D, g);
-        }
         for (int i = 0; i < cur.ntiles; ++i) {
             int good = !*abort_flag;
             if (good) good = mbar_wait(full0 + 8 * stage, phase, p.err);
@@ -740,12 +795,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
 
         // ---- result of this unit
-        const int nparts = cur.L > 0 ? (cur.L + P - 1) / P : 1;
         UnitSink sink;
-        sink.partial = p.split && nparts > 1;
+        sink.partial = cur.partial;
         sink.out_row0 = size_t(cur.s) * p.n_q_heads + qh0;
-        sink.max_parts = p.max_parts;
-        sink.ws_row0 = (size_t(cur.s) * p.n_q_heads + qh0) * p.max_parts + cur.part;
+        if (p.balanced) {
+            // piece slot of this CTA: rows [piece][head of unit][q head of group]
+            const size_t piece = size_t(blockIdx.x) * 2 + cur.slot;
+            sink.ws_row0 = (piece * H + hh) * g;
+            sink.j_stride = 1;
+        } else {
+            sink.ws_row0 = (size_t(cur.s) * p.n_q_heads + qh0) * p.max_parts + cur.part;
+            sink.j_stride = p.max_parts;
+        }
         if constexpr (kMma) st.reduce();
         else st.reduce(g);
         if (TL == 1) {
@@ -781,7 +842,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 const int qh = qu0 + h * g + j;
                 if (sink.partial) {
-                    const size_t row = (size_t(cur.s) * p.n_q_heads + qh) * p.max_parts + cur.part;
+                    const size_t row = p.balanced
+                        ? (size_t(blockIdx.x) * 2 + cur.slot) * H * g + size_t(h) * g + j
+                        : (size_t(cur.s) * p.n_q_heads + qh) * p.max_parts + cur.part;
                     p.ws_o[row * D + d] = num;
                     if (d == 0) {
                         p.ws_m[row] = M * kLn2;
@@ -794,8 +857,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
             }
         }
+        if (!has_next) break;
         cur = nx;
-        s = s_next;
     }
 }
 

@@ -52,7 +52,7 @@ extern "C" int paged_attention_decode_noalloc(const void *q, const void *k_cache
                                               int head_dim, int num_blocks, int block_size,
                                               int max_blocks_per_seq, int partition_tokens,
                                               int dtype, void *stream) {
-    if (partition_tokens <= 0)
+    if (partition_tokens == 0)
         return paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                                       num_seqs, n_q_heads, n_kv_heads, head_dim, num_blocks,
                                       block_size, max_blocks_per_seq, 0, nullptr, 0, dtype, stream);

@@ -39,6 +39,7 @@ struct DecodeParams {
     int part_tokens;      // tokens per partition (multiple of kTile)
     int max_parts;        // partitions per (seq, q head) in the workspace
     int split;            // 1: multi-partition sequences write partition states
+    int balanced;         // 1: balanced split (equal tile shares per CTA, pieces merged)
     int stages;           // ring size (>= 2)
     int heads_per_unit;   // kv heads per unit: 1, 2 or 4 (one consumer warp per head)
     int log2_hpu;

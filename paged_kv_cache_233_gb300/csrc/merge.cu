@@ -85,6 +85,8 @@ lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
 
 // One warp per (sequence, query head), for rows of at most 32 partitions:
 // lane p holds partition p's (m, l); each lane owns head_dim / 32 outputs.
+// Every load is issued before the first reduction, so a row costs about one
+// round trip to L2 (where the partition states still sit).
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
@@ -92,6 +94,7 @@ lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ 
                       T *__restrict__ out, int rows, int n_q_heads, int part_tokens, int max_parts,
                       int cap) {
     constexpr int E = D / 32;
+    constexpr int kBatch = 8;
     using V = typename Vec<E>::type;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -102,28 +105,46 @@ lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ 
     const int np = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
     if (np <= 1) return;  // written directly by the partition kernel
     const size_t row0 = size_t(row) * max_parts;
-    const float mp = lane < np ? ws_m[row0 + lane] : -INFINITY;
+    const float mp = lane < np ? __ldcg(ws_m + row0 + lane) : -INFINITY;
+    const float lp = lane < np ? __ldcg(ws_l + row0 + lane) : 0.f;
+    V x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+        if (k < np) x[k] = __ldcg(reinterpret_cast<const V *>(ws_o + (row0 + k) * D) + lane);
     float M = mp;
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, mask));
     const float w = lane < np ? fast_exp2((mp - M) * kLog2e) : 0.f;
-    float den = lane < np ? w * ws_l[row0 + lane] : 0.f;
+    float den = w * lp;
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < np; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, w, k);
-        const V x = *reinterpret_cast<const V *>(ws_o + (row0 + k) * D + lane * E);
-        const float *xf = reinterpret_cast<const float *>(&x);
+    for (int k0 = 0; k0 < np; k0 += kBatch) {
+        if (k0 > 0) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, xf[e], acc[e]);
+            for (int k = 0; k < kBatch; ++k)
+                if (k0 + k < np)
+                    x[k] = __ldcg(reinterpret_cast<const V *>(ws_o + (row0 + k0 + k) * D) + lane);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+            if (k0 + k < np) {
+                const float *xf = reinterpret_cast<const float *>(&x[k]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, xf[e], acc[e]);
+            }
+        }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
+    float v[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) out[size_t(row) * D + lane * E + e] = Elem<T>::from_float(acc[e] * inv);
+    for (int e = 0; e < E; ++e) v[e] = acc[e] * inv;
+    T *dst = out + size_t(row) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[e] = Elem<T>::from_float(v[e]);
 }
 
 // Launched as a programmatic dependent of the decode kernel when the device
@@ -180,6 +201,139 @@ cudaError_t launch_lse_merge(int dtype, int head_dim, const float *ws_o, const f
             return launch_merge_typed<__nv_bfloat16>(head_dim, ws_o, ws_m, ws_l, context_lens,
                                                      out, num_seqs, n_q_heads, part_tokens,
                                                      max_parts, max_context, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+// Balanced split: one CTA per (sequence, head group). The CTA recomputes where
+// the pair's tiles fall in the global tile list [sequence][head group][tile],
+// which of the decode's equal tile shares they span and, if more than one,
+// combines the pieces those CTAs left in their slots (slot 0 for a share's
+// first unit, slot 1 for its last). Pairs inside one share were written by the
+// decode directly; empty sequences get zero rows here.
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kMergeWarps)
+lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
+                        const float *__restrict__ ws_l, const int32_t *__restrict__ lens,
+                        T *__restrict__ out, int num_seqs, int n_q_heads, int groups,
+                        int rows_per_unit, int decode_grid, int cap) {
+    constexpr int E = D / 32;
+    using V = typename Vec<E>::type;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int s = blockIdx.x / groups;
+    const int hg = blockIdx.x - s * groups;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // tiles before this sequence, and in total (exact integer sums)
+    __shared__ unsigned long long sums[2];
+    if (threadIdx.x == 0) sums[0] = sums[1] = 0ull;
+    __syncthreads();
+    unsigned long long before_t = 0, total_t = 0;
+    for (int t = threadIdx.x; t < num_seqs; t += blockDim.x) {
+        const int Lt = min(max(__ldg(lens + t), 0), cap);
+        const unsigned long long n = (unsigned long long)((Lt + kTile - 1) / kTile) * groups;
+        total_t += n;
+        if (t < s) before_t += n;
+    }
+    atomicAdd(&sums[0], before_t);
+    atomicAdd(&sums[1], total_t);
+    __syncthreads();
+    const unsigned long long before = sums[0], total = sums[1];
+    const int L = min(max(__ldg(lens + s), 0), cap);
+    const int nt = (L + kTile - 1) / kTile;
+    const int qh0 = hg * rows_per_unit;
+    if (nt == 0) {
+        for (int x = threadIdx.x; x < rows_per_unit * D; x += blockDim.x)
+            out[(size_t(s) * n_q_heads + qh0) * D + x] = Elem<T>::from_float(0.f);
+        return;
+    }
+    const long long Tt = (long long)total;
+    const long long A = (long long)before + (long long)hg * nt;   // first tile of this pair
+    const long long Z = A + nt - 1;                               // last tile
+    auto share_start = [&](long long c) { return Tt * c / decode_grid; };
+    auto share_of = [&](long long t) {
+        long long c = t * decode_grid / Tt;
+        while (c + 1 < decode_grid && share_start(c + 1) <= t) ++c;
+        while (c > 0 && share_start(c) > t) --c;
+        return c;
+    };
+    const long long c0 = share_of(A), c1 = share_of(Z);
+    if (c0 == c1) return;   // the decode wrote this pair's rows itself
+    const int slot0 = A == share_start(c0) ? 0 : 1;
+    // shares of CTAs with no tiles (fewer tiles than CTAs) hold no piece
+    auto empty_share = [&](long long c) { return share_start(c) == share_start(c + 1); };
+    for (int r = warp; r < rows_per_unit; r += kMergeWarps) {
+        float M = -INFINITY;
+        for (long long c = c0 + lane; c <= c1; c += 32) {
+            if (empty_share(c)) continue;
+            const size_t row = (size_t(c) * 2 + (c == c0 ? slot0 : 0)) * rows_per_unit + r;
+            M = fmaxf(M, ws_m[row]);
+        }
+#pragma unroll
+        for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, mask));
+        float den = 0.f;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (long long c = c0; c <= c1; ++c) {
+            if (empty_share(c)) continue;
+            const size_t row = (size_t(c) * 2 + (c == c0 ? slot0 : 0)) * rows_per_unit + r;
+            const float w = fast_exp2((ws_m[row] - M) * kLog2e);
+            den = fmaf(w, ws_l[row], den);
+            const V x = *reinterpret_cast<const V *>(ws_o + row * D + lane * E);
+            const float *xf = reinterpret_cast<const float *>(&x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, xf[e], acc[e]);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            out[(size_t(s) * n_q_heads + qh0 + r) * D + lane * E + e] = Elem<T>::from_float(acc[e] * inv);
+    }
+}
+
+template <typename T>
+static cudaError_t launch_pieces_typed(int head_dim, const float *ws_o, const float *ws_m,
+                                       const float *ws_l, const int32_t *lens, void *out, int S,
+                                       int Hq, int groups, int rows_per_unit, int grid, int cap,
+                                       cudaStream_t st) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(S * groups));
+    cfg.blockDim = dim3(32 * kMergeWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    T *o = static_cast<T *>(out);
+    if (head_dim == 64)
+        return cudaLaunchKernelEx(&cfg, lse_merge_pieces_kernel<T, 64>, ws_o, ws_m, ws_l, lens, o, S,
+                                  Hq, groups, rows_per_unit, grid, cap);
+    return cudaLaunchKernelEx(&cfg, lse_merge_pieces_kernel<T, 128>, ws_o, ws_m, ws_l, lens, o, S,
+                              Hq, groups, rows_per_unit, grid, cap);
+}
+
+cudaError_t launch_piece_merge(int dtype, int head_dim, const float *ws_o, const float *ws_m,
+                               const float *ws_l, const int32_t *context_lens, void *out,
+                               int num_seqs, int n_q_heads, int groups, int rows_per_unit,
+                               int decode_grid, int max_context, cudaStream_t stream) {
+    if (num_seqs == 0) return cudaSuccess;
+    switch (dtype) {
+        case PAGEDKV_F32:
+            return launch_pieces_typed<float>(head_dim, ws_o, ws_m, ws_l, context_lens, out,
+                                              num_seqs, n_q_heads, groups, rows_per_unit,
+                                              decode_grid, max_context, stream);
+        case PAGEDKV_F16:
+            return launch_pieces_typed<__half>(head_dim, ws_o, ws_m, ws_l, context_lens, out,
+                                               num_seqs, n_q_heads, groups, rows_per_unit,
+                                               decode_grid, max_context, stream);
+        case PAGEDKV_BF16:
+            return launch_pieces_typed<__nv_bfloat16>(head_dim, ws_o, ws_m, ws_l, context_lens,
+                                                      out, num_seqs, n_q_heads, groups,
+                                                      rows_per_unit, decode_grid, max_context,
+                                                      stream);
         default:
             return cudaErrorInvalidValue;
     }

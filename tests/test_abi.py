@@ -75,6 +75,8 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert _decode(lib, q=(1 << 12) + 8) == INVALID          # misaligned
     assert _decode(lib, out=0) == INVALID                    # null
     assert _decode(lib, P=16, ws=None) == WORKSPACE
+    assert _decode(lib, P=-1, ws=None) == WORKSPACE          # balanced split needs a workspace
+    assert _decode(lib, P=-2) == INVALID
     assert _decode(lib, P=16, ws=1 << 12, ws_bytes=64) == WORKSPACE
     assert _decode(lib, S=0) == 0                            # nothing to do, nothing enqueued
     assert _decode(lib, S=5000) == UNSUPPORTED

@@ -52,7 +52,7 @@ def run_both(orc, wl, partition_tokens=0, path="auto"):
 # The tiny workload, end to end
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("partition_tokens", [0, 16, 32])
+@pytest.mark.parametrize("partition_tokens", [0, 16, 32, -1])
 def test_tiny_workload(orc, partition_tokens):
     wl = preset("tiny")
     r = run_both(orc, wl, partition_tokens)
@@ -90,7 +90,7 @@ def sweep_cases():
                 for g in (1, 2, 4, 8):
                     paths = ["simt"] if dtype == "f32" else ["simt", "mma"]
                     for path in paths:
-                        for P in (0, 48):
+                        for P in (0, 48, -1):
                             yield pytest.param(dtype, D, B, g, path, P,
                                                id=f"{dtype}-D{D}-B{B}-g{g}-{path}-P{P}")
 
@@ -154,11 +154,29 @@ def test_empty_and_single_token_contexts(orc):
     wl.context_lens = np.array([0, 1, 16, 0], dtype=np.int32)
     for path in ("simt", "mma"):
         pk.set_option(pk.OPT_DECODE_PATH, PATHS[path])
-        for P in (0, 16):
+        for P in (0, 16, -1):
             out, _ = gpu_decode(wl, t["q"], kc, vc, bt, P)
             o = to_f64(out)
             assert (o[0] == 0).all() and (o[3] == 0).all()
             assert_close(out, oracle_decode(orc, wl, t["q"], okc, ovc), "bf16", what="edge")
+    assert pk.device_errors() == 0
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 8])
+def test_balanced_split_over_skewed_lengths(orc, ctas):
+    """Balanced shares cut single sequences into many pieces (one very long
+    sequence among short ones, and more CTAs than tiles for the short ones)."""
+    pk.set_option(pk.OPT_CTAS_PER_SM, ctas)
+    try:
+        for dtype, g in (("bf16", 8), ("f16", 1), ("f32", 2)):
+            wl = make_workload("skew", dtype, [4000, 1, 17, 2, 33, 0 + 5], 4 * g, 4, 64, 16, 91)
+            r = run_both(orc, wl, -1)
+            assert_close(r["out"], r["ref"], dtype, what=f"balanced {dtype} ctas={ctas}")
+        tiny = make_workload("few", "f16", [3, 20], 8, 4, 128, 16, 92)
+        r = run_both(orc, tiny, -1)
+        assert_close(r["out"], r["ref"], "f16", what="fewer tiles than CTAs")
+    finally:
+        pk.set_option(pk.OPT_CTAS_PER_SM, 0)
     assert pk.device_errors() == 0
 
 
