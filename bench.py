@@ -488,6 +488,42 @@ def measure_trace(block_size, device, partition=256):
             "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition}
 
 
+def measure_cow(device, samples=4, reps=50):
+    """Copy-on-write block copies of parallel sampling over the bench workload:
+    every sequence of the MHA layer forks `samples` samples, and each sample's
+    first token copies the sequence's shared last block to a fresh block."""
+    import paged_kv_cache_233_gb300 as pk
+    wl = preset("mha7b")
+    shape = (wl.num_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim)
+    kc = torch.zeros(shape, dtype=wl.torch_dtype, device=device)
+    vc = torch.zeros_like(kc)
+    used = set(wl.blocks_in_use().tolist())
+    free = [b for b in range(wl.num_blocks) if b not in used]
+    pairs = []
+    for s in range(wl.num_seqs):
+        last = int(wl.block_tables[s, (int(wl.context_lens[s]) - 1) // wl.block_size])
+        for _ in range(samples):
+            if free:
+                pairs.append([last, free.pop()])
+    pr = torch.tensor(pairs, dtype=torch.int32, device=device)
+    for _ in range(3):
+        pk.paged_kv_copy_blocks(kc, vc, pr)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        pk.paged_kv_copy_blocks(kc, vc, pr)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    block_bytes = wl.block_size * wl.row_bytes
+    moved = 2 * 2 * len(pairs) * block_bytes          # K and V, read + write
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"pairs": len(pairs), "bytes_moved": moved, "median_us": ms * 1e3,
+            "gbs": moved / ms / 1e6}
+
+
 def run_ours(args, ctx):
     import paged_kv_cache_233_gb300 as pk
     from paged_kv_cache_233_gb300 import build as pk_build
@@ -556,6 +592,7 @@ def run_ours(args, ctx):
     if ctx.rank == 0 and not args.no_trace and ctx.world == 1:
         result["trace"] = {f"B{b}": measure_trace(b, device) for b in (8, 16, 32)}
         torch.cuda.empty_cache()
+        result["cow_copy"] = measure_cow(device)
     if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
         import oracle
         orc = oracle.get()

@@ -122,6 +122,27 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
                     int n_kv_heads, int head_dim, int dtype, void *stream);
 
 /*
+ * paged_kv_copy_blocks -- copy whole blocks of both pools, for copy-on-write.
+ *
+ * Page "How a serving engine actually works", section "Copy-on-write, because
+ * you have used fork()": sequences forked from one prompt share its blocks;
+ * the first write into a block that others still reference goes to a fresh
+ * block, which must first receive the shared block's contents. For each pair
+ * i, block_pairs[2i] (source) is copied to block_pairs[2i+1] (destination), K
+ * and V, all block_size * n_kv_heads * head_dim elements: a bit copy.
+ *
+ *   k_cache, v_cache  [num_blocks][block_size][n_kv_heads][head_dim], device, updated
+ *   block_pairs       int32 [num_pairs][2] = {src, dst}, device
+ *
+ * A pair with an id outside [0, num_blocks) is skipped and sets
+ * PAGEDKV_DEVERR_BLOCK_ID; src == dst is a no-op. Destinations must be
+ * distinct and must not be the source of another pair of the same call.
+ */
+int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pairs, int num_pairs,
+                         int num_blocks, int block_size, int n_kv_heads, int head_dim, int dtype,
+                         void *stream);
+
+/*
  * paged_attention_decode -- fused paged-attention decode.
  *
  * The kernel the pages name as the next step and never build (page "Paged-KV +

@@ -64,6 +64,9 @@ class Oracle:
         lib.oracle_append.restype = ctypes.c_int64
         lib.oracle_append.argtypes = [_c_u8p, _c_u8p, _c_i64p, ctypes.c_int64, _c_u8p, _c_u8p,
                                       ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_copy_blocks.restype = ctypes.c_int64
+        lib.oracle_copy_blocks.argtypes = [_c_u8p, _c_u8p, _c_i32p, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64]
         lib.oracle_gather.restype = None
         lib.oracle_gather.argtypes = [ctypes.c_void_p, _c_i32p, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -138,6 +141,19 @@ class Oracle:
         return self.lib.oracle_append(_ptr(k, _c_u8p), _ptr(v, _c_u8p), _ptr(sm, _c_i64p),
                                       sm.shape[0], _ptr(k_cache, _c_u8p), _ptr(v_cache, _c_u8p),
                                       num_slots, row_bytes)
+
+    # -- copy-on-write ------------------------------------------------------------
+    def copy_blocks(self, k_cache, v_cache, pairs):
+        """Copy whole blocks src -> dst (pairs [n][2]) in both pools, in place, in order.
+        Returns the number of pairs skipped for ids outside the pool."""
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        for c in (k_cache, v_cache):
+            if not c.flags.c_contiguous:
+                raise ValueError("pools must be contiguous")
+        block_bytes = k_cache.dtype.itemsize * int(np.prod(k_cache.shape[1:]))
+        return self.lib.oracle_copy_blocks(_ptr(k_cache, _c_u8p), _ptr(v_cache, _c_u8p),
+                                           _ptr(pr, _c_i32p), pr.shape[0], k_cache.shape[0],
+                                           block_bytes)
 
     # -- gather -------------------------------------------------------------------
     def gather(self, cache, block_tables, seq, length, kv_head, dtype):

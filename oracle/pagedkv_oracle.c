@@ -21,6 +21,12 @@
  *     block. Appending a token stores its K/V row at its physical slot; the
  *     same page's closing section says the append is plain indexing.
  *
+ *   oracle_copy_blocks
+ *     "How a serving engine actually works", section "Copy-on-write, because
+ *     you have used fork()": a sequence about to write into a block that others
+ *     still reference gets a fresh block; the fresh block must first hold the
+ *     shared block's contents. Whole-block copy, K and V, pairs in order.
+ *
  *   oracle_gather
  *     "Paged Attention and the Block Manager", section "The measurement": a
  *     sequence's cache is copied out of its blocks, in logical order, into a
@@ -164,6 +170,28 @@ int64_t oracle_append(const uint8_t *k_rows, const uint8_t *v_rows,
         }
         memcpy(k_cache + slot * row_bytes, k_rows + t * row_bytes, (size_t)row_bytes);
         memcpy(v_cache + slot * row_bytes, v_rows + t * row_bytes, (size_t)row_bytes);
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Copy-on-write: copy whole blocks (K and V) from src to dst.               */
+/* ------------------------------------------------------------------------ */
+
+/* pairs: [num_pairs][2] = {src, dst}. block_bytes = block_size * row bytes.
+ * Returns the number of pairs skipped because an id was outside the pool. */
+int64_t oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pairs,
+                           int64_t num_pairs, int64_t num_blocks, int64_t block_bytes)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy(k_cache + dst * block_bytes, k_cache + src * block_bytes, (size_t)block_bytes);
+        memcpy(v_cache + dst * block_bytes, v_cache + src * block_bytes, (size_t)block_bytes);
     }
     return bad;
 }

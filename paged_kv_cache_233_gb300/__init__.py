@@ -29,6 +29,7 @@ __all__ = [
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
+    "paged_kv_copy_blocks",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +42,7 @@ PARTITION_BALANCED = -1            # PAGEDKV_PARTITION_BALANCED
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
-           "pagedkv_abi_version", "paged_attention_decode_noalloc")
+           "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks")
 
 
 class PagedKVError(RuntimeError):
@@ -73,6 +74,8 @@ def load():
     lib.paged_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32,
                                                    i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_attention_decode_noalloc.restype = i32
+    lib.paged_kv_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.paged_kv_copy_blocks.restype = i32
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -155,6 +158,20 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), k.shape[0], NB, B, Hkv, D, _code(k),
         _stream(stream))
     _check(st, "paged_kv_append")
+
+
+def paged_kv_copy_blocks(k_cache, v_cache, block_pairs, stream=None):
+    """Copy-on-write: copy whole blocks block_pairs[i][0] -> block_pairs[i][1] in both pools."""
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise PagedKVError("expected pools [NB][B][Hkv][D] of one element type")
+    if block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise PagedKVError("block_pairs must be [n][2]")
+    NB, B, Hkv, D = k_cache.shape
+    st = load().paged_kv_copy_blocks(
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_pairs, "block_pairs", torch.int32), block_pairs.shape[0], NB, B, Hkv, D,
+        _code(k_cache), _stream(stream))
+    _check(st, "paged_kv_copy_blocks")
 
 
 def paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq, block_size,

@@ -21,6 +21,9 @@ cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *toke
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache,
                           void *v_cache, int num_tokens, long long row_bytes, long long num_slots,
                           int num_sms, unsigned int *err, cudaStream_t st);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
+                               int num_blocks, long long block_bytes, int num_sms,
+                               unsigned int *err, cudaStream_t st);
 }  // namespace pkv
 
 // Sticky error word, one per device that loads the library.
@@ -254,6 +257,28 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
     const cudaError_t e = pkv::launch_append(k, v, slot_mapping, k_cache, v_cache, num_tokens,
                                              row_bytes, (long long)num_blocks * block_size, sms,
                                              err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pairs, int num_pairs,
+                         int num_blocks, int block_size, int n_kv_heads, int head_dim, int dtype,
+                         void *stream) {
+    if (num_pairs < 0 || num_blocks < 1 || block_size < 1 || n_kv_heads < 1 || head_dim < 1 ||
+        !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    const long long block_bytes = (long long)block_size * n_kv_heads * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PAGEDKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PAGEDKV_OK;
+    if (!k_cache || !v_cache || !block_pairs) return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    const cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs,
+                                                  num_blocks, block_bytes, sms, err,
+                                                  static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 

@@ -1,4 +1,5 @@
-// append.cu -- address translation and the paged KV append.
+// append.cu -- address translation, the paged KV append and the copy-on-write
+// block copy.
 //
 // slot_mapping: "How a serving engine actually works", section "The one
 // formula": slot = block_table[seq][pos / B] * B + pos % B.
@@ -6,6 +7,9 @@
 // per layer laid out [num_blocks][block_size][n_kv_heads][head_dim]): each
 // new token's K and V rows are copied, 16 bytes per thread and instruction,
 // to row `slot` of the pools.
+// copy_blocks: "How a serving engine actually works", section "Copy-on-write,
+// because you have used fork()": before a sequence writes into a block others
+// still reference, its fresh private block receives the shared block's bytes.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,6 +72,51 @@ append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
             vd[c] = b;
         }
     }
+}
+
+// Copy-on-write: copy whole blocks (K and V) src -> dst. `tpb` threads copy
+// one block pair at a time, 16 bytes per thread and instruction.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int32_t *__restrict__ pairs, int num_pairs, int num_blocks,
+                   long long vec_per_block, unsigned int *err) {
+    for (int i = blockIdx.y; i < num_pairs; i += gridDim.y) {
+        const int src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, PAGEDKV_DEVERR_BLOCK_ID);
+            continue;
+        }
+        if (src == dst) continue;
+        const uint4 *ks = k_cache + src * vec_per_block;
+        const uint4 *vs = v_cache + src * vec_per_block;
+        uint4 *kd = k_cache + dst * vec_per_block;
+        uint4 *vd = v_cache + dst * vec_per_block;
+        for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < vec_per_block;
+             c += (long long)gridDim.x * blockDim.x) {
+            const uint4 a = __ldcs(ks + c);
+            const uint4 b = __ldcs(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
+                               int num_blocks, long long block_bytes, int num_sms,
+                               unsigned int *err, cudaStream_t st) {
+    const long long vec = block_bytes / 16;
+    // CTAs along x split one block; along y they walk the pairs
+    int per_block = int((vec + 255) / 256);
+    if (per_block > 8) per_block = 8;
+    long long along_y = num_pairs;
+    const long long cap = (long long)num_sms * 16 / per_block;
+    if (along_y > cap) along_y = cap;
+    if (along_y > 65535) along_y = 65535;
+    if (along_y < 1) along_y = 1;
+    copy_blocks_kernel<<<dim3(unsigned(per_block), unsigned(along_y)), 256, 0, st>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, num_pairs,
+        num_blocks, vec, err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,

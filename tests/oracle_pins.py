@@ -216,6 +216,68 @@ def pin_append_scatter(orc):
         assert kpool.tobytes() == ek.tobytes() and vpool.tobytes() == ev.tobytes()
 
 
+def pin_copy_blocks(orc):
+    """Block copy equals numpy whole-block assignment; bad ids are skipped."""
+    rng = np.random.default_rng(8)
+    NB, B, Hkv, D = 7, 4, 2, 8
+    for dtype in ("f32", "bf16"):
+        k = to_storage(rng.standard_normal((NB, B, Hkv, D)), dtype)
+        v = to_storage(rng.standard_normal((NB, B, Hkv, D)), dtype)
+        pairs = np.array([[1, 5], [2, 6], [3, 9], [0, 0]], np.int32)
+        ek, ev = k.copy(), v.copy()
+        ek[5], ev[5] = k[1], v[1]
+        ek[6], ev[6] = k[2], v[2]
+        assert orc.copy_blocks(k, v, pairs) == 1
+        assert k.tobytes() == ek.tobytes() and v.tobytes() == ev.tobytes()
+
+
+def pin_fork_copy_on_write(orc):
+    """The serving page's fork: samples share the prompt's blocks; each sample's
+    first token triggers a copy of the shared last block into a fresh one. After
+    the copy and the append, every sample decodes like the contiguous
+    attention over its own logical sequence."""
+    from workloads.serving import BlockAllocator, Sequence
+    rng = np.random.default_rng(9)
+    B, Hkv, D, dtype = 16, 1, 8, "f32"
+    alloc = BlockAllocator(16, B)
+    prompt = Sequence("p", alloc)
+    prompt.append_tokens(90)
+    samples = [prompt.fork(f"s{i}") for i in range(4)]
+    kpool = poison((16, B, Hkv, D), dtype)
+    vpool = poison((16, B, Hkv, D), dtype)
+    Kp = to_storage(rng.standard_normal((90, Hkv, D)), dtype)
+    Vp = to_storage(rng.standard_normal((90, Hkv, D)), dtype)
+    bt = np.array([prompt.table], np.int32)
+    sm = orc.slot_mapping(bt, np.zeros(90, np.int32), np.arange(90, dtype=np.int32), B)
+    orc.append(Kp, Vp, sm, kpool, vpool)
+    q = to_storage(rng.standard_normal((4, 1, D)), dtype)
+    tables, Ks, Vs = [], [], []
+    for s in samples:
+        shared_last = s.table[-1]
+        s.append_tokens(1)
+        assert s.table[-1] != shared_last
+        orc.copy_blocks(kpool, vpool, [[shared_last, s.table[-1]]])
+        kt = to_storage(rng.standard_normal((1, Hkv, D)), dtype)
+        vt = to_storage(rng.standard_normal((1, Hkv, D)), dtype)
+        tb = np.array([s.table], np.int32)
+        orc.append(kt, vt, orc.slot_mapping(tb, [0], [90], B), kpool, vpool)
+        tables.append(s.table)
+        Ks.append(np.concatenate([widen_lib(Kp, dtype), widen_lib(kt, dtype)]))
+        Vs.append(np.concatenate([widen_lib(Vp, dtype), widen_lib(vt, dtype)]))
+    bts = np.array(tables, np.int32)
+    lens = np.full(4, 91, np.int32)
+    got = orc.decode(q, kpool, vpool, bts, lens, 1.0 / math.sqrt(D), dtype)
+    ref = brute_force(dict(q=q, qc=widen_lib(q, dtype), Kc=Ks, Vc=Vs, Hkv=Hkv, lens=lens,
+                           scale=1.0 / math.sqrt(D)))
+    assert np.abs(got - ref).max() < 1e-12
+    # the prompt's own blocks are untouched: it still decodes its 90 tokens
+    got_p = orc.decode(q[:1], kpool, vpool, bt, np.array([90], np.int32), 1.0 / math.sqrt(D), dtype)
+    ref_p = brute_force(dict(q=q[:1], qc=widen_lib(q[:1], dtype), Kc=[widen_lib(Kp, dtype)],
+                             Vc=[widen_lib(Vp, dtype)], Hkv=Hkv, lens=np.array([90]),
+                             scale=1.0 / math.sqrt(D)))
+    assert np.abs(got_p - ref_p).max() < 1e-12
+
+
 def pin_gather_order(orc):
     """Tokens appended through the slot mapping come back from the gather in
     logical order (row i of the gather holds the value written for position i)."""
@@ -342,6 +404,7 @@ def pin_partition_merge(orc):
 
 
 ALL_PINS = [pin_f16_decoding, pin_bf16_decoding, pin_block_table_example, pin_slot_bijection,
-            pin_append_scatter, pin_gather_order, pin_decode_bruteforce,
+            pin_append_scatter, pin_copy_blocks, pin_fork_copy_on_write, pin_gather_order,
+            pin_decode_bruteforce,
             pin_block_permutation_invariance, pin_shared_prefix, pin_special_cases,
             pin_partition_merge]

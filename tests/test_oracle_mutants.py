@@ -52,6 +52,9 @@ MUTANTS = {
     "append_row_offset": ("memcpy(k_cache + slot * row_bytes, k_rows + t * row_bytes",
                           "memcpy(k_cache + slot * row_bytes, k_rows + slot * row_bytes"),
     "padding_not_skipped": ("if (token_pos[t] < 0) {", "if (token_pos[t] < -1) {"),
+    "copy_only_keys": ("        memcpy(v_cache + dst * block_bytes, v_cache + src * block_bytes, (size_t)block_bytes);\n", ""),
+    "copy_direction_swapped": ("memcpy(k_cache + dst * block_bytes, k_cache + src * block_bytes",
+                               "memcpy(k_cache + src * block_bytes, k_cache + dst * block_bytes"),
 }
 
 
