@@ -488,6 +488,41 @@ def measure_trace(block_size, device, partition=256):
             "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition}
 
 
+def measure_shared_prefix(device, reps=200, partition=320):
+    """The GQA prefix workload through paged_attention_decode_shared_prefix
+    (each 512-token prefix read once per 2-member chunk instead of once per
+    member), against the same roofline numerator as the plain decode."""
+    import paged_kv_cache_233_gb300 as pk
+    wl = preset("gqa8b_prefix")
+    step = Step(wl, device, partition)
+    seq_group = np.full(wl.num_seqs, -1, np.int32)
+    for gi, grp in enumerate(wl.groups):
+        seq_group[grp] = gi
+    sg = torch.from_numpy(seq_group).to(device)
+    gp = torch.full((len(wl.groups),), wl.prefix_blocks * wl.block_size, dtype=torch.int32,
+                    device=device)
+
+    def call():
+        pk.paged_attention_decode_shared_prefix(step.t["q"], step.kc, step.vc, step.bt, step.lens,
+                                                sg, gp, wl.scale, step.out, partition, step.ws)
+    for _ in range(5):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    algo, logical, _ = decode_bytes(wl)
+    peak, _ = measured_peak()
+    del step
+    torch.cuda.empty_cache()
+    return {"decode_ms_median": ms, "achieved_gbs": algo / ms / 1e6, "frac": algo / ms / 1e6 / peak,
+            "logical_gbs": logical / ms / 1e6, "partition_tokens": partition, "reps": reps}
+
+
 def measure_cow(device, samples=4, reps=50):
     """Copy-on-write block copies of parallel sampling over the bench workload:
     every sequence of the MHA layer forks `samples` samples, and each sample's
@@ -589,6 +624,7 @@ def run_ours(args, ctx):
     if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
         result["gates"] = {name: measure_gate(name, args, device)
                            for name in ("gqa8b_prefix", "longctx_splitk")}
+        result["gates"]["gqa8b_prefix_shared_prefix_entry"] = measure_shared_prefix(device)
     if ctx.rank == 0 and not args.no_trace and ctx.world == 1:
         result["trace"] = {f"B{b}": measure_trace(b, device) for b in (8, 16, 32)}
         torch.cuda.empty_cache()

@@ -204,6 +204,45 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
                            int partition_tokens, void *workspace, size_t workspace_bytes,
                            int dtype, void *stream);
 
+/*
+ * paged_attention_decode_shared_prefix -- decode that reads each shared
+ * prefix once per group of sequences instead of once per sequence.
+ *
+ * Pages "Paged-KV + Continuous Batching From Scratch" (section 1: sequences
+ * that share a system prompt share its physical blocks, a reference-count
+ * bump instead of a copy) and "How a serving engine actually works" (sections
+ * "Copy-on-write, because you have used fork()" and "Prefix caching: prefill
+ * you already did"): sharing saves memory; this entry point also saves the
+ * bandwidth of reading the shared blocks once per sharer.
+ *
+ * Same arguments and results as paged_attention_decode (within the same
+ * tolerance) plus the sharing structure:
+ *   seq_group     int32 [num_seqs], device: prefix group of each sequence, -1
+ *                 for none. Members of a group are consecutive sequences.
+ *   group_prefix  int32 [num_groups], device: the number of leading tokens
+ *                 that every member of the group holds in the SAME physical
+ *                 blocks as the group's first member (the caller's
+ *                 reference-counted prefix); it must not exceed any member's
+ *                 context length (else PAGEDKV_DEVERR_CONTEXT_LEN).
+ * The whole partitions of each prefix (floor(group_prefix / partition_tokens))
+ * are computed once per chunk of up to 8 / (n_q_heads / n_kv_heads) members:
+ * the chunk's (member, query head) pairs fill the columns of one tensor-core
+ * tile, so the prefix's K/V are read once per chunk; the rest of each
+ * sequence is computed per sequence and everything is merged as in split-K.
+ * Requires partition_tokens > 0 (with its workspace) and n_kv_heads a
+ * multiple of 4. The kernel trusts the sharing structure: if a member's
+ * prefix blocks differ from the first member's, its result is computed
+ * with the first member's.
+ */
+int paged_attention_decode_shared_prefix(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         const int32_t *seq_group, const int32_t *group_prefix,
+                                         int num_groups, float scale, void *out, int num_seqs,
+                                         int n_q_heads, int n_kv_heads, int head_dim,
+                                         int num_blocks, int block_size, int max_blocks_per_seq,
+                                         int partition_tokens, void *workspace,
+                                         size_t workspace_bytes, int dtype, void *stream);
+
 /* Workspace bytes paged_attention_decode needs for these sizes (0 when
  * partition_tokens == 0). Returns 0 for invalid sizes as well, and for the
  * balanced split when no CUDA device is current. */

@@ -29,7 +29,7 @@ __all__ = [
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
-    "paged_kv_copy_blocks",
+    "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +42,8 @@ PARTITION_BALANCED = -1            # PAGEDKV_PARTITION_BALANCED
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
-           "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks")
+           "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks",
+           "paged_attention_decode_shared_prefix")
 
 
 class PagedKVError(RuntimeError):
@@ -74,6 +75,10 @@ def load():
     lib.paged_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32,
                                                    i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_attention_decode_noalloc.restype = i32
+    lib.paged_attention_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32,
+                                                         ctypes.c_float, vp, i32, i32, i32, i32,
+                                                         i32, i32, i32, i32, vp, sz, i32, vp]
+    lib.paged_attention_decode_shared_prefix.restype = i32
     lib.paged_kv_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_kv_copy_blocks.restype = i32
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -215,6 +220,36 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr, ws_bytes, _code(q),
         _stream(stream))
     _check(st, "paged_attention_decode")
+
+
+def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, seq_group,
+                                         group_prefix, scale, out, partition_tokens, workspace,
+                                         stream=None):
+    """paged_attention_decode for batches whose consecutive sequences share
+    prefixes: seq_group[s] (int32, -1 = none) names each sequence's group and
+    group_prefix[g] (int32) the tokens every member holds in the group's first
+    member's blocks. Each shared prefix partition is read once per chunk of
+    members instead of once per member. Needs a split (partition_tokens > 0)."""
+    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
+    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
+        raise PagedKVError("q, out and the pools must share one element type")
+    S, Hq, D = q.shape
+    NB, B, Hkv, Dk = k_cache.shape
+    if (Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or
+            context_lens.numel() != S or seq_group.numel() != S):
+        raise PagedKVError("shape mismatch between q, the pools, block_tables, lengths and groups")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().paged_attention_decode_shared_prefix(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), _dev(seq_group, "seq_group", torch.int32),
+        _dev(group_prefix, "group_prefix", torch.int32), group_prefix.numel(), float(scale),
+        _dev(out, "out"), S, Hq, Hkv, D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr,
+        ws_bytes, _code(q), _stream(stream))
+    _check(st, "paged_attention_decode_shared_prefix")
 
 
 def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,

@@ -301,12 +301,13 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
     return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
 }
 
-int paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
-                           const int32_t *block_tables, const int32_t *context_lens, float scale,
-                           void *out, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
-                           int num_blocks, int block_size, int max_blocks_per_seq,
-                           int partition_tokens, void *workspace, size_t workspace_bytes,
-                           int dtype, void *stream) {
+static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *context_lens,
+                       const int32_t *seq_group, const int32_t *group_prefix, int num_groups,
+                       float scale, void *out, int num_seqs, int n_q_heads, int n_kv_heads,
+                       int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                       int partition_tokens, void *workspace, size_t workspace_bytes, int dtype,
+                       void *stream) {
     // ---- shapes
     if (num_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1 || num_blocks < 1 ||
         block_size < 1 || max_blocks_per_seq < 1 || !valid_dtype(dtype) ||
@@ -330,11 +331,18 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PAGEDKV_ERR_INVALID_ARG;
+    // ---- shared prefixes (fixed split, one consumer warp per kv head)
+    const bool prefix = seq_group != nullptr;
+    if (prefix) {
+        if (partition_tokens <= 0 || num_groups < 1 || !group_prefix) return PAGEDKV_ERR_INVALID_ARG;
+        if (!aligned(seq_group, 4) || !aligned(group_prefix, 4)) return PAGEDKV_ERR_INVALID_ARG;
+        if (n_kv_heads % 4 != 0) return PAGEDKV_ERR_UNSUPPORTED;
+    }
     // ---- path
     int path = g_opt_path;
     if (path == pkv::kPathAuto)
-        path = (dtype != PAGEDKV_F32 && group >= g_opt_mma_min_group) ? pkv::kPathMma
-                                                                       : pkv::kPathSimt;
+        path = (dtype != PAGEDKV_F32 && (group >= g_opt_mma_min_group || prefix)) ? pkv::kPathMma
+                                                                                  : pkv::kPathSimt;
     if (path == pkv::kPathMma && dtype == PAGEDKV_F32) return PAGEDKV_ERR_UNSUPPORTED;
     int gmax = 8;
     if (path == pkv::kPathSimt) gmax = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : 8;
@@ -405,6 +413,11 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     p.heads_per_unit = hpu;
     p.log2_hpu = hpu == 4 ? 2 : (hpu == 2 ? 1 : 0);
     p.rows_per_box = block_size < pkv::kTile ? block_size : pkv::kTile;
+    p.seq_group = prefix ? seq_group : nullptr;
+    p.group_prefix = prefix ? group_prefix : nullptr;
+    p.num_groups = prefix ? num_groups : 0;
+    // a shared-prefix unit fills the tensor-core tile's 8 columns with (member, q head) pairs
+    p.max_members = (prefix && path == pkv::kPathMma) ? 8 / group : 1;
     a.head_dim = head_dim;
     a.path = path;
     a.gmax = gmax;
@@ -433,6 +446,39 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
     }
     g_last_path = path;
     return PAGEDKV_OK;
+}
+
+int paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, float scale,
+                           void *out, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int partition_tokens, void *workspace, size_t workspace_bytes,
+                           int dtype, void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0, scale,
+                       out, num_seqs, n_q_heads, n_kv_heads, head_dim, num_blocks, block_size,
+                       max_blocks_per_seq, partition_tokens, workspace, workspace_bytes, dtype,
+                       stream);
+}
+
+int paged_attention_decode_shared_prefix(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         const int32_t *seq_group, const int32_t *group_prefix,
+                                         int num_groups, float scale, void *out, int num_seqs,
+                                         int n_q_heads, int n_kv_heads, int head_dim,
+                                         int num_blocks, int block_size, int max_blocks_per_seq,
+                                         int partition_tokens, void *workspace,
+                                         size_t workspace_bytes, int dtype, void *stream) {
+    if (num_groups < 0 || (num_groups > 0 && (!seq_group || !group_prefix)))
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (num_groups == 0)   // nothing is shared: the ordinary decode
+        return paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                      num_seqs, n_q_heads, n_kv_heads, head_dim, num_blocks,
+                                      block_size, max_blocks_per_seq, partition_tokens, workspace,
+                                      workspace_bytes, dtype, stream);
+    return decode_impl(q, k_cache, v_cache, block_tables, context_lens, seq_group, group_prefix,
+                       num_groups, scale, out, num_seqs, n_q_heads, n_kv_heads, head_dim,
+                       num_blocks, block_size, max_blocks_per_seq, partition_tokens, workspace,
+                       workspace_bytes, dtype, stream);
 }
 
 }  // extern "C"

@@ -12,7 +12,8 @@ static cudaError_t launch_decode_instance(DecodeLaunch &a) {
     auto kernel = paged_decode_kernel<T, D, GM, kMma>;
     const int stage_bytes = decode_stage_bytes(int(sizeof(T)), D, a.p.heads_per_unit);
     const int merge = a.p.heads_per_unit < kConsumerWarps ? 1 : 0;
-    const DecodeSmem lay{stage_bytes, a.p.stages, a.p.num_seqs, D, GM, merge};
+    const DecodeSmem lay{stage_bytes, a.p.stages, a.p.num_seqs, D, GM, merge,
+                         a.p.seq_group != nullptr ? 1 : 0};
     const int smem = lay.request();
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

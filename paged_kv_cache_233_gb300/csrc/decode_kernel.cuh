@@ -178,7 +178,9 @@ struct SimtConsumer {
         i = lane % LPR;
     }
 
-    __device__ void prefetch_q(const T *qrow0, int g) {
+    // q rows of q heads qh0 .. qh0+g-1 of sequence s0 (one sequence per unit on this path)
+    __device__ void prefetch_q(const T *qbase, size_t s0, int qh0, int g, int, int Hq) {
+        const T *qrow0 = qbase + (s0 * Hq + qh0) * D;
 #pragma unroll
         for (int j = 0; j < GM; ++j)
             qn[j] = j < g ? __ldg(reinterpret_cast<const uint4 *>(qrow0 + j * D) + i)
@@ -349,9 +351,13 @@ struct MmaConsumer {
         r8 = lane & 7;
     }
 
-    __device__ void prefetch_q(const T *qrow0, int g) {
-        const bool live = grp < g;
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(qrow0 + grp * D);
+    // Column n of the tile is query head qh0 + n % g of sequence s0 + n / g, for
+    // n < members * g (members > 1 only for units of a shared prefix).
+    __device__ void prefetch_q(const T *qbase, size_t s0, int qh0, int g, int members, int Hq) {
+        const int m = grp / g;
+        const bool live = grp < members * g;
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(
+            qbase + ((s0 + m) * Hq + qh0 + (grp - m * g)) * D);
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             qn[kk][0] = live ? __ldg(row + kk * 8 + c) : 0u;
@@ -460,6 +466,42 @@ struct MmaConsumer {
         }
     }
 
+    // Results of a shared-prefix unit: column n belongs to sequence s0 + n / g;
+    // its state is partial unless that sequence fits in one partition.
+    __device__ void store_members(T *out, float *ws_o, float *ws_m, float *ws_l, const int *seq_len,
+                                  size_t s0, int members, int qh0, int g, int Hq, int P, int part,
+                                  int max_parts) {
+#pragma unroll
+        for (int hsel = 0; hsel < 2; ++hsel) {
+            const int h = 2 * c + hsel;
+            if (h >= members * g) continue;
+            const int mem = h / g;
+            const size_t sm = s0 + mem;
+            const int qh = qh0 + h - mem * g;
+            if (seq_len[sm] > P) {
+                const size_t row = (sm * Hq + qh) * max_parts + part;
+                float *dst = ws_o + row * D;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    dst[t * 16 + grp] = o[t][hsel];
+                    dst[t * 16 + grp + 8] = o[t][2 + hsel];
+                }
+                if (grp == 0) {
+                    ws_m[row] = m[hsel] * kLn2;
+                    ws_l[row] = lp[hsel];
+                }
+            } else {
+                const float inv = lp[hsel] > 0.f ? 1.f / lp[hsel] : 0.f;
+                T *dst = out + (sm * Hq + qh) * D;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    dst[t * 16 + grp] = Elem<T>::from_float(o[t][hsel] * inv);
+                    dst[t * 16 + grp + 8] = Elem<T>::from_float(o[t][2 + hsel] * inv);
+                }
+            }
+        }
+    }
+
     __device__ void stash(float *mo, float *mm, float *ml, int g, int stride) {
         const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
@@ -489,6 +531,7 @@ struct Unit {
     int part;       // fixed partitions: partition index within the sequence
     bool partial;   // the result is a partition state, not the final row
     int slot;       // balanced split: which of this CTA's two piece slots
+    int members;    // sequences s .. s+members-1 whose queries the unit serves (shared prefix)
 };
 
 // This CTA's units, in order (producer and consumers walk identical copies).
@@ -503,20 +546,30 @@ struct Unit {
 struct Walk {
     const int *seq_base;   // per-sequence prefix sums of units (fixed) or tiles (balanced)
     const int *seq_len;
+    const int *seq_p0;     // shared prefixes: first partition a sequence reads itself
+    const int *seq_pu;     // shared prefixes: prefix units the sequence leads
+    const int32_t *seq_group;
+    int S, max_members;
     int groups, P, split, balanced;
     int s, pos, end, stride, count;
 
-    __device__ void init(const int *base, const int *len, int S, int groups_, int P_, int split_,
-                         int balanced_) {
+    __device__ void init(const int *base, const int *len, int S_, int groups_, int P_, int split_,
+                         int balanced_, const int *p0 = nullptr, const int *pu = nullptr,
+                         const int32_t *group = nullptr, int max_members_ = 1) {
         seq_base = base;
         seq_len = len;
+        seq_p0 = p0;
+        seq_pu = pu;
+        seq_group = group;
+        S = S_;
+        max_members = max_members_;
         groups = groups_;
         P = P_;
         split = split_;
         balanced = balanced_;
         s = 0;
         count = 0;
-        const long long total = base[S];
+        const long long total = base[S_];
         if (balanced) {
             pos = int(total * blockIdx.x / gridDim.x);
             end = int(total * (blockIdx.x + 1) / gridDim.x);
@@ -547,15 +600,35 @@ struct Walk {
             x.ntiles = tl - tf;
             x.partial = !(tf == 0 && tl == nt);
             x.slot = count == 0 ? 0 : 1;
+            x.members = 1;
             pos += tl - tf;
         } else {
-            x.part = rr / groups;
-            x.hg = rr - x.part * groups;
-            x.t0 = x.part * P;
-            x.t1 = min(x.L, x.t0 + P);
-            x.ntiles = (x.t1 - x.t0 + kTile - 1) / kTile;
-            x.partial = split && x.L > P;
+            const int pu = seq_pu ? seq_pu[s] : 0;
             x.slot = 0;
+            if (rr < pu) {
+                // a partition of a shared prefix, for up to max_members sequences of the group
+                x.part = rr / groups;
+                x.hg = rr - x.part * groups;
+                x.t0 = x.part * P;
+                x.t1 = x.t0 + P;
+                x.ntiles = P / kTile;
+                int m = 1;
+                const int32_t grp = __ldg(seq_group + s);
+                while (m < max_members && s + m < S && __ldg(seq_group + s + m) == grp) ++m;
+                x.members = m;
+                // a one-member unit is an ordinary partition of that sequence
+                x.partial = m > 1 || (split && x.L > P);
+            } else {
+                const int r2 = rr - pu;
+                const int p0 = seq_p0 ? seq_p0[s] : 0;
+                x.part = p0 + r2 / groups;
+                x.hg = r2 - (r2 / groups) * groups;
+                x.t0 = x.part * P;
+                x.t1 = min(x.L, x.t0 + P);
+                x.ntiles = max(0, (x.t1 - x.t0 + kTile - 1) / kTile);
+                x.members = 1;
+                x.partial = split && x.L > P;
+            }
             pos += stride;
         }
         ++count;
@@ -581,12 +654,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int TL = kConsumerWarps >> p.log2_hpu;          // consumer warps per kv head
     const int half_bytes = H * G::kHeadBytes;            // K (or V) part of a stage
     const int stage_bytes = 2 * half_bytes;
-    const DecodeSmem lay{stage_bytes, NS, S, D, GM, TL > 1 ? 1 : 0};
+    const DecodeSmem lay{stage_bytes, NS, S, D, GM, TL > 1 ? 1 : 0, p.seq_group != nullptr ? 1 : 0};
     const uint32_t full0 = base + lay.bars();
     const uint32_t empty0 = full0 + 8 * NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + lay.flag());
     int *seq_base = reinterpret_cast<int *>(sm + lay.seq_base());
     int *seq_len = reinterpret_cast<int *>(sm + lay.seq_len());
+    int *seq_p0 = reinterpret_cast<int *>(sm + lay.seq_p0());
+    int *seq_pu = reinterpret_cast<int *>(sm + lay.seq_pu());
+    const bool prefix = p.seq_group != nullptr;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -611,16 +687,51 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         // groups (fixed mode), or 16-token tiles x head groups (balanced mode)
         const int cap = p.max_blocks * B;
         int carry = 0;
+        int run_carry = -1;   // start of the group run in progress (shared prefixes)
         if (lane == 0) seq_base[0] = 0;
         for (int s0 = 0; s0 < S; s0 += 32) {
             const int s = s0 + lane;
             int cnt = 0;
+            int Lc = 0;
             if (s < S) {
                 const int L = p.context_lens[s];
-                const int Lc = min(max(L, 0), cap);
+                Lc = min(max(L, 0), cap);
                 if (Lc != L) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
                 seq_len[s] = Lc;
                 cnt = (p.balanced ? (Lc + kTile - 1) / kTile : (Lc > 0 ? (Lc + P - 1) / P : 1)) * groups;
+            }
+            if (prefix) {
+                // group runs: a run starts where the group id changes; sequence s is
+                // member (s - run start) of its run; every max_members-th member leads
+                // the units of the run's shared prefix partitions
+                int gsel = s < S ? p.seq_group[s] : -1;
+                if (gsel >= p.num_groups) {
+                    atomicOr(p.err, PAGEDKV_DEVERR_SEQ_INDEX);
+                    gsel = -1;
+                }
+                const int prev = (s > 0 && s < S) ? p.seq_group[s - 1] : -1;
+                int f = (gsel >= 0 && prev != gsel) ? s : -1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(kFull, f, off);
+                    if (lane >= off) f = max(f, y);
+                }
+                const int run_start = max(f, run_carry);
+                run_carry = __shfl_sync(kFull, run_start, 31);
+                if (s < S) {
+                    int p0 = 0, pu = 0;
+                    if (gsel >= 0) {
+                        const int want = p.group_prefix[gsel];
+                        const int Lp = min(max(want, 0), cap);
+                        if (want > Lc) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
+                        p0 = Lp / P;
+                        if ((s - run_start) % p.max_members == 0) pu = p0 * groups;
+                    }
+                    const int own = Lc > 0 ? max(0, (Lc + P - 1) / P - p0) : (p0 > 0 ? 0 : 1);
+                    cnt = pu + own * groups;
+                    seq_p0[s] = p0;
+                    seq_pu[s] = pu;
+                }
             }
             int x = cnt;
 #pragma unroll
@@ -634,7 +745,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     __syncthreads();
     Walk walk;
-    walk.init(seq_base, seq_len, S, groups, P, p.split, p.balanced);
+    walk.init(seq_base, seq_len, S, groups, P, p.split, p.balanced, prefix ? seq_p0 : nullptr,
+              prefix ? seq_pu : nullptr, p.seq_group, p.max_members);
     if (!walk.has_work()) return;
     // a dependent merge launch may start once every CTA got here or exited;
     // it waits on this grid's completion before reading the partition states
@@ -751,7 +863,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const T *qbase = reinterpret_cast<const T *>(p.q);
     Unit cur;
     walk.next(cur);
-    st.prefetch_q(qbase + (size_t(cur.s) * p.n_q_heads + ((cur.hg << p.log2_hpu) + hh) * g) * D, g);
+    st.prefetch_q(qbase, size_t(cur.s), ((cur.hg << p.log2_hpu) + hh) * g, g, cur.members, p.n_q_heads);
     for (;; ++unit_count) {
         const int qh0 = ((cur.hg << p.log2_hpu) + hh) * g;   // first q head of this warp
         if constexpr (kMma) st.begin_unit();
@@ -759,7 +871,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         Unit nx;
         const bool has_next = walk.next(nx);
         if (has_next)
-            st.prefetch_q(qbase + (size_t(nx.s) * p.n_q_heads + ((nx.hg << p.log2_hpu) + hh) * g) * D, g);
+            st.prefetch_q(qbase, size_t(nx.s), ((nx.hg << p.log2_hpu) + hh) * g, g, nx.members, p.n_q_heads);
         for (int i = 0; i < cur.ntiles; ++i) {
             int good = !*abort_flag;
             if (good) good = mbar_wait(full0 + 8 * stage, phase, p.err);
@@ -809,7 +921,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         if constexpr (kMma) st.reduce();
         else st.reduce(g);
-        if (TL == 1) {
+        if (cur.members > 1) {
+            // shared-prefix unit (tensor-core path, one consumer warp per kv head)
+            if constexpr (kMma)
+                st.store_members(reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, seq_len,
+                                 size_t(cur.s), cur.members, qh0, g, p.n_q_heads, P, cur.part,
+                                 p.max_parts);
+        } else if (TL == 1) {
             if constexpr (kMma) st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g);
             else st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g, lane);
         } else {

@@ -44,18 +44,27 @@ struct DecodeParams {
     int heads_per_unit;   // kv heads per unit: 1, 2 or 4 (one consumer warp per head)
     int log2_hpu;
     int rows_per_box;     // tokens per TMA box: min(block_size, kTile)
+    // shared prefixes (fixed split only): consecutive sequences of one group hold
+    // their first group_prefix[g] tokens in the same physical blocks
+    const int32_t *seq_group;     // [num_seqs], -1 = no group; null = feature off
+    const int32_t *group_prefix;  // [num_groups] tokens
+    int num_groups;
+    int max_members;      // sequences whose queries one prefix unit serves
 };
 
 // Byte layout of the dynamic shared memory (host and device agree on it).
-// merge == 0 when every consumer warp owns a whole head (no cross-warp merge).
+// merge == 0 when every consumer warp owns a whole head (no cross-warp merge);
+// prefix == 1 adds two per-sequence arrays for shared-prefix units.
 struct DecodeSmem {
-    int stage_bytes, stages, seqs, head_dim, gmax, merge;
+    int stage_bytes, stages, seqs, head_dim, gmax, merge, prefix;
     __host__ __device__ int ring() const { return stages * stage_bytes; }
     __host__ __device__ int bars() const { return ring(); }                        // full, empty
     __host__ __device__ int flag() const { return bars() + 16 * stages; }
     __host__ __device__ int seq_base() const { return flag() + 16; }               // seqs + 1 ints
     __host__ __device__ int seq_len() const { return seq_base() + 4 * (seqs + 1); }
-    __host__ __device__ int merge_o() const { return (seq_len() + 4 * seqs + 15) & ~15; }
+    __host__ __device__ int seq_p0() const { return seq_len() + 4 * seqs; }        // first own partition
+    __host__ __device__ int seq_pu() const { return seq_p0() + (prefix ? 4 * seqs : 0); }  // prefix units led
+    __host__ __device__ int merge_o() const { return (seq_pu() + (prefix ? 4 * seqs : 0) + 15) & ~15; }
     __host__ __device__ int row_stride() const { return head_dim + 4; }            // floats
     // two slots (double buffer) x consumer warps x gmax heads
     __host__ __device__ int merge_rows() const { return merge ? 2 * kConsumerWarps * gmax : 0; }
