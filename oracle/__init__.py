@@ -67,6 +67,10 @@ class Oracle:
         lib.oracle_copy_blocks.restype = ctypes.c_int64
         lib.oracle_copy_blocks.argtypes = [_c_u8p, _c_u8p, _c_i32p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64]
+        lib.oracle_swap_blocks.restype = ctypes.c_int64
+        lib.oracle_swap_blocks.argtypes = [_c_u8p, _c_u8p, ctypes.c_int64, _c_u8p, _c_u8p,
+                                           ctypes.c_int64, _c_i32p, ctypes.c_int64,
+                                           ctypes.c_int64]
         lib.oracle_gather.restype = None
         lib.oracle_gather.argtypes = [ctypes.c_void_p, _c_i32p, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -154,6 +158,23 @@ class Oracle:
         return self.lib.oracle_copy_blocks(_ptr(k_cache, _c_u8p), _ptr(v_cache, _c_u8p),
                                            _ptr(pr, _c_i32p), pr.shape[0], k_cache.shape[0],
                                            block_bytes)
+
+    # -- swap between pools ---------------------------------------------------------
+    def swap_blocks(self, src_k, src_v, dst_k, dst_v, pairs):
+        """Copy whole blocks from the source pools into the destination pools
+        (pairs [n][2] = (source block, destination block)), in order, in place.
+        Returns the number of pairs skipped for ids outside their pool."""
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        for c in (src_k, src_v, dst_k, dst_v):
+            if not c.flags.c_contiguous:
+                raise ValueError("pools must be contiguous")
+        block_bytes = src_k.dtype.itemsize * int(np.prod(src_k.shape[1:]))
+        if dst_k.dtype.itemsize * int(np.prod(dst_k.shape[1:])) != block_bytes:
+            raise ValueError("source and destination blocks differ in size")
+        return self.lib.oracle_swap_blocks(_ptr(src_k, _c_u8p), _ptr(src_v, _c_u8p),
+                                           src_k.shape[0], _ptr(dst_k, _c_u8p),
+                                           _ptr(dst_v, _c_u8p), dst_k.shape[0],
+                                           _ptr(pr, _c_i32p), pr.shape[0], block_bytes)
 
     # -- gather -------------------------------------------------------------------
     def gather(self, cache, block_tables, seq, length, kv_head, dtype):

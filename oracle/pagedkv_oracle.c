@@ -27,6 +27,13 @@
  *     still reference gets a fresh block; the fresh block must first hold the
  *     shared block's contents. Whole-block copy, K and V, pairs in order.
  *
+ *   oracle_swap_blocks
+ *     "Paged Attention and the Block Manager", section "Running out of memory
+ *     becomes a scheduling decision": a preempted sequence can keep its cache
+ *     by having it copied out to host memory and back in later. The copy moves
+ *     whole blocks (K and V) from one pool to another pool of the same block
+ *     shape; the two pools may hold different numbers of blocks.
+ *
  *   oracle_gather
  *     "Paged Attention and the Block Manager", section "The measurement": a
  *     sequence's cache is copied out of its blocks, in logical order, into a
@@ -192,6 +199,30 @@ int64_t oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pa
         }
         memcpy(k_cache + dst * block_bytes, k_cache + src * block_bytes, (size_t)block_bytes);
         memcpy(v_cache + dst * block_bytes, v_cache + src * block_bytes, (size_t)block_bytes);
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Swap: copy whole blocks (K and V) from one pool into another.             */
+/* ------------------------------------------------------------------------ */
+
+/* pairs: [num_pairs][2] = {block in the source pools, block in the destination
+ * pools}. Returns the number of pairs skipped because an id was outside its
+ * pool. */
+int64_t oracle_swap_blocks(const uint8_t *src_k, const uint8_t *src_v, int64_t src_blocks,
+                           uint8_t *dst_k, uint8_t *dst_v, int64_t dst_blocks,
+                           const int32_t *pairs, int64_t num_pairs, int64_t block_bytes)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t from = pairs[2 * i], to = pairs[2 * i + 1];
+        if (from < 0 || from >= src_blocks || to < 0 || to >= dst_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy(dst_k + to * block_bytes, src_k + from * block_bytes, (size_t)block_bytes);
+        memcpy(dst_v + to * block_bytes, src_v + from * block_bytes, (size_t)block_bytes);
     }
     return bad;
 }

@@ -231,6 +231,64 @@ def pin_copy_blocks(orc):
         assert k.tobytes() == ek.tobytes() and v.tobytes() == ev.tobytes()
 
 
+def pin_swap_blocks(orc):
+    """Swap between pools of different sizes: each destination block equals
+    numpy's whole-block assignment from its source, every other block keeps
+    its bytes, and a pair with an id outside its own pool is skipped."""
+    rng = np.random.default_rng(12)
+    B, Hkv, D = 4, 2, 8
+    for dtype in ("f16", "bf16"):
+        dk = to_storage(rng.standard_normal((9, B, Hkv, D)), dtype)
+        dv = to_storage(rng.standard_normal((9, B, Hkv, D)), dtype)
+        hk = poison((5, B, Hkv, D), dtype)
+        hv = poison((5, B, Hkv, D), dtype)
+        # device -> host: 7 is valid on the device, 4 on the host; 8 -> 5 and
+        # 2 -> 6 name host blocks that do not exist, 9 a device block that does not
+        pairs = np.array([[7, 4], [2, 0], [8, 5], [9, 1], [2, 6]], np.int32)
+        ek, ev = hk.copy(), hv.copy()
+        ek[4], ev[4] = dk[7], dv[7]
+        ek[0], ev[0] = dk[2], dv[2]
+        dk0, dv0 = dk.copy(), dv.copy()
+        assert orc.swap_blocks(dk, dv, hk, hv, pairs) == 3
+        assert hk.tobytes() == ek.tobytes() and hv.tobytes() == ev.tobytes()
+        assert dk.tobytes() == dk0.tobytes() and dv.tobytes() == dv0.tobytes()
+        # host -> device into other blocks
+        back = np.array([[4, 1], [0, 8]], np.int32)
+        ek, ev = dk.copy(), dv.copy()
+        ek[1], ev[1] = dk0[7], dv0[7]
+        ek[8], ev[8] = dk0[2], dv0[2]
+        assert orc.swap_blocks(hk, hv, dk, dv, back) == 0
+        assert dk.tobytes() == ek.tobytes() and dv.tobytes() == ev.tobytes()
+
+
+def pin_swap_preserves_decode(orc):
+    """"Paged Attention and the Block Manager", section "Running out of memory
+    becomes a scheduling decision": a preempted sequence's blocks go out to
+    host memory and come back later, into whichever blocks are free then. With
+    its block table rewritten to the new blocks it decodes exactly as before,
+    and as the contiguous attention over its tokens."""
+    case = paged_case(13, [37, 50, 9], 8, 4, 2, 16, "bf16", spare_blocks=10)
+    before = run_decode(orc, case)
+    assert np.abs(before - brute_force(case)).max() < 1e-12
+    s = 1
+    n = -(-int(case["lens"][s]) // case["B"])
+    victim = case["bt"][s, :n].copy()
+    shape = (n + 2,) + case["k"].shape[1:]
+    hk, hv = poison(shape, "bf16"), poison(shape, "bf16")
+    host_ids = np.arange(2, n + 2, dtype=np.int32)
+    assert orc.swap_blocks(case["k"], case["v"], hk, hv, np.stack([victim, host_ids], 1)) == 0
+    used = set(case["bt"][case["bt"] >= 0].tolist())
+    free = [b for b in range(case["NB"]) if b not in used]
+    for b in victim:                       # the freed blocks are reused by others
+        case["k"][b] = NAN_BITS_BF16
+        case["v"][b] = NAN_BITS_BF16
+    new_ids = np.array(free[:n], np.int32)
+    assert orc.swap_blocks(hk, hv, case["k"], case["v"], np.stack([host_ids, new_ids], 1)) == 0
+    case["bt"][s, :n] = new_ids
+    after = run_decode(orc, case)
+    assert after.tobytes() == before.tobytes()
+
+
 def pin_fork_copy_on_write(orc):
     """The serving page's fork: samples share the prompt's blocks; each sample's
     first token triggers a copy of the shared last block into a fresh one. After
@@ -404,7 +462,8 @@ def pin_partition_merge(orc):
 
 
 ALL_PINS = [pin_f16_decoding, pin_bf16_decoding, pin_block_table_example, pin_slot_bijection,
-            pin_append_scatter, pin_copy_blocks, pin_fork_copy_on_write, pin_gather_order,
+            pin_append_scatter, pin_copy_blocks, pin_swap_blocks, pin_swap_preserves_decode,
+            pin_fork_copy_on_write, pin_gather_order,
             pin_decode_bruteforce,
             pin_block_permutation_invariance, pin_shared_prefix, pin_special_cases,
             pin_partition_merge]

@@ -55,6 +55,10 @@ MUTANTS = {
     "copy_only_keys": ("        memcpy(v_cache + dst * block_bytes, v_cache + src * block_bytes, (size_t)block_bytes);\n", ""),
     "copy_direction_swapped": ("memcpy(k_cache + dst * block_bytes, k_cache + src * block_bytes",
                                "memcpy(k_cache + src * block_bytes, k_cache + dst * block_bytes"),
+    "swap_destination_index": ("memcpy(dst_k + to * block_bytes, src_k + from * block_bytes",
+                               "memcpy(dst_k + from * block_bytes, src_k + from * block_bytes"),
+    "swap_bounds_one_pool": ("to < 0 || to >= dst_blocks", "to < 0 || to >= src_blocks"),
+    "swap_only_keys": ("        memcpy(dst_v + to * block_bytes, src_v + from * block_bytes, (size_t)block_bytes);\n", ""),
 }
 
 
