@@ -559,6 +559,59 @@ def measure_cow(device, samples=4, reps=50):
             "gbs": moved / ms / 1e6}
 
 
+def measure_swap(device, reps=20):
+    """Swap preemption over the bench workload: the blocks of a quarter of the
+    MHA layer's sequences go out to a pinned host pool and back in, one call per
+    direction. Compared with the copy engine moving the same bytes as one
+    contiguous copy between the same kinds of memory (the link's practical rate)."""
+    import paged_kv_cache_233_gb300 as pk
+    wl = preset("mha7b")
+    shape = (wl.num_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim)
+    kc = torch.randn(shape, device=device).to(wl.torch_dtype)
+    vc = torch.randn(shape, device=device).to(wl.torch_dtype)
+    victims = range(0, wl.num_seqs, 4)
+    src = np.concatenate([wl.block_tables[s][wl.block_tables[s] >= 0] for s in victims])
+    n = len(src)
+    hk = torch.empty((n,) + shape[1:], dtype=wl.torch_dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    host_ids = np.arange(n, dtype=np.int32)
+    out_pairs = torch.from_numpy(np.stack([src, host_ids], 1).astype(np.int32)).to(device)
+    in_pairs = torch.from_numpy(np.stack([host_ids, src], 1).astype(np.int32)).to(device)
+    block_bytes = wl.block_size * wl.row_bytes
+    moved = 2 * n * block_bytes                        # K and V blocks across the link
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    out_ms = timed(lambda: pk.paged_kv_swap_blocks(kc, vc, hk, hv, out_pairs))
+    in_ms = timed(lambda: pk.paged_kv_swap_blocks(hk, hv, kc, vc, in_pairs))
+    dev_buf = torch.empty(moved, dtype=torch.uint8, device=device)
+    host_buf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    ce_out_ms = timed(lambda: host_buf.copy_(dev_buf, non_blocking=True))
+    ce_in_ms = timed(lambda: dev_buf.copy_(host_buf, non_blocking=True))
+    assert pk.device_errors() == 0
+    del kc, vc, dev_buf
+    torch.cuda.empty_cache()
+    res = {"blocks": int(n), "bytes_per_direction": int(moved),
+           "out_us": out_ms * 1e3, "in_us": in_ms * 1e3,
+           "out_gbs": moved / out_ms / 1e6, "in_gbs": moved / in_ms / 1e6,
+           "copy_engine_out_gbs": moved / ce_out_ms / 1e6,
+           "copy_engine_in_gbs": moved / ce_in_ms / 1e6}
+    res["out_frac_of_copy_engine"] = res["out_gbs"] / res["copy_engine_out_gbs"]
+    res["in_frac_of_copy_engine"] = res["in_gbs"] / res["copy_engine_in_gbs"]
+    return res
+
+
 def run_ours(args, ctx):
     import paged_kv_cache_233_gb300 as pk
     from paged_kv_cache_233_gb300 import build as pk_build
@@ -629,6 +682,7 @@ def run_ours(args, ctx):
         result["trace"] = {f"B{b}": measure_trace(b, device) for b in (8, 16, 32)}
         torch.cuda.empty_cache()
         result["cow_copy"] = measure_cow(device)
+        result["swap"] = measure_swap(device)
     if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
         import oracle
         orc = oracle.get()

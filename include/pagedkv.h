@@ -143,6 +143,38 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pair
                          void *stream);
 
 /*
+ * paged_kv_swap_blocks -- copy whole blocks from one pair of pools into another.
+ *
+ * Page "Paged Attention and the Block Manager", section "Running out of memory
+ * becomes a scheduling decision": a preempted sequence can keep its cache by
+ * having its blocks copied out to host memory, and copied back on re-admission
+ * into whichever device blocks are free then. For each pair i, block
+ * block_pairs[2i] of the source pools is copied to block block_pairs[2i+1] of
+ * the destination pools, K and V: a bit copy. One call covers every pair.
+ *
+ *   src_k, src_v    [src_num_blocks][block_size][n_kv_heads][head_dim] of dtype
+ *   dst_k, dst_v    [dst_num_blocks][block_size][n_kv_heads][head_dim] of dtype,
+ *                   updated in place
+ *   block_pairs     int32 [num_pairs][2] = {source block, destination block}
+ *
+ * Every pointer may be memory of the current device, managed memory, or
+ * page-locked host memory (cudaHostAlloc, cudaHostRegister, a pinned torch
+ * tensor), which the kernel reads or writes in place over the host link; pool
+ * pointers must be 16-byte aligned. Pageable host memory or another device's
+ * memory: PAGEDKV_ERR_INVALID_ARG, nothing launched. Host memory must stay
+ * allocated and page-locked until the copy has completed on `stream`.
+ *
+ * A pair with an id outside its own pool is skipped and sets
+ * PAGEDKV_DEVERR_BLOCK_ID. Destinations must be distinct; when a source and a
+ * destination pool are the same memory, no block may be both a source and a
+ * destination of one call (such pairs race).
+ */
+int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_blocks, void *dst_k,
+                         void *dst_v, int dst_num_blocks, const int32_t *block_pairs,
+                         int num_pairs, int block_size, int n_kv_heads, int head_dim, int dtype,
+                         void *stream);
+
+/*
  * paged_attention_decode -- fused paged-attention decode.
  *
  * The kernel the pages name as the next step and never build (page "Paged-KV +

@@ -29,7 +29,7 @@ __all__ = [
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
-    "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix",
+    "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +81,8 @@ def load():
     lib.paged_attention_decode_shared_prefix.restype = i32
     lib.paged_kv_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_kv_copy_blocks.restype = i32
+    lib.paged_kv_swap_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
+    lib.paged_kv_swap_blocks.restype = i32
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -177,6 +179,43 @@ def paged_kv_copy_blocks(k_cache, v_cache, block_pairs, stream=None):
         _dev(block_pairs, "block_pairs", torch.int32), block_pairs.shape[0], NB, B, Hkv, D,
         _code(k_cache), _stream(stream))
     _check(st, "paged_kv_copy_blocks")
+
+
+def _reachable(t, name, dtype=None):
+    """A tensor the GPU can address in place: CUDA memory or pinned host memory."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_contiguous():
+        raise PagedKVError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PagedKVError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda and not t.is_pinned():
+        raise PagedKVError(f"{name} must be a CUDA tensor or pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def paged_kv_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
+    """Copy whole blocks block_pairs[i][0] of the source pools to block_pairs[i][1]
+    of the destination pools (swap-out to pinned host pools, or swap-in back).
+
+    Pools are [NB][B][Hkv][D] of one element type; source and destination may
+    hold different numbers of blocks. Any argument may live in CUDA memory or in
+    pinned host memory; the copy runs on the GPU, asynchronously on `stream`.
+    """
+    for a, b, what in ((src_k, src_v, "source"), (dst_k, dst_v, "destination")):
+        if a.dim() != 4 or a.shape != b.shape or a.dtype != b.dtype:
+            raise PagedKVError(f"expected {what} pools [NB][B][Hkv][D] of one element type")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
+        raise PagedKVError("source and destination blocks differ in shape or element type")
+    if block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise PagedKVError("block_pairs must be [n][2]")
+    _, B, Hkv, D = src_k.shape
+    st = load().paged_kv_swap_blocks(
+        _reachable(src_k, "src_k"), _reachable(src_v, "src_v"), src_k.shape[0],
+        _reachable(dst_k, "dst_k"), _reachable(dst_v, "dst_v"), dst_k.shape[0],
+        _reachable(block_pairs, "block_pairs", torch.int32), block_pairs.shape[0], B, Hkv, D,
+        _code(src_k), _stream(stream))
+    _check(st, "paged_kv_swap_blocks")
 
 
 def paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq, block_size,

@@ -24,6 +24,10 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
                                int num_blocks, long long block_bytes, int num_sms,
                                unsigned int *err, cudaStream_t st);
+cudaError_t launch_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               const int32_t *pairs, int num_pairs, int src_blocks,
+                               int dst_blocks, long long block_bytes, int num_sms,
+                               unsigned int *err, cudaStream_t st);
 }  // namespace pkv
 
 // Sticky error word, one per device that loads the library.
@@ -279,6 +283,66 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pair
     const cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs,
                                                   num_blocks, block_bytes, sms, err,
                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The address through which the current device reaches `p`, or null when it
+// cannot: memory of this device, managed memory, or page-locked host memory
+// mapped into the device's address space. Pageable host memory and other
+// devices' memory are refused.
+const void *device_view(const void *p) {
+    if (!p) return nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice: return a.device == dev ? p : nullptr;
+    case cudaMemoryTypeManaged: return p;
+    case cudaMemoryTypeHost: return a.devicePointer;
+    default: return nullptr;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_blocks, void *dst_k,
+                         void *dst_v, int dst_num_blocks, const int32_t *block_pairs,
+                         int num_pairs, int block_size, int n_kv_heads, int head_dim, int dtype,
+                         void *stream) {
+    if (num_pairs < 0 || src_num_blocks < 1 || dst_num_blocks < 1 || block_size < 1 ||
+        n_kv_heads < 1 || head_dim < 1 || !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    const long long block_bytes = (long long)block_size * n_kv_heads * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PAGEDKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PAGEDKV_OK;
+    const void *sk = device_view(src_k), *sv = device_view(src_v);
+    void *dk = const_cast<void *>(device_view(dst_k));
+    void *dv = const_cast<void *>(device_view(dst_v));
+    const int32_t *pairs = static_cast<const int32_t *>(device_view(block_pairs));
+    if (!sk || !sv || !dk || !dv || !pairs) return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(sk, 16) || !aligned(sv, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(pairs, 4))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    const cudaError_t e = pkv::launch_swap_blocks(sk, sv, dk, dv, pairs, num_pairs,
+                                                  src_num_blocks, dst_num_blocks, block_bytes,
+                                                  sms, err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 

@@ -93,6 +93,27 @@ def test_append_and_slot_mapping_reject_bad_arguments(lib):
     assert lib.paged_kv_slot_mapping(vp(0), vp(0), vp(0), vp(0), 0, 2, 4, 16, 8, None) == 0
 
 
+def test_swap_and_copy_blocks_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    # a block of 1 token x 1 head x 3 fp16 elements (6 bytes) is not a multiple of 16
+    assert lib.paged_kv_swap_blocks(vp(16), vp(16), 4, vp(16), vp(16), 4, vp(16), 2, 1, 1, 3, 1,
+                                    None) == INVALID
+    assert lib.paged_kv_swap_blocks(vp(16), vp(16), 0, vp(16), vp(16), 4, vp(16), 2, 8, 1, 8, 1,
+                                    None) == INVALID
+    assert lib.paged_kv_swap_blocks(vp(16), vp(16), 4, vp(16), vp(16), 4, vp(16), -1, 8, 1, 8, 1,
+                                    None) == INVALID
+    assert lib.paged_kv_swap_blocks(vp(16), vp(16), 4, vp(16), vp(16), 4, vp(16), 2, 8, 1, 8, 7,
+                                    None) == INVALID
+    assert lib.paged_kv_swap_blocks(vp(0), vp(0), 4, vp(0), vp(0), 4, vp(0), 0, 8, 1, 8, 1,
+                                    None) == 0
+    # a pool the device cannot reach (no device here at all, or pageable memory)
+    buf = (ctypes.c_uint8 * 4096)()
+    a = ctypes.cast(buf, vp)
+    assert lib.paged_kv_swap_blocks(a, a, 4, a, a, 4, a, 1, 8, 1, 8, 1, None) == INVALID
+    assert lib.paged_kv_copy_blocks(vp(16), vp(16), vp(16), 1, 4, 1, 1, 3, 1, None) == INVALID
+    assert lib.paged_kv_copy_blocks(vp(0), vp(0), vp(0), 0, 4, 8, 1, 8, 1, None) == 0
+
+
 def test_workspace_size_follows_the_documented_layout(lib):
     def r256(x):
         return (x + 255) // 256 * 256
@@ -122,6 +143,9 @@ def test_options_round_trip(lib):
 
 def test_tensors_must_be_on_the_gpu(lib):
     import torch
+    h = torch.zeros(8, 16, 2, 64)     # pageable host memory: the swap refuses it too
+    with pytest.raises(pk.PagedKVError, match="pinned"):
+        pk.paged_kv_swap_blocks(h, h, h, h, torch.zeros(1, 2, dtype=torch.int32))
     x = torch.zeros(4, 2, 64)
     with pytest.raises(pk.PagedKVError, match="CUDA"):
         pk.paged_kv_append(x, x, torch.zeros(4, dtype=torch.int64), torch.zeros(8, 16, 2, 64),

@@ -133,3 +133,75 @@ def test_continuous_batching_trace_invariants(block_size, n_blocks, slots):
         assert all(b.victims_were_newest)
     else:
         assert b.total_preemptions == 0
+
+
+def replay_token_placement(plans, block_size):
+    """Follow every token's label (request, position) through the plans' swap-ins,
+    swap-outs and appends, in the device's order, and check that each decoded
+    row finds exactly its own tokens at the slots its block table names."""
+    dev, host = {}, {}
+    B = block_size
+
+    def move(src, dst, pairs):
+        for a, b in pairs:
+            for o in range(B):
+                if (a, o) in src:
+                    dst[(b, o)] = src[(a, o)]
+                else:
+                    dst.pop((b, o), None)
+
+    for plan in plans:
+        move(host, dev, plan.swap_in.tolist())
+        move(dev, host, plan.swap_out.tolist())
+        for row, pos in zip(plan.token_row.tolist(), plan.token_pos.tolist()):
+            blk = int(plan.block_tables[row, pos // B])
+            dev[(blk, pos % B)] = (plan.rids[row], pos)
+        for b, rid in enumerate(plan.rids):
+            for pos in range(int(plan.context_lens[b])):
+                blk = int(plan.block_tables[b, pos // B])
+                assert dev.get((blk, pos % B)) == (rid, pos), (plan.step, rid, pos)
+
+
+@pytest.mark.parametrize("preempt", ["recompute", "swap"])
+@pytest.mark.parametrize("block_size,n_blocks,slots", [(16, 48, 8), (8, 96, 16), (32, 24, 6)])
+def test_plans_keep_every_token_in_place(preempt, block_size, n_blocks, slots):
+    reqs = synthetic_requests(24, seed=5, prompt_lo=32, prompt_hi=300)
+    b = ContinuousBatcher(reqs, slots, n_blocks, block_size, preempt=preempt,
+                          host_blocks=4 * n_blocks)
+    plans = b.run()
+    assert b.total_preemptions > 0
+    replay_token_placement(plans, block_size)
+    for r in reqs:
+        assert r.delivered == list(range(r.prompt_len, r.prompt_len + r.output_len))
+    assert b.alloc.n_free == b.alloc.n_blocks
+    if preempt == "swap":
+        assert b.swapped_out_blocks > 0
+        assert b.swapped_in_blocks == b.swapped_out_blocks
+        assert b.host.n_free == b.host.n_blocks and not b.swapped
+    else:
+        assert all(len(p.swap_in) == 0 and len(p.swap_out) == 0 for p in plans)
+
+
+def test_swap_appends_less_than_recompute():
+    """Swapped-in sequences are not re-appended: the same trace appends fewer
+    tokens than with recompute, and decodes the same (request, position) rows."""
+    def run(mode):
+        reqs = synthetic_requests(24, seed=5, prompt_lo=32, prompt_hi=300)
+        b = ContinuousBatcher(reqs, 8, 48, 16, preempt=mode, host_blocks=256)
+        plans = b.run()
+        rows = sorted((rid, int(p.query_pos[i])) for p in plans for i, rid in enumerate(p.rids))
+        return b, sum(len(p.token_row) for p in plans), rows
+    rb, r_tokens, r_rows = run("recompute")
+    sb, s_tokens, s_rows = run("swap")
+    assert r_rows == s_rows
+    assert sb.swapped_out_blocks > 0 and s_tokens < r_tokens
+
+
+def test_swap_falls_back_to_recompute_when_the_host_pool_is_full():
+    reqs = synthetic_requests(24, seed=5, prompt_lo=32, prompt_hi=300)
+    b = ContinuousBatcher(reqs, 8, 48, 16, preempt="swap", host_blocks=1)
+    plans = b.run()
+    assert b.total_preemptions > 0 and b.swapped_out_blocks <= 1
+    replay_token_placement(plans, 16)
+    with pytest.raises(ValueError):
+        ContinuousBatcher(reqs, 8, 48, 16, preempt="evict")

@@ -26,7 +26,12 @@ Behaviour follows the pages; the code is this package's own:
   (Tessera page section 3: LIFO), releases all its blocks and puts it at the
   front of the waiting queue with its tokens intact, to be recomputed (its
   KV re-appended) on re-admission ("Paged Attention and the Block Manager",
-  section "Running out of memory becomes a scheduling decision").
+  section "Running out of memory becomes a scheduling decision"). With
+  preempt="swap" (the other choice that section names) the victim's blocks
+  are copied out to a host pool instead and copied back into free device
+  blocks on re-admission, so nothing is re-appended; a victim whose KV was
+  not written yet (admitted by recompute in the same step) or that does not
+  fit in the host pool is recomputed.
 
 Nothing here computes a slot or touches K/V values: a step plan lists
 (request, position) pairs and block tables; the slot mapping, append and
@@ -186,9 +191,17 @@ class StepPlan:
     context_lens    int32 [R]: tokens attended over (the step's token included)
     token_row,
     token_pos       int32 [T]: tokens whose K/V this step appends (batch row, position):
-                    the whole history of sequences (re)admitted this step, then
-                    one new token per running sequence
+                    the whole history of sequences (re)admitted this step by
+                    recompute, then one new token per running sequence
     query_pos       int32 [R]: position of each row's query token
+    swap_in         int32 [n][2]: (host block, device block) copied in this step
+    swap_out        int32 [n][2]: (device block, host block) copied out this step
+
+    On the device a step runs swap_in, then swap_out, then the append, then the
+    decode: a sequence swapped in and preempted again in one step is copied
+    back out after it arrived, a host block freed by a swap-in is read before a
+    swap-out reuses it, and a device block freed by a swap-out is read before
+    an append reuses it.
     """
     step: int
     rids: list
@@ -199,12 +212,24 @@ class StepPlan:
     query_pos: np.ndarray
     admitted: list
     preempted: list
+    swap_in: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int32))
+    swap_out: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int32))
 
 
 class ContinuousBatcher:
-    def __init__(self, requests, slots, n_blocks, block_size, max_blocks=None):
+    def __init__(self, requests, slots, n_blocks, block_size, max_blocks=None,
+                 preempt="recompute", host_blocks=0):
+        if preempt not in ("recompute", "swap"):
+            raise ValueError("preempt must be 'recompute' or 'swap'")
         self.requests = {r.rid: r for r in requests}
         self.alloc = BlockAllocator(n_blocks, block_size)
+        self.preempt = preempt
+        self.host = BlockAllocator(host_blocks, block_size) if preempt == "swap" else None
+        self.swapped = {}            # rid -> (host block table, tokens held)
+        self.swapped_out_blocks = 0
+        self.swapped_in_blocks = 0
+        self._recomputed = set()     # admitted by recompute this step: KV not written yet
+        self._swap_in, self._swap_out = [], []
         self.waiting = deque(sorted(requests, key=lambda r: (r.arrival, r.rid)))
         self.running = []            # admission order, oldest first
         self.seqs = {}
@@ -230,7 +255,19 @@ class ContinuousBatcher:
             admitted.append(self.waiting.popleft())
         for r in admitted:
             seq = Sequence(r.rid, self.alloc)
-            seq.append_tokens(r.n_tokens)  # recompute: the whole history is re-appended
+            held = self.swapped.pop(r.rid, None)
+            if held is None:
+                seq.append_tokens(r.n_tokens)  # recompute: the whole history is re-appended
+                self._recomputed.add(r.rid)
+            else:
+                host_table, n_tokens = held    # swap in: same tokens, fresh device blocks
+                for hb in host_table:
+                    db = self.alloc.allocate()
+                    seq.table.append(db)
+                    self._swap_in.append((hb, db))
+                    self.host.free_block(hb)
+                seq.n_tokens = n_tokens
+                self.swapped_in_blocks += len(host_table)
             self.seqs[r.rid] = seq
             r.admitted_at.append(self.step)
             self.running.append(r)
@@ -240,7 +277,18 @@ class ContinuousBatcher:
         for r in reversed(self.running):   # newest admission first
             if r.rid != protect:
                 self.running.remove(r)
-                self.seqs.pop(r.rid).release()
+                seq = self.seqs.pop(r.rid)
+                # tokens on the device: a victim that already grew this step
+                # has not had that token appended yet (appends follow swap-outs)
+                written = r.n_tokens
+                keep = self.alloc.blocks_needed(written)
+                if (self.preempt == "swap" and r.rid not in self._recomputed
+                        and self.host.n_free >= keep):
+                    host_table = [self.host.allocate() for _ in range(keep)]
+                    self._swap_out.extend(zip(seq.table[:keep], host_table))
+                    self.swapped[r.rid] = (host_table, written)
+                    self.swapped_out_blocks += keep
+                seq.release()
                 r.preemptions += 1
                 self.total_preemptions += 1
                 self.waiting.appendleft(r)
@@ -249,6 +297,8 @@ class ContinuousBatcher:
 
     def schedule(self):
         """Plan the next step, or return None when every request is done."""
+        self._recomputed = set()
+        self._swap_in, self._swap_out = [], []
         admitted = self._admit()
         while not self.running:
             if not self.waiting:
@@ -258,7 +308,7 @@ class ContinuousBatcher:
             self.step = self.waiting[0].arrival      # idle until the next arrival
             admitted = self._admit()
         admitted_ids = {r.rid for r in admitted}
-        history = {r.rid: r.n_tokens for r in admitted}
+        history = {r.rid: r.n_tokens for r in admitted if r.rid in self._recomputed}
         preempted = []
         # grow every running sequence by the token this step writes
         for r in list(self.running):
@@ -290,7 +340,9 @@ class ContinuousBatcher:
             tok_pos.append(self.seqs[r.rid].n_tokens - 1)
         plan = StepPlan(self.step, [r.rid for r in self.running], bt, lens,
                         np.asarray(tok_row, np.int32), np.asarray(tok_pos, np.int32), qpos,
-                        [rid for rid in admitted_ids if rid in rows], preempted)
+                        [rid for rid in admitted_ids if rid in rows], preempted,
+                        np.asarray(self._swap_in, np.int32).reshape(-1, 2),
+                        np.asarray(self._swap_out, np.int32).reshape(-1, 2))
         return plan
 
     def commit(self, plan):

@@ -4,7 +4,8 @@
 [32, 512] and outputs drawn from {8, 16, 32, 64, 128} (weights .3 .25 .15 .15
 .15); up to `slots` of them run at once over a pool of 65,536 token slots
 (4096 blocks of 16, or the same capacity at block size 8 or 32), with LIFO
-preemption by recompute. Llama-2-7B layer shape: 32 heads, head_dim 128, fp16.
+preemption by recompute (or, on request, by swapping to a host pool).
+Llama-2-7B layer shape: 32 heads, head_dim 128, fp16.
 
 Every token of request r has fixed K and V rows and a fixed query row, drawn
 once per request from a generator seeded by (seed, r): a preempted request
@@ -49,14 +50,18 @@ class TraceWorkload:
 
 
 def cb_trace(block_size=16, slots=64, pool_tokens=65536, n_requests=64, seed=BASE_SEED + 4,
-             dtype="f16", n_q_heads=32, n_kv_heads=32, head_dim=128, prompt_hi=512):
+             dtype="f16", n_q_heads=32, n_kv_heads=32, head_dim=128, prompt_hi=512,
+             preempt="recompute", host_tokens=0):
+    """The trace's step plans. preempt="swap" copies victims' blocks to a host
+    pool of `host_tokens` token slots instead of recomputing them."""
     reqs = synthetic_requests(n_requests, seed=seed, prompt_hi=prompt_hi)
     n_blocks = pool_tokens // block_size
-    batcher = ContinuousBatcher(reqs, slots, n_blocks, block_size)
+    batcher = ContinuousBatcher(reqs, slots, n_blocks, block_size, preempt=preempt,
+                                host_blocks=host_tokens // block_size)
     plans = batcher.run()
-    return TraceWorkload(f"cb_trace_B{block_size}_slots{slots}", dtype, n_q_heads, n_kv_heads,
-                         head_dim, block_size, n_blocks, slots, reqs, plans, batcher.max_blocks,
-                         batcher.total_preemptions, seed)
+    name = f"cb_trace_B{block_size}_slots{slots}" + ("_swap" if preempt == "swap" else "")
+    return TraceWorkload(name, dtype, n_q_heads, n_kv_heads, head_dim, block_size, n_blocks,
+                         slots, reqs, plans, batcher.max_blocks, batcher.total_preemptions, seed)
 
 
 def trace_tensors(tw, device="cpu"):
