@@ -81,6 +81,11 @@ class Oracle:
             ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_i32p, ctypes.c_int64, _c_f64p,
             ctypes.c_int]
+        lib.oracle_prefill_units.restype = ctypes.c_int
+        lib.oracle_prefill_units.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _c_i32p, _c_i32p, _c_i32p,
+            ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, _c_i32p, ctypes.c_int64, _c_f64p, ctypes.c_int]
         lib.oracle_decode_partition.restype = ctypes.c_int
         lib.oracle_decode_partition.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _c_i32p, ctypes.c_double,
@@ -212,6 +217,37 @@ class Oracle:
             DTYPE_CODES[dtype], _ptr(u, _c_i32p), u.shape[0], _ptr(out, _c_f64p), int(threads))
         if st != 0:
             raise ValueError("a context length lies outside its block table")
+        return out
+
+    def prefill(self, q, k_cache, v_cache, block_tables, query_start, context_lens, scale,
+                dtype, units=None, threads=0):
+        """Chunked-prefill attention; returns float64 [num_tokens][n_q_heads][head_dim].
+
+        q holds every sequence's chunk of query rows, sequence after sequence;
+        query_start[num_seqs + 1] delimits them; context_lens counts each
+        sequence's cached tokens with its chunk included. units: optional
+        (seq, kv_head) pairs to compute; rows of other units are NaN.
+        """
+        q, k_cache, v_cache = (_raw(x, dtype) for x in (q, k_cache, v_cache))
+        bt, qs, lens = _i32(block_tables), _i32(query_start), _i32(context_lens)
+        num_tokens, n_q_heads, head_dim = q.shape
+        _, block_size, n_kv_heads, hd = k_cache.shape
+        num_seqs = lens.shape[0]
+        if hd != head_dim or v_cache.shape != k_cache.shape:
+            raise ValueError("shape mismatch between q and the pools")
+        if qs.shape[0] != num_seqs + 1 or qs[0] != 0 or qs[-1] != num_tokens or (np.diff(qs) < 0).any():
+            raise ValueError("query_start must run from 0 to num_tokens without decreasing")
+        if units is None:
+            units = [(s, h) for s in range(num_seqs) for h in range(n_kv_heads)]
+        u = _i32(np.asarray(list(units), dtype=np.int32).reshape(-1, 2))
+        out = np.full((num_tokens, n_q_heads, head_dim), np.nan, dtype=np.float64)
+        st = self.lib.oracle_prefill_units(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt, _c_i32p), _ptr(qs, _c_i32p),
+            _ptr(lens, _c_i32p), float(scale), n_q_heads, n_kv_heads, head_dim, block_size,
+            bt.shape[1], DTYPE_CODES[dtype], _ptr(u, _c_i32p), u.shape[0], _ptr(out, _c_f64p),
+            int(threads))
+        if st != 0:
+            raise ValueError("a chunk is longer than its context, or a context lies outside its table")
         return out
 
     def decode_partition(self, q, k_cache, v_cache, block_tables, scale, dtype, seq, qh,

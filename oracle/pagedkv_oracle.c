@@ -50,6 +50,16 @@
  *     group (query head qh reads kv head qh / (n_q_heads / n_kv_heads); the
  *     pages are silent on grouping, this is the consecutive-group reading).
  *
+ *   oracle_prefill_units
+ *     "How a serving engine actually works", section "Prefill and decode are
+ *     two different jobs": a long prompt is prefilled in slices, one chunk per
+ *     iteration. Reading taken (the pages give the schedule, not the
+ *     attention): a chunk's K/V are appended to the cache first, so with
+ *     L = tokens cached (the chunk included) and n = the chunk's length, its
+ *     query j is the token at position L - n + j and attends, by the same
+ *     softmax attention as decode, over the keys at positions 0 .. L - n + j
+ *     (the earlier chunks and itself, causally). Decode is the case n = 1.
+ *
  *   oracle_decode_partition, oracle_lse_merge
  *     The pages do not split a context. These two state the split-context
  *     form used by the partitioned kernel: over tokens [t0, t1) of one query
@@ -330,6 +340,74 @@ int oracle_decode_units(const void *q, const void *k_cache, const void *v_cache,
             for (int d = 0; d < head_dim; ++d)
                 qd[d] = widen(q, qrow + d, dtype);
             attend(qd, K, V, length, head_dim, scale, z, out + qrow);
+        }
+        free(K);
+        free(V);
+        free(qd);
+        free(z);
+    }
+    return status;
+}
+
+/*
+ * Chunked-prefill attention for the listed (seq, kv_head) units.
+ *   q             [num_tokens][n_q_heads][head_dim] (dtype): the chunks' query
+ *                 rows, sequence after sequence
+ *   query_start   [num_seqs + 1]: sequence s owns query rows
+ *                 query_start[s] .. query_start[s + 1] - 1
+ *   context_lens  [num_seqs]: tokens in the cache, the chunk included
+ *   out           [num_tokens][n_q_heads][head_dim] double; only the rows of the
+ *                 listed units are written.
+ * Query row j of sequence s, whose chunk holds n rows, is the token at position
+ * context_lens[s] - n + j; it attends over the keys at positions 0 .. that
+ * position. Returns 0, or -1 on a length that cannot be honoured.
+ */
+int oracle_prefill_units(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *query_start,
+                         const int32_t *context_lens, double scale, int n_q_heads,
+                         int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                         int dtype, const int32_t *units, int64_t num_units, double *out,
+                         int threads)
+{
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+        return -1;
+    int group = n_q_heads / n_kv_heads;
+    int status = 0;
+    (void)threads;
+#ifdef _OPENMP
+    if (threads <= 0)
+        threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int64_t u = 0; u < num_units; ++u) {
+        int seq = units[2 * u];
+        int kv_head = units[2 * u + 1];
+        int length = context_lens[seq];
+        int first = query_start[seq];
+        int rows = query_start[seq + 1] - first;
+        if (length < 0 || length > max_blocks_per_seq * block_size || rows < 0 || rows > length) {
+            status = -1;
+            continue;
+        }
+        if (rows == 0)
+            continue;
+        double *K = (double *)malloc(sizeof(double) * (size_t)length * head_dim);
+        double *V = (double *)malloc(sizeof(double) * (size_t)length * head_dim);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        double *z = (double *)malloc(sizeof(double) * (size_t)length);
+        oracle_gather(k_cache, block_tables, max_blocks_per_seq, seq, length, kv_head,
+                      n_kv_heads, head_dim, block_size, dtype, K);
+        oracle_gather(v_cache, block_tables, max_blocks_per_seq, seq, length, kv_head,
+                      n_kv_heads, head_dim, block_size, dtype, V);
+        for (int r = 0; r < rows; ++r) {
+            int position = length - rows + r;
+            for (int e = 0; e < group; ++e) {
+                int qh = kv_head * group + e;
+                int64_t qrow = ((int64_t)(first + r) * n_q_heads + qh) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    qd[d] = widen(q, qrow + d, dtype);
+                attend(qd, K, V, position + 1, head_dim, scale, z, out + qrow);
+            }
         }
         free(K);
         free(V);

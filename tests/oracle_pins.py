@@ -289,6 +289,73 @@ def pin_swap_preserves_decode(orc):
     assert after.tobytes() == before.tobytes()
 
 
+def causal_brute_force(case, Q):
+    """Contiguous causal attention with numpy/scipy: query row t of sequence s
+    (its token at position t) attends over keys 0..t. Q[s]: [L_s][Hq][D] fp64."""
+    g = case["Hq"] // case["Hkv"]
+    outs = []
+    for s, L in enumerate(case["lens"]):
+        o = np.zeros((L, case["Hq"], case["D"]))
+        for t in range(L):
+            for h in range(case["Hq"]):
+                K = case["Kc"][s][:t + 1, h // g]
+                V = case["Vc"][s][:t + 1, h // g]
+                o[t, h] = scipy.special.softmax(case["scale"] * (K @ Q[s][t, h])) @ V
+        outs.append(o)
+    return outs
+
+
+def pin_prefill_chunks(orc):
+    """"How a serving engine actually works", section "Prefill and decode are two
+    different jobs": a prompt prefilled in chunks, one chunk per call, several
+    sequences per call (some with no chunk in a round), gives every token the
+    contiguous causal attention over the prompt up to and including itself."""
+    chunking = [[5, 17, 1], [9], [1, 1, 30, 8], [16, 16]]
+    lens = [sum(c) for c in chunking]
+    for dtype, B, Hq, Hkv, D in (("f32", 8, 4, 2, 16), ("bf16", 4, 6, 2, 8), ("f16", 16, 2, 2, 8)):
+        case = paged_case(31, lens, B, Hq, Hkv, D, dtype)
+        rng = np.random.default_rng(32)
+        Qs = [to_storage(rng.standard_normal((L, Hq, D)), dtype) for L in lens]
+        want = causal_brute_force(case, [widen_lib(x, dtype) for x in Qs])
+        done = [0] * len(lens)
+        for r in range(max(len(c) for c in chunking)):
+            sizes = [c[r] if r < len(c) else 0 for c in chunking]
+            qs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+            ctx = np.array([done[s] + sizes[s] for s in range(len(lens))], np.int32)
+            q = np.concatenate([Qs[s][done[s]:done[s] + sizes[s]] for s in range(len(lens))])
+            got = orc.prefill(q, case["k"], case["v"], case["bt"], qs, ctx, case["scale"], dtype)
+            for s in range(len(lens)):
+                rows = got[qs[s]:qs[s + 1]]
+                assert np.abs(rows - want[s][done[s]:ctx[s]]).max(initial=0) < 1e-12, (dtype, r, s)
+                done[s] = int(ctx[s])
+        assert done == lens
+
+
+def pin_prefill_special_cases(orc):
+    """A one-row chunk is decode at that length; the very first token of a
+    prompt attends to itself alone, so its output is its own V row exactly;
+    a chunk longer than its context is refused."""
+    case = paged_case(33, [12, 7], 4, 4, 2, 8, "f32")
+    rng = np.random.default_rng(34)
+    q1 = to_storage(rng.standard_normal((2, 4, 8)), "f32")
+    one = orc.prefill(q1, case["k"], case["v"], case["bt"], np.array([0, 1, 2], np.int32),
+                      case["lens"], case["scale"], "f32")
+    dec = orc.decode(q1, case["k"], case["v"], case["bt"], case["lens"], case["scale"], "f32")
+    assert np.abs(one - dec).max() < 1e-12
+    first = orc.prefill(q1, case["k"], case["v"], case["bt"], np.array([0, 1, 2], np.int32),
+                        np.array([1, 1], np.int32), case["scale"], "f32")
+    for s in range(2):
+        for h in range(4):
+            assert (first[s, h] == case["Vc"][s][0, h // 2]).all()
+    try:
+        orc.prefill(q1, case["k"], case["v"], case["bt"], np.array([0, 2, 2], np.int32),
+                    np.array([1, 5], np.int32), case["scale"], "f32")
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a chunk longer than its context was accepted")
+
+
 def pin_fork_copy_on_write(orc):
     """The serving page's fork: samples share the prompt's blocks; each sample's
     first token triggers a copy of the shared last block into a fresh one. After
@@ -463,7 +530,7 @@ def pin_partition_merge(orc):
 
 ALL_PINS = [pin_f16_decoding, pin_bf16_decoding, pin_block_table_example, pin_slot_bijection,
             pin_append_scatter, pin_copy_blocks, pin_swap_blocks, pin_swap_preserves_decode,
-            pin_fork_copy_on_write, pin_gather_order,
+            pin_fork_copy_on_write, pin_gather_order, pin_prefill_chunks, pin_prefill_special_cases,
             pin_decode_bruteforce,
             pin_block_permutation_invariance, pin_shared_prefix, pin_special_cases,
             pin_partition_merge]

@@ -58,6 +58,10 @@ MUTANTS = {
     "swap_destination_index": ("memcpy(dst_k + to * block_bytes, src_k + from * block_bytes",
                                "memcpy(dst_k + from * block_bytes, src_k + from * block_bytes"),
     "swap_bounds_one_pool": ("to < 0 || to >= dst_blocks", "to < 0 || to >= src_blocks"),
+    "prefill_causal_exclusive": ("attend(qd, K, V, position + 1,", "attend(qd, K, V, position,"),
+    "prefill_position_from_chunk_start": ("int position = length - rows + r;", "int position = r;"),
+    "prefill_query_row_offset": ("((int64_t)(first + r) * n_q_heads + qh)",
+                                 "((int64_t)r * n_q_heads + qh)"),
     "swap_only_keys": ("        memcpy(dst_v + to * block_bytes, src_v + from * block_bytes, (size_t)block_bytes);\n", ""),
 }
 
