@@ -35,6 +35,7 @@ from workloads import materialize, new_pools, preset  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s per layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu", "api.cu",
                   "decode_instances.cuh"]
 
@@ -89,6 +90,16 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense 16-bit tensor TFLOP/s of this GPU: the burst figure (a kernel timed alone)."""
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_digest():
@@ -612,6 +623,92 @@ def measure_swap(device, reps=20):
     return res
 
 
+def prefill_flops(context_lens, query_start, n_q_heads, head_dim):
+    """4 * D per (query row, query head, key attended): Q K^T and P V, causal."""
+    total = 0
+    for s in range(len(context_lens)):
+        n = int(query_start[s + 1] - query_start[s])
+        L = int(context_lens[s])
+        # rows attend over L - n + 1 .. L keys
+        total += n * (L - n + 1) + n * (n - 1) // 2
+    return 4 * head_dim * n_q_heads * total
+
+
+def measure_prefill(device, reps=50):
+    """Chunked-prefill attention: (1) a step of 16 Llama-2-7B-layer sequences
+    each appending a 512-token chunk after U[0, 3584] cached tokens; (2) the
+    serving page's scenario, one 2048-token prompt prefilled in one pass or in
+    chunks of 512, 256 or 128 tokens (attention time of the whole prompt)."""
+    import paged_kv_cache_233_gb300 as pk
+    from workloads import chunked_prefill, prefill_mha7b, prefill_queries
+    peak, peak_kind = measured_tensor_peak()
+
+    def fill_pools(wl, dev):
+        """Pools holding every token of the workload, written by slot mapping + append."""
+        t = materialize(wl, dev)
+        kc, vc = new_pools(wl, dev, fill=0.0)
+        bt = torch.from_numpy(wl.block_tables).to(dev)
+        for seq, pos, k, v in ((wl.fill_seq, wl.fill_pos, t["k_fill"], t["v_fill"]),
+                               (wl.step_seq, wl.step_pos, t["k_step"], t["v_step"])):
+            slots = torch.empty(len(seq), dtype=torch.int64, device=dev)
+            pk.paged_kv_slot_mapping(bt, torch.from_numpy(seq).to(dev),
+                                     torch.from_numpy(pos).to(dev), slots, wl.num_blocks,
+                                     wl.block_size)
+            pk.paged_kv_append(k, v, slots, kc, vc)
+        return kc, vc, bt
+
+    def timed(fn, n=reps):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    wl, qs = prefill_mha7b()
+    kc, vc, bt = fill_pools(wl, device)
+    q = prefill_queries(wl, qs, device)
+    out = torch.empty_like(q)
+    qs_d = torch.from_numpy(qs).to(device)
+    lens_d = torch.from_numpy(wl.context_lens).to(device)
+    ms = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out, 512))
+    flops = prefill_flops(wl.context_lens, qs, wl.n_q_heads, wl.head_dim)
+    res = {"workload": "16 seqs x 512-token chunk after U[0,3584] cached tokens, Llama-2-7B "
+                       "layer (32 heads, D128, fp16, B16)",
+           "median_us": ms * 1e3, "flops": flops, "tflops": flops / ms / 1e9,
+           "peak_tflops": peak, "peak_kind": f"{peak_kind} bf16_tflops (cuBLAS burst)",
+           "frac": flops / ms / 1e9 / peak, "kv_bytes": int(2 * wl.context_lens.sum() * wl.row_bytes)}
+    del kc, vc, q, out
+    torch.cuda.empty_cache()
+    # the 2048-token prompt, chunked
+    wl2, qs2 = chunked_prefill("prompt2048", "f16", [0], [2048], 32, 32, 128, 16, seed=17)
+    kc, vc, bt = fill_pools(wl2, device)
+    q = prefill_queries(wl2, qs2, device)
+    out = torch.empty_like(q)
+    chunking = {}
+    for chunk in (2048, 512, 256, 128):
+        calls = []
+        for c0 in range(0, 2048, chunk):
+            rows = q[c0:c0 + chunk]
+            o = out[c0:c0 + chunk]
+            cqs = torch.tensor([0, chunk], dtype=torch.int32, device=device)
+            cl = torch.tensor([c0 + chunk], dtype=torch.int32, device=device)
+            calls.append(timed(lambda: pk.paged_attention_prefill(rows, kc, vc, bt, cqs, cl,
+                                                                  wl2.scale, o, chunk), 20))
+        chunking[str(chunk)] = {"calls": len(calls), "total_us": sum(calls) * 1e3,
+                                "max_call_us": max(calls) * 1e3}
+    res["prompt2048_chunked"] = chunking
+    assert pk.device_errors() == 0
+    del kc, vc, q, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, ctx):
     import paged_kv_cache_233_gb300 as pk
     from paged_kv_cache_233_gb300 import build as pk_build
@@ -683,6 +780,7 @@ def run_ours(args, ctx):
         torch.cuda.empty_cache()
         result["cow_copy"] = measure_cow(device)
         result["swap"] = measure_swap(device)
+        result["prefill"] = measure_prefill(device)
     if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
         import oracle
         orc = oracle.get()

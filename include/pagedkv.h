@@ -175,6 +175,47 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
                          void *stream);
 
 /*
+ * paged_attention_prefill -- chunked-prefill attention over the paged cache.
+ *
+ * Page "How a serving engine actually works", section "Prefill and decode are
+ * two different jobs": a long prompt is prefilled in chunks, one chunk per
+ * iteration, so that sequences decoding beside it are not stalled behind the
+ * whole prompt. The chunk's K/V rows must already be in the pools (appended
+ * with paged_kv_append). Sequence s owns query rows query_start[s] ..
+ * query_start[s+1]-1 (n_s rows); with L_s = context_lens[s] cached tokens, the
+ * chunk included, row j is the token at position L_s - n_s + j and attends over
+ * keys 0 .. L_s - n_s + j of its sequence, read through its block table:
+ *
+ *     out[row][qh][:] = softmax_i(scale * q[row][qh] . K[i][qh / g]) V[i][qh / g]
+ *
+ * Decode is the case n_s = 1. Tensor-core path: fp16 and bf16 only, fp32
+ * accumulation, one rounding of `out` to the input type.
+ *
+ *   q, out         [num_tokens][n_q_heads][head_dim] of dtype, device, 16-byte aligned
+ *   k_cache,
+ *   v_cache        [num_blocks][block_size][n_kv_heads][head_dim], device, 16-byte aligned
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq], device
+ *   query_start    int32 [num_seqs + 1], device, non-decreasing from 0 to num_tokens
+ *   context_lens   int32 [num_seqs], device
+ *   max_query_len  an upper bound of every n_s (sizes the grid)
+ *
+ * Returns PAGEDKV_ERR_UNSUPPORTED for fp32, head_dim other than 64/128, block
+ * size other than 8/16/32 or more than 64 query heads per kv head. On the
+ * device, a sequence whose rows fall outside [0, num_tokens) or exceed the
+ * grid's max_query_len sets PAGEDKV_DEVERR_POSITION; one with n_s > L_s or L_s
+ * beyond its table sets PAGEDKV_DEVERR_CONTEXT_LEN; a block id outside the pool
+ * sets PAGEDKV_DEVERR_BLOCK_ID (block 0 is read instead). The rows of a
+ * flagged sequence are left unwritten. Asynchronous on `stream`; allocates
+ * nothing.
+ */
+int paged_attention_prefill(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *query_start,
+                            const int32_t *context_lens, float scale, void *out, int num_seqs,
+                            int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
+                            int head_dim, int num_blocks, int block_size,
+                            int max_blocks_per_seq, int dtype, void *stream);
+
+/*
  * paged_attention_decode -- fused paged-attention decode.
  *
  * The kernel the pages name as the next step and never build (page "Paged-KV +

@@ -30,6 +30,7 @@ __all__ = [
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
     "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
+    "paged_attention_prefill",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +84,9 @@ def load():
     lib.paged_kv_copy_blocks.restype = i32
     lib.paged_kv_swap_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
     lib.paged_kv_swap_blocks.restype = i32
+    lib.paged_attention_prefill.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32,
+                                            i32, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.paged_attention_prefill.restype = i32
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -216,6 +220,32 @@ def paged_kv_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
         _reachable(block_pairs, "block_pairs", torch.int32), block_pairs.shape[0], B, Hkv, D,
         _code(src_k), _stream(stream))
     _check(st, "paged_kv_swap_blocks")
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale,
+                            out, max_query_len=None, stream=None):
+    """Chunked-prefill attention: q/out [num_tokens][Hq][D] hold every sequence's
+    chunk of query rows, sequence after sequence, delimited by query_start
+    [num_seqs + 1]; context_lens counts each sequence's cached tokens with its
+    chunk (already appended) included. max_query_len bounds every chunk's
+    length; by default it is read from query_start (a device-to-host copy)."""
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise PagedKVError("q and out must be [num_tokens][n_q_heads][head_dim] of one type")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != q.dtype:
+        raise PagedKVError("expected pools [NB][B][Hkv][D] of q's element type")
+    S = context_lens.shape[0]
+    if query_start.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise PagedKVError("query_start must hold num_seqs + 1 offsets, block_tables num_seqs rows")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if S else 0
+    NB, B, Hkv, D = k_cache.shape
+    st = load().paged_attention_prefill(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(query_start, "query_start", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S,
+        q.shape[0], int(max_query_len), q.shape[1], Hkv, D, NB, B, block_tables.shape[1],
+        _code(q), _stream(stream))
+    _check(st, "paged_attention_prefill")
 
 
 def paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq, block_size,

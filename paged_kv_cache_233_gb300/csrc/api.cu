@@ -12,6 +12,7 @@
 
 #include "../../include/pagedkv.h"
 #include "decode_launch.h"
+#include "prefill.h"
 
 namespace pkv {
 cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
@@ -343,6 +344,66 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
     const cudaError_t e = pkv::launch_swap_blocks(sk, sv, dk, dv, pairs, num_pairs,
                                                   src_num_blocks, dst_num_blocks, block_bytes,
                                                   sms, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+int paged_attention_prefill(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *query_start,
+                            const int32_t *context_lens, float scale, void *out, int num_seqs,
+                            int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
+                            int head_dim, int num_blocks, int block_size,
+                            int max_blocks_per_seq, int dtype, void *stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || n_q_heads < 1 || n_kv_heads < 1 ||
+        head_dim < 1 || num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 1 ||
+        !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PAGEDKV_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PAGEDKV_ERR_INVALID_ARG;
+    if (dtype == PAGEDKV_F32) return PAGEDKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PAGEDKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PAGEDKV_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    if (group > pkv::kPfRows || num_seqs > 65535 || n_kv_heads > 65535) return PAGEDKV_ERR_UNSUPPORTED;
+    const long long num_slots = (long long)num_blocks * block_size;
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    if (num_slots > INT_MAX || cap > INT_MAX / 2) return PAGEDKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PAGEDKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !query_start || !context_lens || !out)
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(query_start, 4) || !aligned(context_lens, 4))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    CUtensorMap kmap, vmap;
+    st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+    if (st != PAGEDKV_OK) return st;
+    st = encode_pool_map(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+    if (st != PAGEDKV_OK) return st;
+    pkv::PrefillParams p{};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.query_start = query_start;
+    p.context_lens = context_lens;
+    p.err = err;
+    p.scale_log2 = scale * pkv::kLog2e;
+    p.num_seqs = num_seqs;
+    p.num_tokens = num_tokens;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = group;
+    p.tile_tokens = pkv::kPfRows / group;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    int log2_block = 0;
+    while ((1 << log2_block) < block_size) ++log2_block;
+    p.log2_block = log2_block;
+    p.max_blocks = max_blocks_per_seq;
+    const cudaError_t e = pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
+                                              static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 

@@ -1,0 +1,44 @@
+// prefill.h -- parameters of the chunked-prefill attention kernel, shared by
+// the C ABI layer and the kernel's translation unit.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kPfRows = 64;      // query rows (chunk token, query head) per CTA
+constexpr int kPfKeys = 64;      // keys per pipeline stage
+constexpr int kPfStages = 3;     // depth of the K/V ring
+constexpr int kPfThreads = 160;  // one producer warp + four consumer warps of 16 rows
+
+struct PrefillParams {
+    const void *q;               // [num_tokens][n_q_heads][head_dim]
+    void *out;                   // [num_tokens][n_q_heads][head_dim]
+    const int32_t *block_tables; // [num_seqs][max_blocks]
+    const int32_t *query_start;  // [num_seqs + 1]
+    const int32_t *context_lens; // [num_seqs], the chunk included
+    unsigned int *err;
+    float scale_log2;            // softmax scale * log2(e)
+    int num_seqs;
+    int num_tokens;
+    int n_q_heads;
+    int n_kv_heads;
+    int group;                   // n_q_heads / n_kv_heads
+    int tile_tokens;             // chunk tokens per CTA: kPfRows / group
+    int num_blocks;
+    int block_size;
+    int log2_block;
+    int max_blocks;
+};
+
+// Bytes of dynamic shared memory the kernel asks for at this head_dim (16-bit types).
+int prefill_smem_bytes(int head_dim);
+
+// Grid: (query tiles of the longest chunk, kv heads, sequences).
+cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
+                           cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,177 @@
+"""Chunked-prefill attention, CUDA path against the fp64 oracle (needs a GPU).
+
+The chunk's K/V go into NaN-poisoned pools through the library's slot mapping
+and append, as a serving step would do; then every query row of the chunk
+must match the oracle's causal attention over its sequence within the dtype's
+tolerance. A prompt prefilled chunk by chunk must give bit-identical rows to
+one pass over the whole prompt; one-row chunks must agree with decode; bad
+lengths are flagged on the device error word and leave their rows untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_233_gb300 as pk
+from paged_support import TOL, gpu_fill, oracle_fill, to_f64, to_np
+from workloads import chunked_prefill, materialize, prefill_mha7b, prefill_queries
+
+pytestmark = pytest.mark.gpu
+
+# (tokens cached before the chunk, chunk length): empty and one-row chunks, a
+# chunk that is the whole prompt, ragged tails around 64-key and 64-row tiles
+CASES = [(0, 1), (0, 77), (13, 50), (100, 130), (300, 1), (37, 0), (64, 64), (5, 200)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pk.load()
+    torch.cuda.set_device(0)
+    pk.device_errors(reset=True)
+
+
+def build(dtype, D, B, g, seed, cases=CASES, n_kv=2):
+    before = [c[0] for c in cases]
+    chunk = [c[1] for c in cases]
+    wl, qs = chunked_prefill("prefill_case", dtype, before, chunk, g * n_kv, n_kv, D, B, seed)
+    tensors = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, tensors)
+    q = prefill_queries(wl, qs, "cuda")
+    return wl, qs, tensors, q, kc, vc, bt
+
+
+def prefill(wl, qs, q, kc, vc, bt, lens=None, max_query_len=None):
+    out = torch.full_like(q, float("nan"))
+    lens = wl.context_lens if lens is None else lens
+    pk.paged_attention_prefill(q, kc, vc, bt, torch.from_numpy(np.asarray(qs, np.int32)).cuda(),
+                               torch.from_numpy(np.asarray(lens, np.int32)).cuda(), wl.scale, out,
+                               max_query_len)
+    return out
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_matches_oracle(orc, dtype, D, B, g):
+    wl, qs, tensors, q, kc, vc, bt = build(dtype, D, B, g, seed=100 + D + B + g)
+    out = prefill(wl, qs, q, kc, vc, bt)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, dtype)
+    got = to_f64(out)
+    assert not np.isnan(got).any()
+    err = float(np.abs(got - ref).max())
+    assert err <= TOL[dtype], f"max-abs error {err:.3e}"
+
+
+@pytest.mark.parametrize("g", [3, 16, 64])
+def test_prefill_odd_and_large_groups(orc, g):
+    """Groups that do not divide the 64-row tile evenly, and a whole tile of heads."""
+    cases = [(0, 9), (40, 33), (7, 70)]
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, g, seed=200 + g, cases=cases, n_kv=1)
+    out = prefill(wl, qs, q, kc, vc, bt)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype,B", [("f16", 16), ("bf16", 8)])
+def test_chunk_by_chunk_equals_one_pass(dtype, B):
+    """The prompts' rows come out bit-identical whether a call covers the whole
+    prompt or the prompt is prefilled in chunks over several calls."""
+    chunks = [[128, 128, 45], [1, 100, 49], [64, 1, 1]]
+    prompts = [sum(c) for c in chunks]
+    wl, qs, tensors, q, kc, vc, bt = build(dtype, 128, B, 4, seed=300,
+                                           cases=[(0, n) for n in prompts])
+    whole = prefill(wl, qs, q, kc, vc, bt)
+    done = [0] * len(prompts)
+    for r in range(3):
+        sizes = [c[r] for c in chunks]
+        cqs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        lens = np.array([done[s] + sizes[s] for s in range(len(prompts))], np.int32)
+        rows = torch.cat([q[qs[s] + done[s]:qs[s] + lens[s]] for s in range(len(prompts))])
+        part = prefill(wl, cqs, rows.contiguous(), kc, vc, bt, lens=lens)
+        for s in range(len(prompts)):
+            a = part[cqs[s]:cqs[s + 1]]
+            b = whole[qs[s] + done[s]:qs[s] + lens[s]]
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (r, s)
+            done[s] = int(lens[s])
+    assert pk.device_errors() == 0
+
+
+def test_one_row_chunks_agree_with_decode(orc):
+    wl, qs, tensors, q, kc, vc, bt = build("f16", 128, 16, 4, seed=400,
+                                           cases=[(0, 1), (16, 1), (170, 1), (999, 1)])
+    out = prefill(wl, qs, q, kc, vc, bt)
+    dec = torch.full_like(q, float("nan"))
+    pk.paged_attention_decode(q, kc, vc, bt, torch.from_numpy(wl.context_lens).cuda(), wl.scale,
+                              dec, 0, None)
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.decode(to_np(q), okc, ovc, wl.block_tables, wl.context_lens, wl.scale, "f16")
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+    assert float(np.abs(to_f64(dec) - ref).max()) <= TOL["f16"]
+    assert pk.device_errors() == 0
+
+
+def test_bad_lengths_are_flagged_and_left_unwritten(orc):
+    cases = [(10, 20), (5, 30), (0, 100)]
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, 2, seed=500, cases=cases)
+    # sequence 1 claims fewer cached tokens than its chunk has rows
+    lens = wl.context_lens.copy()
+    lens[1] = 29
+    pk.device_errors(reset=True)
+    out = prefill(wl, qs, q, kc, vc, bt, lens=lens)
+    assert pk.device_errors() & 0x04
+    got = to_f64(out)
+    assert np.isnan(got[qs[1]:qs[2]]).all()
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16",
+                      units=[(0, 0), (0, 1), (2, 0), (2, 1)])
+    keep = np.r_[qs[0]:qs[1], qs[2]:qs[3]]
+    assert float(np.abs(got[keep] - ref[keep]).max()) <= TOL["bf16"]
+    # a chunk longer than the grid that max_query_len sized
+    out = prefill(wl, qs, q, kc, vc, bt, max_query_len=10)
+    assert pk.device_errors() & 0x08
+    assert np.isnan(to_f64(out)[qs[2]:qs[3]]).all()
+    assert pk.device_errors() == 0
+
+
+def test_fp32_and_unsupported_shapes_are_refused():
+    q = torch.zeros(4, 4, 64, device="cuda")
+    kc = torch.zeros(8, 16, 2, 64, device="cuda")
+    bt = torch.zeros(1, 8, dtype=torch.int32, device="cuda")
+    qs = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([4], dtype=torch.int32, device="cuda")
+    with pytest.raises(pk.PagedKVError, match="unsupported"):
+        pk.paged_attention_prefill(q, kc, kc, bt, qs, lens, 0.125, torch.empty_like(q))
+    q16 = torch.zeros(4, 4, 96, device="cuda").half()
+    kc16 = torch.zeros(8, 16, 2, 96, device="cuda").half()
+    with pytest.raises(pk.PagedKVError, match="unsupported"):
+        pk.paged_attention_prefill(q16, kc16, kc16, bt, qs, lens, 0.125, torch.empty_like(q16))
+    assert pk.device_errors() == 0
+
+
+def test_prefill_full_size_sampled(orc):
+    """The bench's chunked-prefill step at full size (Llama-2-7B layer, 16
+    sequences appending 512-token chunks after up to 3584 cached tokens),
+    sampled (sequence, head) units against the oracle."""
+    wl, qs = prefill_mha7b()
+    tensors = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, tensors)
+    q = prefill_queries(wl, qs, "cuda")
+    out = prefill(wl, qs, q, kc, vc, bt, max_query_len=512)
+    assert pk.device_errors() == 0
+    got = to_f64(out)
+    assert not np.isnan(got).any()
+    rng = np.random.default_rng(6)
+    units = [(int(s), int(h)) for s, h in zip(rng.choice(wl.num_seqs, 4, replace=False),
+                                              rng.choice(wl.n_kv_heads, 4, replace=False))]
+    okc, ovc = to_np(kc), to_np(vc)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16",
+                      units=units)
+    for s, h in units:
+        err = float(np.abs(got[qs[s]:qs[s + 1], h] - ref[qs[s]:qs[s + 1], h]).max())
+        assert err <= TOL["f16"], (s, h, err)

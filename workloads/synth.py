@@ -196,6 +196,39 @@ def longctx_splitk(seed=BASE_SEED + 3, num_seqs=8, lo=32768, hi=131072):
                          partition_tokens=512)
 
 
+def chunked_prefill(name, dtype, before, chunk, n_q_heads, n_kv_heads, head_dim, block_size,
+                    seed, **kw):
+    """One chunked-prefill step: sequence s holds `before[s]` cached tokens and
+    appends a chunk of `chunk[s]` tokens whose rows then attend. The workload's
+    lengths count the chunk (every token, the chunk included, is filled into the
+    pools); query_start delimits each sequence's chunk rows."""
+    before = np.asarray(before, dtype=np.int64)
+    chunk = np.asarray(chunk, dtype=np.int64)
+    wl = make_workload(name, dtype, before + chunk, n_q_heads, n_kv_heads, head_dim, block_size,
+                       seed, **kw)
+    query_start = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    return wl, query_start
+
+
+def prefill_mha7b(seed=BASE_SEED + 5, num_seqs=16, chunk=512, max_before=3584):
+    """Llama-2-7B-shaped MHA layer (32 heads, head_dim 128, fp16, B = 16): 16
+    sequences each append a 512-token chunk after U[0, 3584] cached tokens."""
+    rng = np.random.default_rng(seed + 1000)
+    before = rng.integers(0, max_before, size=num_seqs, endpoint=True)
+    return chunked_prefill("prefill_mha7b", "f16", before, np.full(num_seqs, chunk), 32, 32, 128,
+                           16, seed)
+
+
+def prefill_queries(wl, query_start, device="cpu"):
+    """Query rows [num_tokens][n_q_heads][head_dim] of a chunked-prefill step, N(0, 1)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(wl.seed) + 500)
+    n = int(query_start[-1])
+    return torch.randn((n, wl.n_q_heads, wl.head_dim), generator=gen, device=dev,
+                       dtype=torch.float32).to(wl.torch_dtype)
+
+
 PRESETS = {"tiny": tiny, "mha7b": mha7b, "gqa8b_prefix": gqa8b_prefix,
            "longctx_splitk": longctx_splitk}
 
