@@ -37,7 +37,7 @@ METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s pe
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu", "api.cu",
-                  "decode_instances.cuh"]
+                  "decode_instances.cuh", "decode_launch.h"]
 
 # partition size (tokens) used for each workload's decode; 0 = no split
 PARTITION = {"tiny": 0, "mha7b": 320, "gqa8b_prefix": 320, "longctx_splitk": 512}
@@ -102,12 +102,28 @@ def measured_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def decode_part_of_api(text):
+    """The parts of api.cu that decide a decode launch: the pool tensor map, the
+    workspace layout and the decode entry points (other entry points excluded)."""
+    try:
+        a = text.index("int encode_pool_map(")
+        b = text.index("size_t round256(")
+        c = text.index("size_t paged_attention_workspace_bytes(")
+    except ValueError:
+        return text
+    return text[a:b] + text[c:]
+
+
 def kernel_source_digest():
+    """Digest of the sources that determine the decode kernels and their launch."""
     h = hashlib.sha256()
     csrc = os.path.join(REPO, "paged_kv_cache_233_gb300", "csrc")
     for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+            data = f.read()
+        if name == "api.cu":
+            data = decode_part_of_api(data.decode()).encode()
+        h.update(data)
     return h.hexdigest()[:16]
 
 
@@ -634,7 +650,7 @@ def prefill_flops(context_lens, query_start, n_q_heads, head_dim):
     return 4 * head_dim * n_q_heads * total
 
 
-def measure_prefill(device, reps=50):
+def measure_prefill(device, reps=50, chunked=True):
     """Chunked-prefill attention: (1) a step of 16 Llama-2-7B-layer sequences
     each appending a 512-token chunk after U[0, 3584] cached tokens; (2) the
     serving page's scenario, one 2048-token prompt prefilled in one pass or in
@@ -685,6 +701,8 @@ def measure_prefill(device, reps=50):
            "frac": flops / ms / 1e9 / peak, "kv_bytes": int(2 * wl.context_lens.sum() * wl.row_bytes)}
     del kc, vc, q, out
     torch.cuda.empty_cache()
+    if not chunked:
+        return res
     # the 2048-token prompt, chunked
     wl2, qs2 = chunked_prefill("prompt2048", "f16", [0], [2048], 32, 32, 128, 16, seed=17)
     kc, vc, bt = fill_pools(wl2, device)
@@ -814,9 +832,21 @@ def main(argv=None):
     ap.add_argument("--no-gates", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the chunked-prefill measurement (for profiling its kernel)")
+    ap.add_argument("--prefill-reps", type=int, default=50)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.prefill_only:
+        import paged_kv_cache_233_gb300 as pk
+        from paged_kv_cache_233_gb300 import build as pk_build
+        pk_build.build()
+        pk.load()
+        torch.cuda.set_device(0)
+        print(json.dumps({"prefill": measure_prefill(torch.device("cuda", 0), args.prefill_reps,
+                                                     chunked=False)}), flush=True)
+        return
     ctx = DistCtx(connect=args.impl == "ours")
     try:
         result = run_reference(args, ctx) if args.impl == "reference" else run_ours(args, ctx)
