@@ -692,13 +692,20 @@ def measure_prefill(device, reps=50, chunked=True):
     out = torch.empty_like(q)
     qs_d = torch.from_numpy(qs).to(device)
     lens_d = torch.from_numpy(wl.context_lens).to(device)
-    ms = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out, 512))
     flops = prefill_flops(wl.context_lens, qs, wl.n_q_heads, wl.head_dim)
+    call = lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out, 512)
+    pk.set_option(pk.OPT_PREFILL_PATH, 1)
+    ms_mma = timed(call)
+    pk.set_option(pk.OPT_PREFILL_PATH, 0)
+    ms = timed(call)
     res = {"workload": "16 seqs x 512-token chunk after U[0,3584] cached tokens, Llama-2-7B "
                        "layer (32 heads, D128, fp16, B16)",
+           "kernel": "paged_prefill_tc_kernel (tcgen05)",
            "median_us": ms * 1e3, "flops": flops, "tflops": flops / ms / 1e9,
            "peak_tflops": peak, "peak_kind": f"{peak_kind} bf16_tflops (cuBLAS burst)",
-           "frac": flops / ms / 1e9 / peak, "kv_bytes": int(2 * wl.context_lens.sum() * wl.row_bytes)}
+           "frac": flops / ms / 1e9 / peak, "kv_bytes": int(2 * wl.context_lens.sum() * wl.row_bytes),
+           "warp_mma_kernel": {"median_us": ms_mma * 1e3, "tflops": flops / ms_mma / 1e9,
+                               "frac": flops / ms_mma / 1e9 / peak}}
     del kc, vc, q, out
     torch.cuda.empty_cache()
     if not chunked:

@@ -189,7 +189,9 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
  *     out[row][qh][:] = softmax_i(scale * q[row][qh] . K[i][qh / g]) V[i][qh / g]
  *
  * Decode is the case n_s = 1. Tensor-core path: fp16 and bf16 only, fp32
- * accumulation, one rounding of `out` to the input type.
+ * accumulation, one rounding of `out` to the input type. Two kernels compute
+ * it (PAGEDKV_OPT_PREFILL_PATH): tcgen05 MMAs with accumulators in tensor
+ * memory (default), or warp-level m16n8k16 MMAs.
  *
  *   q, out         [num_tokens][n_q_heads][head_dim] of dtype, device, 16-byte aligned
  *   k_cache,
@@ -372,6 +374,7 @@ int pagedkv_device_errors(unsigned int *flags, int reset);
 #define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */
 #define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
 #define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16); 0 = library default */
+#define PAGEDKV_OPT_PREFILL_PATH   5  /* 0 auto (= 2), 1 warp-level MMA prefill kernel, 2 tcgen05 prefill kernel */
 int pagedkv_set_option(int option, int value);
 int pagedkv_get_option(int option);
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIBRARY = os.path.join(HERE, "libpagedkv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "append.cu", "swap.cu", "merge.cu", "prefill.cu", "decode_f32.cu",
+SOURCES = ["api.cu", "append.cu", "swap.cu", "merge.cu", "prefill.cu", "prefill_tc.cu", "decode_f32.cu",
            "decode_f16.cu", "decode_bf16.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

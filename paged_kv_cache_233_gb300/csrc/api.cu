@@ -48,6 +48,7 @@ int g_opt_path = pkv::kPathAuto;
 int g_opt_ctas_per_sm = 0;
 int g_opt_mma_min_group = 4;
 int g_opt_stages = 0;
+int g_opt_prefill_path = 0;
 int g_last_path = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -129,6 +130,32 @@ int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim,
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// TMA view of one pool for the tcgen05 prefill kernel: the same 4-D tensor as
+// encode_pool_map, with a box of one 128-byte column slab of one kv head x 16
+// tokens (8 for 8-token blocks), so that the boxes of a tile can be placed as
+// [slab][keys][128 B], the tensor core's K-major / MN-major operand layout.
+int encode_pool_map_slab(CUtensorMap *map, const void *pool, int dtype, int head_dim,
+                         int n_kv_heads, long long num_slots, int block_size) {
+    EncodeTiledFn fn = nullptr;
+    int st = encoder(&fn);
+    if (st != PAGEDKV_OK) return st;
+    const int eb = elem_bytes(dtype);
+    const int slabs = head_dim * eb / 128;
+    const CUtensorMapDataType dt = dtype == PAGEDKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t dims[4] = {cuuint64_t(128 / eb), cuuint64_t(num_slots), cuuint64_t(slabs),
+                                cuuint64_t(n_kv_heads)};
+    const cuuint64_t strides[3] = {cuuint64_t(n_kv_heads) * head_dim * eb, 128u,
+                                   cuuint64_t(head_dim) * eb};
+    const cuuint32_t box[4] = {cuuint32_t(128 / eb),
+                               cuuint32_t(block_size >= pkv::kTile ? pkv::kTile : block_size), 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
 // SM count of the current device (no error word lookup).
 int current_sm_count(int *sms) {
     int dev = 0, n = 0;
@@ -187,6 +214,10 @@ int pagedkv_set_option(int option, int value) {
             if (value < 0 || value == 1 || value > 16) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_stages = value;
             return PAGEDKV_OK;
+        case PAGEDKV_OPT_PREFILL_PATH:
+            if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_prefill_path = value;
+            return PAGEDKV_OK;
         default:
             return PAGEDKV_ERR_INVALID_ARG;
     }
@@ -198,6 +229,7 @@ int pagedkv_get_option(int option) {
         case PAGEDKV_OPT_CTAS_PER_SM: return g_opt_ctas_per_sm;
         case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
         case PAGEDKV_OPT_STAGES: return g_opt_stages;
+        case PAGEDKV_OPT_PREFILL_PATH: return g_opt_prefill_path;
         default: return PAGEDKV_ERR_INVALID_ARG;
     }
 }
@@ -377,10 +409,18 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     int sms = 0;
     int st = device_state(&err, &sms);
     if (st != PAGEDKV_OK) return st;
+    // path: 1 warp-level MMA kernel, 2 tcgen05 kernel (auto)
+    const bool tc = g_opt_prefill_path != 1;
     CUtensorMap kmap, vmap;
-    st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
-    if (st != PAGEDKV_OK) return st;
-    st = encode_pool_map(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+    if (tc) {
+        st = encode_pool_map_slab(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+        if (st != PAGEDKV_OK) return st;
+        st = encode_pool_map_slab(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+    } else {
+        st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+        if (st != PAGEDKV_OK) return st;
+        st = encode_pool_map(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+    }
     if (st != PAGEDKV_OK) return st;
     pkv::PrefillParams p{};
     p.q = q;
@@ -395,15 +435,18 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     p.n_q_heads = n_q_heads;
     p.n_kv_heads = n_kv_heads;
     p.group = group;
-    p.tile_tokens = pkv::kPfRows / group;
+    p.tile_tokens = (tc ? pkv::kPfTcRows : pkv::kPfRows) / group;
     p.num_blocks = num_blocks;
     p.block_size = block_size;
     int log2_block = 0;
     while ((1 << log2_block) < block_size) ++log2_block;
     p.log2_block = log2_block;
     p.max_blocks = max_blocks_per_seq;
-    const cudaError_t e = pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
-                                              static_cast<cudaStream_t>(stream));
+    const cudaError_t e =
+        tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, p, max_query_len,
+                                    static_cast<cudaStream_t>(stream))
+           : pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
+                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 

@@ -1,0 +1,444 @@
+// prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
+// cores (tcgen05): the same operation as prefill.cu ("How a serving engine
+// actually works", section "Prefill and decode are two different jobs": each
+// query row of a chunk attends causally over its sequence's cached tokens up
+// to its own position, read through the block table), with the contractions
+// moved off the warp-level MMA pipe.
+//
+// One CTA owns (sequence, kv head, 128 query rows of (chunk token, query head
+// of the group)). Six warps:
+//   warp 0     producer: per 64-key tile, looks up the block ids and issues one
+//              TMA box per (16 keys, 64-column block) for K and V into a
+//              three-stage ring, so that each operand lands as [column block]
+//              [64 keys][128 B] with 128-byte swizzle (the canonical layout the
+//              tensor core reads);
+//   warp 1     allocates tensor memory; its lane 0 issues every MMA:
+//              S = Q K^T into one of two S buffers in tensor memory, and, once
+//              the softmax has written P, O_tile = P V into one of two O
+//              buffers; completions are tracked by tcgen05.commit on mbarriers;
+//   warps 2-5  softmax, one thread per query row (= tensor-memory lane): read
+//              the S row, apply scale and the causal limit (a select, so K rows
+//              past the context never matter), keep the base-2 running max and
+//              sum, write P as a swizzled K-major operand in shared memory, and
+//              fold each finished O tile into registers with the running
+//              rescale; V rows past the context are zeroed in shared memory
+//              before their P V (the tensor core would turn 0 * NaN into NaN).
+// Every mbarrier wait is bounded in time; on a timeout the CTA stops, waits
+// for its copies and MMAs in flight, frees its tensor memory and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "prefill.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kTcRows = 128;     // query rows per CTA = tensor-memory lanes
+constexpr int kTcKeys = 64;      // keys per pipeline stage
+constexpr int kTcStages = 3;
+
+template <int D>
+struct TcLayout {
+    static constexpr int kSlabs = D * 2 / 128;             // 64-element column blocks per row
+    static constexpr int kQSlab = kTcRows * 128;           // bytes of one Q column block
+    static constexpr int kKvSlab = kTcKeys * 128;          // bytes of one K (or V) column block
+    static constexpr int kQ = 0;
+    static constexpr int kKv = kQ + kSlabs * kQSlab;       // stage s: K at kKv + s*kStage, V after it
+    static constexpr int kHalf = kSlabs * kKvSlab;
+    static constexpr int kStage = 2 * kHalf;
+    static constexpr int kP = kKv + kTcStages * kStage;    // two P buffers [128 rows][64 keys]
+    static constexpr int kPBytes = kTcRows * kTcKeys * 2;
+    static constexpr int kBars = kP + 2 * kPBytes;
+    static constexpr int kNumBars = 2 * kTcStages + 10;
+    static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+    static constexpr int kFlag = kTmemSlot + 8;
+    static constexpr int kTotal = kFlag + 8;
+    // S buffers: columns [0, 128); O buffers: [128, 128 + 2 D)
+    static constexpr int kTmemCols = 2 * kTcKeys + 2 * D <= 256 ? 256 : 512;
+};
+
+// mbarrier indices
+constexpr int kKvFull = 0;
+constexpr int kKvEmpty = kTcStages;
+constexpr int kSFull = 2 * kTcStages;
+constexpr int kPFull = kSFull + 2;
+constexpr int kOFull = kPFull + 2;
+constexpr int kOFree = kOFull + 2;
+constexpr int kQFull = kOFree + 2;
+constexpr int kDone = kQFull + 1;
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+}  // namespace
+
+template <typename T, int D>
+__global__ void __launch_bounds__(192, 1)
+paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using Ly = TcLayout<D>;
+    constexpr bool kBf16 = Elem<T>::kBf16;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const sm = smem_raw + (base - raw);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Ly::kFlag);
+    auto bar = [&](int i) { return base + Ly::kBars + 8u * uint32_t(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.z;
+    const int h = blockIdx.y;
+    const int qt = int(gridDim.x) - 1 - int(blockIdx.x);   // tiles with the most keys first
+    const int B = p.block_size;
+    const int g = p.group;
+
+    // ---- this CTA's slice of the chunk (uniform across the CTA)
+    const int q0 = __ldg(p.query_start + s);
+    const int q1 = __ldg(p.query_start + s + 1);
+    const int n = q1 - q0;
+    const int L = __ldg(p.context_lens + s);
+    const bool rows_ok = q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens &&
+                         n <= int(gridDim.x) * p.tile_tokens;
+    const bool len_ok = L >= n && L <= p.max_blocks * B;
+    if (!rows_ok || !len_ok) {
+        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0)
+            atomicOr(p.err, rows_ok ? PAGEDKV_DEVERR_CONTEXT_LEN : PAGEDKV_DEVERR_POSITION);
+        return;
+    }
+    const int j0 = qt * p.tile_tokens;
+    if (j0 >= n) return;
+    const int tokens = min(p.tile_tokens, n - j0);
+    const int rows = tokens * g;
+    const int pos0 = L - n + j0;
+    const int nkt = (pos0 + tokens - 1) / kTcKeys + 1;
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kTcStages; ++k) {
+            mbar_init(bar(kKvFull + k), 1);
+            mbar_init(bar(kKvEmpty + k), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kSFull + b), 1);
+            mbar_init(bar(kPFull + b), kTcRows);
+            mbar_init(bar(kOFull + b), 1);
+            mbar_init(bar(kOFree + b), kTcRows);
+        }
+        mbar_init(bar(kQFull), kTcRows);
+        mbar_init(bar(kDone), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(base + Ly::kTmemSlot, Ly::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly::kTmemSlot);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_descriptor(&kmap);
+            tma_prefetch_descriptor(&vmap);
+            const int32_t *table = p.block_tables + size_t(s) * p.max_blocks;
+            int armed = 0;
+            bool ok = true;
+            for (int j = 0; j < nkt; ++j) {
+                const int st = j % kTcStages;
+                if (*abort_flag ||
+                    !mbar_wait(bar(kKvEmpty + st), uint32_t((j / kTcStages) & 1) ^ 1u, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const int k0 = j * kTcKeys;
+                const int present = min(kTcKeys, L - k0);
+                const uint32_t kdst = base + Ly::kKv + st * Ly::kStage;
+                const uint32_t vdst = kdst + Ly::kHalf;
+                const uint32_t fb = bar(kKvFull + st);
+                if (B >= 16) {
+                    const int groups = (present + 15) >> 4;
+                    mbar_arrive_expect_tx(fb, uint32_t(groups * Ly::kSlabs * 2048 * 2));
+                    for (int i = 0; i < groups; ++i) {
+                        const int t = k0 + 16 * i;
+                        int pb = __ldg(table + (t >> p.log2_block));
+                        if (pb < 0 || pb >= p.num_blocks) {
+                            atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
+                            pb = 0;
+                        }
+                        const int z = pb * B + (t & (B - 1));
+                        for (int sl = 0; sl < Ly::kSlabs; ++sl) {
+                            const uint32_t off = sl * Ly::kKvSlab + i * 2048;
+                            tma_load_4d(kdst + off, &kmap, 0, z, sl, h, fb);
+                            tma_load_4d(vdst + off, &vmap, 0, z, sl, h, fb);
+                        }
+                    }
+                } else {
+                    const int blocks = (present + 7) >> 3;
+                    mbar_arrive_expect_tx(fb, uint32_t(blocks * Ly::kSlabs * 1024 * 2));
+                    for (int b = 0; b < blocks; ++b) {
+                        const int t = k0 + 8 * b;
+                        int pb = __ldg(table + (t >> p.log2_block));
+                        if (pb < 0 || pb >= p.num_blocks) {
+                            atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
+                            pb = 0;
+                        }
+                        for (int sl = 0; sl < Ly::kSlabs; ++sl) {
+                            const uint32_t off = sl * Ly::kKvSlab + b * 1024;
+                            tma_load_4d(kdst + off, &kmap, 0, pb * B, sl, h, fb);
+                            tma_load_4d(vdst + off, &vmap, 0, pb * B, sl, h, fb);
+                        }
+                    }
+                }
+                ++armed;
+            }
+            if (!ok) {
+                // stop everyone, then wait (bounded) for this CTA's copies still in flight
+                *abort_flag = 1;
+                const int first = armed > kTcStages ? armed - kTcStages : 0;
+                for (int k = first; k < armed; ++k)
+                    mbar_wait(bar(kKvFull + k % kTcStages), uint32_t((k / kTcStages) & 1), p.err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = tc_idesc_f16(kBf16, false, kTcRows, kTcKeys);
+            constexpr uint32_t kIdO = tc_idesc_f16(kBf16, true, kTcRows, D);
+            auto wait = [&](int i, int phase) {
+                return !*abort_flag && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
+            };
+            auto issue_s = [&](int j) {
+                const uint32_t kb = base + Ly::kKv + (j % kTcStages) * Ly::kStage;
+                const uint32_t d = tmem + uint32_t((j & 1) * kTcKeys);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = tc_desc_sw128(base + Ly::kQ + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = tc_desc_sw128(kb + (kk >> 2) * Ly::kKvSlab + (kk & 3) * 32, 16, 1024);
+                    tc_mma_f16(d, a, b, kIdS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(kSFull + (j & 1)));
+            };
+            auto issue_pv = [&](int j) {
+                const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
+                const uint32_t pb = base + Ly::kP + (j & 1) * Ly::kPBytes;
+                const uint32_t d = tmem + uint32_t(2 * kTcKeys + (j & 1) * D);
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t a = tc_desc_sw128(pb + kk * 32, 16, 1024);
+                    const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
+                    tc_mma_f16(d, a, b, kIdO, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(kOFull + (j & 1)));
+                tc_commit(bar(kKvEmpty + j % kTcStages));
+            };
+            bool ok = wait(kQFull, 0);
+            for (int j = 0; ok && j < 2 && j < nkt; ++j) {
+                ok = wait(kKvFull + j % kTcStages, j / kTcStages);
+                if (!ok) break;
+                tc_fence_after_sync();
+                issue_s(j);
+            }
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int b = j & 1;
+                ok = wait(kPFull + b, j >> 1);
+                if (ok && j >= 2) ok = wait(kOFree + b, (j - 2) >> 1);
+                if (!ok) break;
+                tc_fence_after_sync();
+                issue_pv(j);
+                if (j + 2 < nkt) {
+                    ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    issue_s(j + 2);
+                }
+            }
+            if (!ok) *abort_flag = 1;
+            // every MMA issued so far has completed before tensor memory is freed
+            tc_commit(bar(kDone));
+            mbar_wait(bar(kDone), 0, p.err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quarter = warp & 3;                 // tensor-memory lanes this warp may read
+        const int r = 32 * quarter + lane;            // query row of this thread
+        const uint32_t trow = tmem + (uint32_t(32 * quarter) << 16);
+        const int pos = r < rows ? pos0 + r / g : -1;
+        const size_t qrow = size_t(q0 + j0 + (r < rows ? r / g : 0)) * p.n_q_heads + h * g +
+                            (r < rows ? r % g : 0);
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = r < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                sts128(base + Ly::kQ + (c >> 3) * Ly::kQSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kQFull));
+        }
+        float o[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] = 0.f;
+        float m = -INFINITY, l = 0.f, alpha_pending = 1.f;
+        bool ok = true;
+
+        auto fold = [&](int i, float a) {   // O_reg = O_reg * a + O_tile(i)
+            const int b = i & 1;
+            bool got = !*abort_flag && mbar_wait(bar(kOFull + b), uint32_t((i >> 1) & 1), p.err);
+            if (!__all_sync(kAll, got)) return false;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tmem_ld32(trow + uint32_t(2 * kTcKeys + b * D + 32 * c), v);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) o[32 * c + x] = fmaf(o[32 * c + x], a, v[x]);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(kOFree + b));
+            return true;
+        };
+
+        for (int j = 0; j < nkt; ++j) {
+            const int b = j & 1;
+            bool got = !*abort_flag && mbar_wait(bar(kSFull + b), uint32_t((j >> 1) & 1), p.err);
+            if (!__all_sync(kAll, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            float sa[32], sb[32];   // keys 0-31 and 32-63 of the tile
+            tmem_ld32(trow + uint32_t(b * kTcKeys), sa);
+            tmem_ld32(trow + uint32_t(b * kTcKeys + 32), sb);
+            const int k0 = j * kTcKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sa[i] = k0 + i <= pos ? sa[i] * p.scale_log2 : -INFINITY;
+                sb[i] = k0 + 32 + i <= pos ? sb[i] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
+            }
+            const float mn = fmaxf(m, mx);
+            const float u = mn == -INFINITY ? 0.f : mn;   // a row with no key yet keeps zeros
+            const float alpha = fast_exp2(m - u);
+            m = mn;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sa[i] = fast_exp2(sa[i] - u);
+                sb[i] = fast_exp2(sb[i] - u);
+                sum += sa[i] + sb[i];
+            }
+            l = l * alpha + sum;
+            if (k0 + kTcKeys > L) {
+                // keys past the context: zero their V rows once the tile has landed
+                got = !*abort_flag &&
+                      mbar_wait(bar(kKvFull + j % kTcStages), uint32_t((j / kTcStages) & 1), p.err);
+                if (!__all_sync(kAll, got)) {
+                    ok = false;
+                    break;
+                }
+                if (r < kTcKeys && k0 + r >= L) {
+                    const uint32_t vrow = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf + r * 128;
+#pragma unroll
+                    for (int sl = 0; sl < Ly::kSlabs; ++sl)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            sts128(vrow + sl * Ly::kKvSlab + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                }
+                __syncwarp();
+            }
+            const uint32_t prow = base + Ly::kP + b * Ly::kPBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float *x = c < 4 ? sa + 8 * c : sb + 8 * (c - 4);
+                uint4 w;
+                w.x = Elem<T>::pack2(x[0], x[1]);
+                w.y = Elem<T>::pack2(x[2], x[3]);
+                w.z = Elem<T>::pack2(x[4], x[5]);
+                w.w = Elem<T>::pack2(x[6], x[7]);
+                sts128(prow + ((c ^ (r & 7)) << 4), w);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(bar(kPFull + b));
+            if (j >= 1 && !fold(j - 1, alpha_pending)) {
+                ok = false;
+                break;
+            }
+            alpha_pending = alpha;
+        }
+        if (ok) ok = fold(nkt - 1, alpha_pending);
+        if (!ok) {
+            *abort_flag = 1;
+        } else if (r < rows) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + qrow * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                uint4 w;
+                w.x = Elem<T>::pack2(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+                w.y = Elem<T>::pack2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                w.z = Elem<T>::pack2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                w.w = Elem<T>::pack2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                dst[c] = w;
+            }
+        }
+    }
+
+    // ---- every role is done: release the tensor memory
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, Ly::kTmemCols);
+    }
+}
+
+int prefill_tc_smem_bytes(int head_dim) {
+    return (head_dim == 64 ? TcLayout<64>::kTotal : TcLayout<128>::kTotal) + 1024;
+}
+
+template <typename T, int D>
+static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                      const PrefillParams &p, int max_query_len,
+                                      cudaStream_t stream) {
+    auto kernel = paged_prefill_tc_kernel<T, D>;
+    const int smem = TcLayout<D>::kTotal + 1024;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int opened[64] = {0};
+    if (dev < 64 && opened[dev] < smem) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        opened[dev] = smem;
+    }
+    const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
+    const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
+    kernel<<<grid, 192, smem, stream>>>(kmap, vmap, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
+                              cudaStream_t stream) {
+    const bool bf16 = dtype == PAGEDKV_BF16;
+    if (head_dim == 64)
+        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, p, max_query_len, stream)
+                    : launch_tc_instance<__half, 64>(kmap, vmap, p, max_query_len, stream);
+    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, p, max_query_len, stream)
+                : launch_tc_instance<__half, 128>(kmap, vmap, p, max_query_len, stream);
+}
+
+}  // namespace pkv

@@ -1,0 +1,103 @@
+// tcgen05.cuh -- inline-PTX wrappers for the fifth-generation tensor cores
+// (sm_100 family): tensor-memory allocation, shared-memory operand
+// descriptors, the kind::f16 MMA with fp32 accumulation in tensor memory,
+// completion tracking through mbarriers and tensor-memory loads.
+//
+// Encodings (from the PTX ISA's description of tcgen05):
+//   shared-memory matrix descriptor, 64 bits
+//     [0,14)  start address >> 4          [16,30) leading-dimension byte offset >> 4
+//     [32,46) stride-dimension byte offset >> 4
+//     [46,48) descriptor version (1)      [49,52) base offset (0: atoms 1024-B aligned)
+//     [61,64) layout: 2 = 128-byte swizzle
+//   instruction descriptor for kind::f16, 32 bits
+//     [4,6) accumulator type (1 = f32)    [7,10) A type, [10,13) B type (0 = f16, 1 = bf16)
+//     bit 15 A major, bit 16 B major (0 = K-major, 1 = M/N-major)
+//     [17,23) N >> 3                      [24,29) M >> 4
+// A 128-byte-swizzled operand is stored as 8-row atoms of 128-byte rows whose
+// 16-byte chunks are permuted by XOR with (row & 7): the layout that a TMA
+// load with 128-byte swizzle writes. K-major: rows are M (or N) indices, the
+// K elements of one row are contiguous; the stride-dimension offset is the
+// distance between 8-row atoms. M/N-major: rows are K indices holding 64
+// contiguous M (or N) elements; the leading-dimension offset is the distance
+// between 64-element column blocks, the stride-dimension offset the distance
+// between 8-row atoms along K.
+#pragma once
+
+#include <stdint.h>
+
+namespace pkv {
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// The mbarrier receives one arrival once every tcgen05 operation this thread
+// issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs, fp32 accumulation.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__host__ __device__ constexpr uint32_t tc_idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
+    return (1u << 4) | (uint32_t(bf16) << 7) | (uint32_t(bf16) << 10) |
+           (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t smem, uint32_t lbo_bytes,
+                                                  uint32_t sbo_bytes) {
+    return uint64_t((smem & 0x3FFFFu) >> 4) | (uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
+           (uint64_t(2) << 61);
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane; the wait
+// is part of the same statement, so no use of the values can precede it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace pkv

@@ -3,8 +3,8 @@
 The chunk's K/V go into NaN-poisoned pools through the library's slot mapping
 and append, as a serving step would do; then every query row of the chunk
 must match the oracle's causal attention over its sequence within the dtype's
-tolerance. A prompt prefilled chunk by chunk must give bit-identical rows to
-one pass over the whole prompt; one-row chunks must agree with decode; bad
+tolerance, on both kernels (warp-level MMA and tcgen05). A prompt prefilled
+chunk by chunk must give bit-identical rows to one pass over the whole prompt; one-row chunks must agree with decode; bad
 lengths are flagged on the device error word and leave their rows untouched.
 """
 import numpy as np
@@ -22,13 +22,17 @@ pytestmark = pytest.mark.gpu
 CASES = [(0, 1), (0, 77), (13, 50), (100, 130), (300, 1), (37, 0), (64, 64), (5, 200)]
 
 
-@pytest.fixture(scope="module", autouse=True)
-def gpu():
+@pytest.fixture(scope="module", autouse=True, params=[1, 2], ids=["mma_sync", "tcgen05"])
+def path(request):
+    """Every test runs on both kernels: warp-level MMA (1) and tcgen05 (2)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     pk.load()
     torch.cuda.set_device(0)
     pk.device_errors(reset=True)
+    pk.set_option(pk.OPT_PREFILL_PATH, request.param)
+    yield request.param
+    pk.set_option(pk.OPT_PREFILL_PATH, 0)
 
 
 def build(dtype, D, B, g, seed, cases=CASES, n_kv=2):
