@@ -14,15 +14,19 @@
 //              tensor core reads);
 //   warp 1     allocates tensor memory; its lane 0 issues every MMA:
 //              S = Q K^T into one of two S buffers in tensor memory, and, once
-//              the softmax has written P, O_tile = P V into one of two O
-//              buffers; completions are tracked by tcgen05.commit on mbarriers;
+//              the softmax has written P, O += P V into the O accumulator that
+//              stays in tensor memory for the whole key loop; completions are
+//              tracked by tcgen05.commit on mbarriers;
 //   warps 2-5  softmax, one thread per query row (= tensor-memory lane): read
-//              the S row, apply scale and the causal limit (a select, so K rows
-//              past the context never matter), keep the base-2 running max and
-//              sum, write P as a swizzled K-major operand in shared memory, and
-//              fold each finished O tile into registers with the running
-//              rescale; V rows past the context are zeroed in shared memory
-//              before their P V (the tensor core would turn 0 * NaN into NaN).
+//              the S row, apply the causal limit (a select, so K rows past the
+//              context never matter), exponentiate against a reference maximum
+//              and write P as a swizzled K-major operand in shared memory. The
+//              reference moves only when a tile's maximum exceeds it by more
+//              than 2^8 (P stays below 256, sums stay in fp32); when it moves,
+//              the warp rescales its rows of O in tensor memory before this
+//              tile's P V may start. The result is exact softmax attention.
+//              V rows past the context are zeroed in shared memory before their
+//              P V (the tensor core would turn 0 * NaN into NaN).
 // Every mbarrier wait is bounded in time; on a timeout the CTA stops, waits
 // for its copies and MMAs in flight, frees its tensor memory and exits.
 #include <cuda_bf16.h>
@@ -53,12 +57,12 @@ struct TcLayout {
     static constexpr int kP = kKv + kTcStages * kStage;    // two P buffers [128 rows][64 keys]
     static constexpr int kPBytes = kTcRows * kTcKeys * 2;
     static constexpr int kBars = kP + 2 * kPBytes;
-    static constexpr int kNumBars = 2 * kTcStages + 10;
+    static constexpr int kNumBars = 2 * kTcStages + 8;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
     static constexpr int kTotal = kFlag + 8;
-    // S buffers: columns [0, 128); O buffers: [128, 128 + 2 D)
-    static constexpr int kTmemCols = 2 * kTcKeys + 2 * D <= 256 ? 256 : 512;
+    // S buffers: columns [0, 128); O accumulator: [128, 128 + D)
+    static constexpr int kTmemCols = 2 * kTcKeys + D <= 256 ? 256 : 512;
 };
 
 // mbarrier indices
@@ -66,10 +70,13 @@ constexpr int kKvFull = 0;
 constexpr int kKvEmpty = kTcStages;
 constexpr int kSFull = 2 * kTcStages;
 constexpr int kPFull = kSFull + 2;
+// P V of tile j completes on O barrier j & 1: a wait on tile j's completion
+// then never meets a barrier two completions away from it (the one of tile
+// j - 2 has completed, since the S MMA of tile j was issued after it)
 constexpr int kOFull = kPFull + 2;
-constexpr int kOFree = kOFull + 2;
-constexpr int kQFull = kOFree + 2;
+constexpr int kQFull = kOFull + 2;
 constexpr int kDone = kQFull + 1;
+constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -127,9 +134,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kSFull + b), 1);
             mbar_init(bar(kPFull + b), kTcRows);
-            mbar_init(bar(kOFull + b), 1);
-            mbar_init(bar(kOFree + b), kTcRows);
         }
+        mbar_init(bar(kOFull), 1);
+        mbar_init(bar(kOFull + 1), 1);
         mbar_init(bar(kQFull), kTcRows);
         mbar_init(bar(kDone), 1);
         *abort_flag = 0;
@@ -231,12 +238,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             auto issue_pv = [&](int j) {
                 const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
                 const uint32_t pb = base + Ly::kP + (j & 1) * Ly::kPBytes;
-                const uint32_t d = tmem + uint32_t(2 * kTcKeys + (j & 1) * D);
+                const uint32_t d = tmem + uint32_t(2 * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t a = tc_desc_sw128(pb + kk * 32, 16, 1024);
                     const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
-                    tc_mma_f16(d, a, b, kIdO, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(d, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(kOFull + (j & 1)));
                 tc_commit(bar(kKvEmpty + j % kTcStages));
@@ -249,9 +256,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 issue_s(j);
             }
             for (int j = 0; ok && j < nkt; ++j) {
-                const int b = j & 1;
-                ok = wait(kPFull + b, j >> 1);
-                if (ok && j >= 2) ok = wait(kOFree + b, (j - 2) >> 1);
+                ok = wait(kPFull + (j & 1), j >> 1);
                 if (!ok) break;
                 tc_fence_after_sync();
                 issue_pv(j);
@@ -286,28 +291,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             fence_proxy_async_smem();
             mbar_arrive(bar(kQFull));
         }
-        float o[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.f;
-        float m = -INFINITY, l = 0.f, alpha_pending = 1.f;
+        const uint32_t otile = trow + uint32_t(2 * kTcKeys);
+        float ref = -INFINITY;   // reference maximum (base 2) that P and O are relative to
+        float l = 0.f;
         bool ok = true;
-
-        auto fold = [&](int i, float a) {   // O_reg = O_reg * a + O_tile(i)
-            const int b = i & 1;
-            bool got = !*abort_flag && mbar_wait(bar(kOFull + b), uint32_t((i >> 1) & 1), p.err);
-            if (!__all_sync(kAll, got)) return false;
-            tc_fence_after_sync();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-                tmem_ld32(trow + uint32_t(2 * kTcKeys + b * D + 32 * c), v);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) o[32 * c + x] = fmaf(o[32 * c + x], a, v[x]);
-            }
-            tc_fence_before_sync();
-            mbar_arrive(bar(kOFree + b));
-            return true;
-        };
 
         for (int j = 0; j < nkt; ++j) {
             const int b = j & 1;
@@ -322,21 +309,46 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             tmem_ld32(trow + uint32_t(b * kTcKeys + 32), sb);
             const int k0 = j * kTcKeys;
             float mx = -INFINITY;
+            if (k0 + kTcKeys - 1 <= pos) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sa[i] = k0 + i <= pos ? sa[i] * p.scale_log2 : -INFINITY;
-                sb[i] = k0 + 32 + i <= pos ? sb[i] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    sa[i] = k0 + i <= pos ? sa[i] : -INFINITY;
+                    sb[i] = k0 + 32 + i <= pos ? sb[i] : -INFINITY;
+                    mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
+                }
             }
-            const float mn = fmaxf(m, mx);
-            const float u = mn == -INFINITY ? 0.f : mn;   // a row with no key yet keeps zeros
-            const float alpha = fast_exp2(m - u);
-            m = mn;
+            mx *= p.scale_log2;
+            const bool move = mx > ref + kRescaleLog2;
+            const float alpha = move ? fast_exp2(ref - mx) : 1.f;   // 0 while no key was seen
+            if (move) ref = mx;
+            if (j > 0 && __any_sync(kAll, move)) {
+                // rescale this warp's rows of O (every earlier P V has completed first)
+                got = !*abort_flag &&
+                      mbar_wait(bar(kOFull + ((j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
+                if (!__all_sync(kAll, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(otile + uint32_t(32 * c), v);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] *= alpha;
+                    tmem_st32(otile + uint32_t(32 * c), v);
+                }
+            }
+            const float u = ref == -INFINITY ? 0.f : ref;
+            const float nu = -u;
             float sum = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                sa[i] = fast_exp2(sa[i] - u);
-                sb[i] = fast_exp2(sb[i] - u);
+                sa[i] = fast_exp2(fmaf(sa[i], p.scale_log2, nu));
+                sb[i] = fast_exp2(fmaf(sb[i], p.scale_log2, nu));
                 sum += sa[i] + sb[i];
             }
             l = l * alpha + sum;
@@ -372,26 +384,34 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(bar(kPFull + b));
-            if (j >= 1 && !fold(j - 1, alpha_pending)) {
-                ok = false;
-                break;
-            }
-            alpha_pending = alpha;
         }
-        if (ok) ok = fold(nkt - 1, alpha_pending);
+        if (ok) {
+            // the last P V's completion covers every earlier MMA of this thread
+            const bool got = !*abort_flag &&
+                             mbar_wait(bar(kOFull + ((nkt - 1) & 1)), uint32_t(((nkt - 1) >> 1) & 1), p.err);
+            ok = __all_sync(kAll, got);
+        }
         if (!ok) {
             *abort_flag = 1;
-        } else if (r < rows) {
+        } else {
+            tc_fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + qrow * D);
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                uint4 w;
-                w.x = Elem<T>::pack2(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-                w.y = Elem<T>::pack2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                w.z = Elem<T>::pack2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                w.w = Elem<T>::pack2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-                dst[c] = w;
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tmem_ld32(otile + uint32_t(32 * c), v);
+                if (r < rows) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 w;
+                        w.x = Elem<T>::pack2(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
+                        w.y = Elem<T>::pack2(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
+                        w.z = Elem<T>::pack2(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
+                        w.w = Elem<T>::pack2(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
+                        dst[4 * c + e] = w;
+                    }
+                }
             }
         }
     }
