@@ -38,7 +38,7 @@ int prefill_smem_bytes(int head_dim);
 
 // Grid: (query tiles of the longest chunk, kv heads, sequences). The warp-level
 // MMA kernel takes 64 query rows per CTA and pool maps with boxes of every
-// column block; the tcgen05 kernel takes 128 rows per CTA and pool maps with
+// column block; the tcgen05 kernel takes 256 rows per CTA and pool maps with
 // boxes of one 64-column block.
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
@@ -49,6 +49,6 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
-constexpr int kPfTcRows = 128;   // query rows per CTA of the tcgen05 kernel
+constexpr int kPfTcRows = 256;   // query rows per CTA of the tcgen05 kernel (two tiles of 128)
 
 }  // namespace pkv

@@ -5,30 +5,34 @@
 // to its own position, read through the block table), with the contractions
 // moved off the warp-level MMA pipe.
 //
-// One CTA owns (sequence, kv head, 128 query rows of (chunk token, query head
-// of the group)). Six warps:
+// One CTA owns (sequence, kv head, 256 query rows of (chunk token, query head
+// of the group)), held as two 128-row Q tiles that share every K/V tile. Ten
+// warps:
 //   warp 0     producer: per 64-key tile, looks up the block ids and issues one
 //              TMA box per (16 keys, 64-column block) for K and V into a
 //              three-stage ring, so that each operand lands as [column block]
 //              [64 keys][128 B] with 128-byte swizzle (the canonical layout the
 //              tensor core reads);
-//   warp 1     allocates tensor memory; its lane 0 issues every MMA:
+//   warp 1     allocates tensor memory; its lane 0 issues every MMA. Per Q tile:
 //              S = Q K^T into one of two S buffers in tensor memory, and, once
 //              the softmax has written P, O += P V into the O accumulator that
 //              stays in tensor memory for the whole key loop; completions are
 //              tracked by tcgen05.commit on mbarriers;
-//   warps 2-5  softmax, one thread per query row (= tensor-memory lane): read
-//              the S row, apply the causal limit (a select, so K rows past the
-//              context never matter), exponentiate against a reference maximum
-//              and write P as a swizzled K-major operand in shared memory. The
+//   warps 2-9  softmax, four warps per Q tile, one thread per query row (=
+//              tensor-memory lane), so that every SM sub-partition runs two
+//              softmax warps whose work interleaves. A thread reads its S row,
+//              applies the causal limit (a select, so K rows past the context
+//              never matter), exponentiates against a reference maximum and
+//              writes P as a swizzled K-major operand in shared memory. The
 //              reference moves only when a tile's maximum exceeds it by more
 //              than 2^8 (P stays below 256, sums stay in fp32); when it moves,
-//              the warp rescales its rows of O in tensor memory before this
+//              the warp rescales its rows of O in tensor memory before that
 //              tile's P V may start. The result is exact softmax attention.
-//              V rows past the context are zeroed in shared memory before their
-//              P V (the tensor core would turn 0 * NaN into NaN).
-// Every mbarrier wait is bounded in time; on a timeout the CTA stops, waits
-// for its copies and MMAs in flight, frees its tensor memory and exits.
+//              V rows past the context are zeroed in shared memory before any
+//              P V reads them (the tensor core would turn 0 * NaN into NaN).
+// A Q tile skips the key tiles that lie wholly past its last row. Every
+// mbarrier wait is bounded in time; on a timeout the CTA stops, waits for its
+// copies and MMAs in flight, frees its tensor memory and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,42 +45,44 @@ namespace pkv {
 namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
-constexpr int kTcRows = 128;     // query rows per CTA = tensor-memory lanes
+constexpr int kTcTiles = 2;      // Q tiles per CTA
+constexpr int kTcRows = 128;     // query rows per Q tile = tensor-memory lanes
 constexpr int kTcKeys = 64;      // keys per pipeline stage
 constexpr int kTcStages = 3;
+constexpr int kTcThreads = 64 + kTcTiles * kTcRows;
+constexpr int kTmemTile = 256;   // tensor-memory columns per Q tile: S, S, O
+constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
 
 template <int D>
 struct TcLayout {
     static constexpr int kSlabs = D * 2 / 128;             // 64-element column blocks per row
     static constexpr int kQSlab = kTcRows * 128;           // bytes of one Q column block
     static constexpr int kKvSlab = kTcKeys * 128;          // bytes of one K (or V) column block
-    static constexpr int kQ = 0;
-    static constexpr int kKv = kQ + kSlabs * kQSlab;       // stage s: K at kKv + s*kStage, V after it
+    static constexpr int kQTile = kSlabs * kQSlab;
+    static constexpr int kQ = 0;                           // Q tile t at kQ + t * kQTile
+    static constexpr int kKv = kQ + kTcTiles * kQTile;     // stage s: K at kKv + s*kStage, V after it
     static constexpr int kHalf = kSlabs * kKvSlab;
     static constexpr int kStage = 2 * kHalf;
-    static constexpr int kP = kKv + kTcStages * kStage;    // two P buffers [128 rows][64 keys]
+    static constexpr int kP = kKv + kTcStages * kStage;    // P buffer (t, b) at kP + (2t + b) kPBytes
     static constexpr int kPBytes = kTcRows * kTcKeys * 2;
-    static constexpr int kBars = kP + 2 * kPBytes;
-    static constexpr int kNumBars = 2 * kTcStages + 8;
+    static constexpr int kBars = kP + 2 * kTcTiles * kPBytes;
+    static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 2;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
     static constexpr int kTotal = kFlag + 8;
-    // S buffers: columns [0, 128); O accumulator: [128, 128 + D)
-    static constexpr int kTmemCols = 2 * kTcKeys + D <= 256 ? 256 : 512;
+    static_assert(2 * kTcKeys + D <= kTmemTile, "S buffers and O must fit a Q tile's columns");
 };
 
 // mbarrier indices
 constexpr int kKvFull = 0;
 constexpr int kKvEmpty = kTcStages;
-constexpr int kSFull = 2 * kTcStages;
-constexpr int kPFull = kSFull + 2;
-// P V of tile j completes on O barrier j & 1: a wait on tile j's completion
-// then never meets a barrier two completions away from it (the one of tile
-// j - 2 has completed, since the S MMA of tile j was issued after it)
-constexpr int kOFull = kPFull + 2;
-constexpr int kQFull = kOFull + 2;
+// per Q tile t, buffer b: S full, P full, O full (P V of key tile j completes
+// on O barrier j & 1, so a wait never meets a barrier two completions away)
+__device__ __forceinline__ int bar_s(int t, int b) { return 2 * kTcStages + 6 * t + b; }
+__device__ __forceinline__ int bar_p(int t, int b) { return 2 * kTcStages + 6 * t + 2 + b; }
+__device__ __forceinline__ int bar_o(int t, int b) { return 2 * kTcStages + 6 * t + 4 + b; }
+constexpr int kQFull = 2 * kTcStages + 6 * kTcTiles;
 constexpr int kDone = kQFull + 1;
-constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -86,7 +92,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 }  // namespace
 
 template <typename T, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using Ly = TcLayout<D>;
@@ -121,29 +127,37 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const int j0 = qt * p.tile_tokens;
     if (j0 >= n) return;
-    const int tokens = min(p.tile_tokens, n - j0);
-    const int rows = tokens * g;
-    const int pos0 = L - n + j0;
-    const int nkt = (pos0 + tokens - 1) / kTcKeys + 1;
+    const int rows = min(p.tile_tokens, n - j0) * g;   // rows of the CTA (both Q tiles)
+    const int pos0 = L - n + j0;                       // position of the CTA's first token
+    // key tiles of Q tile t: through the position of its last row
+    auto key_tiles = [&](int t) {
+        const int rt = min(max(rows - t * kTcRows, 0), kTcRows);
+        return rt > 0 ? (pos0 + (t * kTcRows + rt - 1) / g) / kTcKeys + 1 : 0;
+    };
+    const int nk0 = key_tiles(0), nk1 = key_tiles(1);
+    auto nkt_of = [&](int t) { return t ? nk1 : nk0; };
+    const int t_last = nk1 > 0 ? 1 : 0;                // holds the CTA's last row
+    const int nkt = t_last ? nk1 : nk0;
+    const bool tail = nkt * kTcKeys > L;               // the last key tile runs past the context
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kTcStages; ++k) {
             mbar_init(bar(kKvFull + k), 1);
             mbar_init(bar(kKvEmpty + k), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kSFull + b), 1);
-            mbar_init(bar(kPFull + b), kTcRows);
-        }
-        mbar_init(bar(kOFull), 1);
-        mbar_init(bar(kOFull + 1), 1);
-        mbar_init(bar(kQFull), kTcRows);
+        for (int t = 0; t < kTcTiles; ++t)
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar(bar_s(t, b)), 1);
+                mbar_init(bar(bar_p(t, b)), kTcRows);
+                mbar_init(bar(bar_o(t, b)), 1);
+            }
+        mbar_init(bar(kQFull), kTcTiles * kTcRows);
         mbar_init(bar(kDone), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(base + Ly::kTmemSlot, Ly::kTmemCols);
+        tmem_alloc(base + Ly::kTmemSlot, kTcTiles * kTmemTile);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -175,13 +189,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int groups = (present + 15) >> 4;
                     mbar_arrive_expect_tx(fb, uint32_t(groups * Ly::kSlabs * 2048 * 2));
                     for (int i = 0; i < groups; ++i) {
-                        const int t = k0 + 16 * i;
-                        int pb = __ldg(table + (t >> p.log2_block));
+                        const int tok = k0 + 16 * i;
+                        int pb = __ldg(table + (tok >> p.log2_block));
                         if (pb < 0 || pb >= p.num_blocks) {
                             atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
                             pb = 0;
                         }
-                        const int z = pb * B + (t & (B - 1));
+                        const int z = pb * B + (tok & (B - 1));
                         for (int sl = 0; sl < Ly::kSlabs; ++sl) {
                             const uint32_t off = sl * Ly::kKvSlab + i * 2048;
                             tma_load_4d(kdst + off, &kmap, 0, z, sl, h, fb);
@@ -192,8 +206,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int blocks = (present + 7) >> 3;
                     mbar_arrive_expect_tx(fb, uint32_t(blocks * Ly::kSlabs * 1024 * 2));
                     for (int b = 0; b < blocks; ++b) {
-                        const int t = k0 + 8 * b;
-                        int pb = __ldg(table + (t >> p.log2_block));
+                        const int tok = k0 + 8 * b;
+                        int pb = __ldg(table + (tok >> p.log2_block));
                         if (pb < 0 || pb >= p.num_blocks) {
                             atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
                             pb = 0;
@@ -224,47 +238,59 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             auto wait = [&](int i, int phase) {
                 return !*abort_flag && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
             };
-            auto issue_s = [&](int j) {
+            auto issue_s = [&](int t, int j) {
+                const uint32_t qb = base + Ly::kQ + t * Ly::kQTile;
                 const uint32_t kb = base + Ly::kKv + (j % kTcStages) * Ly::kStage;
-                const uint32_t d = tmem + uint32_t((j & 1) * kTcKeys);
+                const uint32_t d = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc_desc_sw128(base + Ly::kQ + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = tc_desc_sw128(qb + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc_desc_sw128(kb + (kk >> 2) * Ly::kKvSlab + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16(d, a, b, kIdS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(kSFull + (j & 1)));
+                tc_commit(bar(bar_s(t, j & 1)));
             };
-            auto issue_pv = [&](int j) {
+            auto issue_pv = [&](int t, int j) {
                 const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
-                const uint32_t pb = base + Ly::kP + (j & 1) * Ly::kPBytes;
-                const uint32_t d = tmem + uint32_t(2 * kTcKeys);
+                const uint32_t pb = base + Ly::kP + (2 * t + (j & 1)) * Ly::kPBytes;
+                const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t a = tc_desc_sw128(pb + kk * 32, 16, 1024);
                     const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
                     tc_mma_f16(d, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(kOFull + (j & 1)));
-                tc_commit(bar(kKvEmpty + j % kTcStages));
+                tc_commit(bar(bar_o(t, j & 1)));
             };
             bool ok = wait(kQFull, 0);
             for (int j = 0; ok && j < 2 && j < nkt; ++j) {
                 ok = wait(kKvFull + j % kTcStages, j / kTcStages);
                 if (!ok) break;
                 tc_fence_after_sync();
-                issue_s(j);
+                for (int t = 0; t < kTcTiles; ++t)
+                    if (j < nkt_of(t)) issue_s(t, j);
             }
             for (int j = 0; ok && j < nkt; ++j) {
-                ok = wait(kPFull + (j & 1), j >> 1);
+                // the last key tile's V rows past the context are zeroed by the
+                // last Q tile's softmax: every P of that tile must be in first
+                const bool all_first = tail && j == nkt - 1;
+                for (int t = 0; ok && all_first && t < kTcTiles; ++t)
+                    if (j < nkt_of(t)) ok = wait(bar_p(t, j & 1), j >> 1);
+                for (int t = 0; ok && t < kTcTiles; ++t) {
+                    if (j >= nkt_of(t)) continue;
+                    if (!all_first) ok = wait(bar_p(t, j & 1), j >> 1);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    issue_pv(t, j);
+                }
                 if (!ok) break;
-                tc_fence_after_sync();
-                issue_pv(j);
+                tc_commit(bar(kKvEmpty + j % kTcStages));
                 if (j + 2 < nkt) {
                     ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_s(j + 2);
+                    for (int t = 0; t < kTcTiles; ++t)
+                        if (j + 2 < nkt_of(t)) issue_s(t, j + 2);
                 }
             }
             if (!ok) *abort_flag = 1;
@@ -275,59 +301,62 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;                 // tensor-memory lanes this warp may read
-        const int r = 32 * quarter + lane;            // query row of this thread
-        const uint32_t trow = tmem + (uint32_t(32 * quarter) << 16);
-        const int pos = r < rows ? pos0 + r / g : -1;
-        const size_t qrow = size_t(q0 + j0 + (r < rows ? r / g : 0)) * p.n_q_heads + h * g +
-                            (r < rows ? r % g : 0);
+        const int t = (warp - 2) >> 2;                 // Q tile of this warp
+        const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
+        const int r = 32 * quarter + lane;             // row within the Q tile
+        const int R = t * kTcRows + r;                 // row within the CTA
+        const uint32_t trow = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(t * kTmemTile);
+        const uint32_t otile = trow + uint32_t(2 * kTcKeys);
+        const int pos = R < rows ? pos0 + R / g : -1;
+        const int nk = nkt_of(t);
+        const size_t qrow = size_t(q0 + j0 + (R < rows ? R / g : 0)) * p.n_q_heads + h * g +
+                            (R < rows ? R % g : 0);
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
+            const uint32_t qdst = base + Ly::kQ + t * Ly::kQTile + r * 128;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = r < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                sts128(base + Ly::kQ + (c >> 3) * Ly::kQSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+                const uint4 v = R < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                sts128(qdst + (c >> 3) * Ly::kQSlab + (((c & 7) ^ (r & 7)) << 4), v);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(kQFull));
         }
-        const uint32_t otile = trow + uint32_t(2 * kTcKeys);
         float ref = -INFINITY;   // reference maximum (base 2) that P and O are relative to
         float l = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < nkt; ++j) {
+        for (int j = 0; j < nk; ++j) {
             const int b = j & 1;
-            bool got = !*abort_flag && mbar_wait(bar(kSFull + b), uint32_t((j >> 1) & 1), p.err);
+            bool got = !*abort_flag && mbar_wait(bar(bar_s(t, b)), uint32_t((j >> 1) & 1), p.err);
             if (!__all_sync(kAll, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            float sa[32], sb[32];   // keys 0-31 and 32-63 of the tile
-            tmem_ld32(trow + uint32_t(b * kTcKeys), sa);
-            tmem_ld32(trow + uint32_t(b * kTcKeys + 32), sb);
+            float sc[kTcKeys];
+            tmem_ld64(trow + uint32_t(b * kTcKeys), sc);
             const int k0 = j * kTcKeys;
-            float mx = -INFINITY;
-            if (k0 + kTcKeys - 1 <= pos) {
+            if (k0 + kTcKeys - 1 > pos) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    sa[i] = k0 + i <= pos ? sa[i] : -INFINITY;
-                    sb[i] = k0 + 32 + i <= pos ? sb[i] : -INFINITY;
-                    mx = fmaxf(mx, fmaxf(sa[i], sb[i]));
-                }
+                for (int i = 0; i < kTcKeys; ++i) sc[i] = k0 + i <= pos ? sc[i] : -INFINITY;
             }
-            mx *= p.scale_log2;
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < kTcKeys; i += 4) {
+                m4[0] = fmaxf(m4[0], sc[i]);
+                m4[1] = fmaxf(m4[1], sc[i + 1]);
+                m4[2] = fmaxf(m4[2], sc[i + 2]);
+                m4[3] = fmaxf(m4[3], sc[i + 3]);
+            }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
             const bool move = mx > ref + kRescaleLog2;
             const float alpha = move ? fast_exp2(ref - mx) : 1.f;   // 0 while no key was seen
             if (move) ref = mx;
             if (j > 0 && __any_sync(kAll, move)) {
                 // rescale this warp's rows of O (every earlier P V has completed first)
                 got = !*abort_flag &&
-                      mbar_wait(bar(kOFull + ((j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
+                      mbar_wait(bar(bar_o(t, (j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
                 if (!__all_sync(kAll, got)) {
                     ok = false;
                     break;
@@ -342,17 +371,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     tmem_st32(otile + uint32_t(32 * c), v);
                 }
             }
-            const float u = ref == -INFINITY ? 0.f : ref;
-            const float nu = -u;
-            float sum = 0.f;
+            const float nu = ref == -INFINITY ? 0.f : -ref;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sa[i] = fast_exp2(fmaf(sa[i], p.scale_log2, nu));
-                sb[i] = fast_exp2(fmaf(sb[i], p.scale_log2, nu));
-                sum += sa[i] + sb[i];
+            for (int i = 0; i < kTcKeys; ++i) {
+                sc[i] = fast_exp2(fmaf(sc[i], p.scale_log2, nu));
+                s4[i & 3] += sc[i];
             }
-            l = l * alpha + sum;
-            if (k0 + kTcKeys > L) {
+            l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+            if (tail && t == t_last && j == nkt - 1) {
                 // keys past the context: zero their V rows once the tile has landed
                 got = !*abort_flag &&
                       mbar_wait(bar(kKvFull + j % kTcStages), uint32_t((j / kTcStages) & 1), p.err);
@@ -370,30 +397,29 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 __syncwarp();
             }
-            const uint32_t prow = base + Ly::kP + b * Ly::kPBytes + r * 128;
+            const uint32_t prow = base + Ly::kP + (2 * t + b) * Ly::kPBytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const float *x = c < 4 ? sa + 8 * c : sb + 8 * (c - 4);
                 uint4 w;
-                w.x = Elem<T>::pack2(x[0], x[1]);
-                w.y = Elem<T>::pack2(x[2], x[3]);
-                w.z = Elem<T>::pack2(x[4], x[5]);
-                w.w = Elem<T>::pack2(x[6], x[7]);
+                w.x = Elem<T>::pack2(sc[8 * c + 0], sc[8 * c + 1]);
+                w.y = Elem<T>::pack2(sc[8 * c + 2], sc[8 * c + 3]);
+                w.z = Elem<T>::pack2(sc[8 * c + 4], sc[8 * c + 5]);
+                w.w = Elem<T>::pack2(sc[8 * c + 6], sc[8 * c + 7]);
                 sts128(prow + ((c ^ (r & 7)) << 4), w);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            mbar_arrive(bar(kPFull + b));
+            mbar_arrive(bar(bar_p(t, b)));
         }
-        if (ok) {
-            // the last P V's completion covers every earlier MMA of this thread
+        if (ok && nk > 0) {
+            // the last P V's completion covers every earlier MMA of the issuing thread
             const bool got = !*abort_flag &&
-                             mbar_wait(bar(kOFull + ((nkt - 1) & 1)), uint32_t(((nkt - 1) >> 1) & 1), p.err);
+                             mbar_wait(bar(bar_o(t, (nk - 1) & 1)), uint32_t(((nk - 1) >> 1) & 1), p.err);
             ok = __all_sync(kAll, got);
         }
         if (!ok) {
             *abort_flag = 1;
-        } else {
+        } else if (nk > 0) {
             tc_fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + qrow * D);
@@ -401,7 +427,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int c = 0; c < D / 32; ++c) {
                 float v[32];
                 tmem_ld32(otile + uint32_t(32 * c), v);
-                if (r < rows) {
+                if (R < rows) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint4 w;
@@ -421,7 +447,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, Ly::kTmemCols);
+        tmem_dealloc(tmem, kTcTiles * kTmemTile);
     }
 }
 
@@ -446,7 +472,7 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     }
     const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
     const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
-    kernel<<<grid, 192, smem, stream>>>(kmap, vmap, p);
+    kernel<<<grid, kTcThreads, smem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 

@@ -121,7 +121,7 @@ def test_one_row_chunks_agree_with_decode(orc):
 
 
 def test_bad_lengths_are_flagged_and_left_unwritten(orc):
-    cases = [(10, 20), (5, 30), (0, 100)]
+    cases = [(10, 20), (5, 30), (0, 300)]
     wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, 2, seed=500, cases=cases)
     # sequence 1 claims fewer cached tokens than its chunk has rows
     lens = wl.context_lens.copy()
@@ -136,7 +136,8 @@ def test_bad_lengths_are_flagged_and_left_unwritten(orc):
                       units=[(0, 0), (0, 1), (2, 0), (2, 1)])
     keep = np.r_[qs[0]:qs[1], qs[2]:qs[3]]
     assert float(np.abs(got[keep] - ref[keep]).max()) <= TOL["bf16"]
-    # a chunk longer than the grid that max_query_len sized
+    # a chunk longer than the grid that max_query_len sized (300 rows; a CTA
+    # covers at most 128 tokens of group 2 on either kernel)
     out = prefill(wl, qs, q, kc, vc, bt, max_query_len=10)
     assert pk.device_errors() & 0x08
     assert np.isnan(to_f64(out)[qs[2]:qs[3]]).all()
