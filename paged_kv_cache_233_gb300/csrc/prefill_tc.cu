@@ -48,7 +48,7 @@ constexpr unsigned kAll = 0xffffffffu;
 constexpr int kTcTiles = 2;      // Q tiles per CTA
 constexpr int kTcRows = 128;     // query rows per Q tile = tensor-memory lanes
 constexpr int kTcKeys = 64;      // keys per pipeline stage
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr int kTcThreads = 64 + kTcTiles * kTcRows;
 constexpr int kTmemTile = 256;   // tensor-memory columns per Q tile: S, S, O
 constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
@@ -63,9 +63,9 @@ struct TcLayout {
     static constexpr int kKv = kQ + kTcTiles * kQTile;     // stage s: K at kKv + s*kStage, V after it
     static constexpr int kHalf = kSlabs * kKvSlab;
     static constexpr int kStage = 2 * kHalf;
-    static constexpr int kP = kKv + kTcStages * kStage;    // P buffer (t, b) at kP + (2t + b) kPBytes
+    static constexpr int kP = kKv + kTcStages * kStage;    // P buffer of Q tile t at kP + t kPBytes
     static constexpr int kPBytes = kTcRows * kTcKeys * 2;
-    static constexpr int kBars = kP + 2 * kTcTiles * kPBytes;
+    static constexpr int kBars = kP + kTcTiles * kPBytes;
     static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 2;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
@@ -252,7 +252,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             };
             auto issue_pv = [&](int t, int j) {
                 const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
-                const uint32_t pb = base + Ly::kP + (2 * t + (j & 1)) * Ly::kPBytes;
+                const uint32_t pb = base + Ly::kP + t * Ly::kPBytes;
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
@@ -397,7 +397,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 __syncwarp();
             }
-            const uint32_t prow = base + Ly::kP + (2 * t + b) * Ly::kPBytes + r * 128;
+            if (j > 0) {
+                // one P buffer per Q tile: the previous key tile's P V must be done with it
+                got = !*abort_flag &&
+                      mbar_wait(bar(bar_o(t, (j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
+                if (!__all_sync(kAll, got)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const uint32_t prow = base + Ly::kP + t * Ly::kPBytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint4 w;
