@@ -374,9 +374,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const float nu = ref == -INFINITY ? 0.f : -ref;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                sc[i] = fast_exp2(fmaf(sc[i], p.scale_log2, nu));
-                s4[i & 3] += sc[i];
+            for (int i = 0; i < kTcKeys; i += 2) {
+                ffma2(sc[i], sc[i + 1], p.scale_log2, nu);
+                sc[i] = fast_exp2(sc[i]);
+                sc[i + 1] = fast_exp2(sc[i + 1]);
+                if (i & 2) fadd2(s4[2], s4[3], sc[i], sc[i + 1]);
+                else fadd2(s4[0], s4[1], sc[i], sc[i + 1]);
             }
             l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
             if (tail && t == t_last && j == nkt - 1) {

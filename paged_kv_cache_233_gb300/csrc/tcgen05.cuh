@@ -67,6 +67,29 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Two-wide fp32 arithmetic of the sm_100 family (one instruction, two lanes
+// of work): (x0, x1) = (x0, x1) * s + c, and (a0, a1) += (x0, x1).
+__device__ __forceinline__ void ffma2(float &x0, float &x1, float s, float c) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %2};\n\t"
+        "mov.b64 c, {%3, %3};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(s), "f"(c));
+}
+
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float x0, float x1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1));
+}
+
 __host__ __device__ constexpr uint32_t tc_idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
     return (1u << 4) | (uint32_t(bf16) << 7) | (uint32_t(bf16) << 10) |
            (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
