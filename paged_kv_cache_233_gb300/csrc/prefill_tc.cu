@@ -15,15 +15,17 @@
 //              tensor core reads);
 //   warp 1     allocates tensor memory; its lane 0 issues every MMA. Per Q tile:
 //              S = Q K^T into one of two S buffers in tensor memory, and, once
-//              the softmax has written P, O += P V into the O accumulator that
-//              stays in tensor memory for the whole key loop; completions are
-//              tracked by tcgen05.commit on mbarriers;
+//              the softmax has written P, O += P V with P read from tensor
+//              memory, into the O accumulator that stays in tensor memory for
+//              the whole key loop; completions are tracked by tcgen05.commit
+//              on mbarriers;
 //   warps 2-9  softmax, four warps per Q tile, one thread per query row (=
 //              tensor-memory lane), so that every SM sub-partition runs two
 //              softmax warps whose work interleaves. A thread reads its S row,
 //              applies the causal limit (a select, so K rows past the context
 //              never matter), exponentiates against a reference maximum and
-//              writes P as a swizzled K-major operand in shared memory. The
+//              writes P (packed 16-bit pairs) over the first half of the same
+//              S buffer in tensor memory, so P never touches shared memory. The
 //              reference moves only when a tile's maximum exceeds it by more
 //              than 2^8 (P stays below 256, sums stay in fp32); when it moves,
 //              the warp rescales its rows of O in tensor memory before that
@@ -63,9 +65,7 @@ struct TcLayout {
     static constexpr int kKv = kQ + kTcTiles * kQTile;     // stage s: K at kKv + s*kStage, V after it
     static constexpr int kHalf = kSlabs * kKvSlab;
     static constexpr int kStage = 2 * kHalf;
-    static constexpr int kP = kKv + kTcStages * kStage;    // P buffer of Q tile t at kP + t kPBytes
-    static constexpr int kPBytes = kTcRows * kTcKeys * 2;
-    static constexpr int kBars = kP + kTcTiles * kPBytes;
+    static constexpr int kBars = kKv + kTcStages * kStage;
     static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 2;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
@@ -252,13 +252,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             };
             auto issue_pv = [&](int t, int j) {
                 const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
-                const uint32_t pb = base + Ly::kP + t * Ly::kPBytes;
+                // P of key tile j: the first 32 columns of S buffer j & 1 (16 keys per 8 columns)
+                const uint32_t pa = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t a = tc_desc_sw128(pb + kk * 32, 16, 1024);
                     const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
-                    tc_mma_f16(d, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(bar_o(t, j & 1)));
             };
@@ -343,11 +343,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kTcKeys; i += 4) {
-                m4[0] = fmaxf(m4[0], sc[i]);
-                m4[1] = fmaxf(m4[1], sc[i + 1]);
-                m4[2] = fmaxf(m4[2], sc[i + 2]);
-                m4[3] = fmaxf(m4[3], sc[i + 3]);
+            for (int i = 0; i < kTcKeys; i += 8) {
+                m4[0] = fmax3(m4[0], sc[i], sc[i + 1]);
+                m4[1] = fmax3(m4[1], sc[i + 2], sc[i + 3]);
+                m4[2] = fmax3(m4[2], sc[i + 4], sc[i + 5]);
+                m4[3] = fmax3(m4[3], sc[i + 6], sc[i + 7]);
             }
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
             const bool move = mx > ref + kRescaleLog2;
@@ -398,28 +398,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         for (int c = 0; c < 8; ++c)
                             sts128(vrow + sl * Ly::kKvSlab + c * 16, make_uint4(0u, 0u, 0u, 0u));
                 }
+                fence_proxy_async_smem();
                 __syncwarp();
             }
-            if (j > 0) {
-                // one P buffer per Q tile: the previous key tile's P V must be done with it
-                got = !*abort_flag &&
-                      mbar_wait(bar(bar_o(t, (j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
-                if (!__all_sync(kAll, got)) {
-                    ok = false;
-                    break;
-                }
-            }
-            const uint32_t prow = base + Ly::kP + t * Ly::kPBytes + r * 128;
+            uint32_t pk[kTcKeys / 2];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 w;
-                w.x = Elem<T>::pack2(sc[8 * c + 0], sc[8 * c + 1]);
-                w.y = Elem<T>::pack2(sc[8 * c + 2], sc[8 * c + 3]);
-                w.z = Elem<T>::pack2(sc[8 * c + 4], sc[8 * c + 5]);
-                w.w = Elem<T>::pack2(sc[8 * c + 6], sc[8 * c + 7]);
-                sts128(prow + ((c ^ (r & 7)) << 4), w);
-            }
-            fence_proxy_async_smem();
+            for (int c = 0; c < kTcKeys / 2; ++c) pk[c] = Elem<T>::pack2(sc[2 * c], sc[2 * c + 1]);
+            tmem_st32u(trow + uint32_t(b * kTcKeys), pk);
             tc_fence_before_sync();
             mbar_arrive(bar(bar_p(t, b)));
         }
