@@ -273,26 +273,77 @@ def time_steps(step, steps, dist_ctx):
 
 
 def time_e2e(step, steps):
-    """Same step through the public API with host inputs: pinned host -> device
-    copies of the step's inputs and a device -> host read of its output."""
+    """Same step through the public API with host inputs: every step copies its
+    inputs from pinned host memory to the device and reads its output back.
+
+    The step's seven input arrays are packed in one pinned host buffer and
+    copied with one transfer into one of two device staging buffers; the copy
+    of step i+1 and the read-back of step i run on a copy stream while step i
+    computes (double-buffered inputs and outputs), as a serving loop would
+    overlap them."""
     wl, t = step.wl, step.t
-    host = {name: x.cpu().pin_memory() for name, x in (
-        ("q", t["q"]), ("k", t["k_step"]), ("v", t["v_step"]), ("bt", step.bt),
-        ("lens", step.lens), ("seq", step.step_seq), ("pos", step.step_pos))}
-    dev = {"q": t["q"], "k": t["k_step"], "v": t["v_step"], "bt": step.bt, "lens": step.lens,
-           "seq": step.step_seq, "pos": step.step_pos}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    names = ("q", "k", "v", "bt", "lens", "seq", "pos")
+    src = dict(zip(names, (t["q"], t["k_step"], t["v_step"], step.bt, step.lens,
+                           step.step_seq, step.step_pos)))
+    offs, size = {}, 0
+    for n in names:
+        offs[n] = size
+        size += (src[n].numel() * src[n].element_size() + 255) // 256 * 256
+    host = torch.empty(size, dtype=torch.uint8).pin_memory()
+    for n in names:
+        x = src[n].contiguous().cpu()
+        nb = x.numel() * x.element_size()
+        host[offs[n]:offs[n] + nb].copy_(x.view(-1).view(torch.uint8))
+    dev = [torch.empty(size, dtype=torch.uint8, device=step.out.device) for _ in range(2)]
+
+    def views(buf):
+        v = {}
+        for n in names:
+            x = src[n]
+            nb = x.numel() * x.element_size()
+            v[n] = buf[offs[n]:offs[n] + nb].view(x.dtype).view(x.shape)
+        return v
+
+    vs = [views(d) for d in dev]
+    outs = [step.out, torch.empty_like(step.out)]
+    out_host = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(src[n].numel() * src[n].element_size() for n in names)
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    pk = step.pk
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def run(v, out):
+        pk.paged_kv_slot_mapping(v["bt"], v["seq"], v["pos"], step.slots, wl.num_blocks,
+                                 wl.block_size)
+        pk.paged_kv_append(v["k"], v["v"], step.slots, step.kc, step.vc)
+        pk.paged_attention_decode(v["q"], step.kc, step.vc, v["bt"], v["lens"], wl.scale, out,
+                                  step.partition, step.ws)
+
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        for name, x in host.items():
-            dev[name].copy_(x, non_blocking=True)
-        step.run()
-        out_host.copy_(step.out, non_blocking=True)
-    e1.record()
+    e0.record(compute)
+    copy.wait_stream(compute)
+    with torch.cuda.stream(copy):
+        dev[0].copy_(host, non_blocking=True)
+        ready[0].record(copy)
+    for i in range(steps):
+        b = i % 2
+        compute.wait_event(ready[b])
+        run(vs[b], outs[b])
+        done[b].record(compute)
+        with torch.cuda.stream(copy):
+            if i + 1 < steps:
+                if i >= 1:
+                    copy.wait_event(done[1 - b])       # step i-1 no longer reads that buffer
+                dev[1 - b].copy_(host, non_blocking=True)
+                ready[1 - b].record(copy)
+            copy.wait_event(done[b])
+            out_host[b].copy_(outs[b], non_blocking=True)
+    compute.wait_stream(copy)
+    e1.record(compute)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
