@@ -175,48 +175,39 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             bool ok = true;
             for (int j = 0; j < nkt; ++j) {
                 const int st = j % kTcStages;
+                const int k0 = j * kTcKeys;
+                const int present = min(kTcKeys, L - k0);
+                // every block id of the tile first, while the slot may still be
+                // busy (independent loads in flight together), then the copies
+                const int rows_per_box = B >= 16 ? 16 : 8;
+                const int boxes = (present + rows_per_box - 1) / rows_per_box;
+                int pbs[kTcKeys / 8];
+#pragma unroll
+                for (int i = 0; i < kTcKeys / 8; ++i)
+                    pbs[i] = i < boxes ? __ldg(table + ((k0 + rows_per_box * i) >> p.log2_block)) : 0;
                 if (*abort_flag ||
                     !mbar_wait(bar(kKvEmpty + st), uint32_t((j / kTcStages) & 1) ^ 1u, p.err)) {
                     ok = false;
                     break;
                 }
-                const int k0 = j * kTcKeys;
-                const int present = min(kTcKeys, L - k0);
                 const uint32_t kdst = base + Ly::kKv + st * Ly::kStage;
                 const uint32_t vdst = kdst + Ly::kHalf;
                 const uint32_t fb = bar(kKvFull + st);
-                if (B >= 16) {
-                    const int groups = (present + 15) >> 4;
-                    mbar_arrive_expect_tx(fb, uint32_t(groups * Ly::kSlabs * 2048 * 2));
-                    for (int i = 0; i < groups; ++i) {
-                        const int tok = k0 + 16 * i;
-                        int pb = __ldg(table + (tok >> p.log2_block));
-                        if (pb < 0 || pb >= p.num_blocks) {
-                            atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
-                            pb = 0;
-                        }
-                        const int z = pb * B + (tok & (B - 1));
-                        for (int sl = 0; sl < Ly::kSlabs; ++sl) {
-                            const uint32_t off = sl * Ly::kKvSlab + i * 2048;
-                            tma_load_4d(kdst + off, &kmap, 0, z, sl, h, fb);
-                            tma_load_4d(vdst + off, &vmap, 0, z, sl, h, fb);
-                        }
+                mbar_arrive_expect_tx(fb, uint32_t(boxes * Ly::kSlabs * rows_per_box * 128 * 2));
+#pragma unroll
+                for (int i = 0; i < kTcKeys / 8; ++i) {
+                    if (i >= boxes) break;
+                    const int tok = k0 + rows_per_box * i;
+                    int pb = pbs[i];
+                    if (pb < 0 || pb >= p.num_blocks) {
+                        atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
+                        pb = 0;
                     }
-                } else {
-                    const int blocks = (present + 7) >> 3;
-                    mbar_arrive_expect_tx(fb, uint32_t(blocks * Ly::kSlabs * 1024 * 2));
-                    for (int b = 0; b < blocks; ++b) {
-                        const int tok = k0 + 8 * b;
-                        int pb = __ldg(table + (tok >> p.log2_block));
-                        if (pb < 0 || pb >= p.num_blocks) {
-                            atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
-                            pb = 0;
-                        }
-                        for (int sl = 0; sl < Ly::kSlabs; ++sl) {
-                            const uint32_t off = sl * Ly::kKvSlab + b * 1024;
-                            tma_load_4d(kdst + off, &kmap, 0, pb * B, sl, h, fb);
-                            tma_load_4d(vdst + off, &vmap, 0, pb * B, sl, h, fb);
-                        }
+                    const int z = pb * B + (tok & (B - 1));
+                    for (int sl = 0; sl < Ly::kSlabs; ++sl) {
+                        const uint32_t off = sl * Ly::kKvSlab + i * rows_per_box * 128;
+                        tma_load_4d(kdst + off, &kmap, 0, z, sl, h, fb);
+                        tma_load_4d(vdst + off, &vmap, 0, z, sl, h, fb);
                     }
                 }
                 ++armed;
