@@ -146,6 +146,29 @@ def test_split_partition_states(orc, dtype, path):
 # Edge cases
 # ---------------------------------------------------------------------------
 
+def test_largest_batch_and_one_past_it(orc):
+    """The largest batch the decode accepts (4096 sequences; their per-sequence
+    unit counts live in shared memory), split and not, against sampled oracle
+    rows; one sequence more is refused on the host."""
+    rng = np.random.default_rng(44)
+    lens = rng.integers(1, 80, size=4096)
+    wl = make_workload("max_batch", "f16", lens, 4, 2, 64, 16, 45)
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    units = [(int(s), int(h)) for s in rng.choice(wl.num_seqs, 24, replace=False) for h in range(2)]
+    ref = oracle_decode(orc, wl, t["q"], okc, ovc, units=units)
+    for P in (0, 32):
+        out, _ = gpu_decode(wl, t["q"], kc, vc, bt, P)
+        assert_close(out, ref, "f16", rows=units_to_rows(wl, units), what=f"P={P}")
+    assert pk.device_errors() == 0
+    q = torch.zeros(4097, 4, 64, dtype=torch.float16, device="cuda")
+    bt2 = torch.zeros(4097, 1, dtype=torch.int32, device="cuda")
+    lens2 = torch.ones(4097, dtype=torch.int32, device="cuda")
+    with pytest.raises(pk.PagedKVError, match="unsupported"):
+        pk.paged_attention_decode(q, kc, vc, bt2, lens2, wl.scale, torch.empty_like(q), 0, None)
+
+
 def test_empty_and_single_token_contexts(orc):
     wl = make_workload("edge", "bf16", [1, 1, 16, 1], 8, 2, 128, 16, 5)
     t = materialize(wl, "cuda")
