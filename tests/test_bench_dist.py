@@ -44,3 +44,22 @@ def test_two_gloo_ranks_reduce_and_use_distinct_seeds():
     assert got[0][0] == got[1][0] == 2.0
     assert got[0][1] == got[1][1] == 30.0
     assert got[0][2] != got[1][2]
+
+
+def test_reference_arm_json_line_on_cpu():
+    """`bench.py --impl reference` times the oracle on the host cores and prints
+    one JSON line in the bench contract (no GPU needed)."""
+    import json
+    import subprocess
+    import sys
+    res = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--steps", "1", "--warmup", "3", "--reference-budget", "2"],
+                         capture_output=True, text=True, timeout=600, cwd=REPO)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config"):
+        assert key in line, key
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
