@@ -512,11 +512,17 @@ def measure_gate(name, args, device):
     return res
 
 
-def measure_trace(block_size, device, partition=256):
+def measure_trace(block_size, device, partition=None):
     """The continuous-batching workload (64 requests, up to 64 slots, 65,536-slot
     pool, LIFO recompute preemption) through the hot path, step by step. Step
-    inputs are gathered on the device beforehand; each step's three calls are
-    timed with CUDA events."""
+    inputs are gathered on the device beforehand; after one untimed pass over
+    the whole trace, each step's calls are timed with CUDA events. The trace's
+    contexts are short (<= 640 tokens): with 16- and 32-token blocks its decode
+    runs unsplit (measured faster than 64- to 512-token partitions); 8-token
+    blocks need a copy per block and head, so there 256-token partitions
+    spread the copies over more CTAs."""
+    if partition is None:
+        partition = 256 if block_size < 16 else 0
     import paged_kv_cache_233_gb300 as pk
     from types import SimpleNamespace
     from workloads import cb_trace, step_inputs, trace_tensors
@@ -532,17 +538,24 @@ def measure_trace(block_size, device, partition=256):
         x["out"] = torch.empty_like(x["q"])
         x["ws"] = pk.new_workspace(x["q"], x["block_tables"], tw.block_size, partition)
         steps.append((plan, x))
+
+    def one_pass(ev=None):
+        for i, (plan, x) in enumerate(steps):
+            if ev is not None:
+                ev[i][0].record()
+            pk.paged_kv_slot_mapping(x["block_tables"], x["token_row"], x["token_pos"],
+                                     x["slots"], tw.num_blocks, tw.block_size)
+            pk.paged_kv_append(x["k"], x["v"], x["slots"], kc, vc)
+            pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"],
+                                      tw.scale, x["out"], partition, x["ws"])
+            if ev is not None:
+                ev[i][1].record()
+
+    one_pass()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in steps]
-    for (plan, x), (a, b) in zip(steps, ev):
-        a.record()
-        pk.paged_kv_slot_mapping(x["block_tables"], x["token_row"], x["token_pos"], x["slots"],
-                                 tw.num_blocks, tw.block_size)
-        pk.paged_kv_append(x["k"], x["v"], x["slots"], kc, vc)
-        pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"], tw.scale,
-                                  x["out"], partition, x["ws"])
-        b.record()
+    one_pass(ev)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(ms)

@@ -22,6 +22,9 @@ slot_mapping_kernel(const int32_t *__restrict__ block_tables, const int32_t *__r
                     const int32_t *__restrict__ token_pos, int64_t *__restrict__ slot_mapping,
                     int num_tokens, int num_seqs, int max_blocks, int block_size, int num_blocks,
                     unsigned int *err) {
+    // the append that follows may start while the slots are computed: it
+    // waits for this grid before reading them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens) return;
     const int pos = token_pos[t];
@@ -50,6 +53,11 @@ append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
               const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache,
               uint4 *__restrict__ v_cache, int num_tokens, int vec_per_row, int tpr,
               long long num_slots, unsigned int *err) {
+    // a decode or prefill that follows may start its set-up now; it waits for
+    // this grid before reading the pools
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the slots (and the pools) of the kernels before this one, complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int rows_per_cta = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int c0 = threadIdx.x - sub * tpr;
@@ -140,11 +148,21 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
     long long blocks = (num_tokens + rows_per_cta - 1) / rows_per_cta;
     const long long cap = (long long)num_sms * 16;
     if (blocks > cap) blocks = cap;
-    append_kernel<<<unsigned(blocks), 256, 0, st>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_tokens, vec_per_row,
-        tpr, num_slots, err);
-    return cudaGetLastError();
+    // programmatic dependent launch: the kernel waits for the previous grid
+    // itself (griddepcontrol.wait) before it reads anything that grid wrote
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4 *>(k),
+                              static_cast<const uint4 *>(v), slots, static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), num_tokens, vec_per_row, tpr,
+                              num_slots, err);
 }
 
 }  // namespace pkv

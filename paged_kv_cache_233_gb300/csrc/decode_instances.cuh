@@ -34,8 +34,20 @@ static cudaError_t launch_decode_instance(DecodeLaunch &a) {
     if (grid > a.max_units) grid = a.max_units;
     if (grid < 1) grid = 1;
     a.grid_used = int(grid);
-    kernel<<<dim3((unsigned)grid), dim3(kDecodeThreads), smem, a.stream>>>(a.kmap, a.vmap, a.p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the set-up (barriers, per-sequence unit
+    // counts) overlaps the previous kernel's tail; the producer waits for that
+    // kernel (griddepcontrol.wait) before its first read of the pools
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a.kmap, a.vmap, a.p);
 }
 
 template <typename T, int D>

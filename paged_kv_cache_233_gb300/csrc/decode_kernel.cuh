@@ -754,6 +754,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // the pools as the kernels before this one left them (an append
+        // launched just before may still be running: launched as its
+        // programmatic dependent, this kernel set itself up meanwhile)
+        grid_dependency_wait();
         uint32_t armed = 0;   // tiles armed so far by this CTA
         int stage = 0;
         uint32_t phase = 0;

@@ -170,6 +170,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) {
             tma_prefetch_descriptor(&kmap);
             tma_prefetch_descriptor(&vmap);
+            // the pools as the kernels before this one left them (launched as
+            // the programmatic dependent of an append that may still be running)
+            grid_dependency_wait();
             const int32_t *table = p.block_tables + size_t(s) * p.max_blocks;
             int armed = 0;
             bool ok = true;
@@ -460,8 +463,17 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     }
     const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
     const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
-    kernel<<<grid, kTcThreads, smem, stream>>>(kmap, vmap, p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p);
 }
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,

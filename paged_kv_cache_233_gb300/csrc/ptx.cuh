@@ -77,6 +77,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with the programmatic-serialization attribute) start its CTAs now, and, in
+// that next kernel, wait until every earlier grid has completed and its
+// memory is visible (immediately true when the earlier grid did not opt in).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Order this thread's earlier generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
