@@ -371,12 +371,12 @@ def oracle_pools(orc, wl, tensors):
     return kc, vc
 
 
-def oracle_rate(orc, wl, q, kc, vc, budget_s, start_unit=0):
+def oracle_rate(orc, wl, q, kc, vc, budget_s, start_unit=0, threads=None):
     """Time the oracle's decode over consecutive (seq, kv head) units, cycling
-    through the workload, until the budget is spent. Returns (bytes, seconds,
-    units, threads)."""
+    through the workload, until the budget is spent (all host cores unless
+    `threads` is given). Returns (bytes, seconds, units, threads)."""
     units = [(s, h) for s in range(wl.num_seqs) for h in range(wl.n_kv_heads)]
-    threads = orc.max_threads()
+    threads = threads or orc.max_threads()
     row = wl.head_dim * wl.element_bytes
     done_bytes, elapsed, n = 0, 0.0, 0
     i = start_unit % len(units)
@@ -878,11 +878,15 @@ def run_ours(args, ctx):
         kc, vc = oracle_pools(orc, wl0, tensors)
         b, s, n, threads = oracle_rate(orc, wl0, host_storage(tensors["q"]), kc, vc,
                                        args.cpu_budget)
+        b1, s1, n1, _ = oracle_rate(orc, wl0, host_storage(tensors["q"]), kc, vc,
+                                    max(1.0, args.cpu_budget / 4), threads=1)
         result["cpu_baseline"] = {
             "value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} (sequence, kv head) units taken in order, cycling over the "
                       f"{wl0.num_seqs * wl0.n_kv_heads} units of the same workload; {s:.1f} s of "
-                      f"fp64 oracle decode on {threads} threads"}
+                      f"fp64 oracle decode on {threads} threads",
+            "single_core": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"{n1} units, {s1:.1f} s on one thread"}}
     return result
 
 

@@ -270,22 +270,26 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 const bool all_first = tail && j == nkt - 1;
                 for (int t = 0; ok && all_first && t < kTcTiles; ++t)
                     if (j < nkt_of(t)) ok = wait(bar_p(t, j & 1), j >> 1);
+                // per Q tile: its P V, then at once its S two key tiles ahead
+                bool k_ready = false;
                 for (int t = 0; ok && t < kTcTiles; ++t) {
                     if (j >= nkt_of(t)) continue;
                     if (!all_first) ok = wait(bar_p(t, j & 1), j >> 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     issue_pv(t, j);
+                    if (j + 2 < nkt_of(t)) {
+                        if (!k_ready) {
+                            ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
+                            if (!ok) break;
+                            tc_fence_after_sync();
+                            k_ready = true;
+                        }
+                        issue_s(t, j + 2);
+                    }
                 }
                 if (!ok) break;
                 tc_commit(bar(kKvEmpty + j % kTcStages));
-                if (j + 2 < nkt) {
-                    ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    for (int t = 0; t < kTcTiles; ++t)
-                        if (j + 2 < nkt_of(t)) issue_s(t, j + 2);
-                }
             }
             if (!ok) *abort_flag = 1;
             // every MMA issued so far has completed before tensor memory is freed
