@@ -6,19 +6,22 @@
 // moved off the warp-level MMA pipe.
 //
 // One CTA owns (sequence, kv head, 256 query rows of (chunk token, query head
-// of the group)), held as two 128-row Q tiles that share every K/V tile. Ten
-// warps:
+// of the group)), held as two 128-row Q tiles that share every K/V tile.
+// Eleven warps:
 //   warp 0     producer: per 64-key tile, looks up the block ids and issues one
 //              TMA box per (16 keys, 64-column block) for K and V into a
-//              three-stage ring, so that each operand lands as [column block]
+//              four-stage ring, so that each operand lands as [column block]
 //              [64 keys][128 B] with 128-byte swizzle (the canonical layout the
 //              tensor core reads);
-//   warp 1     allocates tensor memory; its lane 0 issues every MMA. Per Q tile:
-//              S = Q K^T into one of two S buffers in tensor memory, and, once
-//              the softmax has written P, O += P V with P read from tensor
-//              memory, into the O accumulator that stays in tensor memory for
-//              the whole key loop; completions are tracked by tcgen05.commit
-//              on mbarriers;
+//   warps 1,10 MMA issuers, one per Q tile (warp 1 also allocates tensor
+//              memory); lane 0 issues, for its tile, S = Q K^T into one of two
+//              S buffers in tensor memory and, once the softmax has written P,
+//              O += P V with P read from tensor memory, into the O accumulator
+//              that stays in tensor memory for the whole key loop; completions
+//              are tracked by tcgen05.commit on mbarriers. An issuing thread
+//              runs only about two MMAs ahead of the tensor core, so each of
+//              its waits leaves the tensor core idle unless the other tile's
+//              issuer has MMAs to give it;
 //   warps 2-9  softmax, four warps per Q tile, one thread per query row (=
 //              tensor-memory lane), so that every SM sub-partition runs two
 //              softmax warps whose work interleaves. A thread reads its S row,
@@ -51,7 +54,10 @@ constexpr int kTcTiles = 2;      // Q tiles per CTA
 constexpr int kTcRows = 128;     // query rows per Q tile = tensor-memory lanes
 constexpr int kTcKeys = 64;      // keys per pipeline stage
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 64 + kTcTiles * kTcRows;
+// warp 0 producer, warp 1 MMA issuer of Q tile 0, warps 2-9 softmax, warp 10
+// MMA issuer of Q tile 1
+constexpr int kIssuer1Warp = 2 + kTcTiles * kTcRows / 32;
+constexpr int kTcThreads = 32 * (kIssuer1Warp + 1);
 constexpr int kTmemTile = 256;   // tensor-memory columns per Q tile: S, S, O
 constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
 
@@ -143,7 +149,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) {
         for (int k = 0; k < kTcStages; ++k) {
             mbar_init(bar(kKvFull + k), 1);
-            mbar_init(bar(kKvEmpty + k), 1);
+            mbar_init(bar(kKvEmpty + k), kTcTiles);   // one commit per issuer and key tile
         }
         for (int t = 0; t < kTcTiles; ++t)
             for (int b = 0; b < 2; ++b) {
@@ -152,7 +158,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_init(bar(bar_o(t, b)), 1);
             }
         mbar_init(bar(kQFull), kTcTiles * kTcRows);
-        mbar_init(bar(kDone), 1);
+        mbar_init(bar(kDone), kTcTiles);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -224,16 +230,22 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // -------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == kIssuer1Warp) {
+        // ------------------------------------------------------- MMA issuers
+        // One thread per Q tile issues that tile's MMAs. A thread that issues
+        // tcgen05.mma runs only about two MMAs ahead of the tensor core, so
+        // every wait of an issuing thread is idle tensor time; with one issuer
+        // per tile, one tile's MMAs go in while the other's issuer waits.
         if (lane == 0) {
+            const int t = warp == 1 ? 0 : 1;
+            const int nk = nkt_of(t);
             constexpr uint32_t kIdS = tc_idesc_f16(kBf16, false, kTcRows, kTcKeys);
             constexpr uint32_t kIdO = tc_idesc_f16(kBf16, true, kTcRows, D);
             auto wait = [&](int i, int phase) {
                 return !*abort_flag && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
             };
-            auto issue_s = [&](int t, int j) {
-                const uint32_t qb = base + Ly::kQ + t * Ly::kQTile;
+            const uint32_t qb = base + Ly::kQ + t * Ly::kQTile;
+            auto issue_s = [&](int j) {
                 const uint32_t kb = base + Ly::kKv + (j % kTcStages) * Ly::kStage;
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
 #pragma unroll
@@ -244,7 +256,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 tc_commit(bar(bar_s(t, j & 1)));
             };
-            auto issue_pv = [&](int t, int j) {
+            auto issue_pv = [&](int j) {
                 const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
                 // P of key tile j: the first 32 columns of S buffer j & 1 (16 keys per 8 columns)
                 const uint32_t pa = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
@@ -257,42 +269,39 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 tc_commit(bar(bar_o(t, j & 1)));
             };
             bool ok = wait(kQFull, 0);
-            for (int j = 0; ok && j < 2 && j < nkt; ++j) {
+            for (int j = 0; ok && j < 2 && j < nk; ++j) {
                 ok = wait(kKvFull + j % kTcStages, j / kTcStages);
                 if (!ok) break;
                 tc_fence_after_sync();
-                for (int t = 0; t < kTcTiles; ++t)
-                    if (j < nkt_of(t)) issue_s(t, j);
+                issue_s(j);
             }
             for (int j = 0; ok && j < nkt; ++j) {
-                // the last key tile's V rows past the context are zeroed by the
-                // last Q tile's softmax: every P of that tile must be in first
-                const bool all_first = tail && j == nkt - 1;
-                for (int t = 0; ok && all_first && t < kTcTiles; ++t)
-                    if (j < nkt_of(t)) ok = wait(bar_p(t, j & 1), j >> 1);
-                // per Q tile: its P V, then at once its S two key tiles ahead
-                bool k_ready = false;
-                for (int t = 0; ok && t < kTcTiles; ++t) {
-                    if (j >= nkt_of(t)) continue;
-                    if (!all_first) ok = wait(bar_p(t, j & 1), j >> 1);
+                if (j < nk) {
+                    // the last key tile's V rows past the context are zeroed by the
+                    // last Q tile's softmax before its P: that P must be in first
+                    if (tail && j == nkt - 1 && t != t_last) ok = wait(bar_p(t_last, j & 1), j >> 1);
+                    if (ok) ok = wait(bar_p(t, j & 1), j >> 1);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_pv(t, j);
-                    if (j + 2 < nkt_of(t)) {
-                        if (!k_ready) {
-                            ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
-                            if (!ok) break;
-                            tc_fence_after_sync();
-                            k_ready = true;
-                        }
-                        issue_s(t, j + 2);
+                    issue_pv(j);
+                    // this tile's S two key tiles ahead (its S buffer j & 1 is free
+                    // once the P V just issued has read P)
+                    if (j + 2 < nk) {
+                        ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        issue_s(j + 2);
                     }
+                } else {
+                    // a key tile this Q tile skips: its stage may be released only
+                    // after it landed (the arrival belongs to this phase of the slot)
+                    ok = wait(kKvFull + j % kTcStages, j / kTcStages);
+                    if (!ok) break;
                 }
-                if (!ok) break;
                 tc_commit(bar(kKvEmpty + j % kTcStages));
             }
             if (!ok) *abort_flag = 1;
-            // every MMA issued so far has completed before tensor memory is freed
+            // every MMA of both issuers has completed before tensor memory is freed
             tc_commit(bar(kDone));
             mbar_wait(bar(kDone), 0, p.err);
         }
