@@ -72,7 +72,7 @@ struct TcLayout {
     static constexpr int kHalf = kSlabs * kKvSlab;
     static constexpr int kStage = 2 * kHalf;
     static constexpr int kBars = kKv + kTcStages * kStage;
-    static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 2;
+    static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 3;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
     static constexpr int kTotal = kFlag + 8;
@@ -89,6 +89,9 @@ __device__ __forceinline__ int bar_p(int t, int b) { return 2 * kTcStages + 6 * 
 __device__ __forceinline__ int bar_o(int t, int b) { return 2 * kTcStages + 6 * t + 4 + b; }
 constexpr int kQFull = 2 * kTcStages + 6 * kTcTiles;
 constexpr int kDone = kQFull + 1;
+// the last key tile's V rows past the context are zeroed (one phase per CTA,
+// so a wait on it is never ambiguous however far the Q tiles drift apart)
+constexpr int kVZero = kDone + 1;
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -159,6 +162,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             }
         mbar_init(bar(kQFull), kTcTiles * kTcRows);
         mbar_init(bar(kDone), kTcTiles);
+        mbar_init(bar(kVZero), kTcRows);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -278,8 +282,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int j = 0; ok && j < nkt; ++j) {
                 if (j < nk) {
                     // the last key tile's V rows past the context are zeroed by the
-                    // last Q tile's softmax before its P: that P must be in first
-                    if (tail && j == nkt - 1 && t != t_last) ok = wait(bar_p(t_last, j & 1), j >> 1);
+                    // last Q tile's softmax: no P V may read that tile before
+                    if (tail && j == nkt - 1) ok = wait(kVZero, 0);
                     if (ok) ok = wait(bar_p(t, j & 1), j >> 1);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -407,6 +411,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
+                mbar_arrive(bar(kVZero));
             }
             uint32_t pk[kTcKeys / 2];
 #pragma unroll
