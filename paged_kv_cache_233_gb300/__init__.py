@@ -116,21 +116,32 @@ def _check(status, what):
         raise PagedKVError(f"{what}: {status_string(status)} ({status})")
 
 
+# The current stream's raw handle without building a torch Stream object
+# (about 0.1 us instead of 3 us per call); torch.cuda.current_stream() where
+# this torch lacks the accessor.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    """The CUDA stream handle (an int; 0 is the legacy default stream)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev(t, name, dtype=None):
+    """The device address of a contiguous CUDA tensor (an int), checked."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise PagedKVError(f"{name} must be a CUDA tensor (the paged-KV path has no CPU fallback)")
     if not t.is_contiguous():
         raise PagedKVError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
+    if dtype is not None and t.dtype is not dtype:
         raise PagedKVError(f"{name} must be {dtype}, got {t.dtype}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _code(t):
@@ -156,18 +167,20 @@ def paged_kv_slot_mapping(block_tables, token_seq, token_pos, slot_mapping, num_
 
 def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
     """Scatter k/v [T][Hkv][D] into the pools [NB][B][Hkv][D] at slot_mapping[T]."""
-    if k.dim() != 3 or k.shape != v.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+    ks, cs = k.shape, k_cache.shape
+    if len(ks) != 3 or v.shape != ks or len(cs) != 4 or v_cache.shape != cs:
         raise PagedKVError("expected k, v [T][Hkv][D] and pools [NB][B][Hkv][D]")
-    if k.dtype != k_cache.dtype or v.dtype != k.dtype or v_cache.dtype != k.dtype:
+    if not (k.dtype is v.dtype is k_cache.dtype is v_cache.dtype):
         raise PagedKVError("k, v and the pools must share one element type")
-    if tuple(k.shape[1:]) != tuple(k_cache.shape[2:]):
+    NB, B, Hkv, D = cs
+    T = ks[0]
+    if ks[1] != Hkv or ks[2] != D:
         raise PagedKVError("token rows do not match the pool's [Hkv][D]")
-    if slot_mapping.numel() != k.shape[0]:
+    if slot_mapping.numel() != T:
         raise PagedKVError("slot_mapping length differs from the number of tokens")
-    NB, B, Hkv, D = k_cache.shape
     st = load().paged_kv_append(
         _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64),
-        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), k.shape[0], NB, B, Hkv, D, _code(k),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), T, NB, B, Hkv, D, _code(k),
         _stream(stream))
     _check(st, "paged_kv_append")
 
@@ -196,7 +209,7 @@ def _reachable(t, name, dtype=None):
         raise PagedKVError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda and not t.is_pinned():
         raise PagedKVError(f"{name} must be a CUDA tensor or pinned host memory")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def paged_kv_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
@@ -265,6 +278,20 @@ def new_workspace(q, block_tables, block_size, partition_tokens):
     return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
+def _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out):
+    """(S, Hq, Hkv, D, NB, B, max_blocks) of a decode call, checked."""
+    qs, cs, bs = q.shape, k_cache.shape, block_tables.shape
+    if len(qs) != 3 or out.shape != qs or len(cs) != 4 or v_cache.shape != cs:
+        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
+    if not (q.dtype is out.dtype is k_cache.dtype is v_cache.dtype):
+        raise PagedKVError("q, out and the pools must share one element type")
+    S, Hq, D = qs
+    NB, B, Hkv, Dk = cs
+    if Dk != D or len(bs) != 2 or bs[0] != S or context_lens.numel() != S:
+        raise PagedKVError("shape mismatch between q, the pools, block_tables and context_lens")
+    return S, Hq, Hkv, D, NB, B, bs[1]
+
+
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                            partition_tokens=0, workspace=None, stream=None):
     """out[s][h] = softmax(scale * q[s][h] . K_s) V_s with K_s, V_s read through block_tables.
@@ -272,23 +299,15 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     partition_tokens: 0 = no split, > 0 = split-K in partitions of that many
     tokens, PARTITION_BALANCED = equal tile shares per CTA; splits need a
     workspace (new_workspace)."""
-    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
-    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
-        raise PagedKVError("q, out and the pools must share one element type")
-    S, Hq, D = q.shape
-    NB, B, Hkv, Dk = k_cache.shape
-    if Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
-        raise PagedKVError("shape mismatch between q, the pools, block_tables and context_lens")
-    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    S, Hq, Hkv, D, NB, B, MB = _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out)
+    ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     st = load().paged_attention_decode(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S, Hq, Hkv,
-        D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr, ws_bytes, _code(q),
-        _stream(stream))
+        D, NB, B, MB, int(partition_tokens), ws_ptr, ws_bytes, _code(q), _stream(stream))
     _check(st, "paged_attention_decode")
 
 
@@ -300,16 +319,10 @@ def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, cont
     group_prefix[g] (int32) the tokens every member holds in the group's first
     member's blocks. Each shared prefix partition is read once per chunk of
     members instead of once per member. Needs a split (partition_tokens > 0)."""
-    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
-    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
-        raise PagedKVError("q, out and the pools must share one element type")
-    S, Hq, D = q.shape
-    NB, B, Hkv, Dk = k_cache.shape
-    if (Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or
-            context_lens.numel() != S or seq_group.numel() != S):
+    S, Hq, Hkv, D, NB, B, MB = _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out)
+    if seq_group.numel() != S:
         raise PagedKVError("shape mismatch between q, the pools, block_tables, lengths and groups")
-    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     st = load().paged_attention_decode_shared_prefix(
@@ -317,8 +330,8 @@ def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, cont
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), _dev(seq_group, "seq_group", torch.int32),
         _dev(group_prefix, "group_prefix", torch.int32), group_prefix.numel(), float(scale),
-        _dev(out, "out"), S, Hq, Hkv, D, NB, B, block_tables.shape[1], int(partition_tokens), ws_ptr,
-        ws_bytes, _code(q), _stream(stream))
+        _dev(out, "out"), S, Hq, Hkv, D, NB, B, MB, int(partition_tokens), ws_ptr, ws_bytes,
+        _code(q), _stream(stream))
     _check(st, "paged_attention_decode_shared_prefix")
 
 
@@ -331,19 +344,12 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_le
     fixed library-owned device array of NOALLOC_SCRATCH_BYTES shared by every
     call on the device: order such calls on one stream. A split that needs more
     than that raises PagedKVError (status -5)."""
-    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise PagedKVError("expected q/out [S][Hq][D] and pools [NB][B][Hkv][D]")
-    if len({q.dtype, out.dtype, k_cache.dtype, v_cache.dtype}) != 1:
-        raise PagedKVError("q, out and the pools must share one element type")
-    S, Hq, D = q.shape
-    NB, B, Hkv, Dk = k_cache.shape
-    if Dk != D or block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
-        raise PagedKVError("shape mismatch between q, the pools, block_tables and context_lens")
+    S, Hq, Hkv, D, NB, B, MB = _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out)
     st = load().paged_attention_decode_noalloc(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S, Hq, Hkv,
-        D, NB, B, block_tables.shape[1], int(partition_tokens), _code(q), _stream(stream))
+        D, NB, B, MB, int(partition_tokens), _code(q), _stream(stream))
     _check(st, "paged_attention_decode_noalloc")
 
 
