@@ -517,13 +517,14 @@ def measure_trace(block_size, device, partition=None):
     pool, LIFO recompute preemption) through the hot path, step by step. Step
     inputs are gathered on the device beforehand; after one untimed pass over
     the whole trace, each step's calls are timed with CUDA events. The trace's
-    contexts are short (<= 640 tokens): with 16- and 32-token blocks its decode
-    runs unsplit (measured faster than 64- to 512-token partitions); 8-token
-    blocks need a copy per block and head, so there 256-token partitions
-    spread the copies over more CTAs."""
-    if partition is None:
-        partition = 256 if block_size < 16 else 0
+    contexts are short (<= 640 tokens) and its batches small (<= 64), so a
+    step's decode runs the balanced split: the step's 16-token tiles cut into
+    equal shares, one per CTA (measured on GB300: 1926 / 2026 / 2052 GB/s at
+    B = 8 / 16 / 32, against 1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045
+    with 256-token partitions)."""
     import paged_kv_cache_233_gb300 as pk
+    if partition is None:
+        partition = pk.PARTITION_BALANCED
     from types import SimpleNamespace
     from workloads import cb_trace, step_inputs, trace_tensors
     tw = cb_trace(block_size=block_size, slots=64)
