@@ -44,13 +44,15 @@ lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
     using V = typename Vec<E>::type;
     __shared__ float red[kMergeWarps];
     __shared__ float acc_s[kMergeWarps][D];
-    // partition states are written by the preceding decode launch
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the lengths are the caller's (no kernel of this library writes them), so
+    // they are read while the decode may still run; its partition states only
+    // after griddepcontrol.wait
     const int row = blockIdx.x;   // s * n_q_heads + qh
     const int s = row / n_q_heads;
     const int L = min(max(__ldg(lens + s), 0), cap);
     const int np = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
     if (np <= 1) return;  // written directly by the partition kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t row0 = size_t(row) * max_parts;
     float M = -INFINITY;
@@ -96,14 +98,16 @@ lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ 
     constexpr int E = D / 32;
     constexpr int kBatch = 8;
     using V = typename Vec<E>::type;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
+    // the length first (the caller's, read while the decode may still run),
+    // the partition states only after griddepcontrol.wait
     const int s = row / n_q_heads;
     const int L = min(max(__ldg(lens + s), 0), cap);
     const int np = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
     if (np <= 1) return;  // written directly by the partition kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t row0 = size_t(row) * max_parts;
     const float mp = lane < np ? __ldcg(ws_m + row0 + lane) : -INFINITY;
     const float lp = lane < np ? __ldcg(ws_l + row0 + lane) : 0.f;
