@@ -1,9 +1,10 @@
 """Benchmark: one decode step of one layer over a block-paged KV cache.
 
 A step is the whole hot path over one batch: address translation of the
-step's new tokens (paged_kv_slot_mapping), their K/V append
-(paged_kv_append) and the fused paged-attention decode of every sequence
-(paged_attention_decode, split-K partitions + merge where configured).
+step's new tokens and their K/V append in one launch (paged_kv_append_tokens,
+which computes what paged_kv_slot_mapping + paged_kv_append do) and the fused
+paged-attention decode of every sequence (paged_attention_decode, split-K
+partitions + merge where configured).
 
 Default workload: the Llama-2-7B-shaped MHA layer (64 sequences, 32 heads,
 head_dim 128, fp16, block size 16, lengths uniform in [128, 2048], physical
@@ -208,7 +209,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Step:
-    """Device-resident inputs and the three calls of one decode step."""
+    """Device-resident inputs and the two calls of one decode step: the new
+    tokens' slot mapping and append in one launch, then the decode."""
 
     def __init__(self, wl, device, partition):
         import paged_kv_cache_233_gb300 as pk
@@ -246,13 +248,12 @@ class Step:
         self.fill_ms = statistics.median(fills)
         self.fill_tokens = len(wl.fill_seq)
         del fill_seq, fill_pos, fill_slots
-        self.launches_per_step = 3 + (1 if partition > 0 else 0)
+        self.launches_per_step = 2 + (1 if partition > 0 else 0)
 
     def run(self, ev=None):
         pk, wl = self.pk, self.wl
-        pk.paged_kv_slot_mapping(self.bt, self.step_seq, self.step_pos, self.slots,
-                                 wl.num_blocks, wl.block_size)
-        pk.paged_kv_append(self.t["k_step"], self.t["v_step"], self.slots, self.kc, self.vc)
+        pk.paged_kv_append_tokens(self.t["k_step"], self.t["v_step"], self.bt, self.step_seq,
+                                  self.step_pos, self.kc, self.vc)
         if ev is not None:
             ev[0].record()
         pk.paged_attention_decode(self.t["q"], self.kc, self.vc, self.bt, self.lens, wl.scale,
@@ -323,9 +324,7 @@ def time_e2e(step, steps):
     done = [torch.cuda.Event() for _ in range(2)]
 
     def run(v, out):
-        pk.paged_kv_slot_mapping(v["bt"], v["seq"], v["pos"], step.slots, wl.num_blocks,
-                                 wl.block_size)
-        pk.paged_kv_append(v["k"], v["v"], step.slots, step.kc, step.vc)
+        pk.paged_kv_append_tokens(v["k"], v["v"], v["bt"], v["seq"], v["pos"], step.kc, step.vc)
         pk.paged_attention_decode(v["q"], step.kc, step.vc, v["bt"], v["lens"], wl.scale, out,
                                   step.partition, step.ws)
 

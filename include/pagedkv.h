@@ -122,6 +122,40 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
                     int n_kv_heads, int head_dim, int dtype, void *stream);
 
 /*
+ * paged_kv_append_tokens -- paged_kv_slot_mapping and paged_kv_append in one
+ * launch.
+ *
+ * For each new token t, the slot of "The one formula" (page "How a serving
+ * engine actually works"),
+ *
+ *     slot = block_tables[token_seq[t]][token_pos[t] / block_size] * block_size
+ *            + token_pos[t] % block_size,
+ *
+ * with the checks and device error bits of paged_kv_slot_mapping, then the
+ * token's K and V rows copied to that slot as paged_kv_append does. The pools
+ * end up bit-identical to those two calls' result.
+ *
+ *   k, v          [num_tokens][n_kv_heads][head_dim] of dtype, device
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq], device
+ *   token_seq     int32 [num_tokens], device
+ *   token_pos     int32 [num_tokens], device; a negative position is padding
+ *   slot_mapping  int64 [num_tokens], device, written (-1 for padding and for
+ *                 tokens that fail a check); may be NULL when not wanted
+ *   k_cache,
+ *   v_cache       [num_blocks][block_size][n_kv_heads][head_dim] of dtype,
+ *                 device, updated in place
+ *
+ * A token whose check fails is not copied. Two tokens with the same slot race;
+ * the caller must not do that. Requires n_kv_heads*head_dim*sizeof(dtype) to
+ * be a multiple of 16 bytes. num_tokens == 0 enqueues nothing.
+ */
+int paged_kv_append_tokens(const void *k, const void *v, const int32_t *block_tables,
+                           const int32_t *token_seq, const int32_t *token_pos,
+                           int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
+                           int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                           int n_kv_heads, int head_dim, int dtype, void *stream);
+
+/*
  * paged_kv_copy_blocks -- copy whole blocks of both pools, for copy-on-write.
  *
  * Page "How a serving engine actually works", section "Copy-on-write, because

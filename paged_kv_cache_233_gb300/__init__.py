@@ -10,6 +10,8 @@ The entry points keep the C names:
 
     paged_kv_slot_mapping(block_tables, token_seq, token_pos, slot_mapping, num_blocks, block_size)
     paged_kv_append(k, v, slot_mapping, k_cache, v_cache)
+    paged_kv_append_tokens(k, v, block_tables, token_seq, token_pos, k_cache, v_cache,
+                           slot_mapping=None)
     paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                            partition_tokens=0, workspace=None)
     paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq,
@@ -31,7 +33,7 @@ __all__ = [
     "OPT_PREFILL_PATH",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
     "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
-    "paged_attention_prefill",
+    "paged_attention_prefill", "paged_kv_append_tokens",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,7 +47,7 @@ EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
            "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks",
-           "paged_attention_decode_shared_prefix")
+           "paged_attention_decode_shared_prefix", "paged_kv_append_tokens")
 
 
 class PagedKVError(RuntimeError):
@@ -72,6 +74,9 @@ def load():
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.paged_kv_slot_mapping.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.paged_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.paged_kv_append_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                           i32, i32, i32, vp]
+    lib.paged_kv_append_tokens.restype = i32
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32,
                                            i32, i32, i32, i32, i32, vp, sz, i32, vp]
     lib.paged_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, vp, i32,
@@ -183,6 +188,36 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), T, NB, B, Hkv, D, _code(k),
         _stream(stream))
     _check(st, "paged_kv_append")
+
+
+def paged_kv_append_tokens(k, v, block_tables, token_seq, token_pos, k_cache, v_cache,
+                           slot_mapping=None, stream=None):
+    """paged_kv_slot_mapping and paged_kv_append in one launch: token t's K/V
+    rows go to slot block_tables[seq][pos // B] * B + pos % B (seq, pos =
+    token_seq[t], token_pos[t]; negative pos is padding); the slots are also
+    written to slot_mapping (int64) when it is given."""
+    ks, cs = k.shape, k_cache.shape
+    if len(ks) != 3 or v.shape != ks or len(cs) != 4 or v_cache.shape != cs:
+        raise PagedKVError("expected k, v [T][Hkv][D] and pools [NB][B][Hkv][D]")
+    if not (k.dtype is v.dtype is k_cache.dtype is v_cache.dtype):
+        raise PagedKVError("k, v and the pools must share one element type")
+    NB, B, Hkv, D = cs
+    T = ks[0]
+    if ks[1] != Hkv or ks[2] != D:
+        raise PagedKVError("token rows do not match the pool's [Hkv][D]")
+    if token_seq.numel() != T or token_pos.numel() != T or block_tables.dim() != 2:
+        raise PagedKVError("token_seq and token_pos need one entry per token, block_tables 2 dims")
+    sm = None
+    if slot_mapping is not None:
+        if slot_mapping.numel() != T:
+            raise PagedKVError("slot_mapping length differs from the number of tokens")
+        sm = _dev(slot_mapping, "slot_mapping", torch.int64)
+    st = load().paged_kv_append_tokens(
+        _dev(k, "k"), _dev(v, "v"), _dev(block_tables, "block_tables", torch.int32),
+        _dev(token_seq, "token_seq", torch.int32), _dev(token_pos, "token_pos", torch.int32), sm,
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), T, block_tables.shape[0],
+        block_tables.shape[1], NB, B, Hkv, D, _code(k), _stream(stream))
+    _check(st, "paged_kv_append_tokens")
 
 
 def paged_kv_copy_blocks(k_cache, v_cache, block_pairs, stream=None):

@@ -22,6 +22,12 @@ cudaError_t launch_slot_mapping(const int32_t *block_tables, const int32_t *toke
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache,
                           void *v_cache, int num_tokens, long long row_bytes, long long num_slots,
                           int num_sms, unsigned int *err, cudaStream_t st);
+cudaError_t launch_append_tokens(const void *k, const void *v, const int32_t *block_tables,
+                                 const int32_t *token_seq, const int32_t *token_pos,
+                                 int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 int num_tokens, int num_seqs, int max_blocks, int block_size,
+                                 int num_blocks, long long row_bytes, int num_sms,
+                                 unsigned int *err, cudaStream_t st);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
                                int num_blocks, long long block_bytes, int num_sms,
                                unsigned int *err, cudaStream_t st);
@@ -294,6 +300,35 @@ int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping, v
     const cudaError_t e = pkv::launch_append(k, v, slot_mapping, k_cache, v_cache, num_tokens,
                                              row_bytes, (long long)num_blocks * block_size, sms,
                                              err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+int paged_kv_append_tokens(const void *k, const void *v, const int32_t *block_tables,
+                           const int32_t *token_seq, const int32_t *token_pos,
+                           int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
+                           int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                           int n_kv_heads, int head_dim, int dtype, void *stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        block_size < 1 || n_kv_heads < 1 || head_dim < 1 || !valid_dtype(dtype))
+        return PAGEDKV_ERR_INVALID_ARG;
+    if ((long long)num_blocks * block_size > (1ll << 62)) return PAGEDKV_ERR_INVALID_ARG;
+    const long long row_bytes = (long long)n_kv_heads * head_dim * elem_bytes(dtype);
+    if (row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return PAGEDKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PAGEDKV_OK;
+    if (!k || !v || !block_tables || !token_seq || !token_pos || !k_cache || !v_cache)
+        return PAGEDKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(token_seq, 4) || !aligned(token_pos, 4) ||
+        (slot_mapping && !aligned(slot_mapping, 8)))
+        return PAGEDKV_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    const cudaError_t e = pkv::launch_append_tokens(
+        k, v, block_tables, token_seq, token_pos, slot_mapping, k_cache, v_cache, num_tokens,
+        num_seqs, max_blocks_per_seq, block_size, num_blocks, row_bytes, sms, err,
+        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 

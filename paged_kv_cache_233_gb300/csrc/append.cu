@@ -3,6 +3,7 @@
 //
 // slot_mapping: "How a serving engine actually works", section "The one
 // formula": slot = block_table[seq][pos / B] * B + pos % B.
+// append_tokens: both in one launch (the slot, then the copy of the row).
 // append: "Paged-KV + Continuous Batching From Scratch", section 1 (one pool
 // per layer laid out [num_blocks][block_size][n_kv_heads][head_dim]): each
 // new token's K and V rows are copied, 16 bytes per thread and instruction,
@@ -69,6 +70,62 @@ append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
             if (c0 == 0) atomicOr(err, PAGEDKV_DEVERR_SLOT_RANGE);
             continue;
         }
+        const uint4 *ks = k + t * vec_per_row;
+        const uint4 *vs = v + t * vec_per_row;
+        uint4 *kd = k_cache + slot * vec_per_row;
+        uint4 *vd = v_cache + slot * vec_per_row;
+        for (int c = c0; c < vec_per_row; c += tpr) {
+            const uint4 a = __ldcs(ks + c);
+            const uint4 b = __ldcs(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+// Slot mapping and append in one pass: the `tpr` threads of a row compute its
+// slot with the formula and the checks of slot_mapping_kernel (one of them
+// records an error bit and, when asked, the slot), then copy the row.
+__global__ void __launch_bounds__(256)
+append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                     const int32_t *__restrict__ block_tables, const int32_t *__restrict__ token_seq,
+                     const int32_t *__restrict__ token_pos, int64_t *__restrict__ slot_mapping,
+                     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int num_tokens,
+                     int num_seqs, int max_blocks, int block_size, int num_blocks, int vec_per_row,
+                     int tpr, unsigned int *err) {
+    // a decode or prefill that follows may start its set-up now; it waits for
+    // this grid before reading the pools
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the pools as the kernels before this one left them
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int rows_per_cta = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;
+    const int c0 = threadIdx.x - sub * tpr;
+    for (long long t = (long long)blockIdx.x * rows_per_cta + sub; t < num_tokens;
+         t += (long long)gridDim.x * rows_per_cta) {
+        const int pos = token_pos[t];
+        const int seq = token_seq[t];
+        long long slot = -1;
+        unsigned int bit = 0;
+        if (pos >= 0) {
+            const int j = pos / block_size;
+            if (seq < 0 || seq >= num_seqs) {
+                bit = PAGEDKV_DEVERR_SEQ_INDEX;
+            } else if (j >= max_blocks) {
+                bit = PAGEDKV_DEVERR_POSITION;
+            } else {
+                const int pb = block_tables[int64_t(seq) * max_blocks + j];
+                if (pb < 0 || pb >= num_blocks)
+                    bit = PAGEDKV_DEVERR_BLOCK_ID;
+                else
+                    slot = (long long)pb * block_size + (pos - j * block_size);
+            }
+        }
+        if (c0 == 0) {
+            if (bit) atomicOr(err, bit);
+            if (slot_mapping) slot_mapping[t] = slot;
+        }
+        if (slot < 0) continue;
         const uint4 *ks = k + t * vec_per_row;
         const uint4 *vs = v + t * vec_per_row;
         uint4 *kd = k_cache + slot * vec_per_row;
@@ -163,6 +220,35 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
                               static_cast<const uint4 *>(v), slots, static_cast<uint4 *>(k_cache),
                               static_cast<uint4 *>(v_cache), num_tokens, vec_per_row, tpr,
                               num_slots, err);
+}
+
+cudaError_t launch_append_tokens(const void *k, const void *v, const int32_t *block_tables,
+                                 const int32_t *token_seq, const int32_t *token_pos,
+                                 int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 int num_tokens, int num_seqs, int max_blocks, int block_size,
+                                 int num_blocks, long long row_bytes, int num_sms,
+                                 unsigned int *err, cudaStream_t st) {
+    const int vec_per_row = int(row_bytes / 16);
+    int tpr = 32;
+    while (tpr < vec_per_row && tpr < 256) tpr <<= 1;
+    const int rows_per_cta = 256 / tpr;
+    long long blocks = (num_tokens + rows_per_cta - 1) / rows_per_cta;
+    const long long cap = (long long)num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_tokens_kernel, static_cast<const uint4 *>(k),
+                              static_cast<const uint4 *>(v), block_tables, token_seq, token_pos,
+                              slot_mapping, static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), num_tokens, num_seqs, max_blocks,
+                              block_size, num_blocks, vec_per_row, tpr, err);
 }
 
 }  // namespace pkv

@@ -93,6 +93,30 @@ def test_append_and_slot_mapping_reject_bad_arguments(lib):
     assert lib.paged_kv_slot_mapping(vp(0), vp(0), vp(0), vp(0), 0, 2, 4, 16, 8, None) == 0
 
 
+def test_append_tokens_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(k=16, v=16, bt=16, seq=16, pos=16, sm=None, kc=16, vc=16, T=4, S=2, MB=4, NB=8,
+                 B=16, H=2, D=64, dtype=1)
+        a.update(kw)
+        return lib.paged_kv_append_tokens(vp(a["k"]), vp(a["v"]), vp(a["bt"]), vp(a["seq"]),
+                                          vp(a["pos"]), vp(a["sm"]), vp(a["kc"]), vp(a["vc"]),
+                                          a["T"], a["S"], a["MB"], a["NB"], a["B"], a["H"], a["D"],
+                                          a["dtype"], None)
+
+    assert call(T=-1) == INVALID
+    assert call(MB=0) == INVALID
+    assert call(NB=0) == INVALID
+    assert call(dtype=9) == INVALID
+    assert call(H=3, D=2) == INVALID                 # 12-byte rows
+    assert call(k=24) == INVALID                     # misaligned K rows
+    assert call(bt=18) == INVALID                    # misaligned block table
+    assert call(sm=20) == INVALID                    # misaligned slot output
+    assert call(seq=0) == INVALID                    # no token_seq
+    assert call(T=0, k=0, v=0, bt=0, seq=0, pos=0, kc=0, vc=0) == 0   # nothing to do
+
+
 def test_swap_and_copy_blocks_reject_bad_arguments(lib):
     vp = ctypes.c_void_p
     # a block of 1 token x 1 head x 3 fp16 elements (6 bytes) is not a multiple of 16
