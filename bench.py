@@ -525,9 +525,11 @@ def measure_trace(block_size, device, partition=None):
     the whole trace, each step's calls are timed with CUDA events. The trace's
     contexts are short (<= 640 tokens) and its batches small (<= 64), so a
     step's decode runs the balanced split: the step's 16-token tiles cut into
-    equal shares, one per CTA (measured on GB300: 1926 / 2026 / 2052 GB/s at
-    B = 8 / 16 / 32, against 1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045
-    with 256-token partitions)."""
+    equal shares, one per CTA (measured on GB300 with separate slot mapping and
+    append calls: 1926 / 2026 / 2052 GB/s at B = 8 / 16 / 32, against
+    1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045 with 256-token
+    partitions). A step appends through paged_kv_append_tokens (one launch
+    and one host call for both): 2033 / 2334 / 2350 GB/s."""
     import paged_kv_cache_233_gb300 as pk
     if partition is None:
         partition = pk.PARTITION_BALANCED
@@ -541,7 +543,6 @@ def measure_trace(block_size, device, partition=None):
     steps = []
     for plan in tw.plans:
         x = step_inputs(tw, plan, tensors, device)
-        x["slots"] = torch.empty(len(plan.token_row), dtype=torch.int64, device=device)
         x["out"] = torch.empty_like(x["q"])
         x["ws"] = pk.new_workspace(x["q"], x["block_tables"], tw.block_size, partition)
         steps.append((plan, x))
@@ -550,9 +551,8 @@ def measure_trace(block_size, device, partition=None):
         for i, (plan, x) in enumerate(steps):
             if ev is not None:
                 ev[i][0].record()
-            pk.paged_kv_slot_mapping(x["block_tables"], x["token_row"], x["token_pos"],
-                                     x["slots"], tw.num_blocks, tw.block_size)
-            pk.paged_kv_append(x["k"], x["v"], x["slots"], kc, vc)
+            pk.paged_kv_append_tokens(x["k"], x["v"], x["block_tables"], x["token_row"],
+                                      x["token_pos"], kc, vc)
             pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"],
                                       tw.scale, x["out"], partition, x["ws"])
             if ev is not None:
