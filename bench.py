@@ -262,21 +262,29 @@ class Step:
             ev[1].record()
 
 
+DECODE_SAMPLE = 8   # the decode call is bracketed by events on every 8th timed step
+
+
 def time_steps(step, steps, dist_ctx):
-    """Device time of exactly `steps` steps (max over ranks), plus decode-only time."""
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(steps)]
+    """Device time of exactly `steps` steps (max over ranks), plus decode-only
+    time. An event recorded between two launches ends their programmatic
+    dependent overlap, so the decode call is bracketed by events only on every
+    DECODE_SAMPLE-th step (its mean over those steps); the other steps run as
+    a serving loop would."""
+    sampled = range(0, steps, DECODE_SAMPLE)
+    pairs = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for i in sampled}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()
     torch.cuda.synchronize()
     start.record()
     for i in range(steps):
-        step.run(pairs[i])
+        step.run(pairs.get(i))
     stop.record()
     torch.cuda.synchronize()
     dist_ctx.barrier()
     total_ms = dist_ctx.max(start.elapsed_time(stop))
-    decode_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
+    decode_ms = sum(a.elapsed_time(b) for a, b in pairs.values()) / len(pairs)
     return total_ms, decode_ms
 
 
@@ -863,7 +871,8 @@ def run_ours(args, ctx):
                          "frac": achieved / peak, "traffic": profiled_traffic(args.config, P),
                          "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)",
                          "kernel": "paged_decode_kernel + lse_merge_kernel (one decode call)",
-                         "decode_ms": decode_ms, "algorithmic_bytes_per_launch": algo},
+                         "decode_ms": decode_ms, "algorithmic_bytes_per_launch": algo,
+                         "decode_timed_on": f"every {DECODE_SAMPLE}th timed step"},
         }
     del step
     torch.cuda.empty_cache()
