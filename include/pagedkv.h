@@ -403,6 +403,16 @@ int paged_attention_decode_noalloc(const void *q, const void *k_cache, const voi
  */
 int pagedkv_device_errors(unsigned int *flags, int reset);
 
+/*
+ * pagedkv_check_bounded_wait -- a check of the library's failure path. Enqueues
+ * one small kernel on `stream` whose wait on an mbarrier that nothing arrives
+ * on gives up after the in-kernel time limit (1 s), as every wait of the
+ * library's kernels does when a peer never arrives: it sets
+ * PAGEDKV_DEVERR_TIMEOUT in the sticky device error word and the kernel exits
+ * normally, leaving the context usable. Returns PAGEDKV_OK once enqueued.
+ */
+int pagedkv_check_bounded_wait(void *stream);
+
 /* Tuning knobs, process-wide and not thread-safe; for tests and benchmarks. */
 #define PAGEDKV_OPT_DECODE_PATH    1  /* 0 auto, 1 CUDA-core (SIMT) path, 2 tensor-core (mma) path */
 #define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */

@@ -33,7 +33,7 @@ __all__ = [
     "OPT_PREFILL_PATH",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
     "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
-    "paged_attention_prefill", "paged_kv_append_tokens",
+    "paged_attention_prefill", "paged_kv_append_tokens", "check_bounded_wait", "DEVERR_TIMEOUT",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -43,11 +43,13 @@ DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP, OPT_STAGES, OPT_PREFILL_PATH = 1, 2, 3, 4, 5
 NOALLOC_SCRATCH_BYTES = 64 << 20   # PAGEDKV_NOALLOC_SCRATCH_BYTES
 PARTITION_BALANCED = -1            # PAGEDKV_PARTITION_BALANCED
+DEVERR_TIMEOUT = 0x20              # PAGEDKV_DEVERR_TIMEOUT: a bounded in-kernel wait gave up
 EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "paged_attention_workspace_bytes", "pagedkv_device_errors", "pagedkv_set_option",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
            "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks",
-           "paged_attention_decode_shared_prefix", "paged_kv_append_tokens")
+           "paged_attention_decode_shared_prefix", "paged_kv_append_tokens",
+           "pagedkv_check_bounded_wait")
 
 
 class PagedKVError(RuntimeError):
@@ -96,6 +98,8 @@ def load():
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+    lib.pagedkv_check_bounded_wait.argtypes = [vp]
+    lib.pagedkv_check_bounded_wait.restype = i32
     lib.pagedkv_set_option.argtypes = [i32, i32]
     lib.pagedkv_get_option.argtypes = [i32]
     lib.pagedkv_status_string.argtypes = [i32]
@@ -386,6 +390,12 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_le
         _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S, Hq, Hkv,
         D, NB, B, MB, int(partition_tokens), _code(q), _stream(stream))
     _check(st, "paged_attention_decode_noalloc")
+
+
+def check_bounded_wait(stream=None):
+    """Enqueue a kernel whose bounded wait on a barrier that nothing arrives on
+    gives up (after 1 s) and sets the timeout bit of device_errors()."""
+    _check(load().pagedkv_check_bounded_wait(_stream(stream)), "pagedkv_check_bounded_wait")
 
 
 def device_errors(reset=True):

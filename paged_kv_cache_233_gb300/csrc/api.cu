@@ -28,6 +28,7 @@ cudaError_t launch_append_tokens(const void *k, const void *v, const int32_t *bl
                                  int num_tokens, int num_seqs, int max_blocks, int block_size,
                                  int num_blocks, long long row_bytes, int num_sms,
                                  unsigned int *err, cudaStream_t st);
+cudaError_t launch_bounded_wait_check(unsigned int *err, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
                                int num_blocks, long long block_bytes, int num_sms,
                                unsigned int *err, cudaStream_t st);
@@ -254,6 +255,16 @@ int pagedkv_device_errors(unsigned int *flags, int reset) {
     if (reset && cudaMemset(err, 0, sizeof h) != cudaSuccess) return PAGEDKV_ERR_CUDA;
     *flags = h;
     return h ? PAGEDKV_ERR_BOUNDS : PAGEDKV_OK;
+}
+
+int pagedkv_check_bounded_wait(void *stream) {
+    unsigned int *err = nullptr;
+    int sms = 0;
+    int st = device_state(&err, &sms);
+    if (st != PAGEDKV_OK) return st;
+    return pkv::launch_bounded_wait_check(err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PAGEDKV_OK
+               : PAGEDKV_ERR_CUDA;
 }
 
 int paged_kv_slot_mapping(const int32_t *block_tables, const int32_t *token_seq,
