@@ -354,24 +354,4 @@ int decode_stages(int elem_bytes, int head_dim, int heads_per_unit, int part_tok
     return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-// The bounded-wait check: one thread waits on an mbarrier that nothing ever
-// arrives on. The wait gives up after its time limit, sets
-// PAGEDKV_DEVERR_TIMEOUT and returns false, and the kernel exits normally,
-// which is what every in-kernel wait of the library does when a peer never
-// arrives.
-__global__ void bounded_wait_check_kernel(unsigned int *err) {
-    __shared__ __align__(8) uint64_t bar_storage;
-    const uint32_t bar = smem_addr(&bar_storage);
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
-        mbar_wait(bar, 0, err);
-    }
-}
-
-cudaError_t launch_bounded_wait_check(unsigned int *err, cudaStream_t stream) {
-    bounded_wait_check_kernel<<<1, 32, 0, stream>>>(err);
-    return cudaGetLastError();
-}
-
 }  // namespace pkv

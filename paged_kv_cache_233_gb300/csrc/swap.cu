@@ -8,10 +8,13 @@
 // reads and writes page-locked host memory in place over NVLink-C2C, and one
 // launch keeps enough 16-byte accesses in flight to cover the link latency
 // instead of issuing two driver copies per block.
+//
+// The file also holds the bounded-wait check behind pagedkv_check_bounded_wait.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/pagedkv.h"
+#include "ptx.cuh"
 
 namespace pkv {
 
@@ -71,6 +74,26 @@ cudaError_t launch_swap_blocks(const void *src_k, const void *src_v, void *dst_k
         static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v),
         static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), pairs, num_pairs, src_blocks,
         dst_blocks, vec, int(chunks), err);
+    return cudaGetLastError();
+}
+
+// The bounded-wait check: one thread waits on an mbarrier that nothing ever
+// arrives on. The wait gives up after its time limit, sets
+// PAGEDKV_DEVERR_TIMEOUT and returns false, and the kernel exits normally,
+// which is what every in-kernel wait of the library does when a peer never
+// arrives.
+__global__ void bounded_wait_check_kernel(unsigned int *err) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    const uint32_t bar = smem_addr(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        mbar_wait(bar, 0, err);
+    }
+}
+
+cudaError_t launch_bounded_wait_check(unsigned int *err, cudaStream_t stream) {
+    bounded_wait_check_kernel<<<1, 32, 0, stream>>>(err);
     return cudaGetLastError();
 }
 
