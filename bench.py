@@ -38,7 +38,7 @@ METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s pe
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu", "api.cu",
-                  "decode_instances.cuh", "decode_launch.h"]
+                  "decode_instances.cuh", "decode_launch.h", "launch_cache.h"]
 
 # partition size (tokens) used for each workload's decode; 0 = no split
 PARTITION = {"tiny": 0, "mha7b": 320, "gqa8b_prefix": 320, "longctx_splitk": 512}

@@ -4,6 +4,7 @@
 
 #include "decode_kernel.cuh"
 #include "decode_launch.h"
+#include "launch_cache.h"
 
 namespace pkv {
 
@@ -18,15 +19,13 @@ static cudaError_t launch_decode_instance(DecodeLaunch &a) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // per-device record of the dynamic shared memory this kernel was opened up to
-    static int opened[64] = {0};
-    if (dev < 64 && opened[dev] < smem) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        opened[dev] = smem;
-    }
+    // per-device records of this instantiation: shared memory opened, occupancy
+    static std::atomic<int> opened[kLaunchCacheDevices];
+    static std::atomic<long long> occupancy[kLaunchCacheDevices];
+    e = open_dynamic_smem(opened, dev, kernel, smem);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecodeThreads, smem);
+    e = occupancy_per_sm(occupancy, dev, kernel, kDecodeThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int want = a.ctas_per_sm > 0 ? a.ctas_per_sm : 2;

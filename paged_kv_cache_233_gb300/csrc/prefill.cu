@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "launch_cache.h"
 #include "prefill.h"
 #include "ptx.cuh"
 
@@ -369,12 +370,9 @@ static cudaError_t launch_prefill_instance(const CUtensorMap &kmap, const CUtens
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int opened[64] = {0};
-    if (dev < 64 && opened[dev] < smem) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        opened[dev] = smem;
-    }
+    static std::atomic<int> opened[kLaunchCacheDevices];
+    e = open_dynamic_smem(opened, dev, kernel, smem);
+    if (e != cudaSuccess) return e;
     const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
     const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
     kernel<<<grid, kPfThreads, smem, stream>>>(kmap, vmap, p);

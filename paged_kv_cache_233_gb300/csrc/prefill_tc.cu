@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "launch_cache.h"
 #include "prefill.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -473,12 +474,9 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int opened[64] = {0};
-    if (dev < 64 && opened[dev] < smem) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        opened[dev] = smem;
-    }
+    static std::atomic<int> opened[kLaunchCacheDevices];
+    e = open_dynamic_smem(opened, dev, kernel, smem);
+    if (e != cudaSuccess) return e;
     const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
     const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
     cudaLaunchAttribute attr[1];

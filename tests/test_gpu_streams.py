@@ -126,3 +126,59 @@ def test_prefill_on_a_side_stream(orc):
     ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, wl.dtype)
     err = float(np.abs(to_f64(out) - ref).max())
     assert err <= TOL["f16"], err
+
+
+def test_concurrent_host_threads(orc):
+    """Two host threads decode at once, each on its own stream, with batches of
+    different sizes through the same kernel instantiation: the launchers'
+    per-device records (shared memory opened, occupancy of the last size asked
+    about) are read and replaced by both threads while launches are in flight."""
+    import threading
+
+    cases = []
+    for name, lens, seed in (("threads_a", [3, 70, 500, 17, 900], 34),
+                             ("threads_b", [int(x) for x in np.linspace(1, 1200, 40)], 35)):
+        wl = make_workload(name, "f16", lens, 8, 2, 128, 16, seed)
+        t = materialize(wl, "cuda")
+        kc, vc, q, _ = run_step(wl, t, None)
+        cases.append((wl, t, kc, vc, q))
+    torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def worker(i):
+        try:
+            wl, _, kc, vc, q = cases[i]
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                bt = torch.from_numpy(wl.block_tables).cuda()
+                lens = torch.from_numpy(wl.context_lens).cuda()
+                ws = pk.new_workspace(q, bt, wl.block_size, 32)
+                outs = []
+                for rep in range(40):
+                    out = torch.full_like(q, float("nan"))
+                    pk.paged_attention_decode(q, kc, vc, bt, lens, wl.scale, out, 32 if rep % 2 else 0,
+                                              ws)
+                    outs.append(out)
+            s.synchronize()
+            results[i] = outs
+        except Exception as e:   # surfaced by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert pk.device_errors() == 0
+    for i, (wl, t, kc, vc, q) in enumerate(cases):
+        okc, ovc, _ = oracle_fill(orc, wl, t)
+        ref = oracle_decode(orc, wl, q, okc, ovc)
+        split = to_np(results[i][1]).tobytes()
+        for rep, out in enumerate(results[i]):
+            err = float(np.abs(to_f64(out) - ref).max())
+            assert err <= TOL["f16"], (i, rep, err)
+            if rep % 2:
+                # the same split call gives the same bits every time
+                assert to_np(out).tobytes() == split, (i, rep)
