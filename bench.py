@@ -550,7 +550,8 @@ def measure_trace(block_size, device, partition=None):
     append calls: 1926 / 2026 / 2052 GB/s at B = 8 / 16 / 32, against
     1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045 with 256-token
     partitions). A step appends through paged_kv_append_tokens (one launch
-    and one host call for both): 2033 / 2334 / 2350 GB/s."""
+    and one host call for both): 2033 / 2334 / 2350 GB/s; 2291 / 2255 / 2300
+    with the balanced merge loading its pieces in one round trip."""
     import paged_kv_cache_233_gb300 as pk
     if partition is None:
         partition = pk.PARTITION_BALANCED

@@ -223,15 +223,19 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
                         T *__restrict__ out, int num_seqs, int n_q_heads, int groups,
                         int rows_per_unit, int decode_grid, int cap) {
     constexpr int E = D / 32;
+    constexpr int kBatch = 8;
     using V = typename Vec<E>::type;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x / groups;
     const int hg = blockIdx.x - s * groups;
+    const int warps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // tiles before this sequence, and in total (exact integer sums)
+    // Tiles before this sequence, and in total (exact integer sums). The
+    // lengths are the caller's (no kernel of this library writes them), so
+    // this runs while the decode may still be running; the pieces are read
+    // only after griddepcontrol.wait.
     __shared__ unsigned long long sums[2];
     if (threadIdx.x == 0) sums[0] = sums[1] = 0ull;
-    __syncthreads();
+    const int L = min(max(__ldg(lens + s), 0), cap);
     unsigned long long before_t = 0, total_t = 0;
     for (int t = threadIdx.x; t < num_seqs; t += blockDim.x) {
         const int Lt = min(max(__ldg(lens + t), 0), cap);
@@ -239,18 +243,13 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
         total_t += n;
         if (t < s) before_t += n;
     }
+    __syncthreads();
     atomicAdd(&sums[0], before_t);
     atomicAdd(&sums[1], total_t);
     __syncthreads();
     const unsigned long long before = sums[0], total = sums[1];
-    const int L = min(max(__ldg(lens + s), 0), cap);
     const int nt = (L + kTile - 1) / kTile;
     const int qh0 = hg * rows_per_unit;
-    if (nt == 0) {
-        for (int x = threadIdx.x; x < rows_per_unit * D; x += blockDim.x)
-            out[(size_t(s) * n_q_heads + qh0) * D + x] = Elem<T>::from_float(0.f);
-        return;
-    }
     const long long Tt = (long long)total;
     const long long A = (long long)before + (long long)hg * nt;   // first tile of this pair
     const long long Z = A + nt - 1;                               // last tile
@@ -261,38 +260,81 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
         while (c > 0 && share_start(c) > t) --c;
         return c;
     };
-    const long long c0 = share_of(A), c1 = share_of(Z);
-    if (c0 == c1) return;   // the decode wrote this pair's rows itself
+    const long long c0 = nt > 0 ? share_of(A) : 0, c1 = nt > 0 ? share_of(Z) : 0;
+    if (nt > 0 && c0 == c1) return;   // the decode wrote this pair's rows itself
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (nt == 0) {
+        for (int x = threadIdx.x; x < rows_per_unit * D; x += blockDim.x)
+            out[(size_t(s) * n_q_heads + qh0) * D + x] = Elem<T>::from_float(0.f);
+        return;
+    }
+    const int np = int(c1 - c0 + 1);
     const int slot0 = A == share_start(c0) ? 0 : 1;
-    // shares of CTAs with no tiles (fewer tiles than CTAs) hold no piece
-    auto empty_share = [&](long long c) { return share_start(c) == share_start(c + 1); };
-    for (int r = warp; r < rows_per_unit; r += kMergeWarps) {
-        float M = -INFINITY;
-        for (long long c = c0 + lane; c <= c1; c += 32) {
-            if (empty_share(c)) continue;
-            const size_t row = (size_t(c) * 2 + (c == c0 ? slot0 : 0)) * rows_per_unit + r;
-            M = fmaxf(M, ws_m[row]);
-        }
+    // piece i of a row comes from share c0 + i: the first share's piece sits in
+    // slot0, every later one in slot 0; shares with no tiles (fewer tiles than
+    // CTAs) hold no piece and get weight 0
+    auto piece = [&](int i, int r) {
+        return (size_t(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * rows_per_unit + r;
+    };
+    auto has_piece = [&](int i) {
+        return i < np && share_start(c0 + i) != share_start(c0 + i + 1);
+    };
+    const bool has0 = has_piece(lane);
+    for (int r = warp; r < rows_per_unit; r += warps) {
+        // one round trip: lane i's (m, l) of the first 32 pieces and the first
+        // kBatch pieces' rows
+        const float m0 = has0 ? __ldcg(ws_m + piece(lane, r)) : -INFINITY;
+        const float l0 = has0 ? __ldcg(ws_l + piece(lane, r)) : 0.f;
+        V x[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+            if (k < np) x[k] = __ldcg(reinterpret_cast<const V *>(ws_o + piece(k, r) * D) + lane);
+        float M = m0;
+        for (int b = 32; b < np; b += 32)
+            if (has_piece(b + lane)) M = fmaxf(M, __ldcg(ws_m + piece(b + lane, r)));
 #pragma unroll
         for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, mask));
         float den = 0.f;
         float acc[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
-        for (long long c = c0; c <= c1; ++c) {
-            if (empty_share(c)) continue;
-            const size_t row = (size_t(c) * 2 + (c == c0 ? slot0 : 0)) * rows_per_unit + r;
-            const float w = fast_exp2((ws_m[row] - M) * kLog2e);
-            den = fmaf(w, ws_l[row], den);
-            const V x = *reinterpret_cast<const V *>(ws_o + row * D + lane * E);
-            const float *xf = reinterpret_cast<const float *>(&x);
+        for (int b = 0; b < np; b += 32) {
+            float mp = m0, lp = l0;
+            bool has = has0;
+            if (b > 0) {
+                has = has_piece(b + lane);
+                mp = has ? __ldcg(ws_m + piece(b + lane, r)) : -INFINITY;
+                lp = has ? __ldcg(ws_l + piece(b + lane, r)) : 0.f;
+            }
+            const float w = has ? fast_exp2((mp - M) * kLog2e) : 0.f;
+            den = fmaf(w, lp, den);
+            const int n = min(32, np - b);
+            for (int k0 = 0; k0 < n; k0 += kBatch) {
+                if (b > 0 || k0 > 0) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, xf[e], acc[e]);
+                    for (int k = 0; k < kBatch; ++k)
+                        if (k0 + k < n)
+                            x[k] = __ldcg(reinterpret_cast<const V *>(ws_o + piece(b + k0 + k, r) * D) +
+                                          lane);
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                    // a share without a piece may hold anything: skip it
+                    if (k0 + k < n && wk != 0.f) {
+                        const float *xf = reinterpret_cast<const float *>(&x[k]);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, xf[e], acc[e]);
+                    }
+                }
+            }
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            out[(size_t(s) * n_q_heads + qh0 + r) * D + lane * E + e] = Elem<T>::from_float(acc[e] * inv);
+        for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        T *dst = out + (size_t(s) * n_q_heads + qh0 + r) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dst[e] = Elem<T>::from_float(acc[e] * inv);
     }
 }
 
@@ -306,7 +348,8 @@ static cudaError_t launch_pieces_typed(int head_dim, const float *ws_o, const fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(S * groups));
-    cfg.blockDim = dim3(32 * kMergeWarps);
+    // a warp per row of the pair (at most kMergeWarps warps, each then taking several)
+    cfg.blockDim = dim3(32 * (rows_per_unit < kMergeWarps ? rows_per_unit : kMergeWarps));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;

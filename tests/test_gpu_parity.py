@@ -203,6 +203,30 @@ def test_balanced_split_over_skewed_lengths(orc, ctas):
     assert pk.device_errors() == 0
 
 
+@pytest.mark.parametrize("ctas", [1, 8])
+def test_balanced_split_ignores_stale_workspace(orc, ctas):
+    """The balanced merge reads only the pieces the decode wrote: a workspace
+    full of NaN bytes (every share's slots, including those of CTAs that got no
+    tiles, which lie inside a long sequence's range of shares at 8 CTAs per SM)
+    gives the same result as the oracle."""
+    pk.set_option(pk.OPT_CTAS_PER_SM, ctas)
+    try:
+        for dtype, g, lens in (("f16", 1, [4000, 1, 17, 2, 33, 5]), ("bf16", 4, [3, 700, 20, 1, 64])):
+            wl = make_workload("stale", dtype, lens, 4 * g, 4, 128, 16, 93)
+            t = materialize(wl, "cuda")
+            kc, vc, bt, _ = gpu_fill(wl, t)
+            lens_d = torch.from_numpy(wl.context_lens).cuda()
+            ws = pk.new_workspace(t["q"], bt, wl.block_size, pk.PARTITION_BALANCED)
+            ws.fill_(255)
+            out = torch.full_like(t["q"], float("nan"))
+            pk.paged_attention_decode(t["q"], kc, vc, bt, lens_d, wl.scale, out, pk.PARTITION_BALANCED, ws)
+            okc, ovc, _ = oracle_fill(orc, wl, t)
+            assert_close(out, oracle_decode(orc, wl, t["q"], okc, ovc), dtype, what=f"stale {dtype} ctas={ctas}")
+    finally:
+        pk.set_option(pk.OPT_CTAS_PER_SM, 0)
+    assert pk.device_errors() == 0
+
+
 def test_empty_batch_is_a_no_op():
     q = torch.empty(0, 4, 64, device="cuda", dtype=torch.float16)
     kc = torch.zeros(4, 16, 2, 64, device="cuda", dtype=torch.float16)
