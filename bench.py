@@ -539,19 +539,19 @@ def measure_gate(name, args, device):
     return res
 
 
-def measure_trace(block_size, device, partition=None):
+def measure_trace(block_size, device, partition=None, passes=5):
     """The continuous-batching workload (64 requests, up to 64 slots, 65,536-slot
     pool, LIFO recompute preemption) through the hot path, step by step. Step
-    inputs are gathered on the device beforehand; after one untimed pass over
-    the whole trace, each step's calls are timed with CUDA events. The trace's
+    inputs are gathered on the device beforehand and one workspace serves every
+    step, as a serving loop keeps it. After one untimed pass over the whole
+    trace, each step's calls are timed with CUDA events over `passes` passes;
+    the figures are those of the pass of median total time. The trace's
     contexts are short (<= 640 tokens) and its batches small (<= 64), so a
     step's decode runs the balanced split: the step's 16-token tiles cut into
-    equal shares, one per CTA (measured on GB300 with separate slot mapping and
-    append calls: 1926 / 2026 / 2052 GB/s at B = 8 / 16 / 32, against
-    1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045 with 256-token
-    partitions). A step appends through paged_kv_append_tokens (one launch
-    and one host call for both): 2033 / 2334 / 2350 GB/s; 2291 / 2255 / 2300
-    with the balanced merge loading its pieces in one round trip."""
+    equal shares, one per CTA (measured on GB300, one pass, a workspace per
+    step and separate slot mapping and append calls: 1926 / 2026 / 2052 GB/s at
+    B = 8 / 16 / 32, against 1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045
+    with 256-token partitions)."""
     import paged_kv_cache_233_gb300 as pk
     if partition is None:
         partition = pk.PARTITION_BALANCED
@@ -563,11 +563,16 @@ def measure_trace(block_size, device, partition=None):
     kc = torch.zeros(shape, dtype=tw.torch_dtype, device=device)
     vc = torch.zeros_like(kc)
     steps = []
+    ws_bytes = 0
     for plan in tw.plans:
         x = step_inputs(tw, plan, tensors, device)
         x["out"] = torch.empty_like(x["q"])
-        x["ws"] = pk.new_workspace(x["q"], x["block_tables"], tw.block_size, partition)
+        q, bt = x["q"], x["block_tables"]
+        ws_bytes = max(ws_bytes, pk.paged_attention_workspace_bytes(
+            q.shape[0], q.shape[1], q.shape[2], bt.shape[1], tw.block_size, partition))
         steps.append((plan, x))
+    # one workspace for every step, as a serving loop keeps it
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None
 
     def one_pass(ev=None):
         for i, (plan, x) in enumerate(steps):
@@ -576,17 +581,21 @@ def measure_trace(block_size, device, partition=None):
             pk.paged_kv_append_tokens(x["k"], x["v"], x["block_tables"], x["token_row"],
                                       x["token_pos"], kc, vc)
             pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"],
-                                      tw.scale, x["out"], partition, x["ws"])
+                                      tw.scale, x["out"], partition, ws)
             if ev is not None:
                 ev[i][1].record()
 
     one_pass()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in steps]
-    one_pass(ev)
-    torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in ev]
+    runs = []
+    for _ in range(passes):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in steps]
+        one_pass(ev)
+        torch.cuda.synchronize()
+        runs.append([a.elapsed_time(b) for a, b in ev])
+    # the pass of median total time
+    ms = sorted(runs, key=sum)[len(runs) // 2]
     total_ms = sum(ms)
     dec_bytes = 0
     app_bytes = 0
@@ -605,7 +614,8 @@ def measure_trace(block_size, device, partition=None):
             "total_ms": total_ms, "decode_gbs": dec_bytes / total_ms / 1e6,
             "seq_decodes_per_s": decodes / (total_ms * 1e-3),
             "append_gbs_in_step": app_bytes / total_ms / 1e6,
-            "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition}
+            "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition,
+            "timed_passes": passes, "pass_ms_range": [min(map(sum, runs)), max(map(sum, runs))]}
 
 
 def measure_shared_prefix(device, reps=200, partition=320):
@@ -940,9 +950,20 @@ def main(argv=None):
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the chunked-prefill measurement (for profiling its kernel)")
     ap.add_argument("--prefill-reps", type=int, default=50)
+    ap.add_argument("--trace-only", type=int, default=None, metavar="BLOCK_SIZE",
+                    help="only the continuous-batching trace at this block size (for profiling it)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.trace_only is not None:
+        import paged_kv_cache_233_gb300 as pk
+        from paged_kv_cache_233_gb300 import build as pk_build
+        pk_build.build()
+        pk.load()
+        torch.cuda.set_device(0)
+        b = args.trace_only
+        print(json.dumps({"trace": {f"B{b}": measure_trace(b, torch.device("cuda", 0))}}), flush=True)
+        return
     if args.prefill_only:
         import paged_kv_cache_233_gb300 as pk
         from paged_kv_cache_233_gb300 import build as pk_build

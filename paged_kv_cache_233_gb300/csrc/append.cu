@@ -103,6 +103,15 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
     const int c0 = threadIdx.x - sub * tpr;
     for (long long t = (long long)blockIdx.x * rows_per_cta + sub; t < num_tokens;
          t += (long long)gridDim.x * rows_per_cta) {
+        const uint4 *ks = k + t * vec_per_row;
+        const uint4 *vs = v + t * vec_per_row;
+        // the row's first chunk does not depend on the slot: its loads go out
+        // together with those of the position, the sequence and the table entry
+        uint4 a0 = make_uint4(0u, 0u, 0u, 0u), b0 = a0;
+        if (c0 < vec_per_row) {
+            a0 = __ldcs(ks + c0);
+            b0 = __ldcs(vs + c0);
+        }
         const int pos = token_pos[t];
         const int seq = token_seq[t];
         long long slot = -1;
@@ -126,11 +135,13 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
             if (slot_mapping) slot_mapping[t] = slot;
         }
         if (slot < 0) continue;
-        const uint4 *ks = k + t * vec_per_row;
-        const uint4 *vs = v + t * vec_per_row;
         uint4 *kd = k_cache + slot * vec_per_row;
         uint4 *vd = v_cache + slot * vec_per_row;
-        for (int c = c0; c < vec_per_row; c += tpr) {
+        if (c0 < vec_per_row) {
+            kd[c0] = a0;
+            vd[c0] = b0;
+        }
+        for (int c = c0 + tpr; c < vec_per_row; c += tpr) {
             const uint4 a = __ldcs(ks + c);
             const uint4 b = __ldcs(vs + c);
             kd[c] = a;

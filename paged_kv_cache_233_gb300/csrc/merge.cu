@@ -262,14 +262,8 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
     };
     const long long c0 = nt > 0 ? share_of(A) : 0, c1 = nt > 0 ? share_of(Z) : 0;
     if (nt > 0 && c0 == c1) return;   // the decode wrote this pair's rows itself
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (nt == 0) {
-        for (int x = threadIdx.x; x < rows_per_unit * D; x += blockDim.x)
-            out[(size_t(s) * n_q_heads + qh0) * D + x] = Elem<T>::from_float(0.f);
-        return;
-    }
     const int np = int(c1 - c0 + 1);
-    const int slot0 = A == share_start(c0) ? 0 : 1;
+    const int slot0 = nt > 0 && A != share_start(c0) ? 1 : 0;
     // piece i of a row comes from share c0 + i: the first share's piece sits in
     // slot0, every later one in slot 0; shares with no tiles (fewer tiles than
     // CTAs) hold no piece and get weight 0
@@ -279,7 +273,14 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
     auto has_piece = [&](int i) {
         return i < np && share_start(c0 + i) != share_start(c0 + i + 1);
     };
-    const bool has0 = has_piece(lane);
+    // everything so far follows from the lengths alone
+    const bool has0 = nt > 0 && has_piece(lane);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (nt == 0) {
+        for (int x = threadIdx.x; x < rows_per_unit * D; x += blockDim.x)
+            out[(size_t(s) * n_q_heads + qh0) * D + x] = Elem<T>::from_float(0.f);
+        return;
+    }
     for (int r = warp; r < rows_per_unit; r += warps) {
         // one round trip: lane i's (m, l) of the first 32 pieces and the first
         // kBatch pieces' rows
