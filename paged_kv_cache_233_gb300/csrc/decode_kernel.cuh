@@ -678,6 +678,49 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         *abort_flag = 0;
         fence_barrier_init();
     }
+    // Every thread: the per-sequence inputs into shared memory, four sequences
+    // per thread in flight (the caller's arrays; like the rest of the set-up,
+    // read before the grid dependency wait). Shared prefixes: the group id goes
+    // to seq_pu until the scan below replaces it with the prefix units.
+    const int cap = p.max_blocks * B;
+    {
+        constexpr int kIn = 4;
+        for (int s0 = threadIdx.x; s0 < S; s0 += kIn * kDecodeThreads) {
+            int len[kIn], grp[kIn], want[kIn];
+#pragma unroll
+            for (int k = 0; k < kIn; ++k) {
+                const int s = s0 + k * kDecodeThreads;
+                len[k] = s < S ? __ldg(p.context_lens + s) : 0;
+                grp[k] = prefix && s < S ? __ldg(p.seq_group + s) : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < kIn; ++k)
+                want[k] = grp[k] >= 0 && grp[k] < p.num_groups ? __ldg(p.group_prefix + grp[k]) : 0;
+#pragma unroll
+            for (int k = 0; k < kIn; ++k) {
+                const int s = s0 + k * kDecodeThreads;
+                if (s >= S) continue;
+                const int Lc = min(max(len[k], 0), cap);
+                if (Lc != len[k]) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
+                seq_len[s] = Lc;
+                if (prefix) {
+                    int gsel = grp[k];
+                    if (gsel >= p.num_groups) {
+                        atomicOr(p.err, PAGEDKV_DEVERR_SEQ_INDEX);
+                        gsel = -1;
+                    }
+                    int p0 = 0;
+                    if (gsel >= 0) {
+                        if (want[k] > Lc) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
+                        p0 = min(max(want[k], 0), cap) / P;
+                    }
+                    seq_p0[s] = p0;
+                    seq_pu[s] = gsel;
+                }
+            }
+        }
+    }
+    __syncthreads();
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_descriptor(&kmap);
@@ -685,31 +728,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         // per sequence, prefix-summed: units = max(1, ceil(L / P)) partitions x head
         // groups (fixed mode), or 16-token tiles x head groups (balanced mode)
-        const int cap = p.max_blocks * B;
         int carry = 0;
         int run_carry = -1;   // start of the group run in progress (shared prefixes)
+        int gprev = -1;       // group of the previous chunk's last sequence
         if (lane == 0) seq_base[0] = 0;
         for (int s0 = 0; s0 < S; s0 += 32) {
             const int s = s0 + lane;
-            int cnt = 0;
-            int Lc = 0;
-            if (s < S) {
-                const int L = p.context_lens[s];
-                Lc = min(max(L, 0), cap);
-                if (Lc != L) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
-                seq_len[s] = Lc;
-                cnt = (p.balanced ? (Lc + kTile - 1) / kTile : (Lc > 0 ? (Lc + P - 1) / P : 1)) * groups;
-            }
+            const int Lc = s < S ? seq_len[s] : 0;
+            int cnt = s < S ? (p.balanced ? (Lc + kTile - 1) / kTile : (Lc > 0 ? (Lc + P - 1) / P : 1)) * groups
+                            : 0;
             if (prefix) {
                 // group runs: a run starts where the group id changes; sequence s is
                 // member (s - run start) of its run; every max_members-th member leads
                 // the units of the run's shared prefix partitions
-                int gsel = s < S ? p.seq_group[s] : -1;
-                if (gsel >= p.num_groups) {
-                    atomicOr(p.err, PAGEDKV_DEVERR_SEQ_INDEX);
-                    gsel = -1;
-                }
-                const int prev = (s > 0 && s < S) ? p.seq_group[s - 1] : -1;
+                const int gsel = s < S ? seq_pu[s] : -1;
+                int prev = __shfl_up_sync(kFull, gsel, 1);
+                if (lane == 0) prev = gprev;
+                gprev = __shfl_sync(kFull, gsel, 31);
                 int f = (gsel >= 0 && prev != gsel) ? s : -1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -719,17 +754,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int run_start = max(f, run_carry);
                 run_carry = __shfl_sync(kFull, run_start, 31);
                 if (s < S) {
-                    int p0 = 0, pu = 0;
-                    if (gsel >= 0) {
-                        const int want = p.group_prefix[gsel];
-                        const int Lp = min(max(want, 0), cap);
-                        if (want > Lc) atomicOr(p.err, PAGEDKV_DEVERR_CONTEXT_LEN);
-                        p0 = Lp / P;
-                        if ((s - run_start) % p.max_members == 0) pu = p0 * groups;
-                    }
+                    const int p0 = seq_p0[s];
+                    const int pu = gsel >= 0 && (s - run_start) % p.max_members == 0 ? p0 * groups : 0;
                     const int own = Lc > 0 ? max(0, (Lc + P - 1) / P - p0) : (p0 > 0 ? 0 : 1);
                     cnt = pu + own * groups;
-                    seq_p0[s] = p0;
                     seq_pu[s] = pu;
                 }
             }
