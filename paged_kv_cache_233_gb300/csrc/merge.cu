@@ -253,7 +253,7 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
     const long long Tt = (long long)total;
     const long long A = (long long)before + (long long)hg * nt;   // first tile of this pair
     const long long Z = A + nt - 1;                               // last tile
-    auto share_start = [&](long long c) { return Tt * c / decode_grid; };
+    auto share_start = [=](long long c) { return Tt * c / decode_grid; };
     auto share_of = [&](long long t) {
         long long c = t * decode_grid / Tt;
         while (c + 1 < decode_grid && share_start(c + 1) <= t) ++c;
@@ -267,7 +267,7 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
     // piece i of a row comes from share c0 + i: the first share's piece sits in
     // slot0, every later one in slot 0; shares with no tiles (fewer tiles than
     // CTAs) hold no piece and get weight 0
-    auto piece = [&](int i, int r) {
+    auto piece = [=](int i, int r) {
         return (size_t(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * rows_per_unit + r;
     };
     auto has_piece = [&](int i) {
