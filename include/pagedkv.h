@@ -32,6 +32,13 @@
  *     in a sticky device error word that pagedkv_device_errors() returns.
  *   - Kernels never trap. Every wait inside a kernel is bounded in time; a
  *     wait that gives up sets PAGEDKV_DEVERR_TIMEOUT and the kernel returns.
+ *   - Host threads may call the entry points concurrently, each with its own
+ *     buffers and stream: the library's per-device records (error word,
+ *     shared memory a kernel was opened up to, occupancy) are kept under a
+ *     lock or in atomics. Two exceptions: the tuning options
+ *     (pagedkv_set_option) and the library-owned scratch of
+ *     paged_attention_decode_noalloc, whose calls must be ordered on one
+ *     stream.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
