@@ -49,6 +49,9 @@ def shared_decode(wl, t, kc, vc, bt, P, seq_group, group_prefix):
     ("bf16", 16, 4, 64, 5, 96, 32),         # odd group size, D 64
     ("bf16", 64, 8, 128, 4, 512, 512),      # group of 8 q heads: one member per chunk
     ("f32", 8, 4, 64, 3, 64, 32),           # CUDA-core path: one member per chunk
+    ("bf16", 32, 8, 128, 12, 512, 256),     # runs of 12 (sequences 24-35 straddle the set-up
+                                            # scan's 32-sequence chunks): 2 members per chunk
+    ("f16", 32, 32, 128, 11, 256, 128),     # runs of 11 (22-32 straddle them): 8 members per chunk
 ])
 def test_shared_prefix_matches_oracle(orc, dtype, Hq, Hkv, D, group, prefix, P):
     rng = np.random.default_rng(7)
