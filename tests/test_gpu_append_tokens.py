@@ -33,15 +33,19 @@ def fused_fill(wl, t, with_slots):
     return kc, vc, slots
 
 
-@pytest.mark.parametrize("wl_name", ["tiny", "smoke_bf16", "mha_rows"])
+@pytest.mark.parametrize("wl_name", ["tiny", "smoke_bf16", "mha_rows", "odd_rows"])
 @pytest.mark.parametrize("with_slots", [True, False])
 def test_pools_and_slots_bit_exact_to_the_oracle(orc, wl_name, with_slots):
     if wl_name == "tiny":
         wl = preset("tiny")
     elif wl_name == "smoke_bf16":
         wl = make_workload("fused_bf16", "bf16", [1, 17, 40, 300], 32, 8, 128, 16, 41)
-    else:
+    elif wl_name == "mha_rows":
         wl = make_workload("fused_mha", "f16", [5, 130, 700, 64], 32, 32, 128, 8, 42)
+    else:
+        # 384-byte rows (3 kv heads x 64 x fp16): 24 chunks of 16 bytes for a
+        # row's 32 threads, so some threads of every row copy nothing
+        wl = make_workload("fused_odd", "f16", [3, 50, 17, 129], 6, 3, 64, 16, 44)
     t = materialize(wl, "cuda")
     pk.device_errors(reset=True)
     kc, vc, slots = fused_fill(wl, t, with_slots)
