@@ -72,7 +72,8 @@ typedef enum {
 #define PAGEDKV_DEVERR_BLOCK_ID     0x02u  /* a block table entry outside [0, num_blocks) */
 #define PAGEDKV_DEVERR_CONTEXT_LEN  0x04u  /* context_len < 0 or > max_blocks_per_seq*block_size */
 #define PAGEDKV_DEVERR_POSITION     0x08u  /* slot mapping: position past the block table */
-#define PAGEDKV_DEVERR_SEQ_INDEX    0x10u  /* slot mapping: token_seq outside [0, num_seqs) */
+#define PAGEDKV_DEVERR_SEQ_INDEX    0x10u  /* slot mapping: token_seq outside [0, num_seqs);
+                                              shared-prefix decode: a group id >= num_groups */
 #define PAGEDKV_DEVERR_TIMEOUT      0x20u  /* a bounded in-kernel wait gave up */
 
 /* partition_tokens value of paged_attention_decode selecting the balanced split. */
@@ -334,7 +335,9 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
  * Same arguments and results as paged_attention_decode (within the same
  * tolerance) plus the sharing structure:
  *   seq_group     int32 [num_seqs], device: prefix group of each sequence, -1
- *                 for none. Members of a group are consecutive sequences.
+ *                 for none. Members of a group are consecutive sequences. A
+ *                 group id >= num_groups sets PAGEDKV_DEVERR_SEQ_INDEX and
+ *                 the sequence is decoded as if it had no group.
  *   group_prefix  int32 [num_groups], device: the number of leading tokens
  *                 that every member of the group holds in the SAME physical
  *                 blocks as the group's first member (the caller's

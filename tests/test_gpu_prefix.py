@@ -109,6 +109,23 @@ def test_prefix_longer_than_a_member_is_flagged():
     assert pk.device_errors() & 0x04
 
 
+def test_group_id_past_the_groups_is_flagged(orc):
+    """A group id outside [0, num_groups) sets the sequence-index bit and that
+    sequence is decoded on its own, as by plain decode."""
+    wl = make_workload("badgroup", "bf16", [100, 100, 70], 8, 4, 64, 16, 74)
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    ref = oracle_decode(orc, wl, t["q"], okc, ovc)
+    pk.device_errors(reset=True)
+    sg = torch.tensor([0, 5, -1], dtype=torch.int32, device="cuda")
+    gp = torch.tensor([0], dtype=torch.int32, device="cuda")
+    out = shared_decode(wl, t, kc, vc, bt, 32, sg, gp)
+    torch.cuda.synchronize()
+    assert pk.device_errors() == 0x10
+    assert_close(out, ref, "bf16", what="group id past the groups")
+
+
 def test_gqa_prefix_workload_full_size(orc):
     """The GQA batch-256 workload with its 16-member, 512-token prefix groups."""
     wl = preset("gqa8b_prefix")
