@@ -705,7 +705,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 seq_len[s] = Lc;
                 if (prefix) {
                     int gsel = grp[k];
-                    if (gsel >= p.num_groups) {
+                    // -1 is the only "no group" value: ids past the groups and
+                    // other negative ids are flagged and decoded ungrouped
+                    if (gsel >= p.num_groups || gsel < -1) {
                         atomicOr(p.err, PAGEDKV_DEVERR_SEQ_INDEX);
                         gsel = -1;
                     }
@@ -896,6 +898,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     Unit cur;
     walk.next(cur);
     st.prefetch_q(qbase, size_t(cur.s), ((cur.hg << p.log2_hpu) + hh) * g, g, cur.members, p.n_q_heads);
+    // No store to out or the workspace before the kernels ahead of this one
+    // have completed: a unit with no tiles (an empty context) writes its zero
+    // row without waiting on any stage, and the previous decode of the stream
+    // may still be writing the same rows (it let this grid start early). The
+    // q rows above are the caller's and were safe to read before.
+    grid_dependency_wait();
     for (;; ++unit_count) {
         const int qh0 = ((cur.hg << p.log2_hpu) + hh) * g;   // first q head of this warp
         if constexpr (kMma) st.begin_unit();
