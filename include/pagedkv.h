@@ -73,7 +73,8 @@ typedef enum {
 #define PAGEDKV_DEVERR_CONTEXT_LEN  0x04u  /* context_len < 0 or > max_blocks_per_seq*block_size */
 #define PAGEDKV_DEVERR_POSITION     0x08u  /* slot mapping: position past the block table */
 #define PAGEDKV_DEVERR_SEQ_INDEX    0x10u  /* slot mapping: token_seq outside [0, num_seqs);
-                                              shared-prefix decode: a group id >= num_groups */
+                                              shared-prefix decode: a group id outside
+                                              [-1, num_groups) */
 #define PAGEDKV_DEVERR_TIMEOUT      0x20u  /* a bounded in-kernel wait gave up */
 
 /* partition_tokens value of paged_attention_decode selecting the balanced split. */
@@ -336,8 +337,10 @@ int paged_attention_decode(const void *q, const void *k_cache, const void *v_cac
  * tolerance) plus the sharing structure:
  *   seq_group     int32 [num_seqs], device: prefix group of each sequence, -1
  *                 for none. Members of a group are consecutive sequences. A
- *                 group id >= num_groups sets PAGEDKV_DEVERR_SEQ_INDEX and
- *                 the sequence is decoded as if it had no group.
+ *                 group id >= num_groups or below -1 sets
+ *                 PAGEDKV_DEVERR_SEQ_INDEX and the sequence is decoded as if
+ *                 it had no group (a run of the group's members that it
+ *                 interrupts continues after it as a new run).
  *   group_prefix  int32 [num_groups], device: the number of leading tokens
  *                 that every member of the group holds in the SAME physical
  *                 blocks as the group's first member (the caller's
@@ -387,8 +390,9 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
  *     before anything is enqueued. partition_tokens == 0 needs no scratch;
  *     PAGEDKV_PARTITION_BALANCED uses it like any split.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and so does the first
+ *     call after cudaDeviceReset has replaced the device's context; make
+ *     those calls before any stream capture.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents. Nothing in it needs to start at zero: each call writes
  *     every partition state it later reads. Calls whose work overlaps on the

@@ -126,6 +126,29 @@ def test_group_id_past_the_groups_is_flagged(orc):
     assert_close(out, ref, "bf16", what="group id past the groups")
 
 
+@pytest.mark.parametrize("bad", [5, -5])
+def test_bad_group_id_inside_a_prefix_group(orc, bad):
+    """A bad group id (past the groups, or negative other than -1) between the
+    members of a group whose prefix spans several partitions: the bad sequence
+    is flagged and decoded on its own, the members after it start a new run of
+    the group, and every output matches the oracle."""
+    B, P, prefix = 16, 32, 96
+    lens = [200, 150, 180, 170, 300]
+    wl = make_workload("badmember", "bf16", lens, 32, 8, 128, B, 75, prefix_group=5,
+                       prefix_tokens=prefix)
+    t = materialize(wl, "cuda")
+    kc, vc, bt, _ = gpu_fill(wl, t)
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    ref = oracle_decode(orc, wl, t["q"], okc, ovc)
+    pk.device_errors(reset=True)
+    sg = torch.tensor([0, bad, 0, 0, 0], dtype=torch.int32, device="cuda")
+    gp = torch.tensor([prefix], dtype=torch.int32, device="cuda")
+    out = shared_decode(wl, t, kc, vc, bt, P, sg, gp)
+    torch.cuda.synchronize()
+    assert pk.device_errors() == 0x10
+    assert_close(out, ref, "bf16", what=f"group id {bad} inside a prefix group")
+
+
 def test_gqa_prefix_workload_full_size(orc):
     """The GQA batch-256 workload with its 16-member, 512-token prefix groups."""
     wl = preset("gqa8b_prefix")
@@ -137,8 +160,12 @@ def test_gqa_prefix_workload_full_size(orc):
     pk.paged_attention_decode(t["q"], kc, vc, bt, torch.from_numpy(wl.context_lens).cuda(), wl.scale,
                               plain, 320, pk.new_workspace(t["q"], bt, wl.block_size, 320))
     assert float((out.double() - plain.double()).abs().max()) <= TOL["bf16"]
+    # the oracle decodes its own pools (its slot mapping + append of the same
+    # tokens), and the GPU's pools equal them byte for byte
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    assert to_np(kc).view(np.uint8).tobytes() == okc.view(np.uint8).tobytes()
+    assert to_np(vc).view(np.uint8).tobytes() == ovc.view(np.uint8).tobytes()
     units = [(s, h) for s in (0, 1, 15, 16, 100, 255) for h in (0, 7)]
-    ref = orc.decode(to_np(t["q"]), to_np(kc), to_np(vc), wl.block_tables, wl.context_lens,
-                     wl.scale, "bf16", units=units)
+    ref = oracle_decode(orc, wl, t["q"], okc, ovc, units=units)
     rows = [(s, h * 4 + j) for s, h in units for j in range(4)]
     assert_close(out, ref, "bf16", rows=rows, what="gqa prefix full size")
