@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/pagedkv.h"
+#include "context_id.h"
 #include "decode_launch.h"
 #include "prefill.h"
 
@@ -49,6 +50,7 @@ constexpr int kMaxCtasPerSm = 8;
 
 std::mutex g_mu;
 unsigned int *g_err_ptr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};   // context the error word's address belongs to
 int g_num_sms[kMaxDevices] = {};
 
 int g_opt_path = pkv::kPathAuto;
@@ -72,12 +74,14 @@ bool valid_dtype(int dtype) {
     return dtype == PAGEDKV_F32 || dtype == PAGEDKV_F16 || dtype == PAGEDKV_BF16;
 }
 
-// Error-word address and SM count of the current device (looked up once per device).
+// Error-word address and SM count of the current device (looked up once per
+// device and context: again after cudaDeviceReset has replaced the context).
 int device_state(unsigned int **err, int *sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PAGEDKV_ERR_CUDA;
+    const unsigned long long ctx = pkv::current_context_id();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_err_ptr[dev]) {
+    if (!g_err_ptr[dev] || ctx == 0 || g_err_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_pagedkv_errors) != cudaSuccess || !p) return PAGEDKV_ERR_CUDA;
         int n = 0;
@@ -85,6 +89,7 @@ int device_state(unsigned int **err, int *sms) {
             return PAGEDKV_ERR_CUDA;
         g_num_sms[dev] = n;
         g_err_ptr[dev] = static_cast<unsigned int *>(p);
+        g_err_ctx[dev] = ctx ? ctx : pkv::current_context_id();
     }
     *err = g_err_ptr[dev];
     *sms = g_num_sms[dev];

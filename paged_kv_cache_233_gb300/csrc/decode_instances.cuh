@@ -20,7 +20,7 @@ static cudaError_t launch_decode_instance(DecodeLaunch &a) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     // per-device records of this instantiation: shared memory opened, occupancy
-    static std::atomic<int> opened[kLaunchCacheDevices];
+    static std::atomic<unsigned long long> opened[kLaunchCacheDevices];
     static std::atomic<long long> occupancy[kLaunchCacheDevices];
     e = open_dynamic_smem(opened, dev, kernel, smem);
     if (e != cudaSuccess) return e;

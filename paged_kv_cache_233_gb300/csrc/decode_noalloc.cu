@@ -12,13 +12,15 @@
 // process exits.
 //
 // The array's host-side name is only a stand-in: its device address is looked
-// up once per device with cudaGetSymbolAddress (on the first call made with
-// that device current) and passed to the kernels like any workspace.
+// up with cudaGetSymbolAddress once per device and context (on the first call
+// made with that device current, and again after cudaDeviceReset has replaced
+// the device's context) and passed to the kernels like any workspace.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/pagedkv.h"
+#include "context_id.h"
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PAGEDKV_NOALLOC_SCRATCH_BYTES];
 
@@ -26,20 +28,28 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchRecord {
+    void *addr;
+    unsigned long long context;   // id of the context the address belongs to
+};
+ScratchRecord g_scratch[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.
 int scratch_address(void **addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PAGEDKV_ERR_CUDA;
+    const unsigned long long ctx = pkv::current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchRecord &r = g_scratch[dev];
+    if (!r.addr || ctx == 0 || r.context != ctx) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) return PAGEDKV_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        r.addr = p;
+        // the lookup above makes the device's context current if it was not yet
+        r.context = ctx ? ctx : pkv::current_context_id();
     }
-    *addr = g_scratch_addr[dev];
+    *addr = r.addr;
     return PAGEDKV_OK;
 }
 

@@ -8,25 +8,36 @@
 
 #include <cuda_runtime.h>
 
+#include "context_id.h"
+
 namespace pkv {
 
 constexpr int kLaunchCacheDevices = 64;
 
 // Raises `kernel`'s dynamic shared-memory limit to at least `smem` bytes on
-// device `dev`, calling the runtime only when this record is below `smem`
-// (the attribute call itself is idempotent, so two threads racing here both
-// succeed). Devices past the record's range are opened on every call.
+// device `dev`, calling the runtime only when this record is below `smem` or
+// was made in another context (a kernel attribute belongs to the context the
+// kernel was loaded in; cudaDeviceReset replaces it). The record packs the low
+// 32 bits of the context id with the size; the attribute call itself is
+// idempotent, so two threads racing here both succeed. Devices past the
+// record's range are opened on every call.
 template <typename Kernel>
-cudaError_t open_dynamic_smem(std::atomic<int> *opened, int dev, Kernel kernel, int smem) {
-    if (dev >= 0 && dev < kLaunchCacheDevices &&
-        opened[dev].load(std::memory_order_acquire) >= smem)
-        return cudaSuccess;
+cudaError_t open_dynamic_smem(std::atomic<unsigned long long> *opened, int dev, Kernel kernel,
+                              int smem) {
+    const unsigned long long ctx = current_context_id() & 0xffffffffull;
+    const bool cached = ctx != 0 && dev >= 0 && dev < kLaunchCacheDevices;
+    if (cached) {
+        const unsigned long long r = opened[dev].load(std::memory_order_acquire);
+        if ((r >> 32) == ctx && int(r & 0xffffffffull) >= smem) return cudaSuccess;
+    }
     const cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess || dev < 0 || dev >= kLaunchCacheDevices) return e;
-    int cur = opened[dev].load(std::memory_order_relaxed);
-    while (cur < smem &&
-           !opened[dev].compare_exchange_weak(cur, smem, std::memory_order_acq_rel))
+    if (e != cudaSuccess || !cached) return e;
+    const unsigned long long want = (ctx << 32) | unsigned(smem);
+    unsigned long long cur = opened[dev].load(std::memory_order_relaxed);
+    // keep the larger size of the same context; a record of another context is replaced
+    while (((cur >> 32) != ctx || int(cur & 0xffffffffull) < smem) &&
+           !opened[dev].compare_exchange_weak(cur, want, std::memory_order_acq_rel))
     {
     }
     return cudaSuccess;

@@ -474,7 +474,7 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static std::atomic<int> opened[kLaunchCacheDevices];
+    static std::atomic<unsigned long long> opened[kLaunchCacheDevices];
     e = open_dynamic_smem(opened, dev, kernel, smem);
     if (e != cudaSuccess) return e;
     const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
