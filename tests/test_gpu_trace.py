@@ -67,12 +67,95 @@ def run_trace(tw, tensors, P, orc=None):
     return rows
 
 
+SLOTS = [8, 16, 32, 64, 128, 256]
+
+
+@pytest.mark.parametrize("slots", SLOTS)
 @pytest.mark.parametrize("block_size", [8, 16, 32])
-def test_trace_matches_oracle(orc, block_size):
-    tw = cb_trace(block_size=block_size, slots=64)
+def test_trace_matches_oracle(orc, block_size, slots):
+    """Separate slot-mapping and append calls, 256-token partitions."""
+    tw = cb_trace(block_size=block_size, slots=slots)
     tensors = trace_tensors(tw, "cuda")
     rows = run_trace(tw, tensors, 256, orc)
     assert len(rows) == sum(r.output_len for r in tw.requests)
+    assert max(len(p.rids) for p in tw.plans) <= slots
+
+
+def oracle_trace(orc, tw, tensors):
+    """Every step's decoded rows and the final pools, all on the oracle."""
+    shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
+    okc, ovc = poison(shape, tw.dtype), poison(shape, tw.dtype)
+    refs, slots = [], []
+    for plan in tw.plans:
+        x = step_inputs(tw, plan, tensors, "cpu")
+        sm = orc.slot_mapping(plan.block_tables, plan.token_row, plan.token_pos, tw.block_size)
+        assert orc.append(to_np(x["k"]), to_np(x["v"]), sm, okc, ovc) == 0
+        refs.append(orc.decode(to_np(x["q"]), okc, ovc, plan.block_tables, plan.context_lens,
+                               tw.scale, tw.dtype))
+        slots.append(sm)
+    return refs, slots, okc, ovc
+
+
+@pytest.mark.parametrize("slots", SLOTS)
+@pytest.mark.parametrize("block_size", [8, 16, 32])
+def test_trace_bench_launches_match_oracle(orc, block_size, slots):
+    """The bench's launches: one paged_kv_append_tokens (slots written out too)
+    and one balanced-split decode per step, one workspace for every step."""
+    tw = cb_trace(block_size=block_size, slots=slots)
+    tensors = trace_tensors(tw, "cuda")
+    refs, ref_slots, okc, ovc = oracle_trace(orc, tw, {k: v.cpu() for k, v in tensors.items()})
+    shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=tw.torch_dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    P = pk.PARTITION_BALANCED
+    ws_bytes = max(pk.paged_attention_workspace_bytes(len(p.rids), tw.n_q_heads, tw.head_dim,
+                                                      p.block_tables.shape[1], tw.block_size, P)
+                   for p in tw.plans)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    pk.device_errors(reset=True)
+    for i, plan in enumerate(tw.plans):
+        x = step_inputs(tw, plan, tensors, "cuda")
+        sm = torch.empty(len(plan.token_row), dtype=torch.int64, device="cuda")
+        pk.paged_kv_append_tokens(x["k"], x["v"], x["block_tables"], x["token_row"],
+                                  x["token_pos"], kc, vc, slot_mapping=sm)
+        out = torch.full_like(x["q"], float("nan"))
+        pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"], tw.scale,
+                                  out, P, ws)
+        assert np.array_equal(sm.cpu().numpy(), ref_slots[i]), f"step {plan.step}: slots differ"
+        err = float(np.abs(to_f64(out) - refs[i]).max())
+        assert err <= TOL[tw.dtype], f"step {plan.step}: max-abs error {err:.3e}"
+    assert to_np(kc).view(np.uint8).tobytes() == okc.view(np.uint8).tobytes()
+    assert to_np(vc).view(np.uint8).tobytes() == ovc.view(np.uint8).tobytes()
+    assert pk.device_errors() == 0
+
+
+@pytest.mark.parametrize("block_size,slots", [(16, 8), (16, 64), (8, 32), (32, 16)])
+def test_trace_graph_replay_matches_oracle(orc, block_size, slots):
+    """The bench's graph-issued trace: the whole pass captured once in a CUDA
+    graph; after two replays every step's output and the pools equal the
+    oracle's (appends rewrite the same bytes, so replays are idempotent)."""
+    import bench
+    tw = cb_trace(block_size=block_size, slots=slots)
+    shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
+    pools = (torch.full(shape, float("nan"), dtype=tw.torch_dtype, device="cuda"),
+             torch.full(shape, float("nan"), dtype=tw.torch_dtype, device="cuda"))
+    tr = bench.TraceRun(tw, "cuda", pk.PARTITION_BALANCED, pools=pools)
+    pk.device_errors(reset=True)
+    tr.run_pass()
+    torch.cuda.synchronize()
+    for _, x in tr.steps:
+        x["out"].fill_(float("nan"))
+    g = tr.capture()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    refs, _, okc, ovc = oracle_trace(orc, tw, {k: v.cpu() for k, v in trace_tensors(tw, "cuda").items()})
+    for i, (plan, x) in enumerate(tr.steps):
+        err = float(np.abs(to_f64(x["out"]) - refs[i]).max())
+        assert err <= TOL[tw.dtype], f"step {plan.step}: max-abs error {err:.3e}"
+    assert to_np(tr.kc).view(np.uint8).tobytes() == okc.view(np.uint8).tobytes()
+    assert to_np(tr.vc).view(np.uint8).tobytes() == ovc.view(np.uint8).tobytes()
+    assert pk.device_errors() == 0
 
 
 def test_preemption_by_recompute_changes_no_output(orc):

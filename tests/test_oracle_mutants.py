@@ -66,18 +66,43 @@ MUTANTS = {
 }
 
 
+def run_pins(src_text, tmp_dir):
+    """Compile `src_text` as an oracle library and run every pin against it in
+    the child harness; returns the finished process."""
+    src = tmp_dir / "oracle_copy.c"
+    src.write_text(src_text)
+    lib = oracle_build.build(str(src), str(tmp_dir / "oracle_copy.so"))
+    code = CHILD.format(repo=REPO, tests=HERE, lib=lib)
+    return subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                          timeout=300)
+
+
+@pytest.fixture(scope="module")
+def control(tmp_path_factory):
+    """The unmutated source through the same compile step and child harness: it
+    must exit 0 with no pin failing. Only then does a mutant's non-zero exit
+    count as caught (an import error or a broken harness would otherwise make
+    every mutant look caught)."""
+    res = run_pins(open(oracle_build.SOURCE).read(), tmp_path_factory.mktemp("control"))
+    assert res.returncode == 0, f"control run failed: {res.stderr[-2000:]}"
+    caught = json.loads(res.stdout.strip().splitlines()[-1])
+    assert caught == [], f"pins fail on the unmutated oracle: {caught}"
+    return True
+
+
+def test_control_passes_every_pin(control):
+    assert control
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name, tmp_path):
+def test_mutant_is_caught(name, tmp_path, control):
     old, new = MUTANTS[name]
     src = open(oracle_build.SOURCE).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
-    mutant_src = tmp_path / "mutant.c"
-    mutant_src.write_text(src.replace(old, new))
-    lib = oracle_build.build(str(mutant_src), str(tmp_path / "mutant.so"))
-    code = CHILD.format(repo=REPO, tests=HERE, lib=lib)
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
-                         timeout=300)
+    res = run_pins(src.replace(old, new), tmp_path)
     if res.returncode != 0:
-        return  # the mutant crashed or raised outside a pin: caught
+        # the mutant crashed or raised outside a pin (the control, run the same
+        # way, exited 0): caught
+        return
     caught = json.loads(res.stdout.strip().splitlines()[-1])
     assert caught, f"no pin caught mutant {name}"
