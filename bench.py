@@ -6,13 +6,17 @@ which computes what paged_kv_slot_mapping + paged_kv_append do) and the fused
 paged-attention decode of every sequence (paged_attention_decode, split-K
 partitions + merge where configured).
 
-Default workload: the Llama-2-7B-shaped MHA layer (64 sequences, 32 heads,
-head_dim 128, fp16, block size 16, lengths uniform in [128, 2048], physical
-blocks shuffled over a pool 1.25x the need), synthetic seeded inputs.
+Default workload: the long-context layer, the largest that fits one GPU (8
+sequences, lengths uniform in [32768, 131072], 64 q / 8 kv heads, head_dim
+128, bf16, block size 16, 512-token partitions + LSE merge), synthetic seeded
+inputs. The GQA batch-256 and MHA layers, the continuous-batching trace and
+the next rows (copy-on-write, swap, chunked prefill) are measured after it.
 
 Prints one JSON line (rank 0). `value` is whole-job paged-decode GB/s: the
 step's algorithmic bytes (unique KV bytes + q + out + block-table + length
-bytes) over the device-timed step; `--impl reference` times the fp64 CPU
+bytes) over the device-timed step; `roofline` is the decode call alone, timed
+back to back. The line ends with `targets`, the compact per-workload decode
+fractions of the measured HBM peak. `--impl reference` times the fp64 CPU
 oracle instead on a bounded sample of the same workload.
 """
 import argparse
@@ -32,7 +36,7 @@ if REPO not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import materialize, new_pools, preset  # noqa: E402
+from workloads import materialize, new_pools, preset, subset  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s per layer"
 FALLBACK_HBM_GBS = 6800.0
@@ -250,45 +254,95 @@ class Step:
         del fill_seq, fill_pos, fill_slots
         self.launches_per_step = 2 + (1 if partition > 0 else 0)
 
-    def run(self, ev=None):
-        pk, wl = self.pk, self.wl
-        pk.paged_kv_append_tokens(self.t["k_step"], self.t["v_step"], self.bt, self.step_seq,
-                                  self.step_pos, self.kc, self.vc)
-        if ev is not None:
-            ev[0].record()
-        pk.paged_attention_decode(self.t["q"], self.kc, self.vc, self.bt, self.lens, wl.scale,
-                                  self.out, self.partition, self.ws)
-        if ev is not None:
-            ev[1].record()
+    def run(self):
+        self.pk.paged_kv_append_tokens(self.t["k_step"], self.t["v_step"], self.bt, self.step_seq,
+                                       self.step_pos, self.kc, self.vc)
+        self.decode()
 
-
-DECODE_SAMPLE = 8   # the decode call is bracketed by events on every 8th timed step
+    def decode(self):
+        self.pk.paged_attention_decode(self.t["q"], self.kc, self.vc, self.bt, self.lens,
+                                       self.wl.scale, self.out, self.partition, self.ws)
 
 
 def time_steps(step, steps, dist_ctx):
-    """Device time of exactly `steps` steps (max over ranks), plus decode-only
-    time. An event recorded between two launches ends their programmatic
-    dependent overlap, so the decode call is bracketed by events only on every
-    DECODE_SAMPLE-th step (its mean over those steps); the other steps run as
-    a serving loop would."""
-    sampled = range(0, steps, DECODE_SAMPLE)
-    pairs = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for i in sampled}
+    """Device time of exactly `steps` steps between one pair of events (no
+    event between the launches, which would end their programmatic dependent
+    overlap), max over ranks."""
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()
     torch.cuda.synchronize()
     start.record()
-    for i in range(steps):
-        step.run(pairs.get(i))
+    for _ in range(steps):
+        step.run()
     stop.record()
     torch.cuda.synchronize()
     dist_ctx.barrier()
-    total_ms = dist_ctx.max(start.elapsed_time(stop))
-    decode_ms = sum(a.elapsed_time(b) for a, b in pairs.values()) / len(pairs)
-    return total_ms, decode_ms
+    return dist_ctx.max(start.elapsed_time(stop))
 
 
-def time_e2e(step, steps):
+def time_decode_calls(call, reps, repeats=5):
+    """`reps` decode calls back to back between one pair of events, `repeats`
+    times; returns the mean ms per call of each repeat. Back to back, a call's
+    set-up overlaps the previous call's tail, as along a serving step."""
+    out = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / reps)
+    return out
+
+
+def time_each_call(call, reps):
+    """Median ms of `reps` decode calls, each bracketed by its own events."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in pairs:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in pairs)
+
+
+def spread(xs):
+    """min / median / max of repeated measurements and the max-min range in % of the median."""
+    med = statistics.median(xs)
+    return {"n": len(xs), "min": min(xs), "median": med, "max": max(xs),
+            "range_pct": 100.0 * (max(xs) - min(xs)) / med if med else None}
+
+
+E2E_INPUTS = ("q", "k", "v", "bt", "lens", "seq", "pos")
+
+
+def e2e_sources(step, q=None):
+    """The step's seven input arrays (q replaced by `q` when given)."""
+    t = step.t
+    return dict(zip(E2E_INPUTS, (t["q"] if q is None else q, t["k_step"], t["v_step"], step.bt,
+                                 step.lens, step.step_seq, step.step_pos)))
+
+
+def pack_host_inputs(src):
+    """One pinned host buffer holding every input array of a step, each on a
+    256-byte boundary; returns (buffer, offsets)."""
+    offs, size = {}, 0
+    for n in E2E_INPUTS:
+        offs[n] = size
+        size += (src[n].numel() * src[n].element_size() + 255) // 256 * 256
+    host = torch.empty(size, dtype=torch.uint8).pin_memory()
+    for n in E2E_INPUTS:
+        x = src[n].contiguous().cpu()
+        nb = x.numel() * x.element_size()
+        host[offs[n]:offs[n] + nb].copy_(x.view(-1).view(torch.uint8))
+    return host, offs
+
+
+def time_e2e(step, steps, host_inputs=None, outputs=None):
     """Same step through the public API with host inputs: every step copies its
     inputs from pinned host memory to the device and reads its output back.
 
@@ -296,25 +350,23 @@ def time_e2e(step, steps):
     copied with one transfer into one of two device staging buffers; the copy
     of step i+1 and the read-back of step i run on a copy stream while step i
     computes (double-buffered inputs and outputs), as a serving loop would
-    overlap them."""
-    wl, t = step.wl, step.t
-    names = ("q", "k", "v", "bt", "lens", "seq", "pos")
-    src = dict(zip(names, (t["q"], t["k_step"], t["v_step"], step.bt, step.lens,
-                           step.step_seq, step.step_pos)))
+    overlap them. Step i takes host_inputs[i % len(host_inputs)] (by default
+    one buffer of the step's own inputs) and, when `outputs` (a list of pinned
+    host tensors, one per step) is given, reads back into outputs[i] instead
+    of the two alternating host buffers."""
+    wl = step.wl
+    src = e2e_sources(step)
+    if host_inputs is None:
+        host_inputs = [pack_host_inputs(src)[0]]
     offs, size = {}, 0
-    for n in names:
+    for n in E2E_INPUTS:
         offs[n] = size
         size += (src[n].numel() * src[n].element_size() + 255) // 256 * 256
-    host = torch.empty(size, dtype=torch.uint8).pin_memory()
-    for n in names:
-        x = src[n].contiguous().cpu()
-        nb = x.numel() * x.element_size()
-        host[offs[n]:offs[n] + nb].copy_(x.view(-1).view(torch.uint8))
     dev = [torch.empty(size, dtype=torch.uint8, device=step.out.device) for _ in range(2)]
 
     def views(buf):
         v = {}
-        for n in names:
+        for n in E2E_INPUTS:
             x = src[n]
             nb = x.numel() * x.element_size()
             v[n] = buf[offs[n]:offs[n] + nb].view(x.dtype).view(x.shape)
@@ -323,7 +375,7 @@ def time_e2e(step, steps):
     vs = [views(d) for d in dev]
     outs = [step.out, torch.empty_like(step.out)]
     out_host = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(src[n].numel() * src[n].element_size() for n in names)
+    h2d = sum(src[n].numel() * src[n].element_size() for n in E2E_INPUTS)
     d2h = out_host[0].numel() * out_host[0].element_size()
     pk = step.pk
     compute = torch.cuda.current_stream()
@@ -341,7 +393,7 @@ def time_e2e(step, steps):
     e0.record(compute)
     copy.wait_stream(compute)
     with torch.cuda.stream(copy):
-        dev[0].copy_(host, non_blocking=True)
+        dev[0].copy_(host_inputs[0], non_blocking=True)
         ready[0].record(copy)
     for i in range(steps):
         b = i % 2
@@ -352,10 +404,11 @@ def time_e2e(step, steps):
             if i + 1 < steps:
                 if i >= 1:
                     copy.wait_event(done[1 - b])       # step i-1 no longer reads that buffer
-                dev[1 - b].copy_(host, non_blocking=True)
+                dev[1 - b].copy_(host_inputs[(i + 1) % len(host_inputs)], non_blocking=True)
                 ready[1 - b].record(copy)
             copy.wait_event(done[b])
-            out_host[b].copy_(outs[b], non_blocking=True)
+            dst = outputs[i] if outputs is not None else out_host[b]
+            dst.copy_(outs[b], non_blocking=True)
     compute.wait_stream(copy)
     e1.record(compute)
     torch.cuda.synchronize()
@@ -383,6 +436,23 @@ def oracle_pools(orc, wl, tensors):
         sm = orc.slot_mapping(wl.block_tables, seq, pos, wl.block_size)
         orc.append(host_storage(k), host_storage(v), sm, kc, vc)
     return kc, vc
+
+
+# sequences of each workload the CPU oracle is timed on (a bounded sample: its
+# pools and inputs are built on the host for these sequences only)
+ORACLE_SAMPLE_SEQS = {"tiny": None, "mha7b": None, "gqa8b_prefix": list(range(32)),
+                      "longctx_splitk": [0, 1]}
+
+
+def oracle_sample(orc, name):
+    """The workload (or its sampled sequences) with host q and oracle-filled pools."""
+    wl = preset(name)
+    seqs = ORACLE_SAMPLE_SEQS.get(name)
+    if seqs is not None:
+        wl = subset(wl, seqs)
+    tensors = materialize(wl, "cpu")
+    kc, vc = oracle_pools(orc, wl, tensors)
+    return wl, host_storage(tensors["q"]), kc, vc
 
 
 def oracle_rate(orc, wl, q, kc, vc, budget_s, start_unit=0, threads=None):
@@ -467,10 +537,7 @@ def run_reference(args, ctx):
         return None
     import oracle
     orc = oracle.get()
-    wl = preset(args.config)
-    tensors = materialize(wl, "cpu")
-    kc, vc = oracle_pools(orc, wl, tensors)
-    q = host_storage(tensors["q"])
+    wl, q, kc, vc = oracle_sample(orc, args.config)
     per_step = max(0.05, min(20.0, args.reference_budget / max(1, args.steps + args.warmup)))
     for w in range(args.warmup):
         oracle_rate(orc, wl, q, kc, vc, per_step, start_unit=w)
@@ -481,7 +548,7 @@ def run_reference(args, ctx):
         total_s += s
         total_units += n
     value = total_bytes / total_s / 1e9
-    sample = (f"{total_units} (sequence, kv head) units over {args.steps} steps, "
+    sample = (f"{total_units} (sequence, kv head) units of {wl.name} over {args.steps} steps, "
               f"~{per_step:.2f} s of oracle work per step, of {wl.num_seqs * wl.n_kv_heads} units")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -495,6 +562,22 @@ def run_reference(args, ctx):
     }
 
 
+def decode_figures(wl, call, reps, repeats=5):
+    """Decode-call figures of one workload: the median of `reps` calls each
+    between its own events, and `repeats` runs of `reps` calls back to back."""
+    algo, logical, kv_unique = decode_bytes(wl)
+    peak, _ = measured_peak()
+    per_call = time_each_call(call, reps)
+    b2b = time_decode_calls(call, reps, repeats)
+    med = statistics.median(b2b)
+    return {"algorithmic_bytes": algo, "kv_unique_bytes": kv_unique,
+            "decode_ms_back_to_back": med, "back_to_back_ms_spread": spread(b2b),
+            "achieved_gbs": algo / med / 1e6, "frac": algo / med / 1e6 / peak,
+            "logical_gbs": logical / med / 1e6,
+            "decode_ms_per_call": per_call, "frac_per_call": algo / per_call / 1e6 / peak,
+            "reps": reps}
+
+
 def measure_gate(name, args, device):
     """Decode-only roofline fraction of one workload (for the stated targets)."""
     import paged_kv_cache_233_gb300 as pk
@@ -503,105 +586,22 @@ def measure_gate(name, args, device):
     step = Step(wl, device, P)
     for _ in range(args.warmup):
         step.run()
-    reps = args.gate_reps
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(reps)]
-
-    def call():
-        pk.paged_attention_decode(step.t["q"], step.kc, step.vc, step.bt, step.lens, wl.scale,
-                                  step.out, P, step.ws)
-    torch.cuda.synchronize()
-    for i in range(reps):
-        pairs[i][0].record()
-        call()
-        pairs[i][1].record()
-    torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in pairs]
-    # the same calls back to back between one pair of events: a call's set-up
-    # then overlaps the previous call's tail (programmatic dependent launch)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        call()
-    e1.record()
-    torch.cuda.synchronize()
-    sustained = e0.elapsed_time(e1) / reps
-    algo, logical, kv_unique = decode_bytes(wl)
-    peak, _ = measured_peak()
-    med = statistics.median(ms)
-    res = {"decode_ms_median": med, "achieved_gbs": algo / med / 1e6,
-           "frac": algo / med / 1e6 / peak, "logical_gbs": logical / med / 1e6,
-           "decode_ms_back_to_back": sustained, "frac_back_to_back": algo / sustained / 1e6 / peak,
-           "algorithmic_bytes": algo, "kv_unique_bytes": kv_unique, "partition_tokens": P,
-           "decode_path": pk.last_decode_path(), "reps": reps}
+    res = decode_figures(wl, step.decode, args.gate_reps)
+    res.update(partition_tokens=P, decode_path=pk.last_decode_path())
     del step
     torch.cuda.empty_cache()
     return res
 
 
-def measure_trace(block_size, device, partition=None, passes=5):
-    """The continuous-batching workload (64 requests, up to 64 slots, 65,536-slot
-    pool, LIFO recompute preemption) through the hot path, step by step. Step
-    inputs are gathered on the device beforehand and one workspace serves every
-    step, as a serving loop keeps it. After one untimed pass over the whole
-    trace, each step's calls are timed with CUDA events over `passes` passes;
-    the figures are those of the pass of median total time. The trace's
-    contexts are short (<= 640 tokens) and its batches small (<= 64), so a
-    step's decode runs the balanced split: the step's 16-token tiles cut into
-    equal shares, one per CTA (measured on GB300, one pass, a workspace per
-    step and separate slot mapping and append calls: 1926 / 2026 / 2052 GB/s at
-    B = 8 / 16 / 32, against 1097 / 1821 / 1816 unsplit and 1623 / 2072 / 2045
-    with 256-token partitions)."""
-    import paged_kv_cache_233_gb300 as pk
-    if partition is None:
-        partition = pk.PARTITION_BALANCED
+TRACE_SLOTS = (8, 16, 32, 64, 128, 256)
+
+
+def trace_bytes(tw, plans):
+    """(decode algorithmic bytes, append bytes, sequence-decodes) of the trace's steps."""
     from types import SimpleNamespace
-    from workloads import cb_trace, step_inputs, trace_tensors
-    tw = cb_trace(block_size=block_size, slots=64)
-    tensors = trace_tensors(tw, device)
-    shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
-    kc = torch.zeros(shape, dtype=tw.torch_dtype, device=device)
-    vc = torch.zeros_like(kc)
-    steps = []
-    ws_bytes = 0
-    for plan in tw.plans:
-        x = step_inputs(tw, plan, tensors, device)
-        x["out"] = torch.empty_like(x["q"])
-        q, bt = x["q"], x["block_tables"]
-        ws_bytes = max(ws_bytes, pk.paged_attention_workspace_bytes(
-            q.shape[0], q.shape[1], q.shape[2], bt.shape[1], tw.block_size, partition))
-        steps.append((plan, x))
-    # one workspace for every step, as a serving loop keeps it
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None
-
-    def one_pass(ev=None):
-        for i, (plan, x) in enumerate(steps):
-            if ev is not None:
-                ev[i][0].record()
-            pk.paged_kv_append_tokens(x["k"], x["v"], x["block_tables"], x["token_row"],
-                                      x["token_pos"], kc, vc)
-            pk.paged_attention_decode(x["q"], kc, vc, x["block_tables"], x["context_lens"],
-                                      tw.scale, x["out"], partition, ws)
-            if ev is not None:
-                ev[i][1].record()
-
-    one_pass()
-    torch.cuda.synchronize()
-    runs = []
-    for _ in range(passes):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in steps]
-        one_pass(ev)
-        torch.cuda.synchronize()
-        runs.append([a.elapsed_time(b) for a, b in ev])
-    # the pass of median total time
-    ms = sorted(runs, key=sum)[len(runs) // 2]
-    total_ms = sum(ms)
-    dec_bytes = 0
-    app_bytes = 0
-    decodes = 0
+    dec_bytes = app_bytes = decodes = 0
     row = tw.n_kv_heads * tw.head_dim * tw.element_bytes
-    for plan, _ in steps:
+    for plan in plans:
         view = SimpleNamespace(block_size=tw.block_size, element_bytes=tw.element_bytes,
                                n_kv_heads=tw.n_kv_heads, head_dim=tw.head_dim,
                                n_q_heads=tw.n_q_heads, num_seqs=len(plan.rids),
@@ -609,48 +609,163 @@ def measure_trace(block_size, device, partition=None, passes=5):
         dec_bytes += decode_bytes(view)[0]
         app_bytes += 4 * len(plan.token_row) * row + 8 * len(plan.token_row)
         decodes += len(plan.rids)
-    return {"steps": len(steps), "preemptions": tw.preemptions,
-            "max_running": max(len(p.rids) for p, _ in steps),
-            "total_ms": total_ms, "decode_gbs": dec_bytes / total_ms / 1e6,
-            "seq_decodes_per_s": decodes / (total_ms * 1e-3),
-            "append_gbs_in_step": app_bytes / total_ms / 1e6,
-            "median_step_us": 1e3 * statistics.median(ms), "partition_tokens": partition,
-            "timed_passes": passes, "pass_ms_range": [min(map(sum, runs)), max(map(sum, runs))]}
+    return dec_bytes, app_bytes, decodes
 
 
-def measure_shared_prefix(device, reps=200, partition=320):
+class TraceRun:
+    """The continuous-batching workload's steps, ready on the device: per step
+    the appended tokens' K/V rows and (row, position) pairs, the block tables,
+    lengths and queries, and an output buffer; one workspace for every step, as
+    a serving loop keeps it. run_pass() issues every step's
+    paged_kv_append_tokens and paged_attention_decode on the current stream."""
+
+    def __init__(self, tw, device, partition, pools=None):
+        import paged_kv_cache_233_gb300 as pk
+        from workloads import step_inputs, trace_tensors
+        self.pk, self.tw, self.partition = pk, tw, partition
+        tensors = trace_tensors(tw, device)
+        shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
+        if pools is None:
+            pools = (torch.zeros(shape, dtype=tw.torch_dtype, device=device),
+                     torch.zeros(shape, dtype=tw.torch_dtype, device=device))
+        self.kc, self.vc = pools
+        self.steps = []
+        ws_bytes = 0
+        for plan in tw.plans:
+            x = step_inputs(tw, plan, tensors, device)
+            x["out"] = torch.empty_like(x["q"])
+            q, bt = x["q"], x["block_tables"]
+            ws_bytes = max(ws_bytes, pk.paged_attention_workspace_bytes(
+                q.shape[0], q.shape[1], q.shape[2], bt.shape[1], tw.block_size, partition))
+            self.steps.append((plan, x))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None
+
+    def run_pass(self, ev=None):
+        pk, tw = self.pk, self.tw
+        for i, (plan, x) in enumerate(self.steps):
+            if ev is not None:
+                ev[i][0].record()
+            pk.paged_kv_append_tokens(x["k"], x["v"], x["block_tables"], x["token_row"],
+                                      x["token_pos"], self.kc, self.vc)
+            pk.paged_attention_decode(x["q"], self.kc, self.vc, x["block_tables"],
+                                      x["context_lens"], tw.scale, x["out"], self.partition,
+                                      self.ws)
+            if ev is not None:
+                ev[i][1].record()
+
+    def capture(self):
+        """The whole pass captured in one CUDA graph (run one pass eagerly first,
+        so that every kernel's launch attributes are already set)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.run_pass()
+        return g
+
+
+def measure_trace(block_size, device, slots=64, partition=None, passes=5):
+    """The continuous-batching workload (64 requests, up to `slots` running,
+    65,536-slot pool, LIFO recompute preemption) through the hot path, step by
+    step: each step one paged_kv_append_tokens and one paged_attention_decode
+    (TraceRun).
+
+    Two ways of issuing the same launches, after one untimed pass:
+      graph  the whole pass captured once in a CUDA graph and replayed, so the
+             device runs the steps back to back, as a serving loop that
+             captures its decode step does; `passes` replays, each between
+             its own events (the headline figures: the device's time);
+      eager  the steps issued one by one from Python through the binding,
+             each step between its own events (`passes` passes; the pass of
+             median total time), bounded by the host's issue rate when the
+             device is faster than the host.
+    The trace's contexts are short (<= 640 tokens) and its batches small
+    (<= 32 running), so a step's decode runs the balanced split."""
+    import paged_kv_cache_233_gb300 as pk
+    if partition is None:
+        partition = pk.PARTITION_BALANCED
+    from workloads import cb_trace
+    tw = cb_trace(block_size=block_size, slots=slots)
+    tr = TraceRun(tw, device, partition)
+    tr.run_pass()
+    torch.cuda.synchronize()
+    plans = [p for p, _ in tr.steps]
+    dec_bytes, app_bytes, decodes = trace_bytes(tw, plans)
+    res = {"slots": slots, "steps": len(plans), "preemptions": tw.preemptions,
+           "max_running": max(len(p.rids) for p in plans), "partition_tokens": partition,
+           "decode_bytes": dec_bytes}
+    graph_ms = None
+    try:
+        g = tr.capture()
+        g.replay()
+        torch.cuda.synchronize()
+        runs = []
+        for _ in range(passes):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            runs.append(e0.elapsed_time(e1))
+        graph_ms = statistics.median(runs)
+        res.update({"total_ms": graph_ms, "decode_gbs": dec_bytes / graph_ms / 1e6,
+                    "seq_decodes_per_s": decodes / (graph_ms * 1e-3),
+                    "append_gbs_in_step": app_bytes / graph_ms / 1e6,
+                    "mean_step_us": 1e3 * graph_ms / len(plans), "issued": "one CUDA graph",
+                    "pass_ms_spread": spread(runs)})
+        del g
+    except RuntimeError as exc:   # report, then time eagerly only
+        res["graph_error"] = str(exc)[:200]
+    runs = []
+    for _ in range(passes):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in plans]
+        tr.run_pass(ev)
+        torch.cuda.synchronize()
+        runs.append([a.elapsed_time(b) for a, b in ev])
+    ms = sorted(runs, key=sum)[len(runs) // 2]
+    eager_ms = sum(ms)
+    res["eager"] = {"total_ms": eager_ms, "decode_gbs": dec_bytes / eager_ms / 1e6,
+                    "median_step_us": 1e3 * statistics.median(ms),
+                    "pass_ms_range": [min(map(sum, runs)), max(map(sum, runs))]}
+    if graph_ms is None:
+        res.update({"total_ms": eager_ms, "decode_gbs": dec_bytes / eager_ms / 1e6,
+                    "seq_decodes_per_s": decodes / (eager_ms * 1e-3),
+                    "append_gbs_in_step": app_bytes / eager_ms / 1e6, "issued": "eager"})
+    assert pk.device_errors() == 0
+    del tr
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_shared_prefix(device, reps=200, partitions=(256, 320, 512)):
     """The GQA prefix workload through paged_attention_decode_shared_prefix
-    (each 512-token prefix read once per 2-member chunk instead of once per
-    member), against the same roofline numerator as the plain decode."""
+    (each whole prefix partition read once per chunk of members instead of
+    once per member), against the same roofline numerator as the plain decode,
+    with the plain decode at the same partition size beside it."""
     import paged_kv_cache_233_gb300 as pk
     wl = preset("gqa8b_prefix")
-    step = Step(wl, device, partition)
     seq_group = np.full(wl.num_seqs, -1, np.int32)
     for gi, grp in enumerate(wl.groups):
         seq_group[grp] = gi
-    sg = torch.from_numpy(seq_group).to(device)
-    gp = torch.full((len(wl.groups),), wl.prefix_blocks * wl.block_size, dtype=torch.int32,
-                    device=device)
+    res = {}
+    for P in partitions:
+        step = Step(wl, device, P)
+        sg = torch.from_numpy(seq_group).to(device)
+        gp = torch.full((len(wl.groups),), wl.prefix_blocks * wl.block_size, dtype=torch.int32,
+                        device=device)
 
-    def call():
-        pk.paged_attention_decode_shared_prefix(step.t["q"], step.kc, step.vc, step.bt, step.lens,
-                                                sg, gp, wl.scale, step.out, partition, step.ws)
-    for _ in range(5):
-        call()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    torch.cuda.synchronize()
-    for a, b in ev:
-        a.record()
-        call()
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-    algo, logical, _ = decode_bytes(wl)
-    peak, _ = measured_peak()
-    del step
-    torch.cuda.empty_cache()
-    return {"decode_ms_median": ms, "achieved_gbs": algo / ms / 1e6, "frac": algo / ms / 1e6 / peak,
-            "logical_gbs": logical / ms / 1e6, "partition_tokens": partition, "reps": reps}
+        def call():
+            pk.paged_attention_decode_shared_prefix(step.t["q"], step.kc, step.vc, step.bt,
+                                                    step.lens, sg, gp, wl.scale, step.out, P,
+                                                    step.ws)
+        for _ in range(5):
+            call()
+            step.decode()
+        shared = decode_figures(wl, call, reps, repeats=3)
+        plain = decode_figures(wl, step.decode, reps, repeats=3)
+        res[f"P{P}"] = {"shared_prefix_entry": shared, "plain_decode": plain}
+        del step
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_cow(device, samples=4, reps=50):
@@ -837,6 +952,14 @@ def measure_prefill(device, reps=50, chunked=True):
     return res
 
 
+def compact(fig):
+    """The few numbers of a decode figure that the line's tail repeats."""
+    return {"frac": round(fig["frac"], 4), "gbs": round(fig["achieved_gbs"], 1),
+            "ms": round(fig["decode_ms_back_to_back"], 5),
+            "frac_per_call": round(fig["frac_per_call"], 4),
+            "spread_pct": round(fig["back_to_back_ms_spread"]["range_pct"], 2)}
+
+
 def run_ours(args, ctx):
     import paged_kv_cache_233_gb300 as pk
     from paged_kv_cache_233_gb300 import build as pk_build
@@ -852,6 +975,8 @@ def run_ours(args, ctx):
     if args.ctas is not None:
         pk.set_option(pk.OPT_CTAS_PER_SM, args.ctas)
     wl = workload_for(args.config, ctx.rank)
+    if args.seqs is not None:
+        wl = subset(wl, range(min(args.seqs, wl.num_seqs)))
     P = PARTITION[args.config] if args.partition is None else args.partition
     step = Step(wl, device, P)
     for _ in range(args.warmup):
@@ -860,7 +985,12 @@ def run_ours(args, ctx):
     if pk.device_errors():
         raise RuntimeError("device error flags set during warm-up")
     with ClockSampler(torch.cuda.current_device()) as clk:
-        total_ms, decode_ms = time_steps(step, args.steps, ctx)
+        total_ms = time_steps(step, args.steps, ctx)
+        # the same timed loop again, for the spread of the step time
+        repeats = [total_ms / args.steps] + [time_steps(step, args.steps, ctx) / args.steps
+                                             for _ in range(args.repeats - 1)]
+        # the decode call alone, back to back (the roofline's kernel)
+        dec = decode_figures(wl, step.decode, args.gate_reps, args.repeats)
     clocks = clk.summary()
     ms_per_step = total_ms / args.steps
     algo, logical, kv_unique = decode_bytes(wl)
@@ -871,6 +1001,7 @@ def run_ours(args, ctx):
     e2e_ms, h2d, d2h = time_e2e(step, e2e_steps)
     e2e_ms = ctx.max(e2e_ms)
     peak, peak_kind = measured_peak()
+    decode_ms = dec["decode_ms_back_to_back"]
     achieved = algo / decode_ms / 1e6
     result = None
     if ctx.rank == 0:
@@ -879,10 +1010,12 @@ def run_ours(args, ctx):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic",
-            "config": {"workload": DESCRIPTION[args.config], "partition_tokens": P,
+            "config": {"workload": DESCRIPTION[args.config] if args.seqs is None else wl.name,
+                       "partition_tokens": P,
                        "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
                        "l2": f"inputs larger than L2: KV pool {2 * wl.num_blocks * wl.block_size * wl.row_bytes / 1e9:.2f} GB",
                        "parallelism": f"replicas x{ctx.world} (one workload per GPU)"},
+            "step_ms_spread": spread(repeats),
             "seq_decodes_per_s_per_layer": seq_decodes,
             "kv_logical_gbs": ctx.sum(logical) / ms_per_step / 1e6,
             "append_bulk_gbs": append_bytes(wl, step.fill_tokens) / step.fill_ms / 1e6,
@@ -892,41 +1025,63 @@ def run_ours(args, ctx):
                     "ms_per_step": e2e_ms, "steps": e2e_steps},
             "gpu_launches": step.launches_per_step * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(args.config, P),
-                         "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy)",
-                         "kernel": "paged_decode_kernel + lse_merge_kernel (one decode call)",
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic(args.config, P) if args.seqs is None else None,
+                         "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy), burst",
+                         "kernel": "paged_decode_kernel + its LSE merge (one decode call)",
                          "decode_ms": decode_ms, "algorithmic_bytes_per_launch": algo,
-                         "decode_timed_on": f"every {DECODE_SAMPLE}th timed step"},
+                         "decode_timed_on": f"{args.gate_reps} decode calls back to back, "
+                                            f"median of {args.repeats} repeats",
+                         "decode_ms_spread": dec["back_to_back_ms_spread"],
+                         "decode_ms_per_call": dec["decode_ms_per_call"]},
         }
     del step
     torch.cuda.empty_cache()
-    if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
-        result["gates"] = {name: measure_gate(name, args, device)
-                           for name in ("gqa8b_prefix", "longctx_splitk")}
-        result["gates"]["gqa8b_prefix_shared_prefix_entry"] = measure_shared_prefix(device)
+    targets = {}
+    if ctx.rank == 0 and args.seqs is None:
+        targets[args.config] = compact(dec)
+    if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
+        import oracle
+        orc = oracle.get()
+        wl0, q0, kc, vc = oracle_sample(orc, args.config)
+        b, s, n, threads = oracle_rate(orc, wl0, q0, kc, vc, args.cpu_budget)
+        b1, s1, n1, _ = oracle_rate(orc, wl0, q0, kc, vc, max(1.0, args.cpu_budget / 4),
+                                    threads=1)
+        result["cpu_baseline"] = {
+            "value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} (sequence, kv head) units taken in order, cycling over the "
+                      f"{wl0.num_seqs * wl0.n_kv_heads} units of {wl0.name}; {s:.1f} s of "
+                      f"fp64 oracle decode on {threads} threads",
+            "single_core": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"{n1} units, {s1:.1f} s on one thread"}}
+        del kc, vc
     if ctx.rank == 0 and not args.no_trace and ctx.world == 1:
-        result["trace"] = {f"B{b}": measure_trace(b, device) for b in (8, 16, 32)}
+        result["trace"] = {f"B{b}_slots{n}": measure_trace(b, device, slots=n)
+                           for b in (8, 16, 32) for n in TRACE_SLOTS}
         torch.cuda.empty_cache()
         result["cow_copy"] = measure_cow(device)
         result["swap"] = measure_swap(device)
         result["prefill"] = measure_prefill(device)
-    if ctx.rank == 0 and not args.no_cpu_baseline and ctx.world == 1:
-        import oracle
-        orc = oracle.get()
-        wl0 = preset(args.config)
-        tensors = materialize(wl0, "cpu")
-        kc, vc = oracle_pools(orc, wl0, tensors)
-        b, s, n, threads = oracle_rate(orc, wl0, host_storage(tensors["q"]), kc, vc,
-                                       args.cpu_budget)
-        b1, s1, n1, _ = oracle_rate(orc, wl0, host_storage(tensors["q"]), kc, vc,
-                                    max(1.0, args.cpu_budget / 4), threads=1)
-        result["cpu_baseline"] = {
-            "value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} (sequence, kv head) units taken in order, cycling over the "
-                      f"{wl0.num_seqs * wl0.n_kv_heads} units of the same workload; {s:.1f} s of "
-                      f"fp64 oracle decode on {threads} threads",
-            "single_core": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1,
-                            "sample": f"{n1} units, {s1:.1f} s on one thread"}}
+    if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
+        gates = {name: measure_gate(name, args, device)
+                 for name in ("gqa8b_prefix", "longctx_splitk", "mha7b") if name != args.config}
+        gates["gqa8b_prefix_shared_prefix_entry"] = measure_shared_prefix(device, args.gate_reps)
+        result["gates"] = gates
+        for name in ("gqa8b_prefix", "longctx_splitk", "mha7b"):
+            if name in gates:
+                targets[name] = compact(gates[name])
+        sp = gates["gqa8b_prefix_shared_prefix_entry"]
+        targets["gqa8b_prefix_shared_prefix_entry"] = {
+            k: {"shared": round(v["shared_prefix_entry"]["frac"], 4),
+                "plain": round(v["plain_decode"]["frac"], 4)} for k, v in sp.items()}
+    if ctx.rank == 0 and "trace" in result:
+        targets["trace_decode_gbs"] = {k: round(v["decode_gbs"], 1)
+                                       for k, v in result["trace"].items()}
+    if ctx.rank == 0 and targets:
+        # last key of the line: the decode fractions of the measured HBM peak that
+        # the stated targets are about (80% GQA batch 256, 70% long context)
+        targets["peak_gbs"] = peak
+        result["targets"] = targets
     return result
 
 
@@ -936,7 +1091,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="mha7b", choices=sorted(DESCRIPTION))
+    ap.add_argument("--config", default="longctx_splitk", choices=sorted(DESCRIPTION))
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="only the first N sequences of the workload (a smaller case to profile)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="repeats of the timed loops (their spread is reported)")
     ap.add_argument("--partition", type=int, default=None)
     ap.add_argument("--path", type=int, default=None, help="1 CUDA-core, 2 tensor-core decode")
     ap.add_argument("--ctas", type=int, default=None, help="persistent decode CTAs per SM")
@@ -952,6 +1111,8 @@ def main(argv=None):
     ap.add_argument("--prefill-reps", type=int, default=50)
     ap.add_argument("--trace-only", type=int, default=None, metavar="BLOCK_SIZE",
                     help="only the continuous-batching trace at this block size (for profiling it)")
+    ap.add_argument("--trace-slots", type=int, nargs="+", default=[64],
+                    help="slot counts of --trace-only")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -962,7 +1123,8 @@ def main(argv=None):
         pk.load()
         torch.cuda.set_device(0)
         b = args.trace_only
-        print(json.dumps({"trace": {f"B{b}": measure_trace(b, torch.device("cuda", 0))}}), flush=True)
+        print(json.dumps({"trace": {f"B{b}_slots{n}": measure_trace(b, torch.device("cuda", 0), slots=n)
+                                    for n in args.trace_slots}}), flush=True)
         return
     if args.prefill_only:
         import paged_kv_cache_233_gb300 as pk

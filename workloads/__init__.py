@@ -7,9 +7,9 @@ host-side block allocator and scheduler that decide which physical blocks a
 sequence owns. It never computes a slot, a gather or an attention value.
 """
 from .synth import (PagedWorkload, TORCH_DTYPES, chunked_prefill, make_workload, materialize,
-                    new_pools, prefill_mha7b, prefill_queries, preset, PRESETS)
+                    new_pools, prefill_mha7b, prefill_queries, preset, PRESETS, subset)
 from .trace import TraceWorkload, cb_trace, step_inputs, trace_tensors
 
 __all__ = ["PagedWorkload", "TORCH_DTYPES", "make_workload", "materialize", "new_pools",
            "preset", "PRESETS", "TraceWorkload", "cb_trace", "step_inputs", "trace_tensors",
-           "chunked_prefill", "prefill_mha7b", "prefill_queries"]
+           "chunked_prefill", "prefill_mha7b", "prefill_queries", "subset"]

@@ -54,7 +54,8 @@ class DoubleFree(RuntimeError):
 class BlockAllocator:
     def __init__(self, n_blocks, block_size):
         if n_blocks < 1 or block_size < 1:
-            raise ValueError("n_blocks and block_size must both be positive")
+            raise ValueError(f"a pool needs at least one block of at least one token "
+                             f"(got {n_blocks} blocks of {block_size})")
         self.n_blocks = int(n_blocks)
         self.block_size = int(block_size)
         self._free = deque(range(self.n_blocks))

@@ -229,6 +229,42 @@ def prefill_queries(wl, query_start, device="cpu"):
                        dtype=torch.float32).to(wl.torch_dtype)
 
 
+def subset(wl, seqs):
+    """The same workload restricted to sequences `seqs` (renumbered 0..k-1):
+    their lengths, block-table rows and tokens, in the same pool. A shared
+    prefix is written by the first kept member of its group."""
+    seqs = [int(s) for s in seqs]
+    keep = {s: i for i, s in enumerate(seqs)}
+    prefix_tokens = wl.prefix_blocks * wl.block_size
+    writer = {}
+    groups = []
+    for grp in wl.groups:
+        kept = [s for s in grp if s in keep]
+        for s in kept:
+            writer[s] = kept[0]
+        if len(kept) > 1:
+            groups.append([keep[s] for s in kept])
+    fill_seq, fill_pos = [], []
+    for s in seqs:
+        L = int(wl.context_lens[s])
+        start = prefix_tokens if writer.get(s, s) != s else 0
+        fill_seq.append(np.full(max(L - 1 - start, 0), keep[s], dtype=np.int32))
+        fill_pos.append(np.arange(start, max(L - 1, start), dtype=np.int32))
+    lens = wl.context_lens[seqs].astype(np.int32)
+    step_mask = lens > 0
+    return PagedWorkload(
+        name=f"{wl.name}[{len(seqs)} of {wl.num_seqs} seqs]", dtype=wl.dtype, num_seqs=len(seqs),
+        n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
+        block_size=wl.block_size, num_blocks=wl.num_blocks, context_lens=lens,
+        block_tables=wl.block_tables[seqs].copy(),
+        fill_seq=np.concatenate(fill_seq) if fill_seq else np.zeros(0, np.int32),
+        fill_pos=np.concatenate(fill_pos) if fill_pos else np.zeros(0, np.int32),
+        step_seq=np.nonzero(step_mask)[0].astype(np.int32),
+        step_pos=(lens[step_mask] - 1).astype(np.int32), seed=wl.seed, scale=wl.scale,
+        partition_tokens=wl.partition_tokens, groups=groups,
+        prefix_blocks=wl.prefix_blocks if groups else 0)
+
+
 PRESETS = {"tiny": tiny, "mha7b": mha7b, "gqa8b_prefix": gqa8b_prefix,
            "longctx_splitk": longctx_splitk}
 
