@@ -588,6 +588,16 @@ def measure_gate(name, args, device):
         step.run()
     res = decode_figures(wl, step.decode, args.gate_reps)
     res.update(partition_tokens=P, decode_path=pk.last_decode_path())
+    # the same calls with the separate merge kernel instead of the merge inside
+    # the decode (same box, same buffers): the A/B of that design choice
+    pk.set_option(pk.OPT_FUSED_MERGE, 1)
+    try:
+        alt = time_decode_calls(step.decode, args.gate_reps, 3)
+    finally:
+        pk.set_option(pk.OPT_FUSED_MERGE, 0)
+    algo = res["algorithmic_bytes"]
+    res["merge_kernel_instead"] = {"decode_ms_back_to_back": statistics.median(alt),
+                                   "frac": algo / statistics.median(alt) / 1e6 / measured_peak()[0]}
     del step
     torch.cuda.empty_cache()
     return res
@@ -706,6 +716,25 @@ def measure_trace(block_size, device, slots=64, partition=None, passes=5):
             torch.cuda.synchronize()
             runs.append(e0.elapsed_time(e1))
         graph_ms = statistics.median(runs)
+        del g
+        # the same pass captured with the separate merge kernel (A/B)
+        pk.set_option(pk.OPT_FUSED_MERGE, 1)
+        try:
+            tr.run_pass()
+            g = tr.capture()
+            g.replay()
+            torch.cuda.synchronize()
+            alt = []
+            for _ in range(passes):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                alt.append(e0.elapsed_time(e1))
+        finally:
+            pk.set_option(pk.OPT_FUSED_MERGE, 0)
+        res["merge_kernel_instead_gbs"] = dec_bytes / statistics.median(alt) / 1e6
         res.update({"total_ms": graph_ms, "decode_gbs": dec_bytes / graph_ms / 1e6,
                     "seq_decodes_per_s": decodes / (graph_ms * 1e-3),
                     "append_gbs_in_step": app_bytes / graph_ms / 1e6,

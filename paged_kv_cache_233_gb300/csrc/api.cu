@@ -8,6 +8,7 @@
 #include <limits.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/pagedkv.h"
@@ -58,7 +59,19 @@ int g_opt_ctas_per_sm = 0;
 int g_opt_mma_min_group = 4;
 int g_opt_stages = 0;
 int g_opt_prefill_path = 0;
+int g_opt_fused_merge = 0;
 int g_last_path = 0;
+std::atomic<unsigned int> g_call_count{0};
+
+// Tag of one decode call on the workspace's arrival counters: successive calls
+// get tags that differ (an odd multiplier makes the map from call count to tag
+// a bijection, and spreads the tags over the 32-bit range so that a word left
+// by other data is unlikely to carry the current tag); never 0.
+unsigned int next_call_tag() {
+    unsigned int t = 0;
+    while (t == 0) t = (g_call_count.fetch_add(1, std::memory_order_relaxed) + 1u) * 0x9E3779B1u;
+    return t;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -114,10 +127,11 @@ int encoder(EncodeTiledFn *fn) {
 // TMA view of one pool as a 4-D tensor (x: 128-byte column slab elements,
 // token slot, slab, kv head) so that one box holds [heads][slabs][tokens][128 B]
 // in shared memory; strides in bytes: token n_kv_heads*head_dim*eb, slab 128,
-// head head_dim*eb. The box is every slab of `heads` heads x 16 tokens, or for
-// 8-token blocks one slab of one head x 8 tokens. 128-byte swizzle.
+// head head_dim*eb. The box is every slab of `heads` heads x 16 tokens; for
+// 8-token blocks it is every slab of `heads` heads x 8 tokens (one block), or,
+// when `per_slab8` is set, one slab of one head x 8 tokens. 128-byte swizzle.
 int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim, int n_kv_heads,
-                    long long num_slots, int block_size, int heads) {
+                    long long num_slots, int block_size, int heads, bool per_slab8 = false) {
     EncodeTiledFn fn = nullptr;
     int st = encoder(&fn);
     if (st != PAGEDKV_OK) return st;
@@ -131,8 +145,9 @@ int encode_pool_map(CUtensorMap *map, const void *pool, int dtype, int head_dim,
     const cuuint64_t strides[3] = {cuuint64_t(n_kv_heads) * head_dim * eb, 128u,
                                    cuuint64_t(head_dim) * eb};
     const bool whole = block_size >= pkv::kTile;
+    const bool all = whole || !per_slab8;
     const cuuint32_t box[4] = {cuuint32_t(128 / eb), cuuint32_t(whole ? pkv::kTile : block_size),
-                               cuuint32_t(whole ? slabs : 1), cuuint32_t(whole ? heads : 1)};
+                               cuuint32_t(all ? slabs : 1), cuuint32_t(all ? heads : 1)};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -230,6 +245,10 @@ int pagedkv_set_option(int option, int value) {
             if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_prefill_path = value;
             return PAGEDKV_OK;
+        case PAGEDKV_OPT_FUSED_MERGE:
+            if (value < 0 || value > 1) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_fused_merge = value;
+            return PAGEDKV_OK;
         default:
             return PAGEDKV_ERR_INVALID_ARG;
     }
@@ -242,6 +261,7 @@ int pagedkv_get_option(int option) {
         case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
         case PAGEDKV_OPT_STAGES: return g_opt_stages;
         case PAGEDKV_OPT_PREFILL_PATH: return g_opt_prefill_path;
+        case PAGEDKV_OPT_FUSED_MERGE: return g_opt_fused_merge;
         default: return PAGEDKV_ERR_INVALID_ARG;
     }
 }
@@ -468,9 +488,11 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
         if (st != PAGEDKV_OK) return st;
         st = encode_pool_map_slab(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
     } else {
-        st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+        st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1,
+                             true);
         if (st != PAGEDKV_OK) return st;
-        st = encode_pool_map(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1);
+        st = encode_pool_map(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1,
+                             true);
     }
     if (st != PAGEDKV_OK) return st;
     pkv::PrefillParams p{};
@@ -517,7 +539,9 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
     } else {
         return 0;
     }
-    return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
+    // partition states o, m, l, then one arrival counter per (sequence, q head)
+    return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float)) +
+           round256(size_t(num_seqs) * n_q_heads * sizeof(unsigned long long));
 }
 
 static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -572,6 +596,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     const long long max_parts =
         partition_tokens > 0 ? max_parts_for(max_blocks_per_seq, block_size, P) : 1;
     float *ws_o = nullptr, *ws_m = nullptr, *ws_l = nullptr;
+    unsigned long long *ws_ctr = nullptr;
     if (split) {
         const size_t need = paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim,
                                                             max_blocks_per_seq, block_size,
@@ -591,6 +616,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         ws_m = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)));
         ws_l = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)) +
                                          round256(rows * sizeof(float)));
+        ws_ctr = reinterpret_cast<unsigned long long *>(
+            w + round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float)));
     }
     // ---- device
     unsigned int *err = nullptr;
@@ -637,6 +664,16 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.num_groups = prefix ? num_groups : 0;
     // a shared-prefix unit fills the tensor-core tile's 8 columns with (member, q head) pairs
     p.max_members = (prefix && path == pkv::kPathMma) ? 8 / group : 1;
+    // The merge runs inside the decode when every consumer warp owns a whole kv
+    // head and a merging warp has few states to read: the balanced split (a
+    // few shares per (sequence, head group)) or partitions of at most 32 per
+    // row. Rows of many partitions (long contexts) keep the merge kernel, which
+    // spreads them over the whole GPU.
+    const bool fuse = split && !prefix && hpu == 4 && g_opt_fused_merge == 0 &&
+                      (balanced || max_parts <= 32);
+    p.fuse = fuse ? 1 : 0;
+    p.gen = fuse ? next_call_tag() : 0u;
+    p.ctr = ws_ctr;
     a.head_dim = head_dim;
     a.path = path;
     a.gmax = gmax;
@@ -653,7 +690,9 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         default: e = pkv::launch_decode_bf16(a); break;
     }
     if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
-    if (balanced) {
+    if (fuse) {
+        // merged by the decode kernel itself
+    } else if (balanced) {
         e = pkv::launch_piece_merge(dtype, head_dim, ws_o, ws_m, ws_l, context_lens, out, num_seqs,
                                     n_q_heads, n_kv_heads / hpu, hpu * group, a.grid_used,
                                     int(cap), a.stream);

@@ -96,8 +96,6 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
     // a decode or prefill that follows may start its set-up now; it waits for
     // this grid before reading the pools
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // the pools as the kernels before this one left them
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int rows_per_cta = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int c0 = threadIdx.x - sub * tpr;
@@ -105,12 +103,18 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
          t += (long long)gridDim.x * rows_per_cta) {
         const uint4 *ks = k + t * vec_per_row;
         const uint4 *vs = v + t * vec_per_row;
-        // the row's first chunk does not depend on the slot: its loads go out
-        // together with those of the position, the sequence and the table entry
-        uint4 a0 = make_uint4(0u, 0u, 0u, 0u), b0 = a0;
+        // The row's first two chunks do not depend on the slot: their loads go
+        // out together with those of the position, the sequence and the table
+        // entry. All of these are the caller's inputs, which no kernel of this
+        // library writes, so they are read before the grid dependency wait.
+        uint4 a0 = make_uint4(0u, 0u, 0u, 0u), b0 = a0, a1 = a0, b1 = a0;
         if (c0 < vec_per_row) {
             a0 = __ldcs(ks + c0);
             b0 = __ldcs(vs + c0);
+        }
+        if (c0 + tpr < vec_per_row) {
+            a1 = __ldcs(ks + c0 + tpr);
+            b1 = __ldcs(vs + c0 + tpr);
         }
         const int pos = token_pos[t];
         const int seq = token_seq[t];
@@ -130,6 +134,11 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                     slot = (long long)pb * block_size + (pos - j * block_size);
             }
         }
+        // every store after the kernels before this one have completed (the
+        // previous decode may still read a block this append writes, e.g. one
+        // freed and handed to another sequence; the slot output may be what a
+        // previous append reads); a later wait returns at once
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (c0 == 0) {
             if (bit) atomicOr(err, bit);
             if (slot_mapping) slot_mapping[t] = slot;
@@ -141,7 +150,11 @@ append_tokens_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
             kd[c0] = a0;
             vd[c0] = b0;
         }
-        for (int c = c0 + tpr; c < vec_per_row; c += tpr) {
+        if (c0 + tpr < vec_per_row) {
+            kd[c0 + tpr] = a1;
+            vd[c0 + tpr] = b1;
+        }
+        for (int c = c0 + 2 * tpr; c < vec_per_row; c += tpr) {
             const uint4 a = __ldcs(ks + c);
             const uint4 b = __ldcs(vs + c);
             kd[c] = a;

@@ -44,6 +44,9 @@ lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
     using V = typename Vec<E>::type;
     __shared__ float red[kMergeWarps];
     __shared__ float acc_s[kMergeWarps][D];
+    // the next kernel of the stream may start its set-up now: it waits for
+    // this grid before it reads or writes what this grid touches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the lengths are the caller's (no kernel of this library writes them), so
     // they are read while the decode may still run; its partition states only
     // after griddepcontrol.wait
@@ -98,6 +101,9 @@ lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ 
     constexpr int E = D / 32;
     constexpr int kBatch = 8;
     using V = typename Vec<E>::type;
+    // the next kernel of the stream may start its set-up now: it waits for
+    // this grid before it reads or writes what this grid touches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -225,6 +231,9 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
     constexpr int E = D / 32;
     constexpr int kBatch = 8;
     using V = typename Vec<E>::type;
+    // the next kernel of the stream may start its set-up now: it waits for
+    // this grid before it reads or writes what this grid touches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int s = blockIdx.x / groups;
     const int hg = blockIdx.x - s * groups;
     const int warps = blockDim.x >> 5;
