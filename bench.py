@@ -263,6 +263,24 @@ class Step:
         self.pk.paged_attention_decode(self.t["q"], self.kc, self.vc, self.bt, self.lens,
                                        self.wl.scale, self.out, self.partition, self.ws)
 
+    def use_shared_prefix_entry(self):
+        """Decode through paged_attention_decode_shared_prefix with the
+        workload's prefix groups (consecutive members sharing their first
+        prefix_blocks blocks)."""
+        wl, dev = self.wl, self.out.device
+        seq_group = np.full(wl.num_seqs, -1, np.int32)
+        for gi, grp in enumerate(wl.groups):
+            seq_group[grp] = gi
+        self.seq_group = torch.from_numpy(seq_group).to(dev)
+        self.group_prefix = torch.full((max(1, len(wl.groups)),), wl.prefix_blocks * wl.block_size,
+                                       dtype=torch.int32, device=dev)
+
+        def decode():
+            self.pk.paged_attention_decode_shared_prefix(
+                self.t["q"], self.kc, self.vc, self.bt, self.lens, self.seq_group,
+                self.group_prefix, self.wl.scale, self.out, self.partition, self.ws)
+        self.decode = decode
+
 
 def time_steps(step, steps, dist_ctx):
     """Device time of exactly `steps` steps between one pair of events (no
@@ -588,16 +606,6 @@ def measure_gate(name, args, device):
         step.run()
     res = decode_figures(wl, step.decode, args.gate_reps)
     res.update(partition_tokens=P, decode_path=pk.last_decode_path())
-    # the same calls with the separate merge kernel instead of the merge inside
-    # the decode (same box, same buffers): the A/B of that design choice
-    pk.set_option(pk.OPT_FUSED_MERGE, 1)
-    try:
-        alt = time_decode_calls(step.decode, args.gate_reps, 3)
-    finally:
-        pk.set_option(pk.OPT_FUSED_MERGE, 0)
-    algo = res["algorithmic_bytes"]
-    res["merge_kernel_instead"] = {"decode_ms_back_to_back": statistics.median(alt),
-                                   "frac": algo / statistics.median(alt) / 1e6 / measured_peak()[0]}
     del step
     torch.cuda.empty_cache()
     return res
@@ -716,25 +724,6 @@ def measure_trace(block_size, device, slots=64, partition=None, passes=5):
             torch.cuda.synchronize()
             runs.append(e0.elapsed_time(e1))
         graph_ms = statistics.median(runs)
-        del g
-        # the same pass captured with the separate merge kernel (A/B)
-        pk.set_option(pk.OPT_FUSED_MERGE, 1)
-        try:
-            tr.run_pass()
-            g = tr.capture()
-            g.replay()
-            torch.cuda.synchronize()
-            alt = []
-            for _ in range(passes):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                g.replay()
-                e1.record()
-                torch.cuda.synchronize()
-                alt.append(e0.elapsed_time(e1))
-        finally:
-            pk.set_option(pk.OPT_FUSED_MERGE, 0)
-        res["merge_kernel_instead_gbs"] = dec_bytes / statistics.median(alt) / 1e6
         res.update({"total_ms": graph_ms, "decode_gbs": dec_bytes / graph_ms / 1e6,
                     "seq_decodes_per_s": decodes / (graph_ms * 1e-3),
                     "append_gbs_in_step": app_bytes / graph_ms / 1e6,
@@ -1008,6 +997,8 @@ def run_ours(args, ctx):
         wl = subset(wl, range(min(args.seqs, wl.num_seqs)))
     P = PARTITION[args.config] if args.partition is None else args.partition
     step = Step(wl, device, P)
+    if args.entry == "shared_prefix":
+        step.use_shared_prefix_entry()
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -1040,7 +1031,7 @@ def run_ours(args, ctx):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic",
             "config": {"workload": DESCRIPTION[args.config] if args.seqs is None else wl.name,
-                       "partition_tokens": P,
+                       "partition_tokens": P, "entry": args.entry,
                        "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
                        "l2": f"inputs larger than L2: KV pool {2 * wl.num_blocks * wl.block_size * wl.row_bytes / 1e9:.2f} GB",
                        "parallelism": f"replicas x{ctx.world} (one workload per GPU)"},
@@ -1126,6 +1117,9 @@ def main(argv=None):
     ap.add_argument("--repeats", type=int, default=5,
                     help="repeats of the timed loops (their spread is reported)")
     ap.add_argument("--partition", type=int, default=None)
+    ap.add_argument("--entry", choices=["plain", "shared_prefix"], default="plain",
+                    help="decode entry point of the step (shared_prefix: the workload's prefix "
+                         "groups through paged_attention_decode_shared_prefix)")
     ap.add_argument("--path", type=int, default=None, help="1 CUDA-core, 2 tensor-core decode")
     ap.add_argument("--ctas", type=int, default=None, help="persistent decode CTAs per SM")
     ap.add_argument("--e2e-steps", type=int, default=400)

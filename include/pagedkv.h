@@ -293,7 +293,7 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
  *   every CTA streams the same number of bytes whatever the length mix. A
  *   (sequence, kv head) that falls inside one share is written directly; one
  *   that spans shares leaves one unnormalised state per share (at most two
- *   per CTA) in the workspace, which are combined as below. The
+ *   per CTA) in the workspace, which a merge kernel combines as below. The
  *   workspace layout of this mode is internal; size it with
  *   paged_attention_workspace_bytes(..., PAGEDKV_PARTITION_BALANCED), which
  *   depends on the current device's SM count.
@@ -301,7 +301,7 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
  *   cut into partitions of that many tokens; each (sequence, kv head,
  *   partition) produces an unnormalised state per query head
  *       m_p = max z_i,  l_p = sum e^(z_i - m_p),  o_p = sum e^(z_i - m_p) V_i
- *   over its tokens, and a merge combines them:
+ *   over its tokens, and a merge kernel combines them:
  *       M = max_p m_p,  out = sum_p e^(m_p - M) o_p / sum_p e^(m_p - M) l_p.
  *   Sequences that fit in one partition skip the merge. The states live in
  *   the caller's workspace (see paged_attention_workspace_bytes), as fp32
@@ -309,21 +309,7 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
  *       then l [num_seqs][n_q_heads][P],
  *   P = ceil(max_blocks_per_seq*block_size / partition_tokens), each array
  *   starting on a 256-byte boundary; m is in natural-log units. Entries of
- *   partitions a sequence does not have are left untouched. After them come
- *   uint64 arrival counters [num_seqs][n_q_heads] (256-byte aligned).
- * Where the merge runs. When n_kv_heads is a multiple of 4 and either the
- *   split is balanced or P <= 32, the decode kernel merges by itself: each
- *   partial state is published (a device-wide fence) and its tiles counted on
- *   its (sequence, kv head)'s counter; the warp whose count completes the
- *   context reads every state of that (sequence, kv head) back and writes the
- *   output rows. A counter word carries the tag of the call that counts on it
- *   (tags differ from call to call), so the workspace needs no clearing
- *   between calls; a word whose high half happens to equal the current tag
- *   (about one chance in 2^32 per counter, for workspace bytes left by other
- *   data) would be counted from. Otherwise (long contexts of more than 32
- *   partitions, fewer than 4 kv heads per unit, shared prefixes, or
- *   PAGEDKV_OPT_FUSED_MERGE = 1) a separate merge kernel runs after the
- *   decode kernel.
+ *   partitions a sequence does not have are left untouched.
  *
  * Supported: head_dim 64 or 128; block_size 8, 16 or 32; n_q_heads a multiple
  * of n_kv_heads with n_q_heads / n_kv_heads <= 8; num_seqs <= 4096.
@@ -447,8 +433,6 @@ int pagedkv_check_bounded_wait(void *stream);
 #define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
 #define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16); 0 = library default */
 #define PAGEDKV_OPT_PREFILL_PATH   5  /* 0 auto (= 2), 1 warp-level MMA prefill kernel, 2 tcgen05 prefill kernel */
-#define PAGEDKV_OPT_FUSED_MERGE    6  /* 0 auto: split decodes merge inside the decode kernel where that
-                                         applies; 1 always launch the separate merge kernel */
 int pagedkv_set_option(int option, int value);
 int pagedkv_get_option(int option);
 

@@ -8,7 +8,6 @@
 #include <limits.h>
 #include <stdint.h>
 
-#include <atomic>
 #include <mutex>
 
 #include "../../include/pagedkv.h"
@@ -59,19 +58,7 @@ int g_opt_ctas_per_sm = 0;
 int g_opt_mma_min_group = 4;
 int g_opt_stages = 0;
 int g_opt_prefill_path = 0;
-int g_opt_fused_merge = 0;
 int g_last_path = 0;
-std::atomic<unsigned int> g_call_count{0};
-
-// Tag of one decode call on the workspace's arrival counters: successive calls
-// get tags that differ (an odd multiplier makes the map from call count to tag
-// a bijection, and spreads the tags over the 32-bit range so that a word left
-// by other data is unlikely to carry the current tag); never 0.
-unsigned int next_call_tag() {
-    unsigned int t = 0;
-    while (t == 0) t = (g_call_count.fetch_add(1, std::memory_order_relaxed) + 1u) * 0x9E3779B1u;
-    return t;
-}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -245,10 +232,6 @@ int pagedkv_set_option(int option, int value) {
             if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_prefill_path = value;
             return PAGEDKV_OK;
-        case PAGEDKV_OPT_FUSED_MERGE:
-            if (value < 0 || value > 1) return PAGEDKV_ERR_INVALID_ARG;
-            g_opt_fused_merge = value;
-            return PAGEDKV_OK;
         default:
             return PAGEDKV_ERR_INVALID_ARG;
     }
@@ -261,7 +244,6 @@ int pagedkv_get_option(int option) {
         case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
         case PAGEDKV_OPT_STAGES: return g_opt_stages;
         case PAGEDKV_OPT_PREFILL_PATH: return g_opt_prefill_path;
-        case PAGEDKV_OPT_FUSED_MERGE: return g_opt_fused_merge;
         default: return PAGEDKV_ERR_INVALID_ARG;
     }
 }
@@ -539,9 +521,7 @@ size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim
     } else {
         return 0;
     }
-    // partition states o, m, l, then one arrival counter per (sequence, q head)
-    return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float)) +
-           round256(size_t(num_seqs) * n_q_heads * sizeof(unsigned long long));
+    return round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
 }
 
 static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -596,7 +576,6 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     const long long max_parts =
         partition_tokens > 0 ? max_parts_for(max_blocks_per_seq, block_size, P) : 1;
     float *ws_o = nullptr, *ws_m = nullptr, *ws_l = nullptr;
-    unsigned long long *ws_ctr = nullptr;
     if (split) {
         const size_t need = paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim,
                                                             max_blocks_per_seq, block_size,
@@ -616,8 +595,6 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         ws_m = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)));
         ws_l = reinterpret_cast<float *>(w + round256(rows * head_dim * sizeof(float)) +
                                          round256(rows * sizeof(float)));
-        ws_ctr = reinterpret_cast<unsigned long long *>(
-            w + round256(rows * head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float)));
     }
     // ---- device
     unsigned int *err = nullptr;
@@ -664,16 +641,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.num_groups = prefix ? num_groups : 0;
     // a shared-prefix unit fills the tensor-core tile's 8 columns with (member, q head) pairs
     p.max_members = (prefix && path == pkv::kPathMma) ? 8 / group : 1;
-    // The merge runs inside the decode when every consumer warp owns a whole kv
-    // head and a merging warp has few states to read: the balanced split (a
-    // few shares per (sequence, head group)) or partitions of at most 32 per
-    // row. Rows of many partitions (long contexts) keep the merge kernel, which
-    // spreads them over the whole GPU.
-    const bool fuse = split && !prefix && hpu == 4 && g_opt_fused_merge == 0 &&
-                      (balanced || max_parts <= 32);
-    p.fuse = fuse ? 1 : 0;
-    p.gen = fuse ? next_call_tag() : 0u;
-    p.ctr = ws_ctr;
+
     a.head_dim = head_dim;
     a.path = path;
     a.gmax = gmax;
@@ -690,9 +658,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         default: e = pkv::launch_decode_bf16(a); break;
     }
     if (e != cudaSuccess) return PAGEDKV_ERR_CUDA;
-    if (fuse) {
-        // merged by the decode kernel itself
-    } else if (balanced) {
+    if (balanced) {
         e = pkv::launch_piece_merge(dtype, head_dim, ws_o, ws_m, ws_l, context_lens, out, num_seqs,
                                     n_q_heads, n_kv_heads / hpu, hpu * group, a.grid_used,
                                     int(cap), a.stream);

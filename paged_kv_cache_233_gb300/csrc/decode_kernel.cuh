@@ -646,132 +646,6 @@ struct Walk {
 };
 
 // ---------------------------------------------------------------------------
-// Merge inside the decode: the last partial state of a (sequence, kv head)
-// ---------------------------------------------------------------------------
-
-// Adds `n` tiles to the arrival counter of one (sequence, kv head) and tells
-// whether this arrival completes `total`. The word's high 32 bits name the call
-// that counts on it (a tag that differs from call to call), its low 32 bits
-// the tiles counted in that call, so a word left by an earlier call, or never
-// written, counts as zero. Each failed exchange means another arrival
-// succeeded in between, so the loop ends after at most one try per arrival;
-// the cap only guards against a corrupted word (then nothing is merged and
-// the timeout bit is set).
-__device__ __forceinline__ bool counter_arrive(unsigned long long *c, unsigned int gen,
-                                               unsigned int n, unsigned int total,
-                                               unsigned int *err) {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(c);
-    for (int it = 0; it < (1 << 20); ++it) {
-        const unsigned int have = (unsigned int)(old >> 32) == gen ? (unsigned int)old : 0u;
-        const unsigned long long want = ((unsigned long long)gen << 32) | (have + n);
-        const unsigned long long prev = atomicCAS(c, old, want);
-        if (prev == old) return have + n == total;
-        old = prev;
-    }
-    atomicOr(err, PAGEDKV_DEVERR_TIMEOUT);
-    return false;
-}
-
-// Where the partial states of one (sequence, kv head) sit in the workspace:
-// fixed partitions: piece i of query head j at row row0 + j * jstride + i;
-// balanced split: piece i comes from share c0 + i (slot `slot0` for the first
-// share, slot 0 for later ones), row hh * g + j of the piece; a share that got
-// no tiles holds no piece.
-struct Pieces {
-    int balanced;
-    size_t row0;
-    int jstride;
-    long long c0, total;
-    int slot0, grid, rows_per_piece, r0;
-    __device__ long long share_start(long long c) const { return total * c / grid; }
-    __device__ bool has(int i) const {
-        return !balanced || share_start(c0 + i) != share_start(c0 + i + 1);
-    }
-    __device__ size_t row(int i, int j) const {
-        if (!balanced) return row0 + size_t(j) * jstride + i;
-        return (size_t(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * rows_per_piece + r0 + j;
-    }
-};
-
-// Share (of `grid` equal shares of `total` tiles) that holds tile t.
-__device__ __forceinline__ long long share_of(long long t, long long total, int grid) {
-    long long c = t * grid / total;
-    while (c + 1 < grid && total * (c + 1) / grid <= t) ++c;
-    while (c > 0 && total * c / grid > t) --c;
-    return c;
-}
-
-template <int E> struct MergeVec;
-template <> struct MergeVec<2> { using type = float2; };
-template <> struct MergeVec<4> { using type = float4; };
-
-// One warp combines `np` pieces of each of its g query heads into the output
-// rows out_row0 .. out_row0 + g - 1: M = max m_i, out = sum_i e^(m_i - M) o_i /
-// sum_i e^(m_i - M) l_i (m in natural-log units). The pieces were written by
-// other CTAs; they are read from L2 (ld.global.cg) after the caller's acquire
-// fence. A row's (m, l) of up to 32 pieces come in one round trip (lane i
-// holds piece i), its o rows four pieces per round trip.
-template <typename T, int D>
-__device__ __forceinline__ void merge_pieces_warp(const DecodeParams &p, const Pieces &pc, int np,
-                                                  int g, size_t out_row0, int lane) {
-    constexpr int E = D / 32;
-    constexpr int kBatch = 4;
-    using V = typename MergeVec<E>::type;
-    T *out = reinterpret_cast<T *>(p.out);
-    for (int j = 0; j < g; ++j) {
-        float M = -INFINITY, den = 0.f, acc[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.f;
-        for (int b = 0; b < np; b += 32) {
-            const int i = b + lane;
-            const bool h = i < np && pc.has(i);
-            const size_t r = h ? pc.row(i, j) : 0;
-            const float mi = h ? __ldcg(p.ws_m + r) : -INFINITY;
-            const float li = h ? __ldcg(p.ws_l + r) : 0.f;
-            // a running maximum over chunks of 32 rescales what was summed so far
-            float mx = mi;
-#pragma unroll
-            for (int mask = 16; mask >= 1; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mask));
-            const float Mn = fmaxf(M, mx);
-            const float alpha = M == -INFINITY ? 0.f : fast_exp2((M - Mn) * kLog2e);
-            den *= alpha;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] *= alpha;
-            M = Mn;
-            const float w = h ? fast_exp2((mi - M) * kLog2e) : 0.f;
-            den = fmaf(w, li, den);
-            const int n = min(32, np - b);
-            for (int k0 = 0; k0 < n; k0 += kBatch) {
-                V x[kBatch];
-                float wk[kBatch];
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
-                    wk[k] = __shfl_sync(kFull, w, (k0 + k) & 31);
-                    if (k0 + k < n && wk[k] != 0.f)
-                        x[k] = __ldcg(reinterpret_cast<const V *>(p.ws_o + pc.row(b + k0 + k, j) * D) +
-                                      lane);
-                    else
-                        wk[k] = 0.f;
-                }
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k)
-                    if (wk[k] != 0.f) {
-                        const float *xf = reinterpret_cast<const float *>(&x[k]);
-#pragma unroll
-                        for (int e = 0; e < E; ++e) acc[e] = fmaf(wk[k], xf[e], acc[e]);
-                    }
-            }
-        }
-#pragma unroll
-        for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(kFull, den, mask);
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        T *dst = out + (out_row0 + j) * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) dst[e] = Elem<T>::from_float(acc[e] * inv);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 // CTAs per SM the register budget is sized for: two, except for the CUDA-core
@@ -919,25 +793,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     Walk walk;
     walk.init(seq_base, seq_len, S, groups, P, p.split, p.balanced, prefix ? seq_p0 : nullptr,
               prefix ? seq_pu : nullptr, p.seq_group, p.max_members);
-    // Balanced split merged here: a sequence with an empty context has no
-    // tiles, so no unit writes its zero rows; CTA c writes those of sequences
-    // c, c + grid, ... (after the grid dependency wait, like every store).
-    auto zero_empty_rows = [&](int tid, int nthreads) {
-        T *out = reinterpret_cast<T *>(p.out);
-        const int row_elems = p.n_q_heads * D;
-        for (int s = blockIdx.x; s < S; s += gridDim.x)
-            if (seq_len[s] == 0)
-                for (int x = tid; x < row_elems; x += nthreads)
-                    out[size_t(s) * row_elems + x] = Elem<T>::from_float(0.f);
-    };
-    const bool zero_pass = p.fuse && p.balanced;
-    if (!walk.has_work()) {
-        if (zero_pass) {
-            grid_dependency_wait();
-            zero_empty_rows(threadIdx.x, blockDim.x);
-        }
-        return;
-    }
+    if (!walk.has_work()) return;
     // a dependent merge launch may start once every CTA got here or exited;
     // it waits on this grid's completion before reading the partition states
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1137,46 +993,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         } else if (TL == 1) {
             if constexpr (kMma) st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g);
             else st.store(sink, reinterpret_cast<T *>(p.out), p.ws_o, p.ws_m, p.ws_l, g, lane);
-            if (p.fuse && cur.partial) {
-                // Publish this partial state (every lane fences its own stores),
-                // then count its tiles on the (sequence, kv head): the warp whose
-                // tiles complete the context merges every state of it.
-                __threadfence();
-                __syncwarp();
-                const int kvh = (cur.hg << p.log2_hpu) + hh;
-                const int nt = (cur.L + kTile - 1) / kTile;
-                int last = 0;
-                if (lane == 0)
-                    last = counter_arrive(p.ctr + size_t(cur.s) * p.n_kv_heads + kvh, p.gen,
-                                          unsigned(cur.ntiles), unsigned(nt), p.err);
-                last = __shfl_sync(kFull, last, 0);
-                if (last) {
-                    __threadfence();   // acquire: the other states were published before their counts
-                    Pieces pc;
-                    int np;
-                    pc.balanced = p.balanced;
-                    if (p.balanced) {
-                        const long long total = seq_base[S];
-                        const long long A = seq_base[cur.s] + (long long)cur.hg * nt;
-                        pc.total = total;
-                        pc.grid = gridDim.x;
-                        pc.c0 = share_of(A, total, gridDim.x);
-                        np = int(share_of(A + nt - 1, total, gridDim.x) - pc.c0 + 1);
-                        pc.slot0 = A != pc.share_start(pc.c0) ? 1 : 0;
-                        pc.rows_per_piece = H * g;
-                        pc.r0 = hh * g;
-                        pc.row0 = 0;
-                        pc.jstride = 0;
-                    } else {
-                        np = (cur.L + P - 1) / P;
-                        pc.row0 = (size_t(cur.s) * p.n_q_heads + qh0) * p.max_parts;
-                        pc.jstride = p.max_parts;
-                        pc.c0 = pc.total = 0;
-                        pc.slot0 = pc.grid = pc.rows_per_piece = pc.r0 = 0;
-                    }
-                    merge_pieces_warp<T, D>(p, pc, np, g, size_t(cur.s) * p.n_q_heads + qh0, lane);
-                }
-            }
         } else {
             // warps sharing a kv head combine their states (double-buffered slots,
             // so one barrier per unit suffices)
@@ -1225,7 +1041,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         if (!has_next) break;
         cur = nx;
     }
-    if (zero_pass) zero_empty_rows(threadIdx.x - 32, 32 * kConsumerWarps);
 }
 
 }  // namespace pkv

@@ -50,12 +50,6 @@ struct DecodeParams {
     const int32_t *group_prefix;  // [num_groups] tokens
     int num_groups;
     int max_members;      // sequences whose queries one prefix unit serves
-    // merge inside the decode (split runs with one consumer warp per kv head):
-    // the warp whose partial state completes a (sequence, kv head) combines all
-    // of its states into the output rows
-    int fuse;                   // 1: merge here (no separate merge kernel)
-    unsigned int gen;           // this call's tag on the arrival counters (never 0)
-    unsigned long long *ctr;    // [num_seqs * n_kv_heads] generation-tagged tile counts
 };
 
 // Byte layout of the dynamic shared memory (host and device agree on it).

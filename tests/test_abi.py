@@ -144,8 +144,7 @@ def test_workspace_size_follows_the_documented_layout(lib):
     for S, Hq, D, MB, B, P in [(8, 64, 128, 8192, 16, 512), (4, 4, 64, 5, 16, 16), (3, 2, 64, 7, 8, 48)]:
         parts = -(-(MB * B) // P)
         rows = S * Hq * parts
-        # o, m, l, then one uint64 arrival counter per (sequence, q head)
-        want = r256(rows * D * 4) + 2 * r256(rows * 4) + r256(S * Hq * 8)
+        want = r256(rows * D * 4) + 2 * r256(rows * 4)
         assert pk.paged_attention_workspace_bytes(S, Hq, D, MB, B, P) == want
     assert pk.paged_attention_workspace_bytes(8, 64, 128, 100, 16, 0) == 0
 
@@ -155,11 +154,6 @@ def test_options_round_trip(lib):
     pk.set_option(pk.OPT_MMA_MIN_GROUP, 2)
     assert pk.get_option(pk.OPT_MMA_MIN_GROUP) == 2
     pk.set_option(pk.OPT_MMA_MIN_GROUP, old)
-    pk.set_option(pk.OPT_FUSED_MERGE, 1)
-    assert pk.get_option(pk.OPT_FUSED_MERGE) == 1
-    pk.set_option(pk.OPT_FUSED_MERGE, 0)
-    with pytest.raises(pk.PagedKVError):
-        pk.set_option(pk.OPT_FUSED_MERGE, 2)
     with pytest.raises(pk.PagedKVError):
         pk.set_option(pk.OPT_DECODE_PATH, 9)
     with pytest.raises(pk.PagedKVError):

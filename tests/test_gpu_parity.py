@@ -185,7 +185,7 @@ def test_empty_and_single_token_contexts(orc):
     assert pk.device_errors() == 0
 
 
-def fused_cases():
+def hpu4_cases():
     for dtype in ("f32", "f16", "bf16"):
         for D in (64, 128):
             for B in (8, 16, 32):
@@ -195,18 +195,18 @@ def fused_cases():
                                            id=f"{dtype}-D{D}-B{B}-g{g}-P{P}")
 
 
-@pytest.mark.parametrize("dtype,D,B,g,P", list(fused_cases()))
-def test_fused_merge_matches_oracle_and_merge_kernel(orc, dtype, D, B, g, P):
-    """Four kv heads per unit: split decodes merge inside the decode kernel
-    (partitions of 48 or 256 tokens, at most 32 per row here, and the balanced
-    split); 16-token partitions give rows of up to 69 partitions, which keep
-    the merge kernel. Ragged lengths with empty contexts; both ways of merging
-    against the oracle, each called twice in a row on one workspace whose
-    bytes start as 0xff (stale arrival counters)."""
+@pytest.mark.parametrize("dtype,D,B,g,P", list(hpu4_cases()))
+def test_split_with_four_kv_heads_per_unit(orc, dtype, D, B, g, P):
+    """Four kv heads per unit (one consumer warp each, no cross-warp merge):
+    partitions of 48 or 256 tokens (at most 32 per row, the row-per-warp merge
+    kernel), 16-token partitions (rows of up to 69 partitions, the
+    CTA-per-row merge kernel) and the balanced split; ragged lengths with
+    empty contexts, called twice in a row on one workspace whose bytes start
+    as 0xff, against the oracle."""
     Hkv = 4
     lens = SWEEP_LENS + [0, 1100, 0, 640]
-    seed = zlib.crc32(f"fused-{dtype}-{D}-{B}-{g}".encode()) % 10000
-    wl = make_workload("fused", dtype, lens, Hkv * g, Hkv, D, B, seed, pool_factor=1.5)
+    seed = zlib.crc32(f"hpu4-{dtype}-{D}-{B}-{g}".encode()) % 10000
+    wl = make_workload("hpu4", dtype, lens, Hkv * g, Hkv, D, B, seed, pool_factor=1.5)
     t = materialize(wl, "cuda")
     kc, vc, bt, _ = gpu_fill(wl, t)
     okc, ovc, _ = oracle_fill(orc, wl, t)
@@ -214,15 +214,10 @@ def test_fused_merge_matches_oracle_and_merge_kernel(orc, dtype, D, B, g, P):
     lens_d = torch.from_numpy(wl.context_lens).cuda()
     ws = pk.new_workspace(t["q"], bt, wl.block_size, P)
     ws.fill_(255)
-    try:
-        for fused in (0, 1, 0):   # option value: 0 merge inside the decode, 1 merge kernel
-            pk.set_option(pk.OPT_FUSED_MERGE, fused)
-            for _ in range(2):
-                out = torch.full_like(t["q"], float("nan"))
-                pk.paged_attention_decode(t["q"], kc, vc, bt, lens_d, wl.scale, out, P, ws)
-                assert_close(out, ref, dtype, what=f"{dtype} D{D} B{B} g{g} P{P} option={fused}")
-    finally:
-        pk.set_option(pk.OPT_FUSED_MERGE, 0)
+    for _ in range(2):
+        out = torch.full_like(t["q"], float("nan"))
+        pk.paged_attention_decode(t["q"], kc, vc, bt, lens_d, wl.scale, out, P, ws)
+        assert_close(out, ref, dtype, what=f"{dtype} D{D} B{B} g{g} P{P}")
     assert pk.device_errors() == 0
 
 
