@@ -592,9 +592,26 @@ struct Walk {
 
     __device__ bool has_work() const { return pos < end; }
 
+    // Called by all 32 lanes of a warp together (the producer warp and each
+    // consumer warp walk their own copy). The sequence of the next unit is
+    // found 32 candidates at a time: lane i tests whether sequence s + i ends
+    // past `pos`, and the first such lane is it. Units are dealt with a stride
+    // of the grid size, so the next unit is often dozens of sequences on
+    // (about 30 with 256 sequences of 9 units each): one or two rounds of
+    // shared-memory loads instead of one dependent load per sequence.
     __device__ bool next(Unit &x) {
         if (pos >= end) return false;
-        while (seq_base[s + 1] <= pos) ++s;
+        const int lane = threadIdx.x & 31;
+        for (;;) {
+            const int c = s + 1 + lane;
+            const bool past = c > S || seq_base[c] > pos;
+            const unsigned m = __ballot_sync(kFull, past);
+            if (m) {
+                s += __ffs(m) - 1;
+                break;
+            }
+            s += 32;
+        }
         x.s = s;
         x.L = seq_len[s];
         const int rr = pos - seq_base[s];
