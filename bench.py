@@ -41,11 +41,19 @@ from workloads import materialize, new_pools, preset, subset  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-decodes/s per layer"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129e6
 KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu", "api.cu",
                   "decode_instances.cuh", "decode_launch.h", "launch_cache.h"]
 
-# partition size (tokens) used for each workload's decode; 0 = no split
-PARTITION = {"tiny": 0, "mha7b": 320, "gqa8b_prefix": 320, "longctx_splitk": 512}
+# partition size (tokens) used for each workload's decode; 0 = no split, -1 the
+# balanced split (equal tile shares per CTA). Measured on GB300, back to back:
+# the MHA layer is fastest with the balanced split (0.957 of the copy peak,
+# against 0.925 with 192-token partitions, the best fixed size); the GQA layer
+# with 320-token partitions (0.844; the balanced split's contiguous shares read
+# each group's shared prefix at times too far apart for L2, 0.678); the
+# long-context workload states its 512-token partitions (0.970; the balanced
+# split would read at 1.007, reported beside it).
+PARTITION = {"tiny": 0, "mha7b": -1, "gqa8b_prefix": 320, "longctx_splitk": 512}
 
 DESCRIPTION = {
     "tiny": "tiny: 4 seqs, lens {2,18,34,65}, B16, 4q/2kv heads, D64, fp32",
@@ -252,7 +260,7 @@ class Step:
         self.fill_ms = statistics.median(fills)
         self.fill_tokens = len(wl.fill_seq)
         del fill_seq, fill_pos, fill_slots
-        self.launches_per_step = 2 + (1 if partition > 0 else 0)
+        self.launches_per_step = 2 + (1 if partition != 0 else 0)   # the merge of a split
 
     def run(self):
         self.pk.paged_kv_append_tokens(self.t["k_step"], self.t["v_step"], self.bt, self.step_seq,
@@ -538,6 +546,16 @@ class DistCtx:
             self.pg.destroy_process_group()
 
 
+def workload_config(name, wl, partition, world):
+    """The `config` object of the JSON line, the same for both arms."""
+    pool = 2 * wl.num_blocks * wl.block_size * wl.row_bytes
+    return {"workload": DESCRIPTION[name] if wl.name == name else wl.name,
+            "partition_tokens": partition,
+            "l2": (f"inputs {'larger' if pool > L2_BYTES else 'smaller'} than L2: "
+                   f"KV pool {pool / 1e9:.2f} GB"),
+            "parallelism": f"replicas x{world} (one workload per GPU)"}
+
+
 def workload_for(name, rank):
     wl = preset(name)
     if rank:
@@ -573,7 +591,7 @@ def run_reference(args, ctx):
         "n_gpus": ctx.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": DESCRIPTION[args.config]},
+        "config": workload_config(args.config, preset(args.config), PARTITION[args.config], ctx.world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -596,11 +614,11 @@ def decode_figures(wl, call, reps, repeats=5):
             "reps": reps}
 
 
-def measure_gate(name, args, device):
+def measure_gate(name, args, device, partition=None):
     """Decode-only roofline fraction of one workload (for the stated targets)."""
     import paged_kv_cache_233_gb300 as pk
     wl = preset(name)
-    P = PARTITION[name]
+    P = PARTITION[name] if partition is None else partition
     step = Step(wl, device, P)
     for _ in range(args.warmup):
         step.run()
@@ -1030,11 +1048,9 @@ def run_ours(args, ctx):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic",
-            "config": {"workload": DESCRIPTION[args.config] if args.seqs is None else wl.name,
-                       "partition_tokens": P, "entry": args.entry,
-                       "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
-                       "l2": f"inputs larger than L2: KV pool {2 * wl.num_blocks * wl.block_size * wl.row_bytes / 1e9:.2f} GB",
-                       "parallelism": f"replicas x{ctx.world} (one workload per GPU)"},
+            "config": workload_config(args.config, wl, P, ctx.world),
+            "decode_entry": args.entry,
+            "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
             "step_ms_spread": spread(repeats),
             "seq_decodes_per_s_per_layer": seq_decodes,
             "kv_logical_gbs": ctx.sum(logical) / ms_per_step / 1e6,
@@ -1085,9 +1101,13 @@ def run_ours(args, ctx):
     if ctx.rank == 0 and not args.no_gates and ctx.world == 1:
         gates = {name: measure_gate(name, args, device)
                  for name in ("gqa8b_prefix", "longctx_splitk", "mha7b") if name != args.config}
+        # the long-context workload under the balanced split instead of its stated
+        # 512-token partitions (a split the caller may choose; context only)
+        gates["longctx_splitk_balanced_split"] = measure_gate("longctx_splitk", args, device,
+                                                              partition=-1)
         gates["gqa8b_prefix_shared_prefix_entry"] = measure_shared_prefix(device, args.gate_reps)
         result["gates"] = gates
-        for name in ("gqa8b_prefix", "longctx_splitk", "mha7b"):
+        for name in ("gqa8b_prefix", "longctx_splitk", "mha7b", "longctx_splitk_balanced_split"):
             if name in gates:
                 targets[name] = compact(gates[name])
         sp = gates["gqa8b_prefix_shared_prefix_entry"]
