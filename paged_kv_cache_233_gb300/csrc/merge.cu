@@ -33,8 +33,17 @@ __device__ __forceinline__ float block_reduce(float v, float *scratch) {
     return v;
 }
 
-// One CTA per (sequence, query head), for rows of many partitions. Warps take
-// partitions round-robin; each lane owns head_dim / 32 contiguous outputs.
+// One CTA per (sequence, query head), for rows of many partitions. Each
+// thread loads the (m, l) of partitions t, t + 256, ... once; the block
+// reduces M and the denominator and leaves each partition's weight
+// e^(m_p - M) in shared memory; then every warp takes partitions
+// round-robin and issues the loads of up to kOBatch of its o rows at once
+// (lane i holds head_dim / 32 outputs), so a row costs a few round trips to
+// L2 whatever its partition count. Rows of up to kMaxParts partitions keep
+// their weights in shared memory; longer rows recompute them.
+constexpr int kMaxParts = 1024;
+constexpr int kOBatch = 8;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(32 * kMergeWarps)
 lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
@@ -43,6 +52,7 @@ lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
     constexpr int E = D / 32;
     using V = typename Vec<E>::type;
     __shared__ float red[kMergeWarps];
+    __shared__ float wgt[kMaxParts];
     __shared__ float acc_s[kMergeWarps][D];
     // the next kernel of the stream may start its set-up now: it waits for
     // this grid before it reads or writes what this grid touches
@@ -58,23 +68,43 @@ lse_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t row0 = size_t(row) * max_parts;
+    const bool keep = np <= kMaxParts;
+    // (m, l) of this thread's partitions, loaded once
     float M = -INFINITY;
-    for (int k = threadIdx.x; k < np; k += blockDim.x) M = fmaxf(M, ws_m[row0 + k]);
+    for (int k = threadIdx.x; k < np; k += blockDim.x) {
+        const float mk = __ldcg(ws_m + row0 + k);
+        if (keep) wgt[k] = mk;
+        M = fmaxf(M, mk);
+    }
     M = block_reduce<true>(M, red);
     float den = 0.f;
-    for (int k = threadIdx.x; k < np; k += blockDim.x)
-        den = fmaf(fast_exp2((ws_m[row0 + k] - M) * kLog2e), ws_l[row0 + k], den);
-    den = block_reduce<false>(den, red);
+    for (int k = threadIdx.x; k < np; k += blockDim.x) {
+        const float mk = keep ? wgt[k] : __ldcg(ws_m + row0 + k);
+        const float w = fast_exp2((mk - M) * kLog2e);
+        if (keep) wgt[k] = w;
+        den = fmaf(w, __ldcg(ws_l + row0 + k), den);
+    }
+    den = block_reduce<false>(den, red);   // its barriers also publish wgt
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int k = warp; k < np; k += kMergeWarps) {
-        const float w = fast_exp2((ws_m[row0 + k] - M) * kLog2e);
-        const V x = *reinterpret_cast<const V *>(ws_o + (row0 + k) * D + lane * E);
-        const float *xf = reinterpret_cast<const float *>(&x);
+    for (int k0 = warp; k0 < np; k0 += kMergeWarps * kOBatch) {
+        V x[kOBatch];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, xf[e], acc[e]);
+        for (int b = 0; b < kOBatch; ++b) {
+            const int k = k0 + b * kMergeWarps;
+            if (k < np) x[b] = __ldcg(reinterpret_cast<const V *>(ws_o + (row0 + k) * D) + lane);
+        }
+#pragma unroll
+        for (int b = 0; b < kOBatch; ++b) {
+            const int k = k0 + b * kMergeWarps;
+            if (k < np) {
+                const float w = keep ? wgt[k] : fast_exp2((__ldcg(ws_m + row0 + k) - M) * kLog2e);
+                const float *xf = reinterpret_cast<const float *>(&x[b]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(w, xf[e], acc[e]);
+            }
+        }
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) acc_s[warp][lane * E + e] = acc[e];
@@ -252,9 +282,17 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
         total_t += n;
         if (t < s) before_t += n;
     }
+    // warp sums first, then one shared-memory atomic per warp and sum
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) {
+        before_t += __shfl_xor_sync(0xffffffffu, before_t, mask);
+        total_t += __shfl_xor_sync(0xffffffffu, total_t, mask);
+    }
     __syncthreads();
-    atomicAdd(&sums[0], before_t);
-    atomicAdd(&sums[1], total_t);
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&sums[0], before_t);
+        atomicAdd(&sums[1], total_t);
+    }
     __syncthreads();
     const unsigned long long before = sums[0], total = sums[1];
     const int nt = (L + kTile - 1) / kTile;
