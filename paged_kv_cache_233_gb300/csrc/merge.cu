@@ -15,6 +15,21 @@ template <> struct Vec<4> { using type = float4; };
 
 constexpr int kMergeWarps = 8;
 
+// E consecutive outputs of a row (E = head_dim / 32, one lane's share) as one
+// vector store: 8 or 16 bytes instead of E scalar stores.
+template <typename T, int E>
+__device__ __forceinline__ void store_outputs(T *dst, const float *v) {
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (E == 4) *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        else *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+    } else {
+        if constexpr (E == 4)
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(Elem<T>::pack2(v[0], v[1]), Elem<T>::pack2(v[2], v[3]));
+        else
+            *reinterpret_cast<uint32_t *>(dst) = Elem<T>::pack2(v[0], v[1]);
+    }
+}
+
 // Block-wide reduction helper over kMergeWarps warps (max or sum).
 template <bool kMax>
 __device__ __forceinline__ float block_reduce(float v, float *scratch) {
@@ -182,9 +197,7 @@ lse_merge_rows_kernel(const float *__restrict__ ws_o, const float *__restrict__ 
     float v[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] = acc[e] * inv;
-    T *dst = out + size_t(row) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) dst[e] = Elem<T>::from_float(v[e]);
+    store_outputs<T, E>(out + size_t(row) * D + lane * E, v);
 }
 
 // Launched as a programmatic dependent of the decode kernel when the device
@@ -380,9 +393,10 @@ lse_merge_pieces_kernel(const float *__restrict__ ws_o, const float *__restrict_
 #pragma unroll
         for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        T *dst = out + (size_t(s) * n_q_heads + qh0 + r) * D + lane * E;
+        float v[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) dst[e] = Elem<T>::from_float(acc[e] * inv);
+        for (int e = 0; e < E; ++e) v[e] = acc[e] * inv;
+        store_outputs<T, E>(out + (size_t(s) * n_q_heads + qh0 + r) * D + lane * E, v);
     }
 }
 
