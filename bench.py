@@ -47,12 +47,12 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu",
 
 # partition size (tokens) used for each workload's decode; 0 = no split, -1 the
 # balanced split (equal tile shares per CTA). Measured on GB300, back to back:
-# the MHA layer is fastest with the balanced split (0.957 of the copy peak,
-# against 0.925 with 192-token partitions, the best fixed size); the GQA layer
-# with 320-token partitions (0.844; the balanced split's contiguous shares read
-# each group's shared prefix at times too far apart for L2, 0.678); the
-# long-context workload states its 512-token partitions (0.970; the balanced
-# split would read at 1.007, reported beside it).
+# the MHA layer is fastest with the balanced split (0.989 of the copy peak;
+# 0.925 with 192-token partitions, the best fixed size); the GQA layer with
+# 320-token partitions (0.847; the balanced split's contiguous shares read each
+# group's shared prefix at times too far apart for L2); the long-context
+# workload states its 512-token partitions (0.989; the balanced split, 1.026,
+# is reported beside it).
 PARTITION = {"tiny": 0, "mha7b": -1, "gqa8b_prefix": 320, "longctx_splitk": 512}
 
 DESCRIPTION = {
