@@ -158,12 +158,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int t = 0; t < kTcTiles; ++t)
             for (int b = 0; b < 2; ++b) {
                 mbar_init(bar(bar_s(t, b)), 1);
-                mbar_init(bar(bar_p(t, b)), kTcRows);
+                mbar_init(bar(bar_p(t, b)), kTcRows / 32);   // one arrival per softmax warp
                 mbar_init(bar(bar_o(t, b)), 1);
             }
-        mbar_init(bar(kQFull), kTcTiles * kTcRows);
+        mbar_init(bar(kQFull), kTcTiles * kTcRows / 32);
         mbar_init(bar(kDone), kTcTiles);
-        mbar_init(bar(kVZero), kTcRows);
+        mbar_init(bar(kVZero), kTcRows / 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -331,8 +331,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 const uint4 v = R < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
                 sts128(qdst + (c >> 3) * Ly::kQSlab + (((c & 7) ^ (r & 7)) << 4), v);
             }
+            // every lane's stores are ordered for the tensor core's (async proxy)
+            // reads by its own fence; after the warp barrier one lane arrives
             fence_proxy_async_smem();
-            mbar_arrive(bar(kQFull));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kQFull));
         }
         float ref = -INFINITY;   // reference maximum (base 2) that P and O are relative to
         float l = 0.f;
@@ -412,14 +415,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                mbar_arrive(bar(kVZero));
+                if (lane == 0) mbar_arrive(bar(kVZero));
             }
             uint32_t pk[kTcKeys / 2];
 #pragma unroll
             for (int c = 0; c < kTcKeys / 2; ++c) pk[c] = Elem<T>::pack2(sc[2 * c], sc[2 * c + 1]);
             tmem_st32u(trow + uint32_t(b * kTcKeys), pk);
+            // each lane's tensor-memory store has completed (tmem_st32u waits) and is
+            // ordered before the warp barrier; then one lane arrives for the warp
             tc_fence_before_sync();
-            mbar_arrive(bar(bar_p(t, b)));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bar_p(t, b)));
         }
         if (ok && nk > 0) {
             // the last P V's completion covers every earlier MMA of the issuing thread
