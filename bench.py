@@ -22,7 +22,6 @@ oracle instead on a bounded sample of the same workload.
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -1010,6 +1009,8 @@ def run_ours(args, ctx):
         pk.set_option(pk.OPT_DECODE_PATH, args.path)
     if args.ctas is not None:
         pk.set_option(pk.OPT_CTAS_PER_SM, args.ctas)
+    if args.stages is not None:
+        pk.set_option(pk.OPT_STAGES, args.stages)
     wl = workload_for(args.config, ctx.rank)
     if args.seqs is not None:
         wl = subset(wl, range(min(args.seqs, wl.num_seqs)))
@@ -1142,6 +1143,7 @@ def main(argv=None):
                          "groups through paged_attention_decode_shared_prefix)")
     ap.add_argument("--path", type=int, default=None, help="1 CUDA-core, 2 tensor-core decode")
     ap.add_argument("--ctas", type=int, default=None, help="persistent decode CTAs per SM")
+    ap.add_argument("--stages", type=int, default=None, help="decode stage-ring size (2..16)")
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--gate-reps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
