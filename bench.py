@@ -697,7 +697,7 @@ class TraceRun:
         return g
 
 
-def measure_trace(block_size, device, slots=64, partition=None, passes=5):
+def measure_trace(block_size, device, slots=64, partition=None, passes=5, pool_tokens=65536):
     """The continuous-batching workload (64 requests, up to `slots` running,
     65,536-slot pool, LIFO recompute preemption) through the hot path, step by
     step: each step one paged_kv_append_tokens and one paged_attention_decode
@@ -718,13 +718,14 @@ def measure_trace(block_size, device, slots=64, partition=None, passes=5):
     if partition is None:
         partition = pk.PARTITION_BALANCED
     from workloads import cb_trace
-    tw = cb_trace(block_size=block_size, slots=slots)
+    tw = cb_trace(block_size=block_size, slots=slots, pool_tokens=pool_tokens)
     tr = TraceRun(tw, device, partition)
     tr.run_pass()
     torch.cuda.synchronize()
     plans = [p for p, _ in tr.steps]
     dec_bytes, app_bytes, decodes = trace_bytes(tw, plans)
-    res = {"slots": slots, "steps": len(plans), "preemptions": tw.preemptions,
+    res = {"slots": slots, "pool_tokens": pool_tokens, "steps": len(plans),
+           "preemptions": tw.preemptions,
            "max_running": max(len(p.rids) for p in plans), "partition_tokens": partition,
            "decode_bytes": dec_bytes}
     graph_ms = None
@@ -1095,6 +1096,10 @@ def run_ours(args, ctx):
     if ctx.rank == 0 and not args.no_trace and ctx.world == 1:
         result["trace"] = {f"B{b}_slots{n}": measure_trace(b, device, slots=n)
                            for b in (8, 16, 32) for n in TRACE_SLOTS}
+        # a pool of 4,096 token slots instead of 65,536: LIFO preemption by
+        # recompute fires (its re-appends run inside the timed steps)
+        result["trace"]["B16_slots64_pool4096"] = measure_trace(16, device, slots=64,
+                                                                pool_tokens=4096)
         torch.cuda.empty_cache()
         result["cow_copy"] = measure_cow(device)
         result["swap"] = measure_swap(device)

@@ -96,12 +96,9 @@ def oracle_trace(orc, tw, tensors):
     return refs, slots, okc, ovc
 
 
-@pytest.mark.parametrize("slots", SLOTS)
-@pytest.mark.parametrize("block_size", [8, 16, 32])
-def test_trace_bench_launches_match_oracle(orc, block_size, slots):
+def bench_launches_against_oracle(orc, tw):
     """The bench's launches: one paged_kv_append_tokens (slots written out too)
     and one balanced-split decode per step, one workspace for every step."""
-    tw = cb_trace(block_size=block_size, slots=slots)
     tensors = trace_tensors(tw, "cuda")
     refs, ref_slots, okc, ovc = oracle_trace(orc, tw, {k: v.cpu() for k, v in tensors.items()})
     shape = (tw.num_blocks, tw.block_size, tw.n_kv_heads, tw.head_dim)
@@ -127,6 +124,20 @@ def test_trace_bench_launches_match_oracle(orc, block_size, slots):
     assert to_np(kc).view(np.uint8).tobytes() == okc.view(np.uint8).tobytes()
     assert to_np(vc).view(np.uint8).tobytes() == ovc.view(np.uint8).tobytes()
     assert pk.device_errors() == 0
+
+
+@pytest.mark.parametrize("slots", SLOTS)
+@pytest.mark.parametrize("block_size", [8, 16, 32])
+def test_trace_bench_launches_match_oracle(orc, block_size, slots):
+    bench_launches_against_oracle(orc, cb_trace(block_size=block_size, slots=slots))
+
+
+def test_trace_bench_launches_with_preemption_match_oracle(orc):
+    """The bench's reduced-pool trace (4,096 token slots, 64 slots): LIFO
+    preemption by recompute re-appends the victims' tokens inside the steps."""
+    tw = cb_trace(block_size=16, slots=64, pool_tokens=4096)
+    assert tw.preemptions > 0
+    bench_launches_against_oracle(orc, tw)
 
 
 @pytest.mark.parametrize("block_size,slots", [(16, 8), (16, 64), (8, 32), (32, 16)])
