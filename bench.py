@@ -45,14 +45,17 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu",
                   "decode_instances.cuh", "decode_launch.h", "launch_cache.h"]
 
 # partition size (tokens) used for each workload's decode; 0 = no split, -1 the
-# balanced split (equal tile shares per CTA). Measured on GB300, back to back:
-# the MHA layer is fastest with the balanced split (0.989 of the copy peak;
-# 0.925 with 192-token partitions, the best fixed size); the GQA layer with
-# 320-token partitions (0.847; the balanced split's contiguous shares read each
-# group's shared prefix at times too far apart for L2); the long-context
-# workload states its 512-token partitions (0.989; the balanced split, 1.026,
-# is reported beside it).
-PARTITION = {"tiny": 0, "mha7b": -1, "gqa8b_prefix": 320, "longctx_splitk": 512}
+# balanced split (equal tile shares per CTA). Measured on GB300, back to back,
+# with the decode's L2 priorities (shared blocks evict_last, the rest
+# evict_first): the MHA layer is fastest with the balanced split (0.992 of the
+# copy peak; 0.925 with 192-token partitions, the best fixed size, before the
+# priorities); the GQA layer with the balanced split too (0.888; 320-token
+# partitions, the best fixed size, 0.875, reported beside it; without the
+# priorities the balanced split's contiguous shares read each group's shared
+# prefix at times too far apart for L2, 0.787); the long-context workload
+# states its 512-token partitions (0.989; the balanced split is reported
+# beside it).
+PARTITION = {"tiny": 0, "mha7b": -1, "gqa8b_prefix": -1, "longctx_splitk": 512}
 
 DESCRIPTION = {
     "tiny": "tiny: 4 seqs, lens {2,18,34,65}, B16, 4q/2kv heads, D64, fp32",
@@ -335,6 +338,29 @@ def time_each_call(call, reps):
     return statistics.median(a.elapsed_time(b) for a, b in pairs)
 
 
+_FLUSH = {}
+
+
+def time_each_call_l2_flushed(call, reps=30):
+    """Median ms of `reps` decode calls, each bracketed by its own events after
+    a write of twice the L2's bytes (nothing a call read is left in L2 for the
+    next one: the cold-cache time of one call)."""
+    dev = torch.cuda.current_device()
+    if dev not in _FLUSH:
+        _FLUSH[dev] = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device="cuda")
+    buf = _FLUSH[dev]
+    times = []
+    for _ in range(reps):
+        buf.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
 def spread(xs):
     """min / median / max of repeated measurements and the max-min range in % of the median."""
     med = statistics.median(xs)
@@ -599,10 +625,12 @@ def run_reference(args, ctx):
 
 def decode_figures(wl, call, reps, repeats=5):
     """Decode-call figures of one workload: the median of `reps` calls each
-    between its own events, and `repeats` runs of `reps` calls back to back."""
+    between its own events, the median of 30 such calls each after an L2
+    flush, and `repeats` runs of `reps` calls back to back."""
     algo, logical, kv_unique = decode_bytes(wl)
     peak, _ = measured_peak()
     per_call = time_each_call(call, reps)
+    flushed = time_each_call_l2_flushed(call)
     b2b = time_decode_calls(call, reps, repeats)
     med = statistics.median(b2b)
     return {"algorithmic_bytes": algo, "kv_unique_bytes": kv_unique,
@@ -610,6 +638,7 @@ def decode_figures(wl, call, reps, repeats=5):
             "achieved_gbs": algo / med / 1e6, "frac": algo / med / 1e6 / peak,
             "logical_gbs": logical / med / 1e6,
             "decode_ms_per_call": per_call, "frac_per_call": algo / per_call / 1e6 / peak,
+            "decode_ms_l2_flushed": flushed, "frac_l2_flushed": algo / flushed / 1e6 / peak,
             "reps": reps}
 
 
@@ -993,6 +1022,7 @@ def compact(fig):
     return {"frac": round(fig["frac"], 4), "gbs": round(fig["achieved_gbs"], 1),
             "ms": round(fig["decode_ms_back_to_back"], 5),
             "frac_per_call": round(fig["frac_per_call"], 4),
+            "frac_l2_flushed": round(fig["frac_l2_flushed"], 4),
             "spread_pct": round(fig["back_to_back_ms_spread"]["range_pct"], 2)}
 
 
@@ -1012,6 +1042,8 @@ def run_ours(args, ctx):
         pk.set_option(pk.OPT_CTAS_PER_SM, args.ctas)
     if args.stages is not None:
         pk.set_option(pk.OPT_STAGES, args.stages)
+    if args.l2_hints is not None:
+        pk.set_option(pk.OPT_L2_HINTS, args.l2_hints)
     wl = workload_for(args.config, ctx.rank)
     if args.seqs is not None:
         wl = subset(wl, range(min(args.seqs, wl.num_seqs)))
@@ -1053,6 +1085,8 @@ def run_ours(args, ctx):
             "config": workload_config(args.config, wl, P, ctx.world),
             "decode_entry": args.entry,
             "decode_path": {1: "simt", 2: "mma"}.get(pk.last_decode_path()),
+            "decode_l2_hints": {0: "auto (K/V stream larger than L2)", 1: "never", 2: "always"}[
+                pk.get_option(pk.OPT_L2_HINTS)],
             "step_ms_spread": spread(repeats),
             "seq_decodes_per_s_per_layer": seq_decodes,
             "kv_logical_gbs": ctx.sum(logical) / ms_per_step / 1e6,
@@ -1149,6 +1183,8 @@ def main(argv=None):
     ap.add_argument("--path", type=int, default=None, help="1 CUDA-core, 2 tensor-core decode")
     ap.add_argument("--ctas", type=int, default=None, help="persistent decode CTAs per SM")
     ap.add_argument("--stages", type=int, default=None, help="decode stage-ring size (2..16)")
+    ap.add_argument("--l2-hints", type=int, default=None, choices=(0, 1, 2),
+                    help="L2 priorities on the decode's K/V loads: 0 auto (default), 1 never, 2 always")
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--gate-reps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -433,6 +433,10 @@ int pagedkv_check_bounded_wait(void *stream);
 #define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
 #define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16); 0 = library default */
 #define PAGEDKV_OPT_PREFILL_PATH   5  /* 0 auto (= 2), 1 warp-level MMA prefill kernel, 2 tcgen05 prefill kernel */
+#define PAGEDKV_OPT_L2_HINTS       6  /* L2 priorities on the decode's K/V loads (blocks that the previous or next
+                                         sequence holds at the same table index evict_last, the rest evict_first):
+                                         0 auto = when the call's K/V tokens exceed what the L2 holds, 1 never,
+                                         2 always */
 int pagedkv_set_option(int option, int value);
 int pagedkv_get_option(int option);
 

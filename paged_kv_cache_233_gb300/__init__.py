@@ -30,7 +30,7 @@ __all__ = [
     "paged_attention_workspace_bytes", "new_workspace", "device_errors", "set_option",
     "get_option", "last_decode_path", "status_string", "abi_version", "library_path", "load",
     "DTYPE_CODES", "OPT_DECODE_PATH", "OPT_CTAS_PER_SM", "OPT_MMA_MIN_GROUP", "OPT_STAGES",
-    "OPT_PREFILL_PATH",
+    "OPT_PREFILL_PATH", "OPT_L2_HINTS",
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
     "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
     "paged_attention_prefill", "paged_kv_append_tokens", "check_bounded_wait", "DEVERR_TIMEOUT",
@@ -41,6 +41,7 @@ _LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 OPT_DECODE_PATH, OPT_CTAS_PER_SM, OPT_MMA_MIN_GROUP, OPT_STAGES, OPT_PREFILL_PATH = 1, 2, 3, 4, 5
+OPT_L2_HINTS = 6
 NOALLOC_SCRATCH_BYTES = 64 << 20   # PAGEDKV_NOALLOC_SCRATCH_BYTES
 PARTITION_BALANCED = -1            # PAGEDKV_PARTITION_BALANCED
 DEVERR_TIMEOUT = 0x20              # PAGEDKV_DEVERR_TIMEOUT: a bounded in-kernel wait gave up

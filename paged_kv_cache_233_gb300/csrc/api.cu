@@ -52,12 +52,14 @@ std::mutex g_mu;
 unsigned int *g_err_ptr[kMaxDevices] = {};
 unsigned long long g_err_ctx[kMaxDevices] = {};   // context the error word's address belongs to
 int g_num_sms[kMaxDevices] = {};
+long long g_l2_bytes[kMaxDevices] = {};
 
 int g_opt_path = pkv::kPathAuto;
 int g_opt_ctas_per_sm = 0;
 int g_opt_mma_min_group = 4;
 int g_opt_stages = 0;
 int g_opt_prefill_path = 0;
+int g_opt_l2_hints = 0;
 int g_last_path = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -76,7 +78,7 @@ bool valid_dtype(int dtype) {
 
 // Error-word address and SM count of the current device (looked up once per
 // device and context: again after cudaDeviceReset has replaced the context).
-int device_state(unsigned int **err, int *sms) {
+int device_state(unsigned int **err, int *sms, long long *l2_bytes = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PAGEDKV_ERR_CUDA;
     const unsigned long long ctx = pkv::current_context_id();
@@ -87,12 +89,17 @@ int device_state(unsigned int **err, int *sms) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return PAGEDKV_ERR_CUDA;
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 < 0)
+            return PAGEDKV_ERR_CUDA;
         g_num_sms[dev] = n;
+        g_l2_bytes[dev] = l2;
         g_err_ptr[dev] = static_cast<unsigned int *>(p);
         g_err_ctx[dev] = ctx ? ctx : pkv::current_context_id();
     }
     *err = g_err_ptr[dev];
     *sms = g_num_sms[dev];
+    if (l2_bytes) *l2_bytes = g_l2_bytes[dev];
     return PAGEDKV_OK;
 }
 
@@ -232,6 +239,10 @@ int pagedkv_set_option(int option, int value) {
             if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
             g_opt_prefill_path = value;
             return PAGEDKV_OK;
+        case PAGEDKV_OPT_L2_HINTS:
+            if (value < 0 || value > 2) return PAGEDKV_ERR_INVALID_ARG;
+            g_opt_l2_hints = value;
+            return PAGEDKV_OK;
         default:
             return PAGEDKV_ERR_INVALID_ARG;
     }
@@ -244,6 +255,7 @@ int pagedkv_get_option(int option) {
         case PAGEDKV_OPT_MMA_MIN_GROUP: return g_opt_mma_min_group;
         case PAGEDKV_OPT_STAGES: return g_opt_stages;
         case PAGEDKV_OPT_PREFILL_PATH: return g_opt_prefill_path;
+        case PAGEDKV_OPT_L2_HINTS: return g_opt_l2_hints;
         default: return PAGEDKV_ERR_INVALID_ARG;
     }
 }
@@ -599,7 +611,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     // ---- device
     unsigned int *err = nullptr;
     int sms = 0;
-    int st = device_state(&err, &sms);
+    long long l2_bytes = 0;
+    int st = device_state(&err, &sms, &l2_bytes);
     if (st != PAGEDKV_OK) return st;
     // kv heads per unit: one consumer warp per head when n_kv_heads allows
     const int hpu = n_kv_heads % 4 == 0 ? 4 : (n_kv_heads % 2 == 0 ? 2 : 1);
@@ -641,6 +654,10 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.num_groups = prefix ? num_groups : 0;
     // a shared-prefix unit fills the tensor-core tile's 8 columns with (member, q head) pairs
     p.max_members = (prefix && path == pkv::kPathMma) ? 8 / group : 1;
+    // L2 priorities once the call's K/V stream is larger than the L2 (auto)
+    const long long token_bytes = 2ll * n_kv_heads * head_dim * elem_bytes(dtype);
+    p.hint_min_tokens = g_opt_l2_hints == 1 ? LLONG_MAX
+                      : g_opt_l2_hints == 2 ? 0 : l2_bytes / token_bytes;
 
     a.head_dim = head_dim;
     a.path = path;

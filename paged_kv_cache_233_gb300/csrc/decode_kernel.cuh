@@ -756,6 +756,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
     }
     __syncthreads();
+    long long kv_tokens = 0;   // tokens attended over by the whole call (warp 0)
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_descriptor(&kmap);
@@ -770,6 +771,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int s0 = 0; s0 < S; s0 += 32) {
             const int s = s0 + lane;
             const int Lc = s < S ? seq_len[s] : 0;
+            kv_tokens += Lc;
             int cnt = s < S ? (p.balanced ? (Lc + kTile - 1) / kTile : (Lc > 0 ? (Lc + P - 1) / P : 1)) * groups
                             : 0;
             if (prefix) {
@@ -805,6 +807,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             if (s < S) seq_base[s + 1] = carry + x;
             carry += __shfl_sync(kFull, x, 31);
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) kv_tokens += __shfl_xor_sync(kFull, kv_tokens, off);
     }
     __syncthreads();
     Walk walk;
@@ -821,30 +825,55 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        // lane-parallel window of 32 block-table entries starting at block j0
-        auto load_window = [&](const Unit &x, int j0) {
+        // L2 priority of the K/V lines, once the call streams more K/V than the
+        // L2 holds (a smaller stream is left to the default policy: the next
+        // step reads it again and may find it there). A block that the previous
+        // or the next sequence also holds at the same table index (a shared
+        // prefix, a forked sequence) is read again soon by another unit:
+        // evict_last. Every other block is read once per call: evict_first.
+        const bool hint = kv_tokens > p.hint_min_tokens;
+        uint64_t pol_shared = 0, pol_own = 0;
+        if (hint) {
+            pol_shared = l2_policy_evict_last();
+            pol_own = l2_policy_evict_first();
+        }
+        // lane-parallel window of 32 block-table entries starting at block j0,
+        // and the mask of those held by a neighbouring sequence too
+        auto load_window = [&](const Unit &x, int j0, unsigned &shared) {
             const int nblk = (x.L + B - 1) >> p.log2_block;
             const int j = j0 + lane;
-            return j < nblk ? __ldg(p.block_tables + size_t(x.s) * p.max_blocks + j) : -1;
+            const int v = j < nblk ? __ldg(p.block_tables + size_t(x.s) * p.max_blocks + j) : -1;
+            bool sh = false;
+            if (hint) {
+                const int nprev = x.s > 0 ? (seq_len[x.s - 1] + B - 1) >> p.log2_block : 0;
+                const int nnext = x.s + 1 < S ? (seq_len[x.s + 1] + B - 1) >> p.log2_block : 0;
+                const int a = j < nprev ? __ldg(p.block_tables + size_t(x.s - 1) * p.max_blocks + j) : -1;
+                const int b = j < nnext ? __ldg(p.block_tables + size_t(x.s + 1) * p.max_blocks + j) : -1;
+                sh = v >= 0 && (v == a || v == b);
+            }
+            shared = __ballot_sync(kFull, sh);
+            return v;
         };
         Unit cur;
         walk.next(cur);
         // the block tables are the caller's (no kernel of this library writes
         // them): the first window is in flight during the wait below
         int nxt_base = cur.t0 >> p.log2_block;
-        int nxt_val = load_window(cur, nxt_base);
+        unsigned nxt_sh;
+        int nxt_val = load_window(cur, nxt_base, nxt_sh);
         // the pools as the kernels before this one left them (an append
         // launched just before may still be running: launched as its
         // programmatic dependent, this kernel set itself up meanwhile)
         grid_dependency_wait();
         while (ok) {
             int win_base = nxt_base, win_val = nxt_val;
+            unsigned win_sh = nxt_sh;
             Unit nx;
             const bool has_next = walk.next(nx);
             if (has_next) {
                 // prefetch the first window of this CTA's next unit
                 nxt_base = nx.t0 >> p.log2_block;
-                nxt_val = load_window(nx, nxt_base);
+                nxt_val = load_window(nx, nxt_base, nxt_sh);
             }
             const int h0 = cur.hg << p.log2_hpu;
             for (int i = 0; i < cur.ntiles; ++i) {
@@ -853,10 +882,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 const bool two = (B < kTile) && (tok + B < cur.t1);
                 if (j0 < win_base || j0 + 1 >= win_base + 32) {
                     win_base = j0;
-                    win_val = load_window(cur, j0);
+                    win_val = load_window(cur, j0, win_sh);
                 }
-                int pb0 = __shfl_sync(kFull, win_val, j0 - win_base);
-                int pb1 = __shfl_sync(kFull, win_val, (j0 + 1 - win_base) & 31);
+                const int i0 = j0 - win_base, i1 = (j0 + 1 - win_base) & 31;
+                int pb0 = __shfl_sync(kFull, win_val, i0);
+                int pb1 = __shfl_sync(kFull, win_val, i1);
                 if (lane == 0) {
                     if (*abort_flag || !mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.err)) {
                         ok = false;
@@ -876,8 +906,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             // one box per operand: every slab of H heads x 16 tokens
                             const int z0 = pb0 * B + (tok & (B - 1));
                             mbar_arrive_expect_tx(fb, uint32_t(stage_bytes));
-                            tma_load_4d(kdst, &kmap, 0, z0, 0, h0, fb);
-                            tma_load_4d(vdst, &vmap, 0, z0, 0, h0, fb);
+                            if (hint) {
+                                const uint64_t pol = (win_sh >> i0) & 1u ? pol_shared : pol_own;
+                                tma_load_4d_hint(kdst, &kmap, 0, z0, 0, h0, fb, pol);
+                                tma_load_4d_hint(vdst, &vmap, 0, z0, 0, h0, fb, pol);
+                            } else {
+                                tma_load_4d(kdst, &kmap, 0, z0, 0, h0, fb);
+                                tma_load_4d(vdst, &vmap, 0, z0, 0, h0, fb);
+                            }
                         } else {
                             // 8-token blocks: one box per block and operand (every
                             // slab of H heads x 8 tokens); the second block's box
@@ -887,8 +923,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             for (int b = 0; b < nb; ++b) {
                                 const int z = (b ? pb1 : pb0) * B;
                                 const uint32_t off = uint32_t(b) * uint32_t(half_bytes / 2);
-                                tma_load_4d(kdst + off, &kmap, 0, z, 0, h0, fb);
-                                tma_load_4d(vdst + off, &vmap, 0, z, 0, h0, fb);
+                                if (hint) {
+                                    const uint64_t pol = (win_sh >> (b ? i1 : i0)) & 1u ? pol_shared : pol_own;
+                                    tma_load_4d_hint(kdst + off, &kmap, 0, z, 0, h0, fb, pol);
+                                    tma_load_4d_hint(vdst + off, &vmap, 0, z, 0, h0, fb, pol);
+                                } else {
+                                    tma_load_4d(kdst + off, &kmap, 0, z, 0, h0, fb);
+                                    tma_load_4d(vdst + off, &vmap, 0, z, 0, h0, fb);
+                                }
                             }
                         }
                         ++armed;

@@ -50,6 +50,9 @@ struct DecodeParams {
     const int32_t *group_prefix;  // [num_groups] tokens
     int num_groups;
     int max_members;      // sequences whose queries one prefix unit serves
+    // the K/V loads carry L2 eviction priorities when the call attends over more
+    // tokens than this (0: always; LLONG_MAX: never)
+    long long hint_min_tokens;
 };
 
 // Byte layout of the dynamic shared memory (host and device agree on it).

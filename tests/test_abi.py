@@ -163,6 +163,12 @@ def test_options_round_trip(lib):
     pk.set_option(pk.OPT_STAGES, 3)
     assert pk.get_option(pk.OPT_STAGES) == 3
     pk.set_option(pk.OPT_STAGES, 0)
+    assert pk.get_option(pk.OPT_L2_HINTS) == 0          # automatic by default
+    for mode in (1, 2, 0):
+        pk.set_option(pk.OPT_L2_HINTS, mode)
+        assert pk.get_option(pk.OPT_L2_HINTS) == mode
+    with pytest.raises(pk.PagedKVError):
+        pk.set_option(pk.OPT_L2_HINTS, 3)
 
 
 def test_tensors_must_be_on_the_gpu(lib):

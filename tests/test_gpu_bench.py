@@ -49,3 +49,5 @@ def test_bench_line_keeps_the_contract():
     t = line["targets"]
     for name in ("longctx_splitk", "gqa8b_prefix", "mha7b"):
         assert 0 < t[name]["frac"] < 1.2, name
+        # each call after an L2 flush, between its own events: no faster than back to back
+        assert 0 < t[name]["frac_l2_flushed"] <= t[name]["frac"] * 1.02, name
