@@ -645,7 +645,22 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.max_parts = int(max_parts);
     p.split = split ? 1 : 0;
     p.balanced = balanced ? 1 : 0;
-    p.stages = g_opt_stages ? g_opt_stages : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu, P);
+    // Stage ring. Fixed partitions take the rule of decode_stages. The balanced
+    // split sizes the ring for two stages when even the block tables' full
+    // width of K/V fits in L2 (a small call: shared memory it does not use
+    // costs it launch time); otherwise it holds the short-unit ring and each
+    // CTA falls back to two stages when the mean context is long.
+    const long long token_bytes = 2ll * n_kv_heads * head_dim * elem_bytes(dtype);
+    if (g_opt_stages) {
+        p.stages = p.stages_alt = g_opt_stages;
+    } else if (balanced) {
+        const bool small = (long long)num_seqs * cap <= l2_bytes / token_bytes;
+        p.stages = small ? 2 : pkv::decode_stages(elem_bytes(dtype), head_dim, hpu, pkv::kTile);
+        p.stages_alt = 2;
+    } else {
+        p.stages = p.stages_alt = pkv::decode_stages(elem_bytes(dtype), head_dim, hpu, P);
+    }
+    p.long_seq_tokens = pkv::kLongSeqTokens;
     p.heads_per_unit = hpu;
     p.log2_hpu = hpu == 4 ? 2 : (hpu == 2 ? 1 : 0);
     p.rows_per_box = block_size < pkv::kTile ? block_size : pkv::kTile;
@@ -655,7 +670,6 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     // a shared-prefix unit fills the tensor-core tile's 8 columns with (member, q head) pairs
     p.max_members = (prefix && path == pkv::kPathMma) ? 8 / group : 1;
     // L2 priorities once the call's K/V stream is larger than the L2 (auto)
-    const long long token_bytes = 2ll * n_kv_heads * head_dim * elem_bytes(dtype);
     p.hint_min_tokens = g_opt_l2_hints == 1 ? LLONG_MAX
                       : g_opt_l2_hints == 2 ? 0 : l2_bytes / token_bytes;
 

@@ -681,16 +681,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const sm = smem_raw + (base - raw);
-    const int NS = p.stages;
+    const int NS_cap = p.stages;   // stages the shared memory holds (barriers for all)
     const int S = p.num_seqs;
     const int H = p.heads_per_unit;
     const int TL = kConsumerWarps >> p.log2_hpu;          // consumer warps per kv head
     const int half_bytes = H * G::kHeadBytes;            // K (or V) part of a stage
     const int stage_bytes = 2 * half_bytes;
-    const DecodeSmem lay{stage_bytes, NS, S, D, GM, TL > 1 ? 1 : 0, p.seq_group != nullptr ? 1 : 0};
+    const DecodeSmem lay{stage_bytes, NS_cap, S, D, GM, TL > 1 ? 1 : 0, p.seq_group != nullptr ? 1 : 0};
     const uint32_t full0 = base + lay.bars();
-    const uint32_t empty0 = full0 + 8 * NS;
+    const uint32_t empty0 = full0 + 8 * NS_cap;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + lay.flag());
+    int *ring_stages = reinterpret_cast<int *>(sm + lay.flag() + 4);
     int *seq_base = reinterpret_cast<int *>(sm + lay.seq_base());
     int *seq_len = reinterpret_cast<int *>(sm + lay.seq_len());
     int *seq_p0 = reinterpret_cast<int *>(sm + lay.seq_p0());
@@ -704,7 +705,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int P = p.part_tokens;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NS_cap; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
@@ -809,8 +810,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) kv_tokens += __shfl_xor_sync(kFull, kv_tokens, off);
+        // stages in use: the alternative ring size when the sequences are long
+        // on average (long runs of blocks per unit)
+        if (lane == 0)
+            *ring_stages = kv_tokens >= (long long)p.long_seq_tokens * S ? p.stages_alt : NS_cap;
     }
     __syncthreads();
+    const int NS = *ring_stages;
     Walk walk;
     walk.init(seq_base, seq_len, S, groups, P, p.split, p.balanced, prefix ? seq_p0 : nullptr,
               prefix ? seq_pu : nullptr, p.seq_group, p.max_members);

@@ -15,6 +15,10 @@ constexpr int kTile = 16;                 // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;         // also the largest kv-head group of a unit
 constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
 constexpr int kRowBytes128 = 128;         // width of one swizzled column slab
+// Balanced split: mean context (tokens) from which a call streams long runs of
+// blocks and takes the two-stage ring (measured on GB300: three stages are
+// ahead up to 4K-token means, two from 8K on)
+constexpr int kLongSeqTokens = 6144;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -40,7 +44,9 @@ struct DecodeParams {
     int max_parts;        // partitions per (seq, q head) in the workspace
     int split;            // 1: multi-partition sequences write partition states
     int balanced;         // 1: balanced split (equal tile shares per CTA, pieces merged)
-    int stages;           // ring size (>= 2)
+    int stages;           // ring size the shared memory holds (>= 2)
+    int stages_alt;       // ring size used (<= stages) when the mean context is at least
+    int long_seq_tokens;  // this many tokens
     int heads_per_unit;   // kv heads per unit: 1, 2 or 4 (one consumer warp per head)
     int log2_hpu;
     int rows_per_box;     // tokens per TMA box: min(block_size, kTile)
