@@ -49,8 +49,9 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "decode_params.h", "ptx.cuh", "merge.cu",
 # with the decode's L2 priorities (shared blocks evict_last, the rest
 # evict_first): the MHA layer is fastest with the balanced split (0.992 of the
 # copy peak; 0.925 with 192-token partitions, the best fixed size, before the
-# priorities); the GQA layer with the balanced split too (0.888; 320-token
-# partitions, the best fixed size, 0.875, reported beside it; without the
+# priorities); the GQA layer with the balanced split too (0.944 with its
+# three-stage ring; 320-token partitions, the best fixed size, 0.869-0.882,
+# reported beside it under the shared-prefix entry's figures; without the
 # priorities the balanced split's contiguous shares read each group's shared
 # prefix at times too far apart for L2, 0.787); the long-context workload
 # states its 512-token partitions (0.989; the balanced split is reported
