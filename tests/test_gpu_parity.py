@@ -239,6 +239,33 @@ def test_balanced_split_over_skewed_lengths(orc, ctas):
     assert pk.device_errors() == 0
 
 
+# (name, dtype, q heads, kv heads, lengths low/high, sequences). K/V per token
+# is 4 KiB for 8 kv heads x 128 (bf16) and 16 KiB for 32 x 128 (fp16), so every
+# case's block tables can hold several times the L2's 126 MB: the ring holds
+# three stages. The first two have short mean contexts (all three stages run),
+# the last a mean of about 9,500 tokens (each CTA runs two of the three).
+STAGE_RING_CASES = [
+    ("three_stages_gqa", "bf16", 32, 8, (700, 1400), 48),
+    ("three_stages_mha", "f16", 32, 32, (300, 900), 16),
+    ("two_of_three_long", "bf16", 64, 8, (7000, 12000), 6),
+]
+
+
+@pytest.mark.parametrize("name,dtype,Hq,Hkv,lo_hi,S", STAGE_RING_CASES)
+def test_balanced_split_stage_rings(orc, name, dtype, Hq, Hkv, lo_hi, S):
+    """The balanced split's automatic stage ring, sized on the host from the
+    block tables' width and chosen per CTA from the mean context, against the
+    oracle on every output."""
+    rng = np.random.default_rng(97)
+    lens = rng.integers(lo_hi[0], lo_hi[1], size=S)
+    wl = make_workload(name, dtype, lens, Hq, Hkv, 128, 16, 97)
+    token_bytes = 2 * Hkv * 128 * 2
+    assert S * wl.block_tables.shape[1] * 16 * token_bytes > 129e6   # more than the L2: three stages
+    r = run_both(orc, wl, -1)
+    assert_close(r["out"], r["ref"], dtype, what=f"balanced split, {name}")
+    assert pk.device_errors() == 0
+
+
 @pytest.mark.parametrize("ctas", [1, 8])
 def test_balanced_split_ignores_stale_workspace(orc, ctas):
     """The balanced merge reads only the pieces the decode wrote: a workspace
