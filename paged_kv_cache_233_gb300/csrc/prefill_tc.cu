@@ -8,11 +8,12 @@
 // One CTA owns (sequence, kv head, 256 query rows of (chunk token, query head
 // of the group)), held as two 128-row Q tiles that share every K/V tile.
 // Eleven warps:
-//   warp 0     producer: per 64-key tile, looks up the block ids and issues one
-//              TMA box per (16 keys, 64-column block) for K and V into a
-//              four-stage ring, so that each operand lands as [column block]
-//              [64 keys][128 B] with 128-byte swizzle (the canonical layout the
-//              tensor core reads);
+//   warp 0     producer: per 64-key tile, lane 0 waits for a free stage of a
+//              four-stage ring and arms its barrier; then one lane per (16
+//              keys, 64-column block, operand) looks up its block id and
+//              issues that TMA box, so that each operand lands as [column
+//              block][64 keys][128 B] with 128-byte swizzle (the canonical
+//              layout the tensor core reads);
 //   warps 1,10 MMA issuers, one per Q tile (warp 1 also allocates tensor
 //              memory); lane 0 issues, for its tile, S = Q K^T into one of two
 //              S buffers in tensor memory and, once the softmax has written P,
@@ -178,61 +179,64 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Lane 0 waits for a free stage and arms its barrier with the tile's
+        // bytes; then one lane per (box, column block, operand) issues that copy
+        // (a single thread issuing all of a tile's copies took about 100 cycles
+        // each, most of a key tile's period at D = 128).
         if (lane == 0) {
             tma_prefetch_descriptor(&kmap);
             tma_prefetch_descriptor(&vmap);
-            // the pools as the kernels before this one left them (launched as
-            // the programmatic dependent of an append that may still be running)
-            grid_dependency_wait();
-            const int32_t *table = p.block_tables + size_t(s) * p.max_blocks;
-            int armed = 0;
-            bool ok = true;
-            for (int j = 0; j < nkt; ++j) {
-                const int st = j % kTcStages;
-                const int k0 = j * kTcKeys;
-                const int present = min(kTcKeys, L - k0);
-                // every block id of the tile first, while the slot may still be
-                // busy (independent loads in flight together), then the copies
-                const int rows_per_box = B >= 16 ? 16 : 8;
-                const int boxes = (present + rows_per_box - 1) / rows_per_box;
-                int pbs[kTcKeys / 8];
-#pragma unroll
-                for (int i = 0; i < kTcKeys / 8; ++i)
-                    pbs[i] = i < boxes ? __ldg(table + ((k0 + rows_per_box * i) >> p.log2_block)) : 0;
-                if (*abort_flag ||
-                    !mbar_wait(bar(kKvEmpty + st), uint32_t((j / kTcStages) & 1) ^ 1u, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t kdst = base + Ly::kKv + st * Ly::kStage;
-                const uint32_t vdst = kdst + Ly::kHalf;
-                const uint32_t fb = bar(kKvFull + st);
-                mbar_arrive_expect_tx(fb, uint32_t(boxes * Ly::kSlabs * rows_per_box * 128 * 2));
-#pragma unroll
-                for (int i = 0; i < kTcKeys / 8; ++i) {
-                    if (i >= boxes) break;
-                    const int tok = k0 + rows_per_box * i;
-                    int pb = pbs[i];
-                    if (pb < 0 || pb >= p.num_blocks) {
-                        atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
-                        pb = 0;
-                    }
-                    const int z = pb * B + (tok & (B - 1));
-                    for (int sl = 0; sl < Ly::kSlabs; ++sl) {
-                        const uint32_t off = sl * Ly::kKvSlab + i * rows_per_box * 128;
-                        tma_load_4d(kdst + off, &kmap, 0, z, sl, h, fb);
-                        tma_load_4d(vdst + off, &vmap, 0, z, sl, h, fb);
-                    }
-                }
-                ++armed;
+        }
+        // the pools as the kernels before this one left them (launched as
+        // the programmatic dependent of an append that may still be running)
+        grid_dependency_wait();
+        const int32_t *table = p.block_tables + size_t(s) * p.max_blocks;
+        const int rows_per_box = B >= 16 ? 16 : 8;
+        // this lane's copy: box i (rows_per_box keys), column block sl, operand op
+        constexpr int kCopies = 2 * Ly::kSlabs;              // per box
+        const int ci = lane / kCopies, csl = (lane / 2) % Ly::kSlabs, cop = lane & 1;
+        int armed = 0;
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            const int st = j % kTcStages;
+            const int k0 = j * kTcKeys;
+            const int present = min(kTcKeys, L - k0);
+            const int boxes = (present + rows_per_box - 1) / rows_per_box;
+            const bool mine = ci < boxes && ci < kTcKeys / 8;
+            // the lane's block id first, while the slot may still be busy
+            int pb = mine ? __ldg(table + ((k0 + rows_per_box * ci) >> p.log2_block)) : 0;
+            bool got = true;
+            if (lane == 0) {
+                got = !*abort_flag &&
+                      mbar_wait(bar(kKvEmpty + st), uint32_t((j / kTcStages) & 1) ^ 1u, p.err);
+                if (got)
+                    mbar_arrive_expect_tx(bar(kKvFull + st),
+                                          uint32_t(boxes * Ly::kSlabs * rows_per_box * 128 * 2));
             }
-            if (!ok) {
-                // stop everyone, then wait (bounded) for this CTA's copies still in flight
-                *abort_flag = 1;
-                const int first = armed > kTcStages ? armed - kTcStages : 0;
-                for (int k = first; k < armed; ++k)
-                    mbar_wait(bar(kKvFull + k % kTcStages), uint32_t((k / kTcStages) & 1), p.err);
+            // the arming is ordered before every lane's copy by the warp barrier
+            __syncwarp();
+            if (!__shfl_sync(kAll, got ? 1 : 0, 0)) {
+                ok = false;
+                break;
             }
+            if (mine) {
+                if (pb < 0 || pb >= p.num_blocks) {
+                    atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
+                    pb = 0;
+                }
+                const int z = pb * B + ((k0 + rows_per_box * ci) & (B - 1));
+                const uint32_t dst = base + Ly::kKv + st * Ly::kStage + uint32_t(cop) * Ly::kHalf +
+                                     csl * Ly::kKvSlab + ci * rows_per_box * 128;
+                tma_load_4d(dst, cop ? &vmap : &kmap, 0, z, csl, h, bar(kKvFull + st));
+            }
+            ++armed;
+        }
+        if (!ok && lane == 0) {
+            // stop everyone, then wait (bounded) for this CTA's copies still in flight
+            *abort_flag = 1;
+            const int first = armed > kTcStages ? armed - kTcStages : 0;
+            for (int k = first; k < armed; ++k)
+                mbar_wait(bar(kKvFull + k % kTcStages), uint32_t((k / kTcStages) & 1), p.err);
         }
         __syncwarp();
     } else if (warp == 1 || warp == kIssuer1Warp) {
@@ -289,6 +293,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     if (!ok) break;
                     tc_fence_after_sync();
                     issue_pv(j);
+                    // the stage of key tile j is free once this P V (the last MMA of
+                    // this thread that reads it) completes: release it before this
+                    // thread blocks on issuing the next S, so that the producer
+                    // refills it a whole S earlier
+                    tc_commit(bar(kKvEmpty + j % kTcStages));
                     // this tile's S two key tiles ahead (its S buffer j & 1 is free
                     // once the P V just issued has read P)
                     if (j + 2 < nk) {
@@ -302,8 +311,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     // after it landed (the arrival belongs to this phase of the slot)
                     ok = wait(kKvFull + j % kTcStages, j / kTcStages);
                     if (!ok) break;
+                    tc_commit(bar(kKvEmpty + j % kTcStages));
                 }
-                tc_commit(bar(kKvEmpty + j % kTcStages));
             }
             if (!ok) *abort_flag = 1;
             // every MMA of both issuers has completed before tensor memory is freed
