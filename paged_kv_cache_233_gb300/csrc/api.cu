@@ -510,7 +510,7 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     p.log2_block = log2_block;
     p.max_blocks = max_blocks_per_seq;
     const cudaError_t e =
-        tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, p, max_query_len,
+        tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, p, max_query_len, sms,
                                     static_cast<cudaStream_t>(stream))
            : pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
                                  static_cast<cudaStream_t>(stream));

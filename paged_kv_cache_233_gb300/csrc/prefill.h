@@ -36,17 +36,17 @@ struct PrefillParams {
 // Bytes of dynamic shared memory the kernel asks for at this head_dim (16-bit types).
 int prefill_smem_bytes(int head_dim);
 
-// Grid: (query tiles of the longest chunk, kv heads, sequences). The warp-level
-// MMA kernel takes 64 query rows per CTA and pool maps with boxes of every
-// column block; the tcgen05 kernel takes 256 rows per CTA and pool maps with
-// boxes of one 64-column block.
+// The warp-level MMA kernel: grid (query tiles of the longest chunk, kv heads,
+// sequences), 64 query rows per CTA, pool maps with boxes of every column
+// block. The tcgen05 kernel: one persistent CTA per SM working through items
+// of 256 rows, pool maps with boxes of one 64-column block.
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
                            cudaStream_t stream);
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
-                              cudaStream_t stream);
+                              int num_sms, cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
 constexpr int kPfTcRows = 256;   // query rows per CTA of the tcgen05 kernel (two tiles of 128)

@@ -5,9 +5,13 @@
 // to its own position, read through the block table), with the contractions
 // moved off the warp-level MMA pipe.
 //
-// One CTA owns (sequence, kv head, 256 query rows of (chunk token, query head
-// of the group)), held as two 128-row Q tiles that share every K/V tile.
-// Eleven warps:
+// A work item is (sequence, kv head, 256 query rows of (chunk token, query
+// head of the group)), held as two 128-row Q tiles that share every K/V tile.
+// The kernel is persistent: one CTA per SM works through its share of the
+// items (sequences ranked by context length, dealt in bands whose direction
+// alternates), and every ring, buffer and barrier phase runs on across items,
+// so that an item's Q load, first K/V tiles and first S MMAs overlap the
+// previous item's last P V and epilogue. Twelve warps:
 //   warp 0     producer: per 64-key tile, lane 0 waits for a free stage of a
 //              four-stage ring and arms its barrier; then one lane per (16
 //              keys, 64-column block, operand) looks up its block id and
@@ -34,8 +38,14 @@
 //              than 2^8 (P stays below 256, sums stay in fp32); when it moves,
 //              the warp rescales its rows of O in tensor memory before that
 //              tile's P V may start. The result is exact softmax attention.
-//              V rows past the context are zeroed in shared memory before any
-//              P V reads them (the tensor core would turn 0 * NaN into NaN).
+//              A tile's warps load the next item's Q rows once every S of the
+//              item before has completed, then write out that item's rows
+//              from O and release O for the next item's first P V;
+//   warp 11    zeroes the V rows past a context (below).
+// V rows past the context are zeroed in shared memory before any P V reads
+// them (the tensor core would turn 0 * NaN into NaN): the V copies of a
+// context's last key tile land on a per-stage barrier of their own, and a
+// twelfth warp zeroes those rows and only then completes the stage.
 // A Q tile skips the key tiles that lie wholly past its last row. Every
 // mbarrier wait is bounded in time; on a timeout the CTA stops, waits for its
 // copies and MMAs in flight, frees its tensor memory and exits.
@@ -57,11 +67,38 @@ constexpr int kTcRows = 128;     // query rows per Q tile = tensor-memory lanes
 constexpr int kTcKeys = 64;      // keys per pipeline stage
 constexpr int kTcStages = 4;
 // warp 0 producer, warp 1 MMA issuer of Q tile 0, warps 2-9 softmax, warp 10
-// MMA issuer of Q tile 1
+// MMA issuer of Q tile 1, warp 11 zeroes the V rows past a context
 constexpr int kIssuer1Warp = 2 + kTcTiles * kTcRows / 32;
-constexpr int kTcThreads = 32 * (kIssuer1Warp + 1);
+constexpr int kZeroWarp = kIssuer1Warp + 1;
+constexpr int kTcThreads = 32 * (kZeroWarp + 1);
 constexpr int kTmemTile = 256;   // tensor-memory columns per Q tile: S, S, O
 constexpr float kRescaleLog2 = 8.f;  // the reference maximum moves past 2^8
+
+// mbarrier indices
+constexpr int kKvFull = 0;
+constexpr int kKvEmpty = kTcStages;
+// per Q tile t: S full, P full and O full per buffer b (P V of key tile j
+// completes on O barrier j & 1, so a wait never meets a barrier two
+// completions away); Q full (the tile's softmax warps stored an item's Q
+// rows), Q free (every S MMA of the item, the readers of Q, has completed) and
+// O free (the softmax warps have read the item's O out of tensor memory)
+constexpr int kPerTileBars = 9;
+__device__ __forceinline__ int bar_s(int t, int b) { return 2 * kTcStages + kPerTileBars * t + b; }
+__device__ __forceinline__ int bar_p(int t, int b) { return 2 * kTcStages + kPerTileBars * t + 2 + b; }
+__device__ __forceinline__ int bar_o(int t, int b) { return 2 * kTcStages + kPerTileBars * t + 4 + b; }
+__device__ __forceinline__ int bar_qfull(int t) { return 2 * kTcStages + kPerTileBars * t + 6; }
+__device__ __forceinline__ int bar_qfree(int t) { return 2 * kTcStages + kPerTileBars * t + 7; }
+__device__ __forceinline__ int bar_ofree(int t) { return 2 * kTcStages + kPerTileBars * t + 8; }
+constexpr int kDone = 2 * kTcStages + kPerTileBars * kTcTiles;
+// per stage: the V copies of a context's last key tile land here first; the
+// zeroing warp clears the V rows past the context, then completes the stage
+// (one phase per such use of the stage: it is not reused before the stage
+// completes and both issuers have released it)
+constexpr int kTailV = kDone + 1;
+constexpr int kNumBars = kTailV + kTcStages;
+// sequences ranked by context length in shared memory (beyond this count the
+// items keep the sequences' own order)
+constexpr int kMaxRankedSeqs = 256;
 
 template <int D>
 struct TcLayout {
@@ -74,30 +111,91 @@ struct TcLayout {
     static constexpr int kHalf = kSlabs * kKvSlab;
     static constexpr int kStage = 2 * kHalf;
     static constexpr int kBars = kKv + kTcStages * kStage;
-    static constexpr int kNumBars = 2 * kTcStages + 6 * kTcTiles + 3;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
-    static constexpr int kTotal = kFlag + 8;
+    static constexpr int kOrder = kFlag + 8;               // ranked sequence ids, then their lengths
+    // per softmax thread, the output row of its item (kept here through the key loop)
+    static constexpr int kOutRow = kOrder + 8 * kMaxRankedSeqs;
+    static constexpr int kTotal = kOutRow + 8 * kTcTiles * kTcRows;
     static_assert(2 * kTcKeys + D <= kTmemTile, "S buffers and O must fit a Q tile's columns");
 };
-
-// mbarrier indices
-constexpr int kKvFull = 0;
-constexpr int kKvEmpty = kTcStages;
-// per Q tile t, buffer b: S full, P full, O full (P V of key tile j completes
-// on O barrier j & 1, so a wait never meets a barrier two completions away)
-__device__ __forceinline__ int bar_s(int t, int b) { return 2 * kTcStages + 6 * t + b; }
-__device__ __forceinline__ int bar_p(int t, int b) { return 2 * kTcStages + 6 * t + 2 + b; }
-__device__ __forceinline__ int bar_o(int t, int b) { return 2 * kTcStages + 6 * t + 4 + b; }
-constexpr int kQFull = 2 * kTcStages + 6 * kTcTiles;
-constexpr int kDone = kQFull + 1;
-// the last key tile's V rows past the context are zeroed (one phase per CTA,
-// so a wait on it is never ambiguous however far the Q tiles drift apart)
-constexpr int kVZero = kDone + 1;
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                  ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Shared-memory word at a 32-bit shared address (a generic pointer would hold
+// two registers through the softmax warps' loops).
+__device__ __forceinline__ int lds32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, int v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// One work item: (sequence, kv head, query tile of tile_tokens chunk tokens =
+// 256 rows of (chunk token, query head of the group)), held as two Q tiles.
+struct PfItem {
+    int s, h;
+    int q0, j0, rows, pos0, L;
+    int nk[kTcTiles];   // key tiles of Q tile t: through the position of its last row
+    int nkt;            // key tiles of the item (those of its last row)
+    bool tail;          // the last key tile runs past the context
+};
+
+// Items in one order shared by every CTA: sequences by decreasing context
+// length (ranked, when there are few enough), within a sequence its query
+// tiles from the last (the most keys), then kv heads, so that the items that
+// read a sequence's K/V run close together in time and share it through L2.
+// Item k of that order. Returns false for an item with no rows, or a sequence
+// whose chunk or length is invalid (reported once per sequence when `report`).
+__device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked, int tiles, int k,
+                                        bool report, PfItem &it) {
+    const int per_seq = tiles * p.n_kv_heads;
+    const int r = k / per_seq;
+    const int rem = k - r * per_seq;
+    const int s = ranked ? lds32(ranked + 4u * uint32_t(r)) : r;
+    const int qt = tiles - 1 - rem / p.n_kv_heads;
+    const int h = rem - (rem / p.n_kv_heads) * p.n_kv_heads;
+    const int q0 = __ldg(p.query_start + s);
+    const int q1 = __ldg(p.query_start + s + 1);
+    const int n = q1 - q0;
+    const int L = __ldg(p.context_lens + s);
+    const bool rows_ok = q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens && n <= tiles * p.tile_tokens;
+    const bool len_ok = L >= n && L <= p.max_blocks * p.block_size;
+    if (!rows_ok || !len_ok) {
+        if (report && qt == tiles - 1 && h == 0)
+            atomicOr(p.err, rows_ok ? PAGEDKV_DEVERR_CONTEXT_LEN : PAGEDKV_DEVERR_POSITION);
+        return false;
+    }
+    const int j0 = qt * p.tile_tokens;
+    if (j0 >= n) return false;
+    it.s = s;
+    it.h = h;
+    it.q0 = q0;
+    it.j0 = j0;
+    it.L = L;
+    it.rows = min(p.tile_tokens, n - j0) * p.group;
+    it.pos0 = L - n + j0;
+#pragma unroll
+    for (int t = 0; t < kTcTiles; ++t) {
+        const int rt = min(max(it.rows - t * kTcRows, 0), kTcRows);
+        it.nk[t] = rt > 0 ? (it.pos0 + (t * kTcRows + rt - 1) / p.group) / kTcKeys + 1 : 0;
+    }
+    it.nkt = it.nk[kTcTiles - 1] > 0 ? it.nk[kTcTiles - 1] : it.nk[0];
+    it.tail = it.nkt * kTcKeys > L;
+    return true;
+}
+
+// This CTA's m-th item: bands of gridDim.x items, dealt forwards in even bands
+// and backwards in odd ones (so that every CTA gets a similar share of the
+// ranked work). The item count fits an int (the launcher checks).
+__device__ __forceinline__ int pf_item_index(int m) {
+    const int G = int(gridDim.x), c = int(blockIdx.x);
+    return m * G + ((m & 1) ? G - 1 - c : c);
 }
 
 }  // namespace
@@ -105,72 +203,68 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p, int tiles) {
     using Ly = TcLayout<D>;
     constexpr bool kBf16 = Elem<T>::kBf16;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const sm = smem_raw + (base - raw);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Ly::kFlag);
+    const uint32_t flag = base + Ly::kFlag;   // the abort flag
+    auto aborted = [&]() { return lds32(flag) != 0; };
     auto bar = [&](int i) { return base + Ly::kBars + 8u * uint32_t(i); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int s = blockIdx.z;
-    const int h = blockIdx.y;
-    const int qt = int(gridDim.x) - 1 - int(blockIdx.x);   // tiles with the most keys first
     const int B = p.block_size;
     const int g = p.group;
-
-    // ---- this CTA's slice of the chunk (uniform across the CTA)
-    const int q0 = __ldg(p.query_start + s);
-    const int q1 = __ldg(p.query_start + s + 1);
-    const int n = q1 - q0;
-    const int L = __ldg(p.context_lens + s);
-    const bool rows_ok = q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens &&
-                         n <= int(gridDim.x) * p.tile_tokens;
-    const bool len_ok = L >= n && L <= p.max_blocks * B;
-    if (!rows_ok || !len_ok) {
-        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0)
-            atomicOr(p.err, rows_ok ? PAGEDKV_DEVERR_CONTEXT_LEN : PAGEDKV_DEVERR_POSITION);
-        return;
-    }
-    const int j0 = qt * p.tile_tokens;
-    if (j0 >= n) return;
-    const int rows = min(p.tile_tokens, n - j0) * g;   // rows of the CTA (both Q tiles)
-    const int pos0 = L - n + j0;                       // position of the CTA's first token
-    // key tiles of Q tile t: through the position of its last row
-    auto key_tiles = [&](int t) {
-        const int rt = min(max(rows - t * kTcRows, 0), kTcRows);
-        return rt > 0 ? (pos0 + (t * kTcRows + rt - 1) / g) / kTcKeys + 1 : 0;
-    };
-    const int nk0 = key_tiles(0), nk1 = key_tiles(1);
-    auto nkt_of = [&](int t) { return t ? nk1 : nk0; };
-    const int t_last = nk1 > 0 ? 1 : 0;                // holds the CTA's last row
-    const int nkt = t_last ? nk1 : nk0;
-    const bool tail = nkt * kTcKeys > L;               // the last key tile runs past the context
+    const int num_items = p.num_seqs * tiles * p.n_kv_heads;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kTcStages; ++k) {
             mbar_init(bar(kKvFull + k), 1);
             mbar_init(bar(kKvEmpty + k), kTcTiles);   // one commit per issuer and key tile
         }
-        for (int t = 0; t < kTcTiles; ++t)
+        for (int t = 0; t < kTcTiles; ++t) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(bar(bar_s(t, b)), 1);
                 mbar_init(bar(bar_p(t, b)), kTcRows / 32);   // one arrival per softmax warp
                 mbar_init(bar(bar_o(t, b)), 1);
             }
-        mbar_init(bar(kQFull), kTcTiles * kTcRows / 32);
+            mbar_init(bar(bar_qfull(t)), kTcRows / 32);
+            mbar_init(bar(bar_qfree(t)), 1);
+            mbar_init(bar(bar_ofree(t)), kTcRows / 32);
+        }
         mbar_init(bar(kDone), kTcTiles);
-        mbar_init(bar(kVZero), kTcRows / 32);
-        *abort_flag = 0;
+        for (int k = 0; k < kTcStages; ++k) mbar_init(bar(kTailV + k), 1);
+        sts32(flag, 0);
         fence_barrier_init();
     }
     if (warp == 1) {
         tmem_alloc(base + Ly::kTmemSlot, kTcTiles * kTmemTile);
         tmem_relinquish();
+    }
+    // sequences ranked by decreasing context length (ties by index); the
+    // lengths are the caller's, read before any grid dependency
+    // sequences ranked by decreasing context length (ties by index), when some
+    // CTA gets more than one item; the lengths are the caller's, read before
+    // any grid dependency
+    uint32_t ranked = 0;   // shared address of the ranked sequence ids (0: natural order)
+    if (p.num_seqs > 1 && p.num_seqs <= kMaxRankedSeqs && num_items > int(gridDim.x)) {
+        ranked = base + Ly::kOrder;
+        int *ids = reinterpret_cast<int *>(sm + Ly::kOrder);
+        int *lens = ids + kMaxRankedSeqs;
+        for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) lens[s] = __ldg(p.context_lens + s);
+        __syncthreads();
+        for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+            const int Ls = lens[s];
+            int rank = 0;
+            for (int u = 0; u < p.num_seqs; ++u) {
+                const int Lu = lens[u];
+                rank += (Lu > Ls || (Lu == Ls && u < s)) ? 1 : 0;
+            }
+            ids[rank] = s;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -179,10 +273,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Lane 0 waits for a free stage and arms its barrier with the tile's
-        // bytes; then one lane per (box, column block, operand) issues that copy
-        // (a single thread issuing all of a tile's copies took about 100 cycles
-        // each, most of a key tile's period at D = 128).
+        // Per key tile, lane 0 waits for a free stage and arms its barrier;
+        // then one lane per (box, column block, operand) issues that copy (a
+        // single thread issuing all of a tile's copies took about 100 cycles
+        // each, most of a key tile's period at D = 128). Stages run on across
+        // the CTA's items, so the next item's first tiles load while the
+        // current one finishes.
         if (lane == 0) {
             tma_prefetch_descriptor(&kmap);
             tma_prefetch_descriptor(&vmap);
@@ -190,54 +286,114 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // the pools as the kernels before this one left them (launched as
         // the programmatic dependent of an append that may still be running)
         grid_dependency_wait();
-        const int32_t *table = p.block_tables + size_t(s) * p.max_blocks;
         const int rows_per_box = B >= 16 ? 16 : 8;
-        // this lane's copy: box i (rows_per_box keys), column block sl, operand op
+        // this lane's copy: box ci (rows_per_box keys), column block csl, operand cop
         constexpr int kCopies = 2 * Ly::kSlabs;              // per box
         const int ci = lane / kCopies, csl = (lane / 2) % Ly::kSlabs, cop = lane & 1;
+        int kt = 0;          // key tiles armed before this item (position in the ring)
         int armed = 0;
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            const int st = j % kTcStages;
-            const int k0 = j * kTcKeys;
-            const int present = min(kTcKeys, L - k0);
-            const int boxes = (present + rows_per_box - 1) / rows_per_box;
-            const bool mine = ci < boxes && ci < kTcKeys / 8;
-            // the lane's block id first, while the slot may still be busy
-            int pb = mine ? __ldg(table + ((k0 + rows_per_box * ci) >> p.log2_block)) : 0;
-            bool got = true;
-            if (lane == 0) {
-                got = !*abort_flag &&
-                      mbar_wait(bar(kKvEmpty + st), uint32_t((j / kTcStages) & 1) ^ 1u, p.err);
-                if (got)
-                    mbar_arrive_expect_tx(bar(kKvFull + st),
-                                          uint32_t(boxes * Ly::kSlabs * rows_per_box * 128 * 2));
-            }
-            // the arming is ordered before every lane's copy by the warp barrier
-            __syncwarp();
-            if (!__shfl_sync(kAll, got ? 1 : 0, 0)) {
-                ok = false;
-                break;
-            }
-            if (mine) {
-                if (pb < 0 || pb >= p.num_blocks) {
-                    atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
-                    pb = 0;
+        for (int m = 0; ok; ++m) {
+            const int k = pf_item_index(m);
+            if (k >= num_items) break;
+            PfItem it;
+            if (!pf_item(p, ranked, tiles, k, lane == 0, it)) continue;
+            const int32_t *table = p.block_tables + size_t(it.s) * p.max_blocks;
+            for (int j = 0; j < it.nkt; ++j) {
+                const int gk = kt + j;
+                const int st = gk % kTcStages;
+                const int k0 = j * kTcKeys;
+                const int present = min(kTcKeys, it.L - k0);
+                const int boxes = (present + rows_per_box - 1) / rows_per_box;
+                const bool last_tail = it.tail && j == it.nkt - 1;
+                const bool mine = ci < boxes && ci < kTcKeys / 8;
+                // the lane's block id first, while the slot may still be busy
+                int pb = mine ? __ldg(table + ((k0 + rows_per_box * ci) >> p.log2_block)) : 0;
+                const uint32_t half = uint32_t(boxes * Ly::kSlabs * rows_per_box * 128);
+                bool got = true;
+                if (lane == 0) {
+                    got = !aborted() &&
+                          mbar_wait(bar(kKvEmpty + st), uint32_t((gk / kTcStages) & 1) ^ 1u, p.err);
+                    if (got && !last_tail) {
+                        mbar_arrive_expect_tx(bar(kKvFull + st), 2 * half);
+                    } else if (got) {
+                        // K completes on the stage's barrier, whose arrival comes from
+                        // the zeroing warp once the V rows past the context are zero;
+                        // V lands on the stage's tail barrier
+                        mbar_expect_tx(bar(kKvFull + st), half);
+                        mbar_arrive_expect_tx(bar(kTailV + st), half);
+                    }
                 }
-                const int z = pb * B + ((k0 + rows_per_box * ci) & (B - 1));
-                const uint32_t dst = base + Ly::kKv + st * Ly::kStage + uint32_t(cop) * Ly::kHalf +
-                                     csl * Ly::kKvSlab + ci * rows_per_box * 128;
-                tma_load_4d(dst, cop ? &vmap : &kmap, 0, z, csl, h, bar(kKvFull + st));
+                // the arming is ordered before every lane's copy by the warp barrier
+                __syncwarp();
+                if (!__shfl_sync(kAll, got ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (mine) {
+                    if (pb < 0 || pb >= p.num_blocks) {
+                        atomicOr(p.err, PAGEDKV_DEVERR_BLOCK_ID);
+                        pb = 0;
+                    }
+                    const int z = pb * B + ((k0 + rows_per_box * ci) & (B - 1));
+                    const uint32_t dst = base + Ly::kKv + st * Ly::kStage + uint32_t(cop) * Ly::kHalf +
+                                         csl * Ly::kKvSlab + ci * rows_per_box * 128;
+                    const uint32_t done = (cop && last_tail) ? bar(kTailV + st) : bar(kKvFull + st);
+                    tma_load_4d(dst, cop ? &vmap : &kmap, 0, z, csl, it.h, done);
+                }
+                ++armed;
             }
-            ++armed;
+            kt += it.nkt;
         }
         if (!ok && lane == 0) {
             // stop everyone, then wait (bounded) for this CTA's copies still in flight
-            *abort_flag = 1;
+            // (a tail stage completes only with the zeroing warp's arrival: when that
+            // warp stopped too, the wait ends at its time limit, its copies long done)
+            sts32(flag, 1);
             const int first = armed > kTcStages ? armed - kTcStages : 0;
-            for (int k = first; k < armed; ++k)
-                mbar_wait(bar(kKvFull + k % kTcStages), uint32_t((k / kTcStages) & 1), p.err);
+            for (int x = first; x < armed; ++x)
+                mbar_wait(bar(kKvFull + x % kTcStages), uint32_t((x / kTcStages) & 1), p.err);
         }
+        __syncwarp();
+    } else if (warp == kZeroWarp) {
+        // ------------------------------------------------------------ V tail
+        // V rows past a context (never written for the sequence, or left in the
+        // stage by an earlier tile) become zeros once the tile's V copies have
+        // landed: the tensor core would turn 0 * NaN into NaN. Then the stage is
+        // complete (its K copies may still be landing). The issuers reach that
+        // tile's S two key tiles ahead of its P V, which hides the wait.
+        int kt = 0;
+        uint32_t parity = 0;   // bit st: phase parity of stage st's tail barrier
+        bool ok = true;
+        for (int m = 0; ok; ++m) {
+            const int k = pf_item_index(m);
+            if (k >= num_items) break;
+            PfItem it;
+            if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+            if (it.tail) {
+                const int st = (kt + it.nkt - 1) % kTcStages;
+                const int present = it.L - (it.nkt - 1) * kTcKeys;
+                bool got = true;
+                if (lane == 0)
+                    got = !aborted() && mbar_wait(bar(kTailV + st), (parity >> st) & 1u, p.err);
+                if (!__shfl_sync(kAll, got ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                parity ^= 1u << st;
+                const uint32_t vbase = base + Ly::kKv + st * Ly::kStage + Ly::kHalf;
+                for (int x = lane; x < (kTcKeys - present) * Ly::kSlabs * 8; x += 32) {
+                    const int r = present + x / (Ly::kSlabs * 8);
+                    const int sl = (x / 8) % Ly::kSlabs;
+                    sts128(vbase + sl * Ly::kKvSlab + r * 128 + (x & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kKvFull + st));
+            }
+            kt += it.nkt;
+        }
+        if (!ok && lane == 0) sts32(flag, 1);
         __syncwarp();
     } else if (warp == 1 || warp == kIssuer1Warp) {
         // ------------------------------------------------------- MMA issuers
@@ -247,74 +403,105 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // per tile, one tile's MMAs go in while the other's issuer waits.
         if (lane == 0) {
             const int t = warp == 1 ? 0 : 1;
-            const int nk = nkt_of(t);
             constexpr uint32_t kIdS = tc_idesc_f16(kBf16, false, kTcRows, kTcKeys);
             constexpr uint32_t kIdO = tc_idesc_f16(kBf16, true, kTcRows, D);
             auto wait = [&](int i, int phase) {
-                return !*abort_flag && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
+                return !aborted() && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
             };
             const uint32_t qb = base + Ly::kQ + t * Ly::kQTile;
-            auto issue_s = [&](int j) {
-                const uint32_t kb = base + Ly::kKv + (j % kTcStages) * Ly::kStage;
-                const uint32_t d = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
+            // S of key tile gk of the ring (gj-th key tile of this Q tile) into S buffer gj & 1
+            auto issue_s = [&](int gk, int gj) {
+                const uint32_t kb = base + Ly::kKv + (gk % kTcStages) * Ly::kStage;
+                const uint32_t d = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t a = tc_desc_sw128(qb + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc_desc_sw128(kb + (kk >> 2) * Ly::kKvSlab + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16(d, a, b, kIdS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(bar_s(t, j & 1)));
+                tc_commit(bar(bar_s(t, gj & 1)));
             };
-            auto issue_pv = [&](int j) {
-                const uint32_t vb = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf;
-                // P of key tile j: the first 32 columns of S buffer j & 1 (16 keys per 8 columns)
-                const uint32_t pa = tmem + uint32_t(t * kTmemTile + (j & 1) * kTcKeys);
+            // O (+)= P V; `first` starts the item's accumulator
+            auto issue_pv = [&](int gk, int gj, bool first) {
+                const uint32_t vb = base + Ly::kKv + (gk % kTcStages) * Ly::kStage + Ly::kHalf;
+                // P: the first 32 columns of S buffer gj & 1 (16 keys per 8 columns)
+                const uint32_t pa = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
-                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), b, kIdO, (!first || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(bar_o(t, j & 1)));
+                tc_commit(bar(bar_o(t, gj & 1)));
             };
-            bool ok = wait(kQFull, 0);
-            for (int j = 0; ok && j < 2 && j < nk; ++j) {
-                ok = wait(kKvFull + j % kTcStages, j / kTcStages);
+            int kt = 0;   // ring position of the item's first key tile
+            int jt = 0;   // key tiles of this Q tile before the item (S, P and O barrier phases)
+            int i = 0;    // items so far
+            bool ok = true;
+            for (int m = 0; ok; ++m) {
+                const int k = pf_item_index(m);
+                if (k >= num_items) break;
+                PfItem it;
+                if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+                const int nk = it.nk[t];
+                // the item's Q rows of this tile are in shared memory
+                ok = wait(bar_qfull(t), i);
                 if (!ok) break;
-                tc_fence_after_sync();
-                issue_s(j);
-            }
-            for (int j = 0; ok && j < nkt; ++j) {
-                if (j < nk) {
-                    // the last key tile's V rows past the context are zeroed by the
-                    // last Q tile's softmax: no P V may read that tile before
-                    if (tail && j == nkt - 1) ok = wait(kVZero, 0);
-                    if (ok) ok = wait(bar_p(t, j & 1), j >> 1);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    issue_pv(j);
-                    // the stage of key tile j is free once this P V (the last MMA of
-                    // this thread that reads it) completes: release it before this
-                    // thread blocks on issuing the next S, so that the producer
-                    // refills it a whole S earlier
-                    tc_commit(bar(kKvEmpty + j % kTcStages));
-                    // this tile's S two key tiles ahead (its S buffer j & 1 is free
-                    // once the P V just issued has read P)
-                    if (j + 2 < nk) {
-                        ok = wait(kKvFull + (j + 2) % kTcStages, (j + 2) / kTcStages);
+                if (nk > 0) {
+                    for (int j = 0; ok && j < 2 && j < nk; ++j) {
+                        ok = wait(kKvFull + (kt + j) % kTcStages, (kt + j) / kTcStages);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        issue_s(j + 2);
+                        issue_s(kt + j, jt + j);
                     }
-                } else {
-                    // a key tile this Q tile skips: its stage may be released only
-                    // after it landed (the arrival belongs to this phase of the slot)
-                    ok = wait(kKvFull + j % kTcStages, j / kTcStages);
                     if (!ok) break;
-                    tc_commit(bar(kKvEmpty + j % kTcStages));
+                    // Q may be overwritten once the item's last S has completed
+                    if (nk <= 2) tc_commit(bar(bar_qfree(t)));
                 }
+                for (int j = 0; ok && j < it.nkt; ++j) {
+                    const int gk = kt + j;
+                    if (j < nk) {
+                        ok = wait(bar_p(t, (jt + j) & 1), (jt + j) >> 1);
+                        // the first P V of the item starts O afresh: the previous
+                        // item's O must have been read out first
+                        if (ok && j == 0 && i > 0) ok = wait(bar_ofree(t), i - 1);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        issue_pv(gk, jt + j, j == 0);
+                        // the stage of key tile j is free once this P V (the last MMA of
+                        // this thread that reads it) completes: release it before this
+                        // thread blocks on issuing the next S
+                        tc_commit(bar(kKvEmpty + gk % kTcStages));
+                        // this tile's S two key tiles ahead (its S buffer is free once the
+                        // P V just issued has read P)
+                        if (j + 2 < nk) {
+                            ok = wait(kKvFull + (gk + 2) % kTcStages, (gk + 2) / kTcStages);
+                            if (!ok) break;
+                            tc_fence_after_sync();
+                            issue_s(gk + 2, jt + j + 2);
+                            if (j + 2 == nk - 1) tc_commit(bar(bar_qfree(t)));
+                        }
+                    } else {
+                        // a key tile this Q tile skips: its stage may be released only
+                        // after it landed (the arrival belongs to this phase of the slot)
+                        ok = wait(kKvFull + gk % kTcStages, gk / kTcStages);
+                        if (!ok) break;
+                        tc_commit(bar(kKvEmpty + gk % kTcStages));
+                    }
+                }
+                if (!ok) break;
+                if (nk == 0) {
+                    // no MMA of this tile reads Q or writes O in this item: keep the
+                    // barriers' phases in step with the softmax warps
+                    if (i > 0) ok = wait(bar_ofree(t), i - 1);
+                    if (!ok) break;
+                    mbar_arrive(bar(bar_qfree(t)));
+                }
+                kt += it.nkt;
+                jt += nk;
+                ++i;
             }
-            if (!ok) *abort_flag = 1;
+            if (!ok) sts32(flag, 1);
             // every MMA of both issuers has completed before tensor memory is freed
             tc_commit(bar(kDone));
             mbar_wait(bar(kDone), 0, p.err);
@@ -325,146 +512,174 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const int t = (warp - 2) >> 2;                 // Q tile of this warp
         const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
         const int r = 32 * quarter + lane;             // row within the Q tile
-        const int R = t * kTcRows + r;                 // row within the CTA
+        const int R = t * kTcRows + r;                 // row within the item
         const uint32_t trow = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(t * kTmemTile);
         const uint32_t otile = trow + uint32_t(2 * kTcKeys);
-        const int pos = R < rows ? pos0 + R / g : -1;
-        const int nk = nkt_of(t);
-        const size_t qrow = size_t(q0 + j0 + (R < rows ? R / g : 0)) * p.n_q_heads + h * g +
-                            (R < rows ? R % g : 0);
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
-            const uint32_t qdst = base + Ly::kQ + t * Ly::kQTile + r * 128;
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = R < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                sts128(qdst + (c >> 3) * Ly::kQSlab + (((c & 7) ^ (r & 7)) << 4), v);
-            }
-            // every lane's stores are ordered for the tensor core's (async proxy)
-            // reads by its own fence; after the warp barrier one lane arrives
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kQFull));
-        }
-        float ref = -INFINITY;   // reference maximum (base 2) that P and O are relative to
-        float l = 0.f;
         bool ok = true;
-
-        for (int j = 0; j < nk; ++j) {
-            const int b = j & 1;
-            bool got = !*abort_flag && mbar_wait(bar(bar_s(t, b)), uint32_t((j >> 1) & 1), p.err);
-            if (!__all_sync(kAll, got)) {
-                ok = false;
-                break;
-            }
+        // the previous item's results, stored once its O is complete (while this
+        // tile's MMAs of the next item already run); its output row waits in
+        // shared memory (all ones: a row past the item)
+        const uint32_t out_row = base + Ly::kOutRow + 8u * uint32_t(R);
+        int prev_nk = 0, prev_jend = 0;
+        float prev_l = 0.f;
+        auto epilogue = [&]() -> bool {
+            if (prev_nk == 0) return true;
+            // the last P V's completion covers every earlier MMA of the issuing thread
+            const int e = prev_jend - 1;
+            const bool got = !aborted() && mbar_wait(bar(bar_o(t, e & 1)), uint32_t((e >> 1) & 1), p.err);
+            if (!__all_sync(kAll, got)) return false;
             tc_fence_after_sync();
-            float sc[kTcKeys];
-            tmem_ld64(trow + uint32_t(b * kTcKeys), sc);
-            const int k0 = j * kTcKeys;
-            if (k0 + kTcKeys - 1 > pos) {
+            const float inv = prev_l > 0.f ? 1.f / prev_l : 0.f;
+            const unsigned long long prev_qrow = (unsigned long long)(unsigned)lds32(out_row) |
+                                                 ((unsigned long long)(unsigned)lds32(out_row + 4) << 32);
+            const bool prev_row = prev_qrow != ~0ull;
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + (prev_row ? prev_qrow : 0) * D);
 #pragma unroll
-                for (int i = 0; i < kTcKeys; ++i) sc[i] = k0 + i <= pos ? sc[i] : -INFINITY;
-            }
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tmem_ld32(otile + uint32_t(32 * c), v);
+                if (prev_row) {
 #pragma unroll
-            for (int i = 0; i < kTcKeys; i += 8) {
-                m4[0] = fmax3(m4[0], sc[i], sc[i + 1]);
-                m4[1] = fmax3(m4[1], sc[i + 2], sc[i + 3]);
-                m4[2] = fmax3(m4[2], sc[i + 4], sc[i + 5]);
-                m4[3] = fmax3(m4[3], sc[i + 6], sc[i + 7]);
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        uint4 w;
+                        w.x = Elem<T>::pack2(v[8 * e4 + 0] * inv, v[8 * e4 + 1] * inv);
+                        w.y = Elem<T>::pack2(v[8 * e4 + 2] * inv, v[8 * e4 + 3] * inv);
+                        w.z = Elem<T>::pack2(v[8 * e4 + 4] * inv, v[8 * e4 + 5] * inv);
+                        w.w = Elem<T>::pack2(v[8 * e4 + 6] * inv, v[8 * e4 + 7] * inv);
+                        dst[4 * c + e4] = w;
+                    }
+                }
             }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-            const bool move = mx > ref + kRescaleLog2;
-            const float alpha = move ? fast_exp2(ref - mx) : 1.f;   // 0 while no key was seen
-            if (move) ref = mx;
-            if (j > 0 && __any_sync(kAll, move)) {
-                // rescale this warp's rows of O (every earlier P V has completed first)
-                got = !*abort_flag &&
-                      mbar_wait(bar(bar_o(t, (j - 1) & 1)), uint32_t(((j - 1) >> 1) & 1), p.err);
+            return true;
+        };
+        int jt = 0;   // key tiles of this Q tile before the item
+        int i = 0;
+        for (int m = 0; ok; ++m) {
+            const int k = pf_item_index(m);
+            if (k >= num_items) break;
+            PfItem it;
+            if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+            const int nk = it.nk[t];
+            const bool row = R < it.rows;
+            const int pos = row ? it.pos0 + R / g : -1;
+            const unsigned long long qrow = (unsigned long long)(it.q0 + it.j0 + (row ? R / g : 0)) * p.n_q_heads +
+                                            it.h * g + (row ? R % g : 0);
+            // Q rows of this item, once every S of the previous item has read Q
+            if (i > 0) {
+                const bool got = !aborted() && mbar_wait(bar(bar_qfree(t)), uint32_t((i - 1) & 1), p.err);
+                if (!__all_sync(kAll, got)) {
+                    ok = false;
+                    break;
+                }
+            }
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
+                const uint32_t qdst = base + Ly::kQ + t * Ly::kQTile + r * 128;
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = row ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    sts128(qdst + (c >> 3) * Ly::kQSlab + (((c & 7) ^ (r & 7)) << 4), v);
+                }
+                // every lane's stores are ordered for the tensor core's (async proxy)
+                // reads by its own fence; after the warp barrier one lane arrives
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bar_qfull(t)));
+            }
+            // the previous item's output; then O may be overwritten
+            if (i > 0) {
+                if (!epilogue()) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bar_ofree(t)));
+            }
+            {
+                const unsigned long long v = row ? qrow : ~0ull;
+                sts32(out_row, int(unsigned(v)));
+                sts32(out_row + 4, int(unsigned(v >> 32)));
+            }
+            float ref = -INFINITY;   // reference maximum (base 2) that P and O are relative to
+            float l = 0.f;
+            for (int j = 0; j < nk; ++j) {
+                const int gj = jt + j;
+                const int b = gj & 1;
+                bool got = !aborted() && mbar_wait(bar(bar_s(t, b)), uint32_t((gj >> 1) & 1), p.err);
                 if (!__all_sync(kAll, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
+                float sc[kTcKeys];
+                tmem_ld64(trow + uint32_t(b * kTcKeys), sc);
+                const int k0 = j * kTcKeys;
+                if (k0 + kTcKeys - 1 > pos) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(otile + uint32_t(32 * c), v);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) v[x] *= alpha;
-                    tmem_st32(otile + uint32_t(32 * c), v);
+                    for (int x = 0; x < kTcKeys; ++x) sc[x] = k0 + x <= pos ? sc[x] : -INFINITY;
                 }
-            }
-            const float nu = ref == -INFINITY ? 0.f : -ref;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kTcKeys; i += 2) {
-                ffma2(sc[i], sc[i + 1], p.scale_log2, nu);
-                sc[i] = fast_exp2(sc[i]);
-                sc[i + 1] = fast_exp2(sc[i + 1]);
-                if (i & 2) fadd2(s4[2], s4[3], sc[i], sc[i + 1]);
-                else fadd2(s4[0], s4[1], sc[i], sc[i + 1]);
-            }
-            l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-            if (tail && t == t_last && j == nkt - 1) {
-                // keys past the context: zero their V rows once the tile has landed
-                got = !*abort_flag &&
-                      mbar_wait(bar(kKvFull + j % kTcStages), uint32_t((j / kTcStages) & 1), p.err);
-                if (!__all_sync(kAll, got)) {
-                    ok = false;
-                    break;
+                for (int x = 0; x < kTcKeys; x += 8) {
+                    m4[0] = fmax3(m4[0], sc[x], sc[x + 1]);
+                    m4[1] = fmax3(m4[1], sc[x + 2], sc[x + 3]);
+                    m4[2] = fmax3(m4[2], sc[x + 4], sc[x + 5]);
+                    m4[3] = fmax3(m4[3], sc[x + 6], sc[x + 7]);
                 }
-                if (r < kTcKeys && k0 + r >= L) {
-                    const uint32_t vrow = base + Ly::kKv + (j % kTcStages) * Ly::kStage + Ly::kHalf + r * 128;
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+                const bool move = mx > ref + kRescaleLog2;
+                const float alpha = move ? fast_exp2(ref - mx) : 1.f;   // 0 while no key was seen
+                if (move) ref = mx;
+                if (j > 0 && __any_sync(kAll, move)) {
+                    // rescale this warp's rows of O (every earlier P V has completed first)
+                    got = !aborted() &&
+                          mbar_wait(bar(bar_o(t, (gj - 1) & 1)), uint32_t(((gj - 1) >> 1) & 1), p.err);
+                    if (!__all_sync(kAll, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
 #pragma unroll
-                    for (int sl = 0; sl < Ly::kSlabs; ++sl)
+                    for (int c = 0; c < D / 32; ++c) {
+                        float v[32];
+                        tmem_ld32(otile + uint32_t(32 * c), v);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            sts128(vrow + sl * Ly::kKvSlab + c * 16, make_uint4(0u, 0u, 0u, 0u));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kVZero));
-            }
-            uint32_t pk[kTcKeys / 2];
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 2; ++c) pk[c] = Elem<T>::pack2(sc[2 * c], sc[2 * c + 1]);
-            tmem_st32u(trow + uint32_t(b * kTcKeys), pk);
-            // each lane's tensor-memory store has completed (tmem_st32u waits) and is
-            // ordered before the warp barrier; then one lane arrives for the warp
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bar_p(t, b)));
-        }
-        if (ok && nk > 0) {
-            // the last P V's completion covers every earlier MMA of the issuing thread
-            const bool got = !*abort_flag &&
-                             mbar_wait(bar(bar_o(t, (nk - 1) & 1)), uint32_t(((nk - 1) >> 1) & 1), p.err);
-            ok = __all_sync(kAll, got);
-        }
-        if (!ok) {
-            *abort_flag = 1;
-        } else if (nk > 0) {
-            tc_fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + qrow * D);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-                tmem_ld32(otile + uint32_t(32 * c), v);
-                if (R < rows) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 w;
-                        w.x = Elem<T>::pack2(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
-                        w.y = Elem<T>::pack2(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
-                        w.z = Elem<T>::pack2(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
-                        w.w = Elem<T>::pack2(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
-                        dst[4 * c + e] = w;
+                        for (int x = 0; x < 32; ++x) v[x] *= alpha;
+                        tmem_st32(otile + uint32_t(32 * c), v);
                     }
                 }
+                const float nu = ref == -INFINITY ? 0.f : -ref;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int x = 0; x < kTcKeys; x += 2) {
+                    ffma2(sc[x], sc[x + 1], p.scale_log2, nu);
+                    sc[x] = fast_exp2(sc[x]);
+                    sc[x + 1] = fast_exp2(sc[x + 1]);
+                    if (x & 2) fadd2(s4[2], s4[3], sc[x], sc[x + 1]);
+                    else fadd2(s4[0], s4[1], sc[x], sc[x + 1]);
+                }
+                l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+                uint32_t pk[kTcKeys / 2];
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 2; ++c) pk[c] = Elem<T>::pack2(sc[2 * c], sc[2 * c + 1]);
+                tmem_st32u(trow + uint32_t(b * kTcKeys), pk);
+                // each lane's tensor-memory store has completed (tmem_st32u waits) and is
+                // ordered before the warp barrier; then one lane arrives for the warp
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bar_p(t, b)));
             }
+            if (!ok) break;
+            prev_nk = nk;
+            prev_jend = jt + nk;
+            prev_l = l;
+            jt += nk;
+            ++i;
         }
+        // the last item's output
+        if (ok && i > 0 && !epilogue()) ok = false;
+        if (!ok) sts32(flag, 1);
     }
 
     // ---- every role is done: release the tensor memory
@@ -482,7 +697,7 @@ int prefill_tc_smem_bytes(int head_dim) {
 
 template <typename T, int D>
 static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                      const PrefillParams &p, int max_query_len,
+                                      const PrefillParams &p, int max_query_len, int num_sms,
                                       cudaStream_t stream) {
     auto kernel = paged_prefill_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kTotal + 1024;
@@ -492,8 +707,12 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     static std::atomic<unsigned long long> opened[kLaunchCacheDevices];
     e = open_dynamic_smem(opened, dev, kernel, smem);
     if (e != cudaSuccess) return e;
-    const unsigned tiles = unsigned((max_query_len + p.tile_tokens - 1) / p.tile_tokens);
-    const dim3 grid(tiles, unsigned(p.n_kv_heads), unsigned(p.num_seqs));
+    // persistent: one CTA per SM (its shared memory allows no second), each
+    // working through its share of the items
+    const int tiles = (max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    const long long items = (long long)tiles * p.n_kv_heads * p.num_seqs;
+    if (items > INT_MAX) return cudaErrorInvalidValue;
+    const dim3 grid(unsigned(items < num_sms ? items : num_sms));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -504,18 +723,18 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p);
+    return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p, tiles);
 }
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
-                              cudaStream_t stream) {
+                              int num_sms, cudaStream_t stream) {
     const bool bf16 = dtype == PAGEDKV_BF16;
     if (head_dim == 64)
-        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, p, max_query_len, stream)
-                    : launch_tc_instance<__half, 64>(kmap, vmap, p, max_query_len, stream);
-    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, p, max_query_len, stream)
-                : launch_tc_instance<__half, 128>(kmap, vmap, p, max_query_len, stream);
+        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, p, max_query_len, num_sms, stream)
+                    : launch_tc_instance<__half, 64>(kmap, vmap, p, max_query_len, num_sms, stream);
+    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, p, max_query_len, num_sms, stream)
+                : launch_tc_instance<__half, 128>(kmap, vmap, p, max_query_len, num_sms, stream);
 }
 
 }  // namespace pkv
