@@ -174,9 +174,57 @@ def test_prefill_full_size_sampled(orc):
     rng = np.random.default_rng(6)
     units = [(int(s), int(h)) for s, h in zip(rng.choice(wl.num_seqs, 4, replace=False),
                                               rng.choice(wl.n_kv_heads, 4, replace=False))]
-    okc, ovc = to_np(kc), to_np(vc)
+    # the oracle attends over its own pools (its slot mapping + append of the
+    # same tokens), and the GPU's pools equal them byte for byte
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    assert to_np(kc).view(np.uint8).tobytes() == okc.view(np.uint8).tobytes()
+    assert to_np(vc).view(np.uint8).tobytes() == ovc.view(np.uint8).tobytes()
     ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16",
                       units=units)
     for s, h in units:
         err = float(np.abs(got[qs[s]:qs[s + 1], h] - ref[qs[s]:qs[s + 1], h]).max())
         assert err <= TOL["f16"], (s, h, err)
+
+
+def test_many_items_per_cta(orc):
+    """Far more (sequence, query tile, kv head) items than SMs, so that the
+    tcgen05 kernel's persistent CTAs each work through many: chunks of one
+    row to three query tiles, chunks whose second Q tile is empty, contexts
+    on a 64-key boundary and ragged ones, every output row against the oracle."""
+    rng = np.random.default_rng(520)
+    before = rng.integers(0, 900, size=40)
+    chunk = rng.integers(1, 600, size=40)
+    before[:4] = [0, 64, 128, 0]          # contexts ending on a 64-key boundary
+    chunk[:4] = [64, 64, 128, 100]
+    cases = list(zip(before.tolist(), chunk.tolist()))
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, 1, seed=521, cases=cases, n_kv=8)
+    pk.device_errors(reset=True)
+    out = prefill(wl, qs, q, kc, vc, bt)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+    err = float(np.abs(to_f64(out) - ref).max())
+    assert err <= TOL["bf16"], err
+
+
+def test_more_sequences_than_the_ranking_holds_with_a_bad_one(orc):
+    """300 sequences (the tcgen05 kernel ranks at most 256 by length and
+    keeps the given order beyond that), one of them with a length shorter
+    than its chunk: it is flagged and left unwritten, every other row matches
+    the oracle."""
+    rng = np.random.default_rng(530)
+    cases = list(zip(rng.integers(0, 200, size=300).tolist(), rng.integers(1, 40, size=300).tolist()))
+    wl, qs, tensors, q, kc, vc, bt = build("f16", 64, 16, 2, seed=531, cases=cases, n_kv=2)
+    lens = wl.context_lens.copy()
+    bad = 150
+    lens[bad] = int(qs[bad + 1] - qs[bad]) - 1
+    pk.device_errors(reset=True)
+    out = prefill(wl, qs, q, kc, vc, bt, lens=lens)
+    assert pk.device_errors() == 0x04
+    got = to_f64(out)
+    assert np.isnan(got[qs[bad]:qs[bad + 1]]).all()
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16")
+    keep = np.r_[0:qs[bad], qs[bad + 1]:qs[-1]]
+    err = float(np.abs(got[keep] - ref[keep]).max())
+    assert err <= TOL["f16"], err
