@@ -431,7 +431,11 @@ int pagedkv_check_bounded_wait(void *stream);
 #define PAGEDKV_OPT_DECODE_PATH    1  /* 0 auto, 1 CUDA-core (SIMT) path, 2 tensor-core (mma) path */
 #define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */
 #define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
-#define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16); 0 = library default */
+#define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16) for every call; 0 = automatic: fixed
+                                         partitions take 2 from 512 tokens up, else about 96 KB of stages; the
+                                         balanced split takes 2 when the block tables' full width of K/V fits in
+                                         L2, else about 96 KB of stages of which each CTA uses 2 when the mean
+                                         context is 6144 tokens or more */
 #define PAGEDKV_OPT_PREFILL_PATH   5  /* 0 auto (= 2), 1 warp-level MMA prefill kernel, 2 tcgen05 prefill kernel */
 #define PAGEDKV_OPT_L2_HINTS       6  /* L2 priorities on the decode's K/V loads (blocks that the previous or next
                                          sequence holds at the same table index evict_last, the rest evict_first):
