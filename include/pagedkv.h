@@ -242,7 +242,9 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
  *   block_tables   int32 [num_seqs][max_blocks_per_seq], device
  *   query_start    int32 [num_seqs + 1], device, non-decreasing from 0 to num_tokens
  *   context_lens   int32 [num_seqs], device
- *   max_query_len  an upper bound of every n_s (sizes the grid)
+ *   max_query_len  an upper bound of every n_s (sizes the work: query tiles per
+ *                  sequence; the tcgen05 kernel runs one persistent CTA per SM
+ *                  over them)
  *
  * Returns PAGEDKV_ERR_UNSUPPORTED for fp32, head_dim other than 64/128, block
  * size other than 8/16/32 or more than 64 query heads per kv head. On the
