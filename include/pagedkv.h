@@ -432,7 +432,8 @@ int pagedkv_check_bounded_wait(void *stream);
 /* Tuning knobs, process-wide and not thread-safe; for tests and benchmarks. */
 #define PAGEDKV_OPT_DECODE_PATH    1  /* 0 auto, 1 CUDA-core (SIMT) path, 2 tensor-core (mma) path */
 #define PAGEDKV_OPT_CTAS_PER_SM    2  /* persistent decode CTAs per SM; 0 = library default */
-#define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path */
+#define PAGEDKV_OPT_MMA_MIN_GROUP  3  /* auto path: smallest q-per-kv group that takes the mma path (default 1:
+                                         every 16-bit pool; fp32 always takes the CUDA-core path) */
 #define PAGEDKV_OPT_STAGES         4  /* decode stage-ring size (2..16) for every call; 0 = automatic: fixed
                                          partitions take 2 from 512 tokens up, else about 96 KB of stages; the
                                          balanced split takes 2 when the block tables' full width of K/V fits in
