@@ -119,15 +119,17 @@ def measured_tensor_peak():
 
 
 def decode_part_of_api(text):
-    """The parts of api.cu that decide a decode launch: the pool tensor map, the
-    workspace layout and the decode entry points (other entry points excluded)."""
+    """The parts of api.cu that decide a decode launch: the options' defaults,
+    the pool tensor map, the workspace layout and the decode entry points (other
+    entry points excluded)."""
     try:
         a = text.index("int encode_pool_map(")
         b = text.index("size_t round256(")
         c = text.index("size_t paged_attention_workspace_bytes(")
     except ValueError:
         return text
-    return text[a:b] + text[c:]
+    options = "".join(line for line in text.splitlines(True) if line.startswith("int g_opt_"))
+    return options + text[a:b] + text[c:]
 
 
 def kernel_source_digest():
