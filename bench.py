@@ -132,16 +132,42 @@ def decode_part_of_api(text):
     return options + text[a:b] + text[c:]
 
 
+def code_only(text):
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_digest():
-    """Digest of the sources that determine the decode kernels and their launch."""
+    """Digest of the code (comments aside) that determines the decode kernels
+    and their launch."""
     h = hashlib.sha256()
     csrc = os.path.join(REPO, "paged_kv_cache_233_gb300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            data = f.read()
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
         if name == "api.cu":
-            data = decode_part_of_api(data.decode()).encode()
-        h.update(data)
+            text = decode_part_of_api(text)
+        h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -21,7 +21,12 @@
 //               16-token tile, one 4-D TMA load of K and one of V covering all
 //               H heads and all 128-byte column slabs of those tokens, into a
 //               ring of shared-memory stages (mbarrier transaction counts
-//               signal arrival; all four consumers release a stage).
+//               signal arrival; all four consumers release a stage). The ring
+//               holds params.stages stages; every CTA uses stages_alt of them
+//               instead when the call's mean context is long. When the call
+//               streams more K/V than the L2 holds, each load carries an L2
+//               priority: evict_last for blocks a neighbouring sequence
+//               shares, evict_first for the rest.
 //   warps 1..4  consumers. Warp w owns kv head (w mod H) of the unit and, when
 //               H < 4, every (4/H)-th tile of it. Each keeps an fp32
 //               online-softmax state (running max m, running sum l,
@@ -44,10 +49,10 @@
 //         lane computes partial dot products for its rows and a butterfly
 //         transpose-reduction turns them into full scores.
 //   MMA   tensor cores (mma.sync m16n8k16, fp32 accumulate), for 16-bit types
-//         when the query group is large enough to fill a tile: tokens are the
-//         M dimension (a 16-token tile is exactly M = 16) and the query group
-//         is N (8, padded): S^T = K Q^T, then O^T += V^T P^T with P^T moved
-//         from accumulator layout to operand layout by movmatrix.
+//         at any query-group size: tokens are the M dimension (a 16-token
+//         tile is exactly M = 16) and the query group is N (8, padded with
+//         zero columns): S^T = K Q^T, then O^T += V^T P^T with P^T moved from
+//         accumulator layout to operand layout by movmatrix.
 #pragma once
 
 #include <type_traits>
