@@ -247,7 +247,8 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
  *                  over them)
  *
  * Returns PAGEDKV_ERR_UNSUPPORTED for fp32, head_dim other than 64/128, block
- * size other than 8/16/32 or more than 64 query heads per kv head. On the
+ * size other than 8/16/32, more than 64 query heads per kv head, or (tcgen05
+ * kernel) more than 2^30 work items of (sequence, kv head, 256 query rows). On the
  * device, a sequence whose rows fall outside [0, num_tokens) or exceed the
  * grid's max_query_len sets PAGEDKV_DEVERR_POSITION; one with n_s > L_s or L_s
  * beyond its table sets PAGEDKV_DEVERR_CONTEXT_LEN; a block id outside the pool

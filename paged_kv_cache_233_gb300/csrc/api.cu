@@ -505,6 +505,11 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     p.n_kv_heads = n_kv_heads;
     p.group = group;
     p.tile_tokens = (tc ? pkv::kPfTcRows : pkv::kPfRows) / group;
+    if (tc) {
+        // the persistent kernel counts its work items in ints
+        const long long per_seq = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens * n_kv_heads;
+        if (per_seq > (INT_MAX / 2) / num_seqs) return PAGEDKV_ERR_UNSUPPORTED;
+    }
     p.num_blocks = num_blocks;
     p.block_size = block_size;
     int log2_block = 0;

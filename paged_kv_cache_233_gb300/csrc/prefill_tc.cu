@@ -709,9 +709,13 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (its shared memory allows no second), each
     // working through its share of the items
-    const int tiles = (max_query_len + p.tile_tokens - 1) / p.tile_tokens;
-    const long long items = (long long)tiles * p.n_kv_heads * p.num_seqs;
-    if (items > INT_MAX) return cudaErrorInvalidValue;
+    // items (and a CTA's band index, at most items + grid) must fit an int
+    // (the API refuses larger calls)
+    const long long tiles_ll = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    const long long per_seq = tiles_ll * p.n_kv_heads;
+    if (per_seq > (INT_MAX / 2) / p.num_seqs) return cudaErrorInvalidValue;
+    const int tiles = int(tiles_ll);
+    const long long items = per_seq * p.num_seqs;
     const dim3 grid(unsigned(items < num_sms ? items : num_sms));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
