@@ -444,7 +444,9 @@ int pagedkv_check_bounded_wait(void *stream);
 #define PAGEDKV_OPT_L2_HINTS       6  /* L2 priorities on the decode's K/V loads (blocks that the previous or next
                                          sequence holds at the same table index evict_last, the rest evict_first):
                                          0 auto = when the call's K/V tokens exceed what the L2 holds, 1 never,
-                                         2 always */
+                                         2 always. Only neighbouring sequences' blocks are compared: order the
+                                         batch so that sequences sharing blocks sit next to each other (e.g. by
+                                         first block id) */
 int pagedkv_set_option(int option, int value);
 int pagedkv_get_option(int option);
 
