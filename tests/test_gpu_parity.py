@@ -108,6 +108,19 @@ def test_decode_sweep(orc, dtype, D, B, g, path, P):
     assert pk.device_errors() == 0
 
 
+@pytest.mark.parametrize("dtype,g,want", [("f16", 1, "mma"), ("bf16", 2, "mma"), ("f16", 8, "mma"),
+                                          ("f32", 1, "simt"), ("f32", 4, "simt")])
+def test_automatic_path_choice(orc, dtype, g, want):
+    """The automatic decode path takes the tensor-core consumer for every
+    16-bit pool (it measured faster at every group size) and the CUDA-core
+    consumer for fp32; either way the result matches the oracle."""
+    wl = make_workload("auto", dtype, [5, 40, 130], 2 * g, 2, 64, 16, 61)
+    r = run_both(orc, wl, 0, "auto")
+    assert pk.last_decode_path() == PATHS[want]
+    assert_close(r["out"], r["ref"], dtype, what=f"auto path {dtype} g{g}")
+    assert pk.device_errors() == 0
+
+
 @pytest.mark.parametrize("dtype,path", [("bf16", "mma"), ("f16", "simt"), ("f32", "simt")])
 def test_split_partition_states(orc, dtype, path):
     """The split-K partition states in the workspace match the oracle's
