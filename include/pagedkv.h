@@ -236,11 +236,16 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
  * it (PAGEDKV_OPT_PREFILL_PATH): tcgen05 MMAs with accumulators in tensor
  * memory (default), or warp-level m16n8k16 MMAs.
  *
- *   q, out         [num_tokens][n_q_heads][head_dim] of dtype, device, 16-byte aligned
+ *   q, out         [num_tokens][n_q_heads][head_dim] of dtype, device, 16-byte aligned;
+ *                  every row of q may be read (the tcgen05 kernel copies whole
+ *                  128-row Q tiles by TMA when the group divides 128), but a row
+ *                  outside a chunk, such as padding past query_start[num_seqs],
+ *                  never reaches an output row and its out row is not written
  *   k_cache,
  *   v_cache        [num_blocks][block_size][n_kv_heads][head_dim], device, 16-byte aligned
  *   block_tables   int32 [num_seqs][max_blocks_per_seq], device
- *   query_start    int32 [num_seqs + 1], device, non-decreasing from 0 to num_tokens
+ *   query_start    int32 [num_seqs + 1], device, non-decreasing from 0 (num_tokens
+ *                  may be larger than query_start[num_seqs])
  *   context_lens   int32 [num_seqs], device
  *   max_query_len  an upper bound of every n_s (sizes the work: query tiles per
  *                  sequence; the tcgen05 kernel runs one persistent CTA per SM

@@ -179,6 +179,32 @@ int encode_pool_map_slab(CUtensorMap *map, const void *pool, int dtype, int head
     return r == CUDA_SUCCESS ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 
+// TMA view of the queries of a prefill call for the tcgen05 kernel: q as a
+// 4-D tensor (x: 128-byte column slab elements, slab, query head, token) with
+// a box of one slab x `group` heads x 128 / group tokens, so that one box is a
+// Q tile's 128 rows (token, head of the group) of one column slab, 128-byte
+// swizzle. Strides in bytes: slab 128, head head_dim*eb, token
+// n_q_heads*head_dim*eb. Only for groups that divide 128.
+int encode_q_map(CUtensorMap *map, const void *q, int dtype, int head_dim, int n_q_heads,
+                 int num_tokens, int group) {
+    EncodeTiledFn fn = nullptr;
+    int st = encoder(&fn);
+    if (st != PAGEDKV_OK) return st;
+    const int eb = elem_bytes(dtype);
+    const int slabs = head_dim * eb / 128;
+    const CUtensorMapDataType dt = dtype == PAGEDKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t dims[4] = {cuuint64_t(128 / eb), cuuint64_t(slabs), cuuint64_t(n_q_heads),
+                                cuuint64_t(num_tokens)};
+    const cuuint64_t strides[3] = {128u, cuuint64_t(head_dim) * eb, cuuint64_t(n_q_heads) * head_dim * eb};
+    const cuuint32_t box[4] = {cuuint32_t(128 / eb), 1u, cuuint32_t(group), cuuint32_t(128 / group)};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = fn(map, dt, 4, const_cast<void *>(q), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
 // SM count of the current device (no error word lookup).
 int current_sm_count(int *sms) {
     int dev = 0, n = 0;
@@ -478,11 +504,15 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     if (st != PAGEDKV_OK) return st;
     // path: 1 warp-level MMA kernel, 2 tcgen05 kernel (auto)
     const bool tc = g_opt_prefill_path != 1;
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap, qmap = {};
+    // the tcgen05 kernel copies Q tiles by TMA when the group divides a tile's 128 rows
+    const bool q_tma = tc && 128 % group == 0;
     if (tc) {
         st = encode_pool_map_slab(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
         if (st != PAGEDKV_OK) return st;
         st = encode_pool_map_slab(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
+        if (st == PAGEDKV_OK && q_tma)
+            st = encode_q_map(&qmap, q, dtype, head_dim, n_q_heads, num_tokens, group);
     } else {
         st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1,
                              true);
@@ -516,8 +546,9 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     while ((1 << log2_block) < block_size) ++log2_block;
     p.log2_block = log2_block;
     p.max_blocks = max_blocks_per_seq;
+    p.q_tma = q_tma ? 1 : 0;
     const cudaError_t e =
-        tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, p, max_query_len, sms,
+        tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, qmap, p, max_query_len, sms,
                                     static_cast<cudaStream_t>(stream))
            : pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
                                  static_cast<cudaStream_t>(stream));

@@ -31,6 +31,7 @@ struct PrefillParams {
     int block_size;
     int log2_block;
     int max_blocks;
+    int q_tma;                   // tcgen05 kernel: Q tiles copied by TMA (the group divides 128)
 };
 
 // Bytes of dynamic shared memory the kernel asks for at this head_dim (16-bit types).
@@ -39,14 +40,17 @@ int prefill_smem_bytes(int head_dim);
 // The warp-level MMA kernel: grid (query tiles of the longest chunk, kv heads,
 // sequences), 64 query rows per CTA, pool maps with boxes of every column
 // block. The tcgen05 kernel: one persistent CTA per SM working through items
-// of 256 rows, pool maps with boxes of one 64-column block.
+// of 256 rows, pool maps with boxes of one 64-column block, and (when
+// p.q_tma) a map of q with boxes of [128 / group tokens][group heads][one
+// 64-column block].
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
                            cudaStream_t stream);
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
-                              const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
-                              int num_sms, cudaStream_t stream);
+                              const CUtensorMap &vmap, const CUtensorMap &qmap,
+                              const PrefillParams &p, int max_query_len, int num_sms,
+                              cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
 constexpr int kPfTcRows = 256;   // query rows per CTA of the tcgen05 kernel (two tiles of 128)

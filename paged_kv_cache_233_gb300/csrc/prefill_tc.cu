@@ -38,10 +38,15 @@
 //              than 2^8 (P stays below 256, sums stay in fp32); when it moves,
 //              the warp rescales its rows of O in tensor memory before that
 //              tile's P V may start. The result is exact softmax attention.
-//              A tile's warps load the next item's Q rows once every S of the
-//              item before has completed, then write out that item's rows
-//              from O and release O for the next item's first P V;
-//   warp 11    zeroes the V rows past a context (below).
+//              Between items a tile's warps write out the item's rows from O,
+//              before their first P of the next item (so the issuer's wait for
+//              that P also frees O for the item's first P V);
+//   warp 11    copies each item's Q tiles by TMA as soon as every S of the
+//              item before has completed (about two key tiles before the
+//              softmax warps finish it), and zeroes the V rows past a context
+//              (below). For a group that does not divide 128 (a Q tile's rows
+//              would split a token's heads) the softmax warps load Q instead,
+//              between items.
 // V rows past the context are zeroed in shared memory before any P V reads
 // them (the tensor core would turn 0 * NaN into NaN): the V copies of a
 // context's last key tile land on a per-stage barrier of their own, and a
@@ -79,16 +84,17 @@ constexpr int kKvFull = 0;
 constexpr int kKvEmpty = kTcStages;
 // per Q tile t: S full, P full and O full per buffer b (P V of key tile j
 // completes on O barrier j & 1, so a wait never meets a barrier two
-// completions away); Q full (the tile's softmax warps stored an item's Q
-// rows), Q free (every S MMA of the item, the readers of Q, has completed) and
-// O free (the softmax warps have read the item's O out of tensor memory)
-constexpr int kPerTileBars = 9;
+// completions away); Q full (an item's Q rows of the tile are in shared
+// memory) and Q free (every S MMA of the item, the readers of Q, has
+// completed). A softmax warp reads an item's O out of tensor memory before it
+// writes the next item's first P, so the wait for that P also tells the
+// issuer that O may start afresh.
+constexpr int kPerTileBars = 8;
 __device__ __forceinline__ int bar_s(int t, int b) { return 2 * kTcStages + kPerTileBars * t + b; }
 __device__ __forceinline__ int bar_p(int t, int b) { return 2 * kTcStages + kPerTileBars * t + 2 + b; }
 __device__ __forceinline__ int bar_o(int t, int b) { return 2 * kTcStages + kPerTileBars * t + 4 + b; }
 __device__ __forceinline__ int bar_qfull(int t) { return 2 * kTcStages + kPerTileBars * t + 6; }
 __device__ __forceinline__ int bar_qfree(int t) { return 2 * kTcStages + kPerTileBars * t + 7; }
-__device__ __forceinline__ int bar_ofree(int t) { return 2 * kTcStages + kPerTileBars * t + 8; }
 constexpr int kDone = 2 * kTcStages + kPerTileBars * kTcTiles;
 // per stage: the V copies of a context's last key tile land here first; the
 // zeroing warp clears the V rows past the context, then completes the stage
@@ -203,7 +209,8 @@ __device__ __forceinline__ int pf_item_index(int m) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p, int tiles) {
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap qmap, const PrefillParams p, int tiles) {
     using Ly = TcLayout<D>;
     constexpr bool kBf16 = Elem<T>::kBf16;
     extern __shared__ uint8_t smem_raw[];
@@ -231,9 +238,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_init(bar(bar_p(t, b)), kTcRows / 32);   // one arrival per softmax warp
                 mbar_init(bar(bar_o(t, b)), 1);
             }
-            mbar_init(bar(bar_qfull(t)), kTcRows / 32);
+            // Q full: the copy's bytes (one arrival), or one arrival per softmax warp
+            mbar_init(bar(bar_qfull(t)), p.q_tma ? 1 : kTcRows / 32);
             mbar_init(bar(bar_qfree(t)), 1);
-            mbar_init(bar(bar_ofree(t)), kTcRows / 32);
         }
         mbar_init(bar(kDone), kTcTiles);
         for (int k = 0; k < kTcStages; ++k) mbar_init(bar(kTailV + k), 1);
@@ -244,8 +251,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tmem_alloc(base + Ly::kTmemSlot, kTcTiles * kTmemTile);
         tmem_relinquish();
     }
-    // sequences ranked by decreasing context length (ties by index); the
-    // lengths are the caller's, read before any grid dependency
     // sequences ranked by decreasing context length (ties by index), when some
     // CTA gets more than one item; the lengths are the caller's, read before
     // any grid dependency
@@ -356,13 +361,27 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         __syncwarp();
     } else if (warp == kZeroWarp) {
-        // ------------------------------------------------------------ V tail
-        // V rows past a context (never written for the sequence, or left in the
-        // stage by an earlier tile) become zeros once the tile's V copies have
-        // landed: the tensor core would turn 0 * NaN into NaN. Then the stage is
-        // complete (its K copies may still be landing). The issuers reach that
-        // tile's S two key tiles ahead of its P V, which hides the wait.
+        // ------------------------------------------------ Q copies and V tails
+        // Q: when the group divides a tile's 128 rows, lane 0 copies each Q
+        // tile of an item with one TMA box per 64-column block ([128/g tokens]
+        // [g heads][64 columns], which lands as the tile's rows (token, head)
+        // in the swizzled layout the tensor core reads), as soon as every S
+        // MMA of the item before has completed: about two key tiles before
+        // the softmax warps finish that item, so the copy is off their path.
+        // V: the rows past a context (never written for the sequence, or left
+        // in the stage by an earlier tile) become zeros once the tile's V
+        // copies have landed: the tensor core would turn 0 * NaN into NaN.
+        // Then the stage is complete (its K copies may still be landing). The
+        // issuers reach that tile's S two key tiles ahead of its P V, which
+        // hides the wait. An item's Q copies go first: its S MMAs, which the
+        // item's last stage waits for, need them.
+        if (lane == 0 && p.q_tma) tma_prefetch_descriptor(&qmap);
         int kt = 0;
+        int i = 0;
+        // per Q tile, the last item that took a phase of its Q full barrier (a
+        // copy or a plain arrival): each phase waits for the one before to be
+        // consumed, so that phase is the only one that may still be pending
+        int qlast[kTcTiles] = {-1, -1};
         uint32_t parity = 0;   // bit st: phase parity of stage st's tail barrier
         bool ok = true;
         for (int m = 0; ok; ++m) {
@@ -370,6 +389,35 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             if (k >= num_items) break;
             PfItem it;
             if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+            if (p.q_tma) {
+                bool got = true;
+                if (lane == 0) {
+#pragma unroll
+                    for (int t = 0; t < kTcTiles; ++t) {
+                        if (i > 0) got = got && !aborted() &&
+                                         mbar_wait(bar(bar_qfree(t)), uint32_t((i - 1) & 1), p.err);
+                        if (!got) break;
+                        if (it.nk[t] > 0) {
+                            const uint32_t full = bar(bar_qfull(t));
+                            mbar_arrive_expect_tx(full, uint32_t(Ly::kQTile));
+                            // rows past the item are another sequence's tokens, or zeros past
+                            // the last token: the softmax masks every key of such a row
+                            const int tok = it.q0 + it.j0 + t * (kTcRows / g);
+                            for (int sl = 0; sl < Ly::kSlabs; ++sl)
+                                tma_load_4d(base + Ly::kQ + t * Ly::kQTile + sl * Ly::kQSlab, &qmap, 0, sl,
+                                            it.h * g, tok, full);
+                        } else {
+                            // no row of this tile: the issuer still takes the phase
+                            mbar_arrive(bar(bar_qfull(t)));
+                        }
+                        qlast[t] = i;
+                    }
+                }
+                if (!__shfl_sync(kAll, got ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (it.tail) {
                 const int st = (kt + it.nkt - 1) % kTcStages;
                 const int present = it.L - (it.nkt - 1) * kTcKeys;
@@ -392,8 +440,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 if (lane == 0) mbar_arrive(bar(kKvFull + st));
             }
             kt += it.nkt;
+            ++i;
         }
-        if (!ok && lane == 0) sts32(flag, 1);
+        if (lane == 0) {
+            if (!ok) sts32(flag, 1);
+            // this CTA's Q copies have landed before it may exit (a bounded
+            // wait; the issuers have waited for them unless the CTA stopped)
+#pragma unroll
+            for (int t = 0; t < kTcTiles; ++t)
+                if (qlast[t] >= 0) mbar_wait(bar(bar_qfull(t)), uint32_t(qlast[t] & 1), p.err);
+        }
         __syncwarp();
     } else if (warp == 1 || warp == kIssuer1Warp) {
         // ------------------------------------------------------- MMA issuers
@@ -461,10 +517,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int j = 0; ok && j < it.nkt; ++j) {
                     const int gk = kt + j;
                     if (j < nk) {
+                        // (the first P of an item comes after the softmax warps have read
+                        // the previous item's O: its P V may start O afresh)
                         ok = wait(bar_p(t, (jt + j) & 1), (jt + j) >> 1);
-                        // the first P V of the item starts O afresh: the previous
-                        // item's O must have been read out first
-                        if (ok && j == 0 && i > 0) ok = wait(bar_ofree(t), i - 1);
                         if (!ok) break;
                         tc_fence_after_sync();
                         issue_pv(gk, jt + j, j == 0);
@@ -490,13 +545,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                 }
                 if (!ok) break;
-                if (nk == 0) {
-                    // no MMA of this tile reads Q or writes O in this item: keep the
-                    // barriers' phases in step with the softmax warps
-                    if (i > 0) ok = wait(bar_ofree(t), i - 1);
-                    if (!ok) break;
-                    mbar_arrive(bar(bar_qfree(t)));
-                }
+                // no MMA of this tile reads Q in this item: Q is free at once
+                if (nk == 0) mbar_arrive(bar(bar_qfree(t)));
                 kt += it.nkt;
                 jt += nk;
                 ++i;
@@ -564,15 +614,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const int pos = row ? it.pos0 + R / g : -1;
             const unsigned long long qrow = (unsigned long long)(it.q0 + it.j0 + (row ? R / g : 0)) * p.n_q_heads +
                                             it.h * g + (row ? R % g : 0);
-            // Q rows of this item, once every S of the previous item has read Q
-            if (i > 0) {
+            // Q rows of this item (unless a TMA copy brings them), once every S of
+            // the previous item has read Q
+            if (i > 0 && !p.q_tma) {
                 const bool got = !aborted() && mbar_wait(bar(bar_qfree(t)), uint32_t((i - 1) & 1), p.err);
                 if (!__all_sync(kAll, got)) {
                     ok = false;
                     break;
                 }
             }
-            {
+            if (!p.q_tma) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
                 const uint32_t qdst = base + Ly::kQ + t * Ly::kQTile + r * 128;
 #pragma unroll
@@ -586,15 +637,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bar_qfull(t)));
             }
-            // the previous item's output; then O may be overwritten
-            if (i > 0) {
-                if (!epilogue()) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_ofree(t)));
+            // the previous item's output (its tensor-memory loads complete before
+            // this warp's next arrival on a P barrier, which lets O be overwritten)
+            if (i > 0 && !epilogue()) {
+                ok = false;
+                break;
             }
             {
                 const unsigned long long v = row ? qrow : ~0ull;
@@ -697,7 +744,7 @@ int prefill_tc_smem_bytes(int head_dim) {
 
 template <typename T, int D>
 static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                      const PrefillParams &p, int max_query_len, int num_sms,
+                                      const CUtensorMap &qmap, const PrefillParams &p, int max_query_len, int num_sms,
                                       cudaStream_t stream) {
     auto kernel = paged_prefill_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kTotal + 1024;
@@ -727,18 +774,19 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p, tiles);
+    return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, qmap, p, tiles);
 }
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
-                              const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
-                              int num_sms, cudaStream_t stream) {
+                              const CUtensorMap &vmap, const CUtensorMap &qmap,
+                              const PrefillParams &p, int max_query_len, int num_sms,
+                              cudaStream_t stream) {
     const bool bf16 = dtype == PAGEDKV_BF16;
     if (head_dim == 64)
-        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, p, max_query_len, num_sms, stream)
-                    : launch_tc_instance<__half, 64>(kmap, vmap, p, max_query_len, num_sms, stream);
-    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, p, max_query_len, num_sms, stream)
-                : launch_tc_instance<__half, 128>(kmap, vmap, p, max_query_len, num_sms, stream);
+        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                    : launch_tc_instance<__half, 64>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
+    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                : launch_tc_instance<__half, 128>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
 }
 
 }  // namespace pkv

@@ -186,18 +186,21 @@ def test_prefill_full_size_sampled(orc):
         assert err <= TOL["f16"], (s, h, err)
 
 
-def test_many_items_per_cta(orc):
+@pytest.mark.parametrize("g,n_kv", [(1, 8), (3, 4), (8, 4)])
+def test_many_items_per_cta(orc, g, n_kv):
     """Far more (sequence, query tile, kv head) items than SMs, so that the
     tcgen05 kernel's persistent CTAs each work through many: chunks of one
     row to three query tiles, chunks whose second Q tile is empty, contexts
-    on a 64-key boundary and ragged ones, every output row against the oracle."""
+    on a 64-key boundary and ragged ones, every output row against the oracle
+    (groups that divide 128, whose Q tiles are copied by TMA, and one that
+    does not, whose Q rows the softmax warps load)."""
     rng = np.random.default_rng(520)
     before = rng.integers(0, 900, size=40)
     chunk = rng.integers(1, 600, size=40)
     before[:4] = [0, 64, 128, 0]          # contexts ending on a 64-key boundary
     chunk[:4] = [64, 64, 128, 100]
     cases = list(zip(before.tolist(), chunk.tolist()))
-    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, 1, seed=521, cases=cases, n_kv=8)
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, g, seed=521 + g, cases=cases, n_kv=n_kv)
     pk.device_errors(reset=True)
     out = prefill(wl, qs, q, kc, vc, bt)
     assert pk.device_errors() == 0
@@ -228,3 +231,28 @@ def test_more_sequences_than_the_ranking_holds_with_a_bad_one(orc):
     keep = np.r_[0:qs[bad], qs[bad + 1]:qs[-1]]
     err = float(np.abs(got[keep] - ref[keep]).max())
     assert err <= TOL["f16"], err
+
+
+@pytest.mark.parametrize("g", [1, 8])
+def test_query_rows_past_every_chunk_stay_out(orc, g):
+    """q holds 50 NaN rows after the last chunk (num_tokens past the chunks'
+    end): a Q tile that reaches past its chunk reads them (or the next
+    sequence's rows), and none of it may reach a chunk's output row; the
+    output rows past the chunks stay as they were."""
+    cases = [(10, 30), (0, 77), (200, 100), (5, 3)]
+    wl, qs, tensors, q, kc, vc, bt = build("f16", 128, 16, g, seed=540 + g, cases=cases, n_kv=2)
+    pad = torch.full((50,) + tuple(q.shape[1:]), float("nan"), dtype=q.dtype, device=q.device)
+    qp = torch.cat([q, pad])
+    out = torch.full_like(qp, float("nan"))
+    out[q.shape[0]:] = 7.0
+    pk.device_errors(reset=True)
+    pk.paged_attention_prefill(qp, kc, vc, bt, torch.from_numpy(np.asarray(qs, np.int32)).cuda(),
+                               torch.from_numpy(np.asarray(wl.context_lens, np.int32)).cuda(),
+                               wl.scale, out)
+    assert pk.device_errors() == 0
+    assert bool((out[q.shape[0]:] == 7.0).all())
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16")
+    got = to_f64(out[:q.shape[0]])
+    assert not np.isnan(got).any()
+    assert float(np.abs(got - ref).max()) <= TOL["f16"]
