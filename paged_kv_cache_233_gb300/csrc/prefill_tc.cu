@@ -517,23 +517,34 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int j = 0; ok && j < it.nkt; ++j) {
                     const int gk = kt + j;
                     if (j < nk) {
-                        // (the first P of an item comes after the softmax warps have read
-                        // the previous item's O: its P V may start O afresh)
+                        // P of key tile j (the first P of an item comes after the softmax
+                        // warps have read the previous item's O: its P V may start O
+                        // afresh); beside it, without blocking, whether the K/V of key
+                        // tile j + 2 has landed. A shared-memory access by the issuing
+                        // thread waits for its MMAs in flight, so a check between the P V
+                        // and the S would idle the tensor core; only when the K/V is not
+                        // there yet (an item's first key tiles) does the thread wait for
+                        // it after the P V
                         ok = wait(bar_p(t, (jt + j) & 1), (jt + j) >> 1);
+                        const bool ahead = j + 2 < nk;
+                        const int gk2 = gk + 2;
+                        const bool kv_in = ok && ahead &&
+                                           mbar_test_wait(bar(kKvFull + gk2 % kTcStages), uint32_t((gk2 / kTcStages) & 1));
                         if (!ok) break;
                         tc_fence_after_sync();
                         issue_pv(gk, jt + j, j == 0);
                         // the stage of key tile j is free once this P V (the last MMA of
-                        // this thread that reads it) completes: release it before this
-                        // thread blocks on issuing the next S
+                        // this thread that reads it) completes
                         tc_commit(bar(kKvEmpty + gk % kTcStages));
                         // this tile's S two key tiles ahead (its S buffer is free once the
                         // P V just issued has read P)
-                        if (j + 2 < nk) {
-                            ok = wait(kKvFull + (gk + 2) % kTcStages, (gk + 2) / kTcStages);
-                            if (!ok) break;
-                            tc_fence_after_sync();
-                            issue_s(gk + 2, jt + j + 2);
+                        if (ahead) {
+                            if (!kv_in) {
+                                ok = wait(kKvFull + gk2 % kTcStages, gk2 / kTcStages);
+                                if (!ok) break;
+                                tc_fence_after_sync();
+                            }
+                            issue_s(gk2, jt + j + 2);
                             if (j + 2 == nk - 1) tc_commit(bar(bar_qfree(t)));
                         }
                     } else {

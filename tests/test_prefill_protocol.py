@@ -161,10 +161,15 @@ def run_cta(items, q_tma, rng, ofree=False):
                     yield ("p", t, (jt + j) & 1), (jt + j) >> 1
                     if ofree and j == 0 and i > 0:
                         yield ("ofree", t), i - 1
+                    # beside the P wait, a look (no wait) at the K/V of key tile j + 2
+                    ahead = j + 2 < nk
+                    full2 = ("full", (gk + 2) % STAGES), (gk + 2) // STAGES
+                    kv_in = ahead and B(full2[0]).passes(full2[1])
                     B(("o", t, (jt + j) & 1)).arrive()
                     B(("empty", gk % STAGES)).arrive()
-                    if j + 2 < nk:
-                        yield ("full", (gk + 2) % STAGES), (gk + 2) // STAGES
+                    if ahead:
+                        if not kv_in:
+                            yield full2
                         B(("s", t, (jt + j + 2) & 1)).arrive()
                         if j + 2 == nk - 1:
                             B(("qfree", t)).arrive()
