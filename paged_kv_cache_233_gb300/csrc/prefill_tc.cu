@@ -464,30 +464,40 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             auto wait = [&](int i, int phase) {
                 return !aborted() && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
             };
+            // The issuing thread shares its SM sub-partition with two softmax warps,
+            // so every instruction it spends per MMA slows the MMAs' issue: the
+            // shared-memory descriptors are built once (Q's for the whole kernel,
+            // a stage's per use) and a K step only offsets a descriptor's start
+            // address, a constant once the loop is unrolled.
             const uint32_t qb = base + Ly::kQ + t * Ly::kQTile;
+            uint64_t qdesc[D / 16];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                qdesc[kk] = tc_desc_sw128(qb + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
             // S of key tile gk of the ring (gj-th key tile of this Q tile) into S buffer gj & 1
             auto issue_s = [&](int gk, int gj) {
-                const uint32_t kb = base + Ly::kKv + (gk % kTcStages) * Ly::kStage;
+                const uint64_t kdesc = tc_desc_sw128(base + Ly::kKv + (gk % kTcStages) * Ly::kStage, 16, 1024);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc_desc_sw128(qb + (kk >> 2) * Ly::kQSlab + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = tc_desc_sw128(kb + (kk >> 2) * Ly::kKvSlab + (kk & 3) * 32, 16, 1024);
-                    tc_mma_f16(d, a, b, kIdS, kk > 0 ? 1u : 0u);
+                    // (start addresses stay below 2^18 bytes: the offset never carries
+                    // out of the descriptor's 14-bit address field)
+                    const uint64_t b = kdesc + uint64_t(((kk >> 2) * Ly::kKvSlab + (kk & 3) * 32) >> 4);
+                    tc_mma_f16(d, qdesc[kk], b, kIdS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(bar_s(t, gj & 1)));
             };
             // O (+)= P V; `first` starts the item's accumulator
             auto issue_pv = [&](int gk, int gj, bool first) {
-                const uint32_t vb = base + Ly::kKv + (gk % kTcStages) * Ly::kStage + Ly::kHalf;
+                const uint64_t vdesc =
+                    tc_desc_sw128(base + Ly::kKv + (gk % kTcStages) * Ly::kStage + Ly::kHalf, Ly::kKvSlab, 1024);
                 // P: the first 32 columns of S buffer gj & 1 (16 keys per 8 columns)
                 const uint32_t pa = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t b = tc_desc_sw128(vb + kk * 2048, Ly::kKvSlab, 1024);
-                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), b, kIdO, (!first || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), vdesc + uint64_t((kk * 2048) >> 4), kIdO,
+                                      (!first || kk > 0) ? 1u : 0u);
                 tc_commit(bar(bar_o(t, gj & 1)));
             };
             int kt = 0;   // ring position of the item's first key tile
