@@ -461,7 +461,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const int t = warp == 1 ? 0 : 1;
             constexpr uint32_t kIdS = tc_idesc_f16(kBf16, false, kTcRows, kTcKeys);
             constexpr uint32_t kIdO = tc_idesc_f16(kBf16, true, kTcRows, D);
+            // (a phase already complete passes at once; the abort flag is read only
+            // when the thread has to wait)
             auto wait = [&](int i, int phase) {
+                if (mbar_try_wait(bar(i), uint32_t(phase & 1))) return true;
                 return !aborted() && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
             };
             // The issuing thread shares its SM sub-partition with two softmax warps,
