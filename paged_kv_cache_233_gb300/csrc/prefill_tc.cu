@@ -546,11 +546,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         // P of key tile j (the first P of an item comes after the softmax
                         // warps have read the previous item's O: its P V may start O
                         // afresh); beside it, without blocking, whether the K/V of key
-                        // tile j + 2 has landed. A shared-memory access by the issuing
-                        // thread waits for its MMAs in flight, so a check between the P V
-                        // and the S would idle the tensor core; only when the K/V is not
-                        // there yet (an item's first key tiles) does the thread wait for
-                        // it after the P V
+                        // tile j + 2 has landed, so that the P V and the S go in as one run
+                        // (a check between them, with both issuers making it at the same
+                        // time, left the tensor core idle for hundreds of cycles per key
+                        // tile). Only when the K/V is not there yet (an item's first key
+                        // tiles) does the thread wait for it, after the P V
                         ok = wait(bar_p(t, (jt + j) & 1), (jt + j) >> 1);
                         const bool ahead = j + 2 < nk;
                         const int gk2 = gk + 2;
