@@ -181,10 +181,10 @@ int encode_pool_map_slab(CUtensorMap *map, const void *pool, int dtype, int head
 
 // TMA view of the queries of a prefill call for the tcgen05 kernel: q as a
 // 4-D tensor (x: 128-byte column slab elements, slab, query head, token) with
-// a box of one slab x `group` heads x 128 / group tokens, so that one box is a
-// Q tile's 128 rows (token, head of the group) of one column slab, 128-byte
-// swizzle. Strides in bytes: slab 128, head head_dim*eb, token
-// n_q_heads*head_dim*eb. Only for groups that divide 128.
+// a box of one slab x `group` heads x 128 / group whole tokens, so that one box
+// is a Q tile's rows (token, head of the group) of one column slab, 128-byte
+// swizzle: all 128 of them when the group divides 128. Strides in bytes: slab
+// 128, head head_dim*eb, token n_q_heads*head_dim*eb.
 int encode_q_map(CUtensorMap *map, const void *q, int dtype, int head_dim, int n_q_heads,
                  int num_tokens, int group) {
     EncodeTiledFn fn = nullptr;
@@ -505,13 +505,11 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     // path: 1 warp-level MMA kernel, 2 tcgen05 kernel (auto)
     const bool tc = g_opt_prefill_path != 1;
     CUtensorMap kmap, vmap, qmap = {};
-    // the tcgen05 kernel copies Q tiles by TMA when the group divides a tile's 128 rows
-    const bool q_tma = tc && 128 % group == 0;
     if (tc) {
         st = encode_pool_map_slab(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
         if (st != PAGEDKV_OK) return st;
         st = encode_pool_map_slab(&vmap, v_cache, dtype, head_dim, n_kv_heads, num_slots, block_size);
-        if (st == PAGEDKV_OK && q_tma)
+        if (st == PAGEDKV_OK)
             st = encode_q_map(&qmap, q, dtype, head_dim, n_q_heads, num_tokens, group);
     } else {
         st = encode_pool_map(&kmap, k_cache, dtype, head_dim, n_kv_heads, num_slots, block_size, 1,
@@ -534,7 +532,9 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     p.n_q_heads = n_q_heads;
     p.n_kv_heads = n_kv_heads;
     p.group = group;
-    p.tile_tokens = (tc ? pkv::kPfTcRows : pkv::kPfRows) / group;
+    // chunk tokens per item: the tcgen05 kernel's two Q tiles hold 128 / group
+    // whole tokens each
+    p.tile_tokens = tc ? 2 * (128 / group) : pkv::kPfRows / group;
     if (tc) {
         // the persistent kernel counts its work items in ints
         const long long per_seq = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens * n_kv_heads;
@@ -546,7 +546,6 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     while ((1 << log2_block) < block_size) ++log2_block;
     p.log2_block = log2_block;
     p.max_blocks = max_blocks_per_seq;
-    p.q_tma = q_tma ? 1 : 0;
     const cudaError_t e =
         tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, qmap, p, max_query_len, sms,
                                     static_cast<cudaStream_t>(stream))

@@ -26,12 +26,12 @@ struct PrefillParams {
     int n_q_heads;
     int n_kv_heads;
     int group;                   // n_q_heads / n_kv_heads
-    int tile_tokens;             // chunk tokens per CTA: kPfRows / group
+    int tile_tokens;             // chunk tokens per item: kPfRows / group (warp-level MMA
+                                 // kernel), 2 * (128 / group) (tcgen05 kernel)
     int num_blocks;
     int block_size;
     int log2_block;
     int max_blocks;
-    int q_tma;                   // tcgen05 kernel: Q tiles copied by TMA (the group divides 128)
 };
 
 // Bytes of dynamic shared memory the kernel asks for at this head_dim (16-bit types).
@@ -40,9 +40,9 @@ int prefill_smem_bytes(int head_dim);
 // The warp-level MMA kernel: grid (query tiles of the longest chunk, kv heads,
 // sequences), 64 query rows per CTA, pool maps with boxes of every column
 // block. The tcgen05 kernel: one persistent CTA per SM working through items
-// of 256 rows, pool maps with boxes of one 64-column block, and (when
-// p.q_tma) a map of q with boxes of [128 / group tokens][group heads][one
-// 64-column block].
+// of two Q tiles of 128 / group whole tokens each (tile_tokens = 2 * (128 /
+// group)), pool maps with boxes of one 64-column block, and a map of q with
+// boxes of [128 / group tokens][group heads][one 64-column block].
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, int max_query_len,
                            cudaStream_t stream);

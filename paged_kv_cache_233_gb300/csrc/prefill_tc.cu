@@ -5,8 +5,10 @@
 // to its own position, read through the block table), with the contractions
 // moved off the warp-level MMA pipe.
 //
-// A work item is (sequence, kv head, 256 query rows of (chunk token, query
-// head of the group)), held as two 128-row Q tiles that share every K/V tile.
+// A work item is (sequence, kv head, 2 * tq chunk tokens), held as two Q tiles
+// that share every K/V tile; a Q tile holds tq = 128 / group whole tokens, its
+// rows (token, query head of the group), 128 rows when the group divides 128
+// (126 for groups of 3, 6 or 7: the rows past them are masked).
 // The kernel is persistent: one CTA per SM works through its share of the
 // items (sequences ranked by context length, dealt in bands whose direction
 // alternates), and every ring, buffer and barrier phase runs on across items,
@@ -44,9 +46,7 @@
 //   warp 11    copies each item's Q tiles by TMA as soon as every S of the
 //              item before has completed (about two key tiles before the
 //              softmax warps finish it), and zeroes the V rows past a context
-//              (below). For a group that does not divide 128 (a Q tile's rows
-//              would split a token's heads) the softmax warps load Q instead,
-//              between items.
+//              (below).
 // V rows past the context are zeroed in shared memory before any P V reads
 // them (the tensor core would turn 0 * NaN into NaN): the V copies of a
 // context's last key tile land on a per-stage barrier of their own, and a
@@ -159,7 +159,7 @@ __device__ __forceinline__ void sts32(uint32_t addr, int v) {
 // 256 rows of (chunk token, query head of the group)), held as two Q tiles.
 struct PfItem {
     int s, h;
-    int q0, j0, rows, pos0, L;
+    int q0, j0, ntok, pos0, L;   // ntok: chunk tokens of the item
     int nk[kTcTiles];   // key tiles of Q tile t: through the position of its last row
     int nkt;            // key tiles of the item (those of its last row)
     bool tail;          // the last key tile runs past the context
@@ -197,12 +197,15 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
     it.q0 = q0;
     it.j0 = j0;
     it.L = L;
-    it.rows = min(p.tile_tokens, n - j0) * p.group;
+    it.ntok = min(p.tile_tokens, n - j0);
     it.pos0 = L - n + j0;
+    // Q tile t holds the item's tokens t*tq .. t*tq + tq - 1, tq = 128 / group
+    // whole tokens (all of a token's heads in one tile)
+    const int tq = kTcRows / p.group;
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) {
-        const int rt = min(max(it.rows - t * kTcRows, 0), kTcRows);
-        it.nk[t] = rt > 0 ? (it.pos0 + (t * kTcRows + rt - 1) / p.group) / kTcKeys + 1 : 0;
+        const int nt = min(max(it.ntok - t * tq, 0), tq);
+        it.nk[t] = nt > 0 ? (it.pos0 + t * tq + nt - 1) / kTcKeys + 1 : 0;
     }
     it.nkt = it.nk[kTcTiles - 1] > 0 ? it.nk[kTcTiles - 1] : it.nk[0];
     it.tail = it.nkt * kTcKeys > L;
@@ -251,8 +254,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_init(bar(bar_p(t, b)), kTcRows / 32);   // one arrival per softmax warp
                 mbar_init(bar(bar_o(t, b)), 1);
             }
-            // Q full: the copy's bytes (one arrival), or one arrival per softmax warp
-            mbar_init(bar(bar_qfull(t)), p.q_tma ? 1 : kTcRows / 32);
+            mbar_init(bar(bar_qfull(t)), 1);   // the Q copy's arrival and bytes
             mbar_init(bar(bar_qfree(t)), 1);
         }
         mbar_init(bar(kDone), kTcTiles);
@@ -375,12 +377,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         __syncwarp();
     } else if (warp == kZeroWarp) {
         // ------------------------------------------------ Q copies and V tails
-        // Q: when the group divides a tile's 128 rows, lane 0 copies each Q
-        // tile of an item with one TMA box per 64-column block ([128/g tokens]
-        // [g heads][64 columns], which lands as the tile's rows (token, head)
-        // in the swizzled layout the tensor core reads), as soon as every S
-        // MMA of the item before has completed: about two key tiles before
-        // the softmax warps finish that item, so the copy is off their path.
+        // Q: lane 0 copies each Q tile of an item with one TMA box per
+        // 64-column block ([tq = 128/g whole tokens][g heads][64 columns],
+        // which lands as the tile's first tq*g rows (token, head) in the
+        // swizzled layout the tensor core reads; the rows past them, when g
+        // does not divide 128, hold whatever they held: the softmax masks every
+        // key of such a row), as soon as every S MMA of the item
+        // before has completed: about two key tiles before the softmax warps
+        // finish that item, so the copy is off their path.
         // V: the rows past a context (never written for the sequence, or left
         // in the stage by an earlier tile) become zeros once the tile's V
         // copies have landed: the tensor core would turn 0 * NaN into NaN.
@@ -388,7 +392,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // issuers reach that tile's S two key tiles ahead of its P V, which
         // hides the wait. An item's Q copies go first: its S MMAs, which the
         // item's last stage waits for, need them.
-        if (lane == 0 && p.q_tma) tma_prefetch_descriptor(&qmap);
+        if (lane == 0) tma_prefetch_descriptor(&qmap);
+        const int tq = kTcRows / g;
         int kt = 0;
         int i = 0;
         // per Q tile, the last item that took a phase of its Q full barrier (a
@@ -402,7 +407,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             if (k >= num_items) break;
             PfItem it;
             if (!pf_item(p, ranked, tiles, k, false, it)) continue;
-            if (p.q_tma) {
+            {
                 bool got = true;
                 if (lane == 0) {
 #pragma unroll
@@ -412,10 +417,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         if (!got) break;
                         if (it.nk[t] > 0) {
                             const uint32_t full = bar(bar_qfull(t));
-                            mbar_arrive_expect_tx(full, uint32_t(Ly::kQTile));
+                            mbar_arrive_expect_tx(full, uint32_t(Ly::kSlabs * tq * g * 128));
                             // rows past the item are another sequence's tokens, or zeros past
                             // the last token: the softmax masks every key of such a row
-                            const int tok = it.q0 + it.j0 + t * (kTcRows / g);
+                            const int tok = it.q0 + it.j0 + t * tq;
                             for (int sl = 0; sl < Ly::kSlabs; ++sl)
                                 tma_load_4d(base + Ly::kQ + t * Ly::kQTile + sl * Ly::kQSlab, &qmap, 0, sl,
                                             it.h * g, tok, full);
@@ -599,7 +604,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const int t = (warp - 2) >> 2;                 // Q tile of this warp
         const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
         const int r = 32 * quarter + lane;             // row within the Q tile
-        const int R = t * kTcRows + r;                 // row within the item
+        const int R = t * kTcRows + r;                 // row slot within the item
+        const int tq = kTcRows / g;                    // whole tokens per Q tile
         const uint32_t trow = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(t * kTmemTile);
         const uint32_t otile = trow + uint32_t(2 * kTcKeys);
         bool ok = true;
@@ -647,33 +653,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             PfItem it;
             if (!pf_item(p, ranked, tiles, k, false, it)) continue;
             const int nk = it.nk[t];
-            const bool row = R < it.rows;
-            const int pos = row ? it.pos0 + R / g : -1;
-            const unsigned long long qrow = (unsigned long long)(it.q0 + it.j0 + (row ? R / g : 0)) * p.n_q_heads +
-                                            it.h * g + (row ? R % g : 0);
-            // Q rows of this item (unless a TMA copy brings them), once every S of
-            // the previous item has read Q
-            if (i > 0 && !p.q_tma) {
-                const bool got = !aborted() && mbar_wait(bar(bar_qfree(t)), uint32_t((i - 1) & 1), p.err);
-                if (!__all_sync(kAll, got)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!p.q_tma) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + qrow * D);
-                const uint32_t qdst = base + Ly::kQ + t * Ly::kQTile + r * 128;
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 v = row ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                    sts128(qdst + (c >> 3) * Ly::kQSlab + (((c & 7) ^ (r & 7)) << 4), v);
-                }
-                // every lane's stores are ordered for the tensor core's (async proxy)
-                // reads by its own fence; after the warp barrier one lane arrives
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_qfull(t)));
-            }
+            // this thread's row: token tok of the item (t*tq + r/g), head r%g of the
+            // group; none past the tile's tq*g rows or the item's tokens
+            const int tok = t * tq + r / g;
+            const bool row = r < tq * g && tok < it.ntok;
+            const int pos = row ? it.pos0 + tok : -1;
+            const unsigned long long qrow =
+                (unsigned long long)(it.q0 + it.j0 + (row ? tok : 0)) * p.n_q_heads + it.h * g + (row ? r % g : 0);
             // the previous item's output (its tensor-memory loads complete before
             // this warp's next arrival on a P barrier, which lets O be overwritten)
             if (i > 0 && !epilogue()) {

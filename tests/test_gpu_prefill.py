@@ -70,9 +70,11 @@ def test_prefill_matches_oracle(orc, dtype, D, B, g):
     assert err <= TOL[dtype], f"max-abs error {err:.3e}"
 
 
-@pytest.mark.parametrize("g", [3, 16, 64])
+@pytest.mark.parametrize("g", [3, 5, 6, 7, 16, 48, 64])
 def test_prefill_odd_and_large_groups(orc, g):
-    """Groups that do not divide the 64-row tile evenly, and a whole tile of heads."""
+    """Groups that do not divide a tile's rows (the warp-level kernel's 64, the
+    tcgen05 kernel's 128: its Q tiles then hold 128 // g whole tokens, 96 rows
+    for 48), and a whole tile of heads."""
     cases = [(0, 9), (40, 33), (7, 70)]
     wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, g, seed=200 + g, cases=cases, n_kv=1)
     out = prefill(wl, qs, q, kc, vc, bt)
@@ -192,8 +194,8 @@ def test_many_items_per_cta(orc, g, n_kv):
     tcgen05 kernel's persistent CTAs each work through many: chunks of one
     row to three query tiles, chunks whose second Q tile is empty, contexts
     on a 64-key boundary and ragged ones, every output row against the oracle
-    (groups that divide 128, whose Q tiles are copied by TMA, and one that
-    does not, whose Q rows the softmax warps load)."""
+    (groups that divide 128, and 3, whose Q tiles hold 42 whole tokens, 126
+    rows)."""
     rng = np.random.default_rng(520)
     before = rng.integers(0, 900, size=40)
     chunk = rng.integers(1, 600, size=40)

@@ -63,7 +63,8 @@ def make_items(cta, grid, before, chunk, g, n_kv):
     """The items of CTA `cta`, in the kernel's order."""
     lens = [b + c for b, c in zip(before, chunk)]
     qs = np.concatenate([[0], np.cumsum(chunk)])
-    tile_tokens = 2 * ROWS // g
+    tq = ROWS // g                  # whole tokens per Q tile
+    tile_tokens = 2 * tq
     tiles = -(-max(chunk) // tile_tokens)
     S = len(chunk)
     ranked = sorted(range(S), key=lambda s: (-lens[s], s)) if S > 1 else list(range(S))
@@ -82,15 +83,15 @@ def make_items(cta, grid, before, chunk, g, n_kv):
         j0 = qt * tile_tokens
         if j0 >= n:
             continue
-        rows = min(tile_tokens, n - j0) * g
+        ntok = min(tile_tokens, n - j0)
         pos0 = L - n + j0
-        nk = [(pos0 + (t * ROWS + min(max(rows - t * ROWS, 0), ROWS) - 1) // g) // KEYS + 1
-              if rows > t * ROWS else 0 for t in range(TILES)]
+        nk = [(pos0 + t * tq + min(ntok - t * tq, tq) - 1) // KEYS + 1 if ntok > t * tq else 0
+              for t in range(TILES)]
         nkt = nk[1] if nk[1] > 0 else nk[0]
         items.append(dict(nk=nk, nkt=nkt, tail=nkt * KEYS > L))
 
 
-def run_cta(items, q_tma, rng, ofree=False):
+def run_cta(items, rng, ofree=False):
     """Runs one CTA's roles to the end; returns the roles left waiting (empty
     when every role finished)."""
     bars = {}
@@ -127,16 +128,15 @@ def run_cta(items, q_tma, rng, ofree=False):
         kt = 0
         tail_phase = [0] * STAGES
         for i, it in enumerate(items):
-            if q_tma:
-                for t in range(TILES):
-                    if i > 0:
-                        yield ("qfree", t), i - 1
-                    if it["nk"][t] > 0:
-                        B(("qfull", t)).expect(1)
-                        B(("qfull", t)).arrive()
-                        B(("qfull", t)).land(1)
-                    else:
-                        B(("qfull", t)).arrive()
+            for t in range(TILES):
+                if i > 0:
+                    yield ("qfree", t), i - 1
+                if it["nk"][t] > 0:
+                    B(("qfull", t)).expect(1)
+                    B(("qfull", t)).arrive()
+                    B(("qfull", t)).land(1)
+                else:
+                    B(("qfull", t)).arrive()
             if it["tail"]:
                 st = (kt + it["nkt"] - 1) % STAGES
                 yield ("tailv", st), tail_phase[st]
@@ -187,10 +187,6 @@ def run_cta(items, q_tma, rng, ofree=False):
         jt = prev_nk = prev_end = 0
         for i, it in enumerate(items):
             nk = it["nk"][t]
-            if not q_tma:
-                if i > 0:
-                    yield ("qfree", t), i - 1
-                B(("qfull", t)).arrive()
             if i > 0:
                 if prev_nk:
                     yield ("o", t, (prev_end - 1) & 1), (prev_end - 1) >> 1
@@ -233,11 +229,10 @@ def many_items_workload():
 
 
 def check(before, chunk, g, n_kv, grid, seeds, ofree=False):
-    q_tma = 128 % g == 0
     for cta in range(grid):
         items = make_items(cta, grid, before, chunk, g, n_kv)
         for seed in range(seeds):
-            left = run_cta(items, q_tma, np.random.default_rng(seed), ofree=ofree)
+            left = run_cta(items, np.random.default_rng(seed), ofree=ofree)
             assert not left, f"cta {cta} seed {seed}: deadlock, waiting {left}"
 
 
@@ -246,8 +241,8 @@ def check(before, chunk, g, n_kv, grid, seeds, ofree=False):
 def test_no_deadlock_or_phase_hazard(g, n_kv, grid):
     """Chunks of one row to three query tiles, contexts on a 64-key boundary
     and ragged, second Q tiles empty: every interleaving tried ends, with no
-    barrier two phases past a waiter (groups that divide 128, whose Q tiles a
-    TMA copy brings, and 3, whose Q rows the softmax warps load)."""
+    barrier two phases past a waiter or one behind it (groups that divide 128
+    and 3, whose Q tiles hold 42 whole tokens)."""
     before, chunk = many_items_workload()
     check(before, chunk, g, n_kv, grid, seeds=3)
 
