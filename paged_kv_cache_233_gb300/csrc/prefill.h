@@ -53,6 +53,5 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
-constexpr int kPfTcRows = 256;   // query rows per CTA of the tcgen05 kernel (two tiles of 128)
 
 }  // namespace pkv
