@@ -53,5 +53,4 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
-
 }  // namespace pkv
