@@ -471,21 +471,30 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         __syncwarp();
     } else if (warp == 1 || warp == kIssuer1Warp) {
         // ------------------------------------------------------- MMA issuers
-        // One thread per Q tile issues that tile's MMAs. A thread that issues
+        // One warp per Q tile issues that tile's MMAs. A thread that issues
         // tcgen05.mma runs only about two MMAs ahead of the tensor core, so
-        // every wait of an issuing thread is idle tensor time; with one issuer
-        // per tile, one tile's MMAs go in while the other's issuer waits.
-        if (lane == 0) {
+        // every wait of an issuing warp is idle tensor time; with one issuer
+        // per tile, one tile's MMAs go in while the other's issuer waits. The
+        // whole warp runs the loop and its waits (so that the descriptors and
+        // addresses are warp-uniform values), and lane 0 alone issues each
+        // tcgen05.mma and tcgen05.commit (a commit tracks its own thread's MMAs).
+        {
             const int t = warp == 1 ? 0 : 1;
+            const bool leader = lane == 0;
             constexpr uint32_t kIdS = tc_idesc_f16(kBf16, false, kTcRows, kTcKeys);
             constexpr uint32_t kIdO = tc_idesc_f16(kBf16, true, kTcRows, D);
+            // every lane waits; the warp goes on only if all of them saw the phase
             // (a phase already complete passes at once; the abort flag is read only
-            // when the thread has to wait)
+            // when the lane has to wait)
             auto wait = [&](int i, int phase) {
-                if (mbar_try_wait(bar(i), uint32_t(phase & 1))) return true;
-                return !aborted() && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
+                bool got = mbar_try_wait(bar(i), uint32_t(phase & 1));
+                if (!got) got = !aborted() && mbar_wait(bar(i), uint32_t(phase & 1), p.err);
+                return __all_sync(kAll, got);
             };
-            // The issuing thread shares its SM sub-partition with two softmax warps,
+            auto commit = [&](int i) {
+                if (leader) tc_commit(bar(i));
+            };
+            // The issuing warp shares its SM sub-partition with two softmax warps,
             // so every instruction it spends per MMA slows the MMAs' issue: the
             // shared-memory descriptors are built once (Q's for the whole kernel,
             // a stage's per use) and a K step only offsets a descriptor's start
@@ -499,14 +508,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             auto issue_s = [&](int gk, int gj) {
                 const uint64_t kdesc = tc_desc_sw128(base + Ly::kKv + (gk % kTcStages) * Ly::kStage, 16, 1024);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // (start addresses stay below 2^18 bytes: the offset never carries
-                    // out of the descriptor's 14-bit address field)
-                    const uint64_t b = kdesc + uint64_t(((kk >> 2) * Ly::kKvSlab + (kk & 3) * 32) >> 4);
-                    tc_mma_f16(d, qdesc[kk], b, kIdS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        // (start addresses stay below 2^18 bytes: the offset never carries
+                        // out of the descriptor's 14-bit address field)
+                        const uint64_t b = kdesc + uint64_t(((kk >> 2) * Ly::kKvSlab + (kk & 3) * 32) >> 4);
+                        tc_mma_f16(d, qdesc[kk], b, kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(bar_s(t, gj & 1)));
                 }
-                tc_commit(bar(bar_s(t, gj & 1)));
             };
             // O (+)= P V; `first` starts the item's accumulator
             auto issue_pv = [&](int gk, int gj, bool first) {
@@ -515,11 +526,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 // P: the first 32 columns of S buffer gj & 1 (16 keys per 8 columns)
                 const uint32_t pa = tmem + uint32_t(t * kTmemTile + (gj & 1) * kTcKeys);
                 const uint32_t d = tmem + uint32_t(t * kTmemTile + 2 * kTcKeys);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), vdesc + uint64_t((kk * 2048) >> 4), kIdO,
-                                      (!first || kk > 0) ? 1u : 0u);
-                tc_commit(bar(bar_o(t, gj & 1)));
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                        tc_mma_f16_tmem_a(d, pa + uint32_t(8 * kk), vdesc + uint64_t((kk * 2048) >> 4), kIdO,
+                                          (!first || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(bar_o(t, gj & 1)));
+                }
             };
             int kt = 0;   // ring position of the item's first key tile
             int jt = 0;   // key tiles of this Q tile before the item (S, P and O barrier phases)
@@ -543,7 +556,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                     if (!ok) break;
                     // Q may be overwritten once the item's last S has completed
-                    if (nk <= 2) tc_commit(bar(bar_qfree(t)));
+                    if (nk <= 2) commit(bar_qfree(t));
                 }
                 for (int j = 0; ok && j < it.nkt; ++j) {
                     const int gk = kt + j;
@@ -555,18 +568,19 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         // (a check between them, with both issuers making it at the same
                         // time, left the tensor core idle for hundreds of cycles per key
                         // tile). Only when the K/V is not there yet (an item's first key
-                        // tiles) does the thread wait for it, after the P V
+                        // tiles) does the warp wait for it, after the P V
                         ok = wait(bar_p(t, (jt + j) & 1), (jt + j) >> 1);
                         const bool ahead = j + 2 < nk;
                         const int gk2 = gk + 2;
-                        const bool kv_in = ok && ahead &&
-                                           mbar_test_wait(bar(kKvFull + gk2 % kTcStages), uint32_t((gk2 / kTcStages) & 1));
+                        const bool kv_in = __all_sync(
+                            kAll, ok && ahead &&
+                                      mbar_test_wait(bar(kKvFull + gk2 % kTcStages), uint32_t((gk2 / kTcStages) & 1)));
                         if (!ok) break;
                         tc_fence_after_sync();
                         issue_pv(gk, jt + j, j == 0);
                         // the stage of key tile j is free once this P V (the last MMA of
                         // this thread that reads it) completes
-                        tc_commit(bar(kKvEmpty + gk % kTcStages));
+                        commit(kKvEmpty + gk % kTcStages);
                         // this tile's S two key tiles ahead (its S buffer is free once the
                         // P V just issued has read P)
                         if (ahead) {
@@ -576,27 +590,29 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                 tc_fence_after_sync();
                             }
                             issue_s(gk2, jt + j + 2);
-                            if (j + 2 == nk - 1) tc_commit(bar(bar_qfree(t)));
+                            if (j + 2 == nk - 1) commit(bar_qfree(t));
                         }
                     } else {
                         // a key tile this Q tile skips: its stage may be released only
                         // after it landed (the arrival belongs to this phase of the slot)
                         ok = wait(kKvFull + gk % kTcStages, gk / kTcStages);
                         if (!ok) break;
-                        tc_commit(bar(kKvEmpty + gk % kTcStages));
+                        commit(kKvEmpty + gk % kTcStages);
                     }
                 }
                 if (!ok) break;
                 // no MMA of this tile reads Q in this item: Q is free at once
-                if (nk == 0) mbar_arrive(bar(bar_qfree(t)));
+                if (nk == 0 && leader) mbar_arrive(bar(bar_qfree(t)));
                 kt += it.nkt;
                 jt += nk;
                 ++i;
             }
-            if (!ok) sts32(flag, 1);
-            // every MMA of both issuers has completed before tensor memory is freed
-            tc_commit(bar(kDone));
-            mbar_wait(bar(kDone), 0, p.err);
+            if (leader) {
+                if (!ok) sts32(flag, 1);
+                // every MMA of both issuers has completed before tensor memory is freed
+                tc_commit(bar(kDone));
+                mbar_wait(bar(kDone), 0, p.err);
+            }
         }
         __syncwarp();
     } else {
