@@ -237,10 +237,11 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
  * memory (default), or warp-level m16n8k16 MMAs.
  *
  *   q, out         [num_tokens][n_q_heads][head_dim] of dtype, device, 16-byte aligned;
- *                  every row of q may be read (the tcgen05 kernel copies whole
- *                  128-row Q tiles by TMA when the group divides 128), but a row
- *                  outside a chunk, such as padding past query_start[num_seqs],
- *                  never reaches an output row and its out row is not written
+ *                  every row of q may be read (the tcgen05 kernel copies Q
+ *                  tiles of 128 / group whole tokens by TMA, past a chunk's end
+ *                  too), but a row outside a chunk, such as padding past
+ *                  query_start[num_seqs], never reaches an output row and its
+ *                  out row is not written
  *   k_cache,
  *   v_cache        [num_blocks][block_size][n_kv_heads][head_dim], device, 16-byte aligned
  *   block_tables   int32 [num_seqs][max_blocks_per_seq], device
