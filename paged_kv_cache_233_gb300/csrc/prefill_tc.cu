@@ -12,7 +12,7 @@
 // The kernel is persistent: one CTA per SM works through its share of the
 // items (sequences ranked by context length, dealt in bands whose direction
 // alternates), and every ring, buffer and barrier phase runs on across items,
-// so that an item's Q load, first K/V tiles and first S MMAs overlap the
+// so that an item's Q copy, first K/V tiles and first S MMAs overlap the
 // previous item's last P V and epilogue. Twelve warps:
 //   warp 0     producer: per 64-key tile, lane 0 waits for a free stage of a
 //              four-stage ring and arms its barrier; then one lane per (16
@@ -21,13 +21,14 @@
 //              block][64 keys][128 B] with 128-byte swizzle (the canonical
 //              layout the tensor core reads);
 //   warps 1,10 MMA issuers, one per Q tile (warp 1 also allocates tensor
-//              memory); lane 0 issues, for its tile, S = Q K^T into one of two
-//              S buffers in tensor memory and, once the softmax has written P,
-//              O += P V with P read from tensor memory, into the O accumulator
-//              that stays in tensor memory for the whole key loop; completions
-//              are tracked by tcgen05.commit on mbarriers. An issuing thread
-//              runs only about two MMAs ahead of the tensor core, so each of
-//              its waits leaves the tensor core idle unless the other tile's
+//              memory): the warp runs the loop and its waits, and lane 0
+//              issues, for its tile, S = Q K^T into one of two S buffers in
+//              tensor memory and, once the softmax has written P, O += P V
+//              with P read from tensor memory, into the O accumulator that
+//              stays in tensor memory for the whole key loop; completions are
+//              tracked by tcgen05.commit on mbarriers. An issuing thread runs
+//              only about two MMAs ahead of the tensor core, so each of its
+//              waits leaves the tensor core idle unless the other tile's
 //              issuer has MMAs to give it;
 //   warps 2-9  softmax, four warps per Q tile, one thread per query row (=
 //              tensor-memory lane), so that every SM sub-partition runs two
@@ -72,7 +73,8 @@ constexpr int kTcRows = 128;     // query rows per Q tile = tensor-memory lanes
 constexpr int kTcKeys = 64;      // keys per pipeline stage
 constexpr int kTcStages = 4;
 // warp 0 producer, warp 1 MMA issuer of Q tile 0, warps 2-9 softmax, warp 10
-// MMA issuer of Q tile 1, warp 11 zeroes the V rows past a context
+// MMA issuer of Q tile 1, warp 11 copies Q tiles and zeroes the V rows past a
+// context
 constexpr int kIssuer1Warp = 2 + kTcTiles * kTcRows / 32;
 constexpr int kZeroWarp = kIssuer1Warp + 1;
 constexpr int kTcThreads = 32 * (kZeroWarp + 1);
