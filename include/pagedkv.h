@@ -270,6 +270,49 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
                             int max_blocks_per_seq, int dtype, void *stream);
 
 /*
+ * paged_attention_prefill_split -- the same attention with each item's keys
+ * split over key_parts work items (a split-K over the key range), for calls
+ * with fewer items than SMs (one short chunk, few sequences): every (sequence,
+ * 2 * (128 / group) chunk tokens, kv head) item of the tcgen05 kernel becomes
+ * key_parts items over contiguous ranges of its 64-key tiles. Each writes its
+ * rows' unnormalised fp32 output and softmax state to `workspace`, and a merge
+ * kernel on the same stream combines them into `out` (softmax's LSE identity,
+ * the same one split-K decode uses). The result equals
+ * paged_attention_prefill's within rounding.
+ *
+ *   key_parts        1 .. 16; 1 is paged_attention_prefill itself; 0 picks
+ *                    the most parts whose items still fit one wave of the SMs
+ *                    (the items counted from max_query_len), as many as the
+ *                    workspace holds (1 without one)
+ *   workspace        device, 256-byte aligned, caller-owned, at least
+ *                    paged_attention_prefill_workspace_bytes(num_tokens,
+ *                    n_q_heads, head_dim, key_parts) bytes; its contents on
+ *                    entry do not matter and are garbage afterwards
+ *   other arguments  as for paged_attention_prefill
+ *
+ * Returns PAGEDKV_ERR_WORKSPACE when key_parts >= 2 and the workspace is
+ * missing or too small, PAGEDKV_ERR_INVALID_ARG for key_parts outside 0 .. 16
+ * or a misaligned workspace; otherwise as paged_attention_prefill (whose
+ * device errors it sets the same way). With PAGEDKV_OPT_PREFILL_PATH = 1 (the
+ * warp-level MMA kernel) the keys are not split. Asynchronous on `stream`;
+ * allocates nothing.
+ */
+int paged_attention_prefill_split(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *query_start,
+                                  const int32_t *context_lens, float scale, void *out, int num_seqs,
+                                  int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int num_blocks, int block_size,
+                                  int max_blocks_per_seq, int dtype, int key_parts, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of paged_attention_prefill_split for key_parts (2 .. 16;
+ * 0 for anything else): fp32 outputs [key_parts][num_tokens * n_q_heads]
+ * [head_dim], then two fp32 [key_parts][num_tokens * n_q_heads] arrays, each
+ * on a 256-byte boundary. */
+size_t paged_attention_prefill_workspace_bytes(int num_tokens, int n_q_heads, int head_dim,
+                                               int key_parts);
+
+/*
  * paged_attention_decode -- fused paged-attention decode.
  *
  * The kernel the pages name as the next step and never build (page "Paged-KV +

@@ -34,6 +34,7 @@ __all__ = [
     "paged_attention_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "PARTITION_BALANCED",
     "paged_kv_copy_blocks", "paged_attention_decode_shared_prefix", "paged_kv_swap_blocks",
     "paged_attention_prefill", "paged_kv_append_tokens", "check_bounded_wait", "DEVERR_TIMEOUT",
+    "prefill_workspace_bytes", "prefill_workspace",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,7 +51,8 @@ EXPORTS = ("paged_kv_slot_mapping", "paged_kv_append", "paged_attention_decode",
            "pagedkv_get_option", "pagedkv_last_decode_path", "pagedkv_status_string",
            "pagedkv_abi_version", "paged_attention_decode_noalloc", "paged_kv_copy_blocks",
            "paged_attention_decode_shared_prefix", "paged_kv_append_tokens",
-           "pagedkv_check_bounded_wait")
+           "pagedkv_check_bounded_wait", "paged_attention_prefill_split",
+           "paged_attention_prefill_workspace_bytes")
 
 
 class PagedKVError(RuntimeError):
@@ -96,6 +98,12 @@ def load():
     lib.paged_attention_prefill.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32,
                                             i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.paged_attention_prefill.restype = i32
+    lib.paged_attention_prefill_split.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, i32,
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                                  vp, sz, vp]
+    lib.paged_attention_prefill_split.restype = i32
+    lib.paged_attention_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.paged_attention_prefill_workspace_bytes.restype = sz
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
     lib.pagedkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -277,12 +285,15 @@ def paged_kv_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
 
 
 def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale,
-                            out, max_query_len=None, stream=None):
+                            out, max_query_len=None, stream=None, workspace=None, key_parts=1):
     """Chunked-prefill attention: q/out [num_tokens][Hq][D] hold every sequence's
     chunk of query rows, sequence after sequence, delimited by query_start
     [num_seqs + 1]; context_lens counts each sequence's cached tokens with its
     chunk (already appended) included. max_query_len bounds every chunk's
-    length; by default it is read from query_start (a device-to-host copy)."""
+    length; by default it is read from query_start (a device-to-host copy).
+    With a workspace (see prefill_workspace) the keys of each work item may be
+    split over key_parts items (0: as many as fill the SMs and the workspace),
+    whose states a merge kernel combines."""
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise PagedKVError("q and out must be [num_tokens][n_q_heads][head_dim] of one type")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != q.dtype:
@@ -293,13 +304,31 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, cont
     if max_query_len is None:
         max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if S else 0
     NB, B, Hkv, D = k_cache.shape
-    st = load().paged_attention_prefill(
-        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        _dev(block_tables, "block_tables", torch.int32), _dev(query_start, "query_start", torch.int32),
-        _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S,
-        q.shape[0], int(max_query_len), q.shape[1], Hkv, D, NB, B, block_tables.shape[1],
-        _code(q), _stream(stream))
-    _check(st, "paged_attention_prefill")
+    args = (_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32), _dev(query_start, "query_start", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32), float(scale), _dev(out, "out"), S,
+            q.shape[0], int(max_query_len), q.shape[1], Hkv, D, NB, B, block_tables.shape[1], _code(q))
+    if workspace is None and key_parts == 1:
+        st = load().paged_attention_prefill(*args, _stream(stream))
+        _check(st, "paged_attention_prefill")
+        return
+    ws = _dev(workspace, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().paged_attention_prefill_split(*args, int(key_parts), ws, nbytes, _stream(stream))
+    _check(st, "paged_attention_prefill_split")
+
+
+def prefill_workspace_bytes(num_tokens, n_q_heads, head_dim, key_parts):
+    """Workspace bytes of a prefill whose keys are split key_parts ways (0 below 2)."""
+    return load().paged_attention_prefill_workspace_bytes(int(num_tokens), int(n_q_heads), int(head_dim),
+                                                          int(key_parts))
+
+
+def prefill_workspace(q, key_parts):
+    """A device buffer for paged_attention_prefill(..., workspace=..., key_parts=...)
+    (key_parts 0 gets room for the largest split, 16)."""
+    n = prefill_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], key_parts if key_parts else 16)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
 
 
 def paged_attention_workspace_bytes(num_seqs, n_q_heads, head_dim, max_blocks_per_seq, block_size,

@@ -472,12 +472,24 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 
-int paged_attention_prefill(const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *block_tables, const int32_t *query_start,
-                            const int32_t *context_lens, float scale, void *out, int num_seqs,
-                            int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
-                            int head_dim, int num_blocks, int block_size,
-                            int max_blocks_per_seq, int dtype, void *stream) {
+namespace {
+
+constexpr int kMaxKeyParts = 16;
+
+// Bytes of the key split's workspace: fp32 O [parts][rows][head_dim], then m
+// and l [parts][rows], each on a 256-byte boundary (rows = tokens x query heads).
+size_t prefill_split_bytes(long long rows, int head_dim, int parts) {
+    return round256(size_t(parts) * size_t(rows) * size_t(head_dim) * 4) +
+           2 * round256(size_t(parts) * size_t(rows) * 4);
+}
+
+int prefill_impl(const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *query_start,
+                 const int32_t *context_lens, float scale, void *out, int num_seqs, int num_tokens,
+                 int max_query_len, int n_q_heads, int n_kv_heads, int head_dim, int num_blocks,
+                 int block_size, int max_blocks_per_seq, int dtype, int key_parts, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    if (key_parts < 0 || key_parts > kMaxKeyParts) return PAGEDKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || n_q_heads < 1 || n_kv_heads < 1 ||
         head_dim < 1 || num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 1 ||
         !valid_dtype(dtype))
@@ -535,9 +547,31 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     // chunk tokens per item: the tcgen05 kernel's two Q tiles hold 128 / group
     // whole tokens each
     p.tile_tokens = tc ? 2 * (128 / group) : pkv::kPfRows / group;
+    // key split (tcgen05 kernel only): 0 picks the most parts whose items still
+    // fit one wave of the SMs, as far as the workspace holds them
+    const long long tiles = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    const long long rows = (long long)num_tokens * n_q_heads;
+    int parts = tc ? key_parts : 1;
+    if (parts == 0) {
+        const long long items = tiles * n_kv_heads * num_seqs;
+        parts = int(items >= sms ? 1 : sms / items);
+        if (parts > kMaxKeyParts) parts = kMaxKeyParts;
+        while (parts > 1 && (!workspace || prefill_split_bytes(rows, head_dim, parts) > workspace_bytes))
+            --parts;
+    }
+    if (parts > 1) {
+        if (!workspace || prefill_split_bytes(rows, head_dim, parts) > workspace_bytes)
+            return PAGEDKV_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return PAGEDKV_ERR_INVALID_ARG;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        p.ws_o = reinterpret_cast<float *>(ws);
+        p.ws_m = reinterpret_cast<float *>(ws + round256(size_t(parts) * size_t(rows) * size_t(head_dim) * 4));
+        p.ws_l = p.ws_m + round256(size_t(parts) * size_t(rows) * 4) / 4;
+    }
+    p.key_parts = parts;
     if (tc) {
         // the persistent kernel counts its work items in ints
-        const long long per_seq = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens * n_kv_heads;
+        const long long per_seq = tiles * n_kv_heads * parts;
         if (per_seq > (INT_MAX / 2) / num_seqs) return PAGEDKV_ERR_UNSUPPORTED;
     }
     p.num_blocks = num_blocks;
@@ -546,12 +580,47 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
     while ((1 << log2_block) < block_size) ++log2_block;
     p.log2_block = log2_block;
     p.max_blocks = max_blocks_per_seq;
-    const cudaError_t e =
+    cudaError_t e =
         tc ? pkv::launch_prefill_tc(dtype, head_dim, kmap, vmap, qmap, p, max_query_len, sms,
                                     static_cast<cudaStream_t>(stream))
            : pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
                                  static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && parts > 1)
+        e = pkv::launch_prefill_merge(dtype, head_dim, p, max_query_len, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
+}
+
+}  // namespace
+
+int paged_attention_prefill(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *query_start,
+                            const int32_t *context_lens, float scale, void *out, int num_seqs,
+                            int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
+                            int head_dim, int num_blocks, int block_size,
+                            int max_blocks_per_seq, int dtype, void *stream) {
+    return prefill_impl(q, k_cache, v_cache, block_tables, query_start, context_lens, scale, out,
+                        num_seqs, num_tokens, max_query_len, n_q_heads, n_kv_heads, head_dim,
+                        num_blocks, block_size, max_blocks_per_seq, dtype, 1, nullptr, 0, stream);
+}
+
+int paged_attention_prefill_split(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *query_start,
+                                  const int32_t *context_lens, float scale, void *out, int num_seqs,
+                                  int num_tokens, int max_query_len, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int num_blocks, int block_size,
+                                  int max_blocks_per_seq, int dtype, int key_parts, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    return prefill_impl(q, k_cache, v_cache, block_tables, query_start, context_lens, scale, out,
+                        num_seqs, num_tokens, max_query_len, n_q_heads, n_kv_heads, head_dim,
+                        num_blocks, block_size, max_blocks_per_seq, dtype, key_parts, workspace,
+                        workspace_bytes, stream);
+}
+
+size_t paged_attention_prefill_workspace_bytes(int num_tokens, int n_q_heads, int head_dim,
+                                               int key_parts) {
+    if (num_tokens < 1 || n_q_heads < 1 || head_dim < 1 || key_parts < 2 || key_parts > kMaxKeyParts)
+        return 0;
+    return prefill_split_bytes((long long)num_tokens * n_q_heads, head_dim, key_parts);
 }
 
 size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,

@@ -32,6 +32,15 @@ struct PrefillParams {
     int block_size;
     int log2_block;
     int max_blocks;
+    // tcgen05 kernel, key split: each item's key tiles are dealt to key_parts
+    // items of contiguous ranges, which write their rows' unnormalised fp32 O,
+    // reference maximum m (base 2, scaled) and sum l to ws_o [part][row][D],
+    // ws_m and ws_l [part][row] (row = token * n_q_heads + query head) for
+    // launch_prefill_merge; key_parts == 1 writes `out` itself
+    int key_parts;
+    float *ws_o;
+    float *ws_m;
+    float *ws_l;
 };
 
 // Bytes of dynamic shared memory the kernel asks for at this head_dim (16-bit types).
@@ -52,5 +61,10 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               const PrefillParams &p, int max_query_len, int num_sms,
                               cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
+
+// The key split's merge: per row of every item, the parts' states combined
+// into `out` (rows of a flagged sequence left unwritten, as the kernel does).
+cudaError_t launch_prefill_merge(int dtype, int head_dim, const PrefillParams &p, int max_query_len,
+                                 cudaStream_t stream);
 
 }  // namespace pkv

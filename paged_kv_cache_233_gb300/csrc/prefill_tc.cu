@@ -104,6 +104,9 @@ constexpr int kDone = 2 * kTcStages + kPerTileBars * kTcTiles;
 // completes and both issuers have released it)
 constexpr int kTailV = kDone + 1;
 constexpr int kNumBars = kTailV + kTcStages;
+// key split: no part of an item gets fewer key tiles than this (below it the
+// merge and the fp32 states cost more than the shorter key loop saves)
+constexpr int kMinPartTiles = 16;
 // sequences ranked by context length in shared memory (beyond this count the
 // items keep the sequences' own order)
 constexpr int kMaxRankedSeqs = 256;
@@ -122,9 +125,12 @@ struct TcLayout {
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 8;
     static constexpr int kOrder = kFlag + 8;               // ranked sequence ids, then their lengths
-    // per softmax thread, the output row of its item (kept here through the key loop)
+    // per softmax thread, the output row of its item (kept here through the key
+    // loop; under a key split the item's part in bits 48-63), then the row's
+    // reference maximum at the item's end (key split)
     static constexpr int kOutRow = kOrder + 8 * kMaxRankedSeqs;
-    static constexpr int kTotal = kOutRow + 8 * kTcTiles * kTcRows;
+    static constexpr int kRefRow = kOutRow + 8 * kTcTiles * kTcRows;
+    static constexpr int kTotal = kRefRow + 4 * kTcTiles * kTcRows;
     static_assert(2 * kTcKeys + D <= kTmemTile, "S buffers and O must fit a Q tile's columns");
 };
 
@@ -162,25 +168,33 @@ __device__ __forceinline__ void sts32(uint32_t addr, int v) {
 struct PfItem {
     int s, h;
     int q0, j0, ntok, pos0, L;   // ntok: chunk tokens of the item
-    int nk[kTcTiles];   // key tiles of Q tile t: through the position of its last row
-    int nkt;            // key tiles of the item (those of its last row)
-    bool tail;          // the last key tile runs past the context
+    int part, kb;       // key split: this item's part and its first key tile
+    bool split;         // the item's keys are split (its rows leave states for the merge)
+    int nk[kTcTiles];   // key tiles of Q tile t from kb: through the position of its last row
+    int nkt;            // key tiles of the item from kb (the part's range)
+    bool tail;          // the item's last key tile runs past the context
 };
 
 // Items in one order shared by every CTA: sequences by decreasing context
 // length (ranked, when there are few enough), within a sequence its query
-// tiles from the last (the most keys), then kv heads, so that the items that
-// read a sequence's K/V run close together in time and share it through L2.
-// Item k of that order. Returns false for an item with no rows, or a sequence
-// whose chunk or length is invalid (reported once per sequence when `report`).
+// tiles from the last (the most keys), then kv heads, then key parts, so that
+// the items that read a sequence's K/V run close together in time and share it
+// through L2. Item k of that order. Returns false for an item with no rows or
+// no key tiles (a part past the item's keys), or a sequence whose chunk or
+// length is invalid (reported once per sequence when `report`).
+template <bool kSplit>
 __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked, int tiles, int k,
                                         bool report, PfItem &it) {
-    const int per_seq = tiles * p.n_kv_heads;
+    const int parts = kSplit ? p.key_parts : 1;
+    const int per_tile = p.n_kv_heads * parts;
+    const int per_seq = tiles * per_tile;
     const int r = k / per_seq;
     const int rem = k - r * per_seq;
     const int s = ranked ? lds32(ranked + 4u * uint32_t(r)) : r;
-    const int qt = tiles - 1 - rem / p.n_kv_heads;
-    const int h = rem - (rem / p.n_kv_heads) * p.n_kv_heads;
+    const int qt = tiles - 1 - rem / per_tile;
+    const int rem2 = rem - (rem / per_tile) * per_tile;
+    const int h = rem2 / parts;
+    const int part = rem2 - h * parts;
     const int q0 = __ldg(p.query_start + s);
     const int q1 = __ldg(p.query_start + s + 1);
     const int n = q1 - q0;
@@ -188,7 +202,7 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
     const bool rows_ok = q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens && n <= tiles * p.tile_tokens;
     const bool len_ok = L >= n && L <= p.max_blocks * p.block_size;
     if (!rows_ok || !len_ok) {
-        if (report && qt == tiles - 1 && h == 0)
+        if (report && qt == tiles - 1 && h == 0 && part == 0)
             atomicOr(p.err, rows_ok ? PAGEDKV_DEVERR_CONTEXT_LEN : PAGEDKV_DEVERR_POSITION);
         return false;
     }
@@ -204,13 +218,28 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
     // Q tile t holds the item's tokens t*tq .. t*tq + tq - 1, tq = 128 / group
     // whole tokens (all of a token's heads in one tile)
     const int tq = kTcRows / p.group;
+    int nk_all[kTcTiles];
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) {
         const int nt = min(max(it.ntok - t * tq, 0), tq);
-        it.nk[t] = nt > 0 ? (it.pos0 + t * tq + nt - 1) / kTcKeys + 1 : 0;
+        nk_all[t] = nt > 0 ? (it.pos0 + t * tq + nt - 1) / kTcKeys + 1 : 0;
     }
-    it.nkt = it.nk[kTcTiles - 1] > 0 ? it.nk[kTcTiles - 1] : it.nk[0];
-    it.tail = it.nkt * kTcKeys > L;
+    // the part's key tiles: [kb, ke) of the item's N (a tile's own count ends
+    // at its last row's position), in as many parts as keep kMinPartTiles key
+    // tiles each (a part past them is no item; an item of one part writes its
+    // rows itself)
+    const int N = nk_all[kTcTiles - 1] > 0 ? nk_all[kTcTiles - 1] : nk_all[0];
+    const int eff = min(parts, max(1, (N + kMinPartTiles - 1) / kMinPartTiles));
+    if (part >= eff) return false;
+    const int kb = int((long long)N * part / eff);
+    const int ke = int((long long)N * (part + 1) / eff);
+    it.part = part;
+    it.kb = kb;
+    it.split = eff > 1;
+#pragma unroll
+    for (int t = 0; t < kTcTiles; ++t) it.nk[t] = max(min(nk_all[t], ke) - kb, 0);
+    it.nkt = ke - kb;
+    it.tail = ke == N && N * kTcKeys > L;
     return true;
 }
 
@@ -224,7 +253,7 @@ __device__ __forceinline__ int pf_item_index(int m) {
 
 }  // namespace
 
-template <typename T, int D>
+template <typename T, int D, bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -243,7 +272,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int lane = threadIdx.x & 31;
     const int B = p.block_size;
     const int g = p.group;
-    const int num_items = p.num_seqs * tiles * p.n_kv_heads;
+    const int num_items = p.num_seqs * tiles * p.n_kv_heads * (kSplit ? p.key_parts : 1);
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kTcStages; ++k) {
@@ -319,12 +348,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const int k = pf_item_index(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item(p, ranked, tiles, k, lane == 0, it)) continue;
+            if (!pf_item<kSplit>(p, ranked, tiles, k, lane == 0, it)) continue;
             const int32_t *table = p.block_tables + size_t(it.s) * p.max_blocks;
             for (int j = 0; j < it.nkt; ++j) {
                 const int gk = kt + j;
                 const int st = gk % kTcStages;
-                const int k0 = j * kTcKeys;
+                const int k0 = (it.kb + j) * kTcKeys;
                 const int present = min(kTcKeys, it.L - k0);
                 const int boxes = (present + rows_per_box - 1) / rows_per_box;
                 const bool last_tail = it.tail && j == it.nkt - 1;
@@ -395,6 +424,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // hides the wait. An item's Q copies go first: its S MMAs, which the
         // item's last stage waits for, need them.
         if (lane == 0) tma_prefetch_descriptor(&qmap);
+        // key split: the merge that follows on the stream may launch now (it
+        // waits for this grid before it reads the states or exits; should this
+        // warp's signal not count for the CTA, it launches at the grid's end)
+        if (kSplit) grid_launch_dependents();
         const int tq = kTcRows / g;
         int kt = 0;
         int i = 0;
@@ -408,7 +441,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const int k = pf_item_index(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+            if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
             {
                 bool got = true;
                 if (lane == 0) {
@@ -440,7 +473,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             if (it.tail) {
                 const int st = (kt + it.nkt - 1) % kTcStages;
-                const int present = it.L - (it.nkt - 1) * kTcKeys;
+                const int present = it.L - (it.kb + it.nkt - 1) * kTcKeys;
                 bool got = true;
                 if (lane == 0)
                     got = !aborted() && mbar_wait(bar(kTailV + st), (parity >> st) & 1u, p.err);
@@ -544,7 +577,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int k = pf_item_index(m);
                 if (k >= num_items) break;
                 PfItem it;
-                if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+                if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
                 const int nk = it.nk[t];
                 // the item's Q rows of this tile are in shared memory
                 ok = wait(bar_qfull(t), i);
@@ -631,25 +664,43 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // tile's MMAs of the next item already run); its output row waits in
         // shared memory (all ones: a row past the item)
         const uint32_t out_row = base + Ly::kOutRow + 8u * uint32_t(R);
+        const uint32_t ref_row = base + Ly::kRefRow + 4u * uint32_t(R);
         int prev_nk = 0, prev_jend = 0;
         float prev_l = 0.f;
         auto epilogue = [&]() -> bool {
+            const unsigned long long v_row = (unsigned long long)(unsigned)lds32(out_row) |
+                                             ((unsigned long long)(unsigned)lds32(out_row + 4) << 32);
+            const bool prev_row = v_row != ~0ull;
+            const unsigned long long prev_qrow = prev_row ? v_row & ((1ull << 48) - 1) : 0ull;
+            const bool split = kSplit && prev_row && ((v_row >> 62) & 1ull);
+            // key split: every row of the item leaves its part's state, m = -inf
+            // when the part held none of its keys (its O is then not written)
+            const size_t wrow = size_t((v_row >> 48) & 0x3fffull) * (size_t(p.num_tokens) * size_t(p.n_q_heads)) +
+                                prev_qrow;
+            if (split && prev_row) {
+                p.ws_m[wrow] = prev_nk > 0 ? __int_as_float(lds32(ref_row)) : -INFINITY;
+                p.ws_l[wrow] = prev_nk > 0 ? prev_l : 0.f;
+            }
             if (prev_nk == 0) return true;
             // the last P V's completion covers every earlier MMA of the issuing thread
             const int e = prev_jend - 1;
             const bool got = !aborted() && mbar_wait(bar(bar_o(t, e & 1)), uint32_t((e >> 1) & 1), p.err);
             if (!__all_sync(kAll, got)) return false;
             tc_fence_after_sync();
+            // the row normalised into `out`, or (key split) its part's O as it is
             const float inv = prev_l > 0.f ? 1.f / prev_l : 0.f;
-            const unsigned long long prev_qrow = (unsigned long long)(unsigned)lds32(out_row) |
-                                                 ((unsigned long long)(unsigned)lds32(out_row + 4) << 32);
-            const bool prev_row = prev_qrow != ~0ull;
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + (prev_row ? prev_qrow : 0) * D);
+            const bool keep = prev_row && (!split || prev_l > 0.f);
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + prev_qrow * D);
+            float4 *wo = reinterpret_cast<float4 *>(p.ws_o + wrow * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float v[32];
                 tmem_ld32(otile + uint32_t(32 * c), v);
-                if (prev_row) {
+                if (keep && split) {
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4)
+                        wo[8 * c + e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+                } else if (keep) {
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         uint4 w;
@@ -669,7 +720,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const int k = pf_item_index(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item(p, ranked, tiles, k, false, it)) continue;
+            if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
             const int nk = it.nk[t];
             // this thread's row: token tok of the item (t*tq + r/g), head r%g of the
             // group; none past the tile's tq*g rows or the item's tokens
@@ -685,7 +736,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 break;
             }
             {
-                const unsigned long long v = row ? qrow : ~0ull;
+                // (an item of a split: its part in bits 48-61, bit 62 set)
+                const unsigned long long v =
+                    row ? (kSplit ? qrow | ((unsigned long long)it.part << 48) | (it.split ? 1ull << 62 : 0ull) : qrow)
+                        : ~0ull;
                 sts32(out_row, int(unsigned(v)));
                 sts32(out_row + 4, int(unsigned(v >> 32)));
             }
@@ -702,7 +756,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 tc_fence_after_sync();
                 float sc[kTcKeys];
                 tmem_ld64(trow + uint32_t(b * kTcKeys), sc);
-                const int k0 = j * kTcKeys;
+                const int k0 = (it.kb + j) * kTcKeys;   // absolute key index of the tile's first key
                 if (k0 + kTcKeys - 1 > pos) {
 #pragma unroll
                     for (int x = 0; x < kTcKeys; ++x) sc[x] = k0 + x <= pos ? sc[x] : -INFINITY;
@@ -762,6 +816,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             prev_nk = nk;
             prev_jend = jt + nk;
             prev_l = l;
+            if (kSplit) sts32(ref_row, __float_as_int(ref));
             jt += nk;
             ++i;
         }
@@ -779,15 +834,91 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 }
 
+// Key split: the merge. A warp per row of an item (a CTA per 8 row slots of
+// one (sequence, query tile, kv head)), so that every row is merged at once:
+// lane p loads part p's state, the warp reduces M = max m_p and
+// den = sum 2^(m_p - M) l_p (m_p in the kernel's base-2 units), and each lane
+// loads its columns of every part's O before it accumulates
+// out = sum 2^(m_p - M) O_p / den. A part that held none of the row's keys
+// left m_p = -inf and is skipped (its O was not written); a part past the
+// item's keys was no item at all. A flagged sequence's rows stay unwritten, as
+// the kernel leaves them.
+constexpr int kMergeRowsPerCta = 8;
+constexpr int kMaxMergeParts = 16;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta)
+paged_prefill_merge_kernel(const PrefillParams p, int tiles) {
+    constexpr int E = D / 32;
+    constexpr int kSlices = kTcTiles * kTcRows / kMergeRowsPerCta;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int parts = p.key_parts;
+    const int grp = blockIdx.x / kSlices;
+    const int R = (blockIdx.x - grp * kSlices) * kMergeRowsPerCta + warp;   // row slot of the item
+    PfItem it;
+    const bool valid = lane < parts && pf_item<true>(p, 0u, tiles, grp * parts + lane, false, it);
+    const unsigned present = __ballot_sync(kAll, valid);
+    // the states (and, for the stream's order, the kernel's end: this grid does
+    // not complete before it)
+    grid_dependency_wait();
+    // no item, or one whose keys were not split (it wrote its rows itself)
+    if (__popc(present) < 2) return;
+    const int src = __ffs(present) - 1;
+    const int q0 = __shfl_sync(kAll, it.q0, src), j0 = __shfl_sync(kAll, it.j0, src);
+    const int ntok = __shfl_sync(kAll, it.ntok, src), h = __shfl_sync(kAll, it.h, src);
+    const int g = p.group, tq = kTcRows / g;
+    const int t = R / kTcRows, r = R - t * kTcRows;
+    const int tok = t * tq + r / g;
+    if (r >= tq * g || tok >= ntok) return;
+    const size_t rows_total = size_t(p.num_tokens) * size_t(p.n_q_heads);
+    const size_t qrow = size_t(q0 + j0 + tok) * p.n_q_heads + size_t(h) * g + r % g;
+    float mp = -INFINITY, lp = 0.f;
+    if ((present >> lane) & 1u) {
+        mp = __ldcg(p.ws_m + size_t(lane) * rows_total + qrow);
+        lp = __ldcg(p.ws_l + size_t(lane) * rows_total + qrow);
+    }
+    float M = mp;
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, mask));
+    const float w = mp > -INFINITY ? exp2f(mp - M) : 0.f;
+    float den = w * lp;
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(kAll, den, mask);
+    // every part's columns of this lane first (one round trip: a part's slot
+    // exists even where it holds nothing), then the sums over the parts that
+    // hold something (the others may hold anything, NaN included)
+    float x[kMaxMergeParts][E];
+#pragma unroll
+    for (int q = 0; q < kMaxMergeParts; ++q) {
+        const float *o = p.ws_o + (size_t(q < parts ? q : 0) * rows_total + qrow) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[q][e] = q < parts ? __ldcg(o + e) : 0.f;
+    }
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxMergeParts; ++q) {
+        const float wq = __shfl_sync(kAll, w, q);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = wq != 0.f ? fmaf(wq, x[q][e], acc[e]) : acc[e];
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    T *dst = reinterpret_cast<T *>(p.out) + qrow * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t *>(dst + e) = Elem<T>::pack2(acc[e] * inv, acc[e + 1] * inv);
+}
+
 int prefill_tc_smem_bytes(int head_dim) {
     return (head_dim == 64 ? TcLayout<64>::kTotal : TcLayout<128>::kTotal) + 1024;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kSplit>
 static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                       const CUtensorMap &qmap, const PrefillParams &p, int max_query_len, int num_sms,
                                       cudaStream_t stream) {
-    auto kernel = paged_prefill_tc_kernel<T, D>;
+    auto kernel = paged_prefill_tc_kernel<T, D, kSplit>;
     const int smem = TcLayout<D>::kTotal + 1024;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -800,7 +931,7 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     // items (and a CTA's band index, at most items + grid) must fit an int
     // (the API refuses larger calls)
     const long long tiles_ll = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
-    const long long per_seq = tiles_ll * p.n_kv_heads;
+    const long long per_seq = tiles_ll * p.n_kv_heads * (kSplit ? p.key_parts : 1);
     if (per_seq > (INT_MAX / 2) / p.num_seqs) return cudaErrorInvalidValue;
     const int tiles = int(tiles_ll);
     const long long items = per_seq * p.num_seqs;
@@ -818,16 +949,55 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     return cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, qmap, p, tiles);
 }
 
+template <typename T, int D>
+static cudaError_t launch_merge_instance(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    const long long tiles = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    const long long groups = tiles * p.n_kv_heads * p.num_seqs;
+    const long long ctas = groups * (kTcTiles * kTcRows / kMergeRowsPerCta);
+    if (ctas > INT_MAX || p.key_parts > kMaxMergeParts) return cudaErrorInvalidValue;
+    // the programmatic dependent of the prefill kernel: its launch and its
+    // items' set-up overlap the kernel's end
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(ctas));
+    cfg.blockDim = dim3(32 * kMergeRowsPerCta);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D>, p, int(tiles));
+}
+
+cudaError_t launch_prefill_merge(int dtype, int head_dim, const PrefillParams &p, int max_query_len,
+                                 cudaStream_t stream) {
+    const bool bf16 = dtype == PAGEDKV_BF16;
+    if (head_dim == 64)
+        return bf16 ? launch_merge_instance<__nv_bfloat16, 64>(p, max_query_len, stream)
+                    : launch_merge_instance<__half, 64>(p, max_query_len, stream);
+    return bf16 ? launch_merge_instance<__nv_bfloat16, 128>(p, max_query_len, stream)
+                : launch_merge_instance<__half, 128>(p, max_query_len, stream);
+}
+
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const CUtensorMap &qmap,
                               const PrefillParams &p, int max_query_len, int num_sms,
                               cudaStream_t stream) {
     const bool bf16 = dtype == PAGEDKV_BF16;
+    // the key split has an instance of its own: the whole-item kernel keeps
+    // none of its per-item arithmetic
+    if (p.key_parts > 1) {
+        if (head_dim == 64)
+            return bf16 ? launch_tc_instance<__nv_bfloat16, 64, true>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                        : launch_tc_instance<__half, 64, true>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
+        return bf16 ? launch_tc_instance<__nv_bfloat16, 128, true>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                    : launch_tc_instance<__half, 128, true>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
+    }
     if (head_dim == 64)
-        return bf16 ? launch_tc_instance<__nv_bfloat16, 64>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
-                    : launch_tc_instance<__half, 64>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
-    return bf16 ? launch_tc_instance<__nv_bfloat16, 128>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
-                : launch_tc_instance<__half, 128>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
+        return bf16 ? launch_tc_instance<__nv_bfloat16, 64, false>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                    : launch_tc_instance<__half, 64, false>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
+    return bf16 ? launch_tc_instance<__nv_bfloat16, 128, false>(kmap, vmap, qmap, p, max_query_len, num_sms, stream)
+                : launch_tc_instance<__half, 128, false>(kmap, vmap, qmap, p, max_query_len, num_sms, stream);
 }
 
 }  // namespace pkv

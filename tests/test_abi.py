@@ -180,3 +180,30 @@ def test_tensors_must_be_on_the_gpu(lib):
     with pytest.raises(pk.PagedKVError, match="CUDA"):
         pk.paged_kv_append(x, x, torch.zeros(4, dtype=torch.int64), torch.zeros(8, 16, 2, 64),
                            torch.zeros(8, 16, 2, 64))
+
+
+def test_prefill_key_split_host_checks(lib):
+    """The key split's part count is checked before anything reaches the
+    device, and its workspace size is plain arithmetic: fp32 outputs
+    [parts][tokens * heads][head_dim], then m and l [parts][tokens * heads],
+    each rounded up to 256 bytes."""
+    vp = ctypes.c_void_p
+
+    def call(parts):
+        return lib.paged_attention_prefill_split(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 0.1,
+                                                 vp(16), 2, 64, 32, 32, 32, 128, 64, 16, 8, 1, parts,
+                                                 None, 0, None)
+
+    assert call(17) == INVALID
+    assert call(-1) == INVALID
+
+    def r256(x):
+        return (x + 255) // 256 * 256
+
+    rows = 100 * 32
+    for parts in (2, 4, 16):
+        assert lib.paged_attention_prefill_workspace_bytes(100, 32, 128, parts) == \
+            r256(parts * rows * 128 * 4) + 2 * r256(parts * rows * 4)
+    for parts in (-1, 0, 1, 17):
+        assert lib.paged_attention_prefill_workspace_bytes(100, 32, 128, parts) == 0
+    assert lib.paged_attention_prefill_workspace_bytes(0, 32, 128, 4) == 0

@@ -258,3 +258,84 @@ def test_query_rows_past_every_chunk_stay_out(orc, g):
     got = to_f64(out[:q.shape[0]])
     assert not np.isnan(got).any()
     assert float(np.abs(got - ref).max()) <= TOL["f16"]
+
+
+def prefill_split(wl, qs, q, kc, vc, bt, parts, lens=None, workspace=None, out=None):
+    out = torch.full_like(q, float("nan")) if out is None else out
+    lens = wl.context_lens if lens is None else lens
+    ws = pk.prefill_workspace(q, parts) if workspace is None else workspace
+    pk.paged_attention_prefill(q, kc, vc, bt, torch.from_numpy(np.asarray(qs, np.int32)).cuda(),
+                               torch.from_numpy(np.asarray(lens, np.int32)).cuda(), wl.scale, out,
+                               workspace=ws, key_parts=parts)
+    return out
+
+
+# long cached contexts (items of 33 to 72 key tiles, split in up to 4 parts of
+# at least 16) beside short ones (not split) in one call
+SPLIT_CASES = [(0, 1), (1100, 1), (2500, 77), (1024, 50), (3000, 130), (37, 0), (1984, 64),
+               (4300, 200)]
+
+
+@pytest.mark.parametrize("parts", [2, 3, 16])
+@pytest.mark.parametrize("g", [1, 3, 8])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_key_split_matches_oracle(orc, dtype, D, g, parts):
+    """Each long item's keys split over up to 2, 3 or 16 parts (as many as keep
+    16 key tiles each; a part's range can lie past a Q tile's rows), short
+    items whole, the parts' states merged: every row against the oracle."""
+    wl, qs, tensors, q, kc, vc, bt = build(dtype, D, 16, g, seed=600 + D + g + parts, cases=SPLIT_CASES)
+    pk.device_errors(reset=True)
+    out = prefill_split(wl, qs, q, kc, vc, bt, parts)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, dtype)
+    got = to_f64(out)
+    assert not np.isnan(got).any()
+    err = float(np.abs(got - ref).max())
+    assert err <= TOL[dtype], f"max-abs error {err:.3e}"
+
+
+def test_key_split_automatic_parts_and_a_short_workspace(orc, path):
+    """key_parts 0 picks enough parts to fill the SMs (as many as the workspace
+    holds); a workspace smaller than an explicit split needs is refused (on the
+    tcgen05 kernel: the warp-level MMA kernel does not split, and needs none)."""
+    cases = [(1920, 128)]   # one sequence, one 128-token chunk after 1920 cached tokens
+    wl, qs, tensors, q, kc, vc, bt = build("f16", 128, 16, 1, seed=640, cases=cases, n_kv=32)
+    out = prefill_split(wl, qs, q, kc, vc, bt, 0)
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16")
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+    short = torch.empty(pk.prefill_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], 4) - 256,
+                        dtype=torch.uint8, device=q.device)
+    if path == 2:
+        with pytest.raises(pk.PagedKVError):
+            prefill_split(wl, qs, q, kc, vc, bt, 4, workspace=short)
+    else:
+        out = prefill_split(wl, qs, q, kc, vc, bt, 4, workspace=short)
+        assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+
+
+def test_key_split_leaves_flagged_and_padding_rows_alone(orc):
+    """Under a key split a sequence whose length is shorter than its chunk is
+    flagged and its rows left unwritten, and output rows past the chunks keep
+    what they held, as without the split."""
+    cases = [(2100, 30), (0, 77), (3000, 100), (5, 3)]
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 128, 16, 2, seed=650, cases=cases, n_kv=2)
+    pad = torch.zeros((20,) + tuple(q.shape[1:]), dtype=q.dtype, device=q.device)
+    qp = torch.cat([q, pad])
+    out = torch.full_like(qp, float("nan"))
+    out[q.shape[0]:] = 7.0
+    lens = wl.context_lens.copy()
+    bad = 2
+    lens[bad] = int(qs[bad + 1] - qs[bad]) - 1
+    pk.device_errors(reset=True)
+    prefill_split(wl, qs, qp, kc, vc, bt, 3, lens=lens, out=out)
+    assert pk.device_errors() == 0x04
+    assert bool((out[q.shape[0]:] == 7.0).all())
+    got = to_f64(out[:q.shape[0]])
+    assert np.isnan(got[qs[bad]:qs[bad + 1]]).all()
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+    keep = np.r_[0:qs[bad], qs[bad + 1]:qs[-1]]
+    assert float(np.abs(got[keep] - ref[keep]).max()) <= TOL["bf16"]

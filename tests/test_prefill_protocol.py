@@ -19,6 +19,7 @@ import numpy as np
 import pytest
 
 KEYS, ROWS, TILES, STAGES = 64, 128, 2, 4
+MIN_PART_TILES = 16   # the kernel's least key tiles per part of a split item
 
 
 class Hazard(Exception):
@@ -59,8 +60,9 @@ class Barrier:
         return (self.phase & 1) != (n & 1)
 
 
-def make_items(cta, grid, before, chunk, g, n_kv):
-    """The items of CTA `cta`, in the kernel's order."""
+def make_items(cta, grid, before, chunk, g, n_kv, parts=1, min_part=MIN_PART_TILES):
+    """The items of CTA `cta`, in the kernel's order (key parts innermost; an
+    item's keys in at most ceil(N / min_part) parts)."""
     lens = [b + c for b, c in zip(before, chunk)]
     qs = np.concatenate([[0], np.cumsum(chunk)])
     tq = ROWS // g                  # whole tokens per Q tile
@@ -68,7 +70,8 @@ def make_items(cta, grid, before, chunk, g, n_kv):
     tiles = -(-max(chunk) // tile_tokens)
     S = len(chunk)
     ranked = sorted(range(S), key=lambda s: (-lens[s], s)) if S > 1 else list(range(S))
-    per_seq = tiles * n_kv
+    per_tile = n_kv * parts
+    per_seq = tiles * per_tile
     num_items = S * per_seq
     items, m = [], 0
     while True:
@@ -78,7 +81,8 @@ def make_items(cta, grid, before, chunk, g, n_kv):
             return items
         r, rem = divmod(k, per_seq)
         s = ranked[r]
-        qt = tiles - 1 - rem // n_kv
+        qt = tiles - 1 - rem // per_tile
+        part = rem % per_tile % parts
         n, L = int(qs[s + 1] - qs[s]), lens[s]
         j0 = qt * tile_tokens
         if j0 >= n:
@@ -87,8 +91,13 @@ def make_items(cta, grid, before, chunk, g, n_kv):
         pos0 = L - n + j0
         nk = [(pos0 + t * tq + min(ntok - t * tq, tq) - 1) // KEYS + 1 if ntok > t * tq else 0
               for t in range(TILES)]
-        nkt = nk[1] if nk[1] > 0 else nk[0]
-        items.append(dict(nk=nk, nkt=nkt, tail=nkt * KEYS > L))
+        N = nk[1] if nk[1] > 0 else nk[0]
+        eff = min(parts, max(1, -(-N // min_part)))
+        if part >= eff:
+            continue
+        kb, ke = N * part // eff, N * (part + 1) // eff
+        items.append(dict(nk=[max(min(x, ke) - kb, 0) for x in nk], nkt=ke - kb,
+                          tail=ke == N and N * KEYS > L))
 
 
 def run_cta(items, rng, ofree=False):
@@ -228,23 +237,26 @@ def many_items_workload():
     return before.tolist(), chunk.tolist()
 
 
-def check(before, chunk, g, n_kv, grid, seeds, ofree=False):
+def check(before, chunk, g, n_kv, grid, seeds, ofree=False, parts=1, min_part=MIN_PART_TILES):
     for cta in range(grid):
-        items = make_items(cta, grid, before, chunk, g, n_kv)
+        items = make_items(cta, grid, before, chunk, g, n_kv, parts, min_part)
         for seed in range(seeds):
             left = run_cta(items, np.random.default_rng(seed), ofree=ofree)
             assert not left, f"cta {cta} seed {seed}: deadlock, waiting {left}"
 
 
 @pytest.mark.parametrize("g,n_kv", [(1, 8), (3, 4), (8, 4), (64, 1)])
-@pytest.mark.parametrize("grid", [1, 5, 37])
-def test_no_deadlock_or_phase_hazard(g, n_kv, grid):
+@pytest.mark.parametrize("grid,parts", [(1, 1), (5, 1), (37, 1), (5, 3), (37, 3)])
+def test_no_deadlock_or_phase_hazard(g, n_kv, grid, parts):
     """Chunks of one row to three query tiles, contexts on a 64-key boundary
     and ragged, second Q tiles empty: every interleaving tried ends, with no
     barrier two phases past a waiter or one behind it (groups that divide 128
-    and 3, whose Q tiles hold 42 whole tokens)."""
+    and 3, whose Q tiles hold 42 whole tokens), whole items and items whose
+    keys are split in up to three parts (a part's first tile past a tile's
+    rows, a tail only in the last part; parts of one key tile or more, to split
+    far more items than the kernel's 16-tile least part would)."""
     before, chunk = many_items_workload()
-    check(before, chunk, g, n_kv, grid, seeds=3)
+    check(before, chunk, g, n_kv, grid, seeds=3, parts=parts, min_part=1 if parts > 1 else MIN_PART_TILES)
 
 
 def test_model_finds_the_removed_o_free_hazard():
