@@ -44,6 +44,10 @@ def test_bench_line_keeps_the_contract():
     e = line["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+    # the prefill figures, the key split's among them: a short chunk over a long
+    # cached context runs faster split than whole
+    c = line["prefill"]["chunk128_after16k"]
+    assert 0 < c["split_us"] < c["whole_us"]
     # the compact targets are the line's last key
     assert list(line.keys())[-1] == "targets"
     t = line["targets"]
