@@ -1020,6 +1020,26 @@ def measure_prefill(device, reps=50, chunked=True):
                                "frac": flops / ms_mma / 1e9 / peak}}
     del kc, vc, q, out
     torch.cuda.empty_cache()
+    # a short chunk over a long cached context: 32 items for 152 SMs, whole and
+    # with each item's keys split (paged_attention_prefill_split, parts chosen
+    # by the library)
+    wl3, qs3 = chunked_prefill("chunk128_after16k", "f16", [16384], [128], 32, 32, 128, 16, seed=19)
+    kc, vc, bt = fill_pools(wl3, device)
+    q = prefill_queries(wl3, qs3, device)
+    out = torch.empty_like(q)
+    qs_d = torch.from_numpy(qs3).to(device)
+    lens_d = torch.from_numpy(wl3.context_lens).to(device)
+    ws = pk.prefill_workspace(q, 0)
+    whole = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128), 20)
+    split = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128,
+                                                     workspace=ws, key_parts=0), 20)
+    f3 = prefill_flops(wl3.context_lens, qs3, 32, 128)
+    res["chunk128_after16k"] = {"workload": "1 seq, 128-token chunk after 16384 cached tokens, 32 heads, D128, fp16",
+                                "whole_us": whole * 1e3, "split_us": split * 1e3,
+                                "split_frac": f3 / split / 1e9 / peak}
+    assert pk.device_errors() == 0
+    del kc, vc, q, out, ws
+    torch.cuda.empty_cache()
     if not chunked:
         return res
     # the 2048-token prompt, chunked
@@ -1042,26 +1062,6 @@ def measure_prefill(device, reps=50, chunked=True):
     res["prompt2048_chunked"] = chunking
     assert pk.device_errors() == 0
     del kc, vc, q, out
-    torch.cuda.empty_cache()
-    # a short chunk over a long cached context: 32 items for 152 SMs, whole and
-    # with each item's keys split (paged_attention_prefill_split, parts chosen
-    # by the library)
-    wl3, qs3 = chunked_prefill("chunk128_after16k", "f16", [16384], [128], 32, 32, 128, 16, seed=19)
-    kc, vc, bt = fill_pools(wl3, device)
-    q = prefill_queries(wl3, qs3, device)
-    out = torch.empty_like(q)
-    qs_d = torch.from_numpy(qs3).to(device)
-    lens_d = torch.from_numpy(wl3.context_lens).to(device)
-    ws = pk.prefill_workspace(q, 0)
-    whole = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128), 20)
-    split = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128,
-                                                     workspace=ws, key_parts=0), 20)
-    f3 = prefill_flops(wl3.context_lens, qs3, 32, 128)
-    res["chunk128_after16k"] = {"workload": "1 seq, 128-token chunk after 16384 cached tokens, 32 heads, D128, fp16",
-                                "whole_us": whole * 1e3, "split_us": split * 1e3,
-                                "split_frac": f3 / split / 1e9 / peak}
-    assert pk.device_errors() == 0
-    del kc, vc, q, out, ws
     torch.cuda.empty_cache()
     return res
 

@@ -44,10 +44,6 @@ def test_bench_line_keeps_the_contract():
     e = line["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
-    # the prefill figures, the key split's among them: a short chunk over a long
-    # cached context runs faster split than whole
-    c = line["prefill"]["chunk128_after16k"]
-    assert 0 < c["split_us"] < c["whole_us"]
     # the compact targets are the line's last key
     assert list(line.keys())[-1] == "targets"
     t = line["targets"]
@@ -55,3 +51,16 @@ def test_bench_line_keeps_the_contract():
         assert 0 < t[name]["frac"] < 1.2, name
         # each call after an L2 flush, between its own events: no faster than back to back
         assert 0 < t[name]["frac_l2_flushed"] <= t[name]["frac"] * 1.02, name
+
+
+def test_bench_prefill_figures():
+    """bench.py --prefill-only: the bench step's prefill figure, and a short chunk
+    over a long cached context faster with its keys split than whole."""
+    res = subprocess.run(
+        [sys.executable, os.path.join(REPO, "bench.py"), "--prefill-only", "--prefill-reps", "5"],
+        capture_output=True, text=True, timeout=900, cwd=REPO)
+    assert res.returncode == 0, res.stderr[-3000:]
+    pf = json.loads(res.stdout.strip().splitlines()[-1])["prefill"]
+    assert 0 < pf["frac"] < 1.2
+    c = pf["chunk128_after16k"]
+    assert 0 < c["split_us"] < c["whole_us"]
