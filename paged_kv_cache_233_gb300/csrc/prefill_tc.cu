@@ -872,10 +872,21 @@ paged_prefill_merge_kernel(const PrefillParams p, int tiles) {
     if (r >= tq * g || tok >= ntok) return;
     const size_t rows_total = size_t(p.num_tokens) * size_t(p.n_q_heads);
     const size_t qrow = size_t(q0 + j0 + tok) * p.n_q_heads + size_t(h) * g + r % g;
+    // one round trip: lane p's (m, l) of part p, and every part's columns of
+    // this lane's O (a part's slot exists even where it holds nothing: the sums
+    // below take only the parts that hold something; the others may hold
+    // anything, NaN included)
     float mp = -INFINITY, lp = 0.f;
     if ((present >> lane) & 1u) {
         mp = __ldcg(p.ws_m + size_t(lane) * rows_total + qrow);
         lp = __ldcg(p.ws_l + size_t(lane) * rows_total + qrow);
+    }
+    float x[kMaxMergeParts][E];
+#pragma unroll
+    for (int q = 0; q < kMaxMergeParts; ++q) {
+        const float *o = p.ws_o + (size_t(q < parts ? q : 0) * rows_total + qrow) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[q][e] = q < parts ? __ldcg(o + e) : 0.f;
     }
     float M = mp;
 #pragma unroll
@@ -884,16 +895,6 @@ paged_prefill_merge_kernel(const PrefillParams p, int tiles) {
     float den = w * lp;
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(kAll, den, mask);
-    // every part's columns of this lane first (one round trip: a part's slot
-    // exists even where it holds nothing), then the sums over the parts that
-    // hold something (the others may hold anything, NaN included)
-    float x[kMaxMergeParts][E];
-#pragma unroll
-    for (int q = 0; q < kMaxMergeParts; ++q) {
-        const float *o = p.ws_o + (size_t(q < parts ? q : 0) * rows_total + qrow) * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) x[q][e] = q < parts ? __ldcg(o + e) : 0.f;
-    }
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
