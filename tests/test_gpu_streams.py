@@ -128,6 +128,50 @@ def test_prefill_on_a_side_stream(orc):
     assert err <= TOL["f16"], err
 
 
+def test_prefill_key_split_on_a_side_stream_and_in_a_graph(orc):
+    """The key split (two kernels, the merge the programmatic dependent of the
+    prefill kernel) on a side stream against the oracle, then captured in a
+    CUDA graph: a replay on new queries equals an eager call on them, bit for
+    bit."""
+    wl, qs = chunked_prefill("streams_split", "f16", [2100, 0, 3300], [50, 130, 17], 8, 2, 128, 16, 34)
+    t = materialize(wl, "cuda")
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        kc, vc = new_pools(wl, "cuda")
+        bt = torch.from_numpy(wl.block_tables).cuda()
+        for seq, pos, k, v in ((wl.fill_seq, wl.fill_pos, t["k_fill"], t["v_fill"]),
+                               (wl.step_seq, wl.step_pos, t["k_step"], t["v_step"])):
+            sm = torch.empty(len(seq), dtype=torch.int64, device="cuda")
+            pk.paged_kv_slot_mapping(bt, torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda(),
+                                     sm, wl.num_blocks, wl.block_size)
+            pk.paged_kv_append(k, v, sm, kc, vc)
+        q = prefill_queries(wl, qs, "cuda")
+        qs_d = torch.from_numpy(qs).cuda()
+        lens_d = torch.from_numpy(wl.context_lens).cuda()
+        ws = pk.prefill_workspace(q, 4)
+        out = torch.full_like(q, float("nan"))
+        pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out, 130, workspace=ws, key_parts=4)
+    side.synchronize()
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, t)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, wl.dtype)
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+    # captured once, replayed on new queries
+    graph = torch.cuda.CUDAGraph()
+    out_g = torch.full_like(q, float("nan"))
+    with torch.cuda.graph(graph):
+        pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out_g, 130, workspace=ws,
+                                   key_parts=4)
+    q.copy_(q.flip(0))
+    graph.replay()
+    out_e = torch.full_like(q, float("nan"))
+    pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out_e, 130, workspace=ws, key_parts=4)
+    torch.cuda.synchronize()
+    assert pk.device_errors() == 0
+    assert torch.equal(out_g, out_e)
+
+
 def test_concurrent_host_threads(orc):
     """Two host threads decode at once, each on its own stream, with batches of
     different sizes through the same kernel instantiation: the launchers'
