@@ -748,7 +748,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int j = 0; j < nk; ++j) {
                 const int gj = jt + j;
                 const int b = gj & 1;
-                bool got = !aborted() && mbar_wait(bar(bar_s(t, b)), uint32_t((gj >> 1) & 1), p.err);
+                // (a phase already complete passes at once; the abort flag is read
+                // only when the warp has to wait)
+                bool got = mbar_try_wait(bar(bar_s(t, b)), uint32_t((gj >> 1) & 1));
+                if (!got) got = !aborted() && mbar_wait(bar(bar_s(t, b)), uint32_t((gj >> 1) & 1), p.err);
                 if (!__all_sync(kAll, got)) {
                     ok = false;
                     break;
