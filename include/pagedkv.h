@@ -274,11 +274,12 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
  * split over key_parts work items (a split-K over the key range), for calls
  * with fewer items than SMs (one short chunk, few sequences): every (sequence,
  * 2 * (128 / group) chunk tokens, kv head) item of the tcgen05 kernel becomes
- * key_parts items over contiguous ranges of its 64-key tiles. Each writes its
- * rows' unnormalised fp32 output and softmax state to `workspace`, and a merge
- * kernel on the same stream combines them into `out` (softmax's LSE identity,
- * the same one split-K decode uses). The result equals
- * paged_attention_prefill's within rounding.
+ * up to key_parts items over contiguous ranges of its N 64-key tiles (at most
+ * ceil(N / 16) of them: an item of 16 tiles or fewer stays whole and writes
+ * `out` itself). Each part writes its rows' unnormalised fp32 output and
+ * softmax state to `workspace`, and a merge kernel on the same stream combines
+ * them into `out` (softmax's LSE identity, the same one split-K decode uses).
+ * The result equals paged_attention_prefill's within rounding.
  *
  *   key_parts        1 .. 16; 1 is paged_attention_prefill itself; 0 picks
  *                    the most parts whose items still fit one wave of the SMs

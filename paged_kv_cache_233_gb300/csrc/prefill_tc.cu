@@ -104,8 +104,10 @@ constexpr int kDone = 2 * kTcStages + kPerTileBars * kTcTiles;
 // completes and both issuers have released it)
 constexpr int kTailV = kDone + 1;
 constexpr int kNumBars = kTailV + kTcStages;
-// key split: no part of an item gets fewer key tiles than this (below it the
-// merge and the fp32 states cost more than the shorter key loop saves)
+// key split: an item of N key tiles takes at most ceil(N / kMinPartTiles)
+// parts, so that a part holds 8 to 16 key tiles (N > 16) and an item of 16 or
+// fewer is not split (shorter parts save less key loop than the merge and the
+// fp32 states cost)
 constexpr int kMinPartTiles = 16;
 // sequences ranked by context length in shared memory (beyond this count the
 // items keep the sequences' own order)
@@ -225,9 +227,8 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
         nk_all[t] = nt > 0 ? (it.pos0 + t * tq + nt - 1) / kTcKeys + 1 : 0;
     }
     // the part's key tiles: [kb, ke) of the item's N (a tile's own count ends
-    // at its last row's position), in as many parts as keep kMinPartTiles key
-    // tiles each (a part past them is no item; an item of one part writes its
-    // rows itself)
+    // at its last row's position), in at most ceil(N / kMinPartTiles) parts (a
+    // part past them is no item; an item of one part writes its rows itself)
     const int N = nk_all[kTcTiles - 1] > 0 ? nk_all[kTcTiles - 1] : nk_all[0];
     const int eff = min(parts, max(1, (N + kMinPartTiles - 1) / kMinPartTiles));
     if (part >= eff) return false;

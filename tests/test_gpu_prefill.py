@@ -270,8 +270,8 @@ def prefill_split(wl, qs, q, kc, vc, bt, parts, lens=None, workspace=None, out=N
     return out
 
 
-# long cached contexts (items of 33 to 72 key tiles, split in up to 4 parts of
-# at least 16) beside short ones (not split) in one call
+# long cached contexts (items of 33 to 72 key tiles, split in up to 5 parts of
+# 8 to 16 key tiles) beside short ones (not split) in one call
 SPLIT_CASES = [(0, 1), (1100, 1), (2500, 77), (1024, 50), (3000, 130), (37, 0), (1984, 64),
                (4300, 200)]
 
@@ -281,8 +281,8 @@ SPLIT_CASES = [(0, 1), (1100, 1), (2500, 77), (1024, 50), (3000, 130), (37, 0), 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_key_split_matches_oracle(orc, dtype, D, g, parts):
-    """Each long item's keys split over up to 2, 3 or 16 parts (as many as keep
-    16 key tiles each; a part's range can lie past a Q tile's rows), short
+    """Each long item's keys split over up to 2, 3 or 16 parts (at most one per
+    16 of its key tiles; a part's range can lie past a Q tile's rows), short
     items whole, the parts' states merged: every row against the oracle."""
     wl, qs, tensors, q, kc, vc, bt = build(dtype, D, 16, g, seed=600 + D + g + parts, cases=SPLIT_CASES)
     pk.device_errors(reset=True)

@@ -254,7 +254,7 @@ def test_no_deadlock_or_phase_hazard(g, n_kv, grid, parts):
     and 3, whose Q tiles hold 42 whole tokens), whole items and items whose
     keys are split in up to three parts (a part's first tile past a tile's
     rows, a tail only in the last part; parts of one key tile or more, to split
-    far more items than the kernel's 16-tile least part would)."""
+    far more items than the kernel's rule of one part per 16 key tiles would)."""
     before, chunk = many_items_workload()
     check(before, chunk, g, n_kv, grid, seeds=3, parts=parts, min_part=1 if parts > 1 else MIN_PART_TILES)
 
