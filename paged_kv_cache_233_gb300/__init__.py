@@ -291,9 +291,10 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, cont
     [num_seqs + 1]; context_lens counts each sequence's cached tokens with its
     chunk (already appended) included. max_query_len bounds every chunk's
     length; by default it is read from query_start (a device-to-host copy).
-    With a workspace (see prefill_workspace) the keys of each work item may be
-    split over key_parts items (0: as many as fill the SMs and the workspace),
-    whose states a merge kernel combines."""
+    With key_parts other than 1 the keys of each work item may be split over
+    key_parts items (0: as many as fill the SMs and the workspace), whose
+    states a merge kernel combines; the workspace (see prefill_workspace) is
+    taken from torch's allocator when none is given."""
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise PagedKVError("q and out must be [num_tokens][n_q_heads][head_dim] of one type")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != q.dtype:
@@ -312,8 +313,10 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, cont
         st = load().paged_attention_prefill(*args, _stream(stream))
         _check(st, "paged_attention_prefill")
         return
-    ws = _dev(workspace, "workspace") if workspace is not None else None
-    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if workspace is None:
+        workspace = prefill_workspace(q, key_parts)
+    ws = _dev(workspace, "workspace")
+    nbytes = workspace.numel() * workspace.element_size()
     st = load().paged_attention_prefill_split(*args, int(key_parts), ws, nbytes, _stream(stream))
     _check(st, "paged_attention_prefill_split")
 

@@ -296,6 +296,19 @@ def test_key_split_matches_oracle(orc, dtype, D, g, parts):
     assert err <= TOL[dtype], f"max-abs error {err:.3e}"
 
 
+def test_key_split_without_a_workspace_takes_one_from_torch(orc):
+    """The binding allocates the split's workspace when the caller passes none."""
+    cases = [(3000, 100)]
+    wl, qs, tensors, q, kc, vc, bt = build("f16", 64, 16, 1, seed=660, cases=cases, n_kv=4)
+    out = torch.full_like(q, float("nan"))
+    pk.paged_attention_prefill(q, kc, vc, bt, torch.from_numpy(np.asarray(qs, np.int32)).cuda(),
+                               torch.from_numpy(np.asarray(wl.context_lens, np.int32)).cuda(), wl.scale,
+                               out, key_parts=0)
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16")
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+
+
 def test_key_split_automatic_parts_and_a_short_workspace(orc, path):
     """key_parts 0 picks enough parts to fill the SMs (as many as the workspace
     holds); a workspace smaller than an explicit split needs is refused (on the
