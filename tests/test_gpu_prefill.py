@@ -296,6 +296,20 @@ def test_key_split_matches_oracle(orc, dtype, D, g, parts):
     assert err <= TOL[dtype], f"max-abs error {err:.3e}"
 
 
+@pytest.mark.parametrize("g", [16, 64])
+def test_key_split_large_groups(orc, g):
+    """The key split at groups of 16 and 64 (Q tiles of 8 and 2 whole tokens):
+    long and short contexts in one call against the oracle."""
+    cases = [(2000, 9), (0, 33), (3100, 70), (1500, 1)]
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, g, seed=670 + g, cases=cases, n_kv=1)
+    pk.device_errors(reset=True)
+    out = prefill_split(wl, qs, q, kc, vc, bt, 4)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
+
+
 def test_key_split_without_a_workspace_takes_one_from_torch(orc):
     """The binding allocates the split's workspace when the caller passes none."""
     cases = [(3000, 100)]
