@@ -1029,7 +1029,7 @@ def measure_prefill(device, reps=50, chunked=True):
     out = torch.empty_like(q)
     qs_d = torch.from_numpy(qs3).to(device)
     lens_d = torch.from_numpy(wl3.context_lens).to(device)
-    ws = pk.prefill_workspace(q, 0)
+    ws = pk.prefill_workspace(q)
     whole = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128), 20)
     split = timed(lambda: pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl3.scale, out, 128,
                                                      workspace=ws, key_parts=0), 20)

@@ -270,33 +270,39 @@ int paged_attention_prefill(const void *q, const void *k_cache, const void *v_ca
                             int max_blocks_per_seq, int dtype, void *stream);
 
 /*
- * paged_attention_prefill_split -- the same attention with each item's keys
- * split over key_parts work items (a split-K over the key range), for calls
- * with fewer items than SMs (one short chunk, few sequences): every (sequence,
- * 2 * (128 / group) chunk tokens, kv head) item of the tcgen05 kernel becomes
- * up to key_parts items over contiguous ranges of its N 64-key tiles (at most
- * ceil(N / 16) of them: an item of 16 tiles or fewer stays whole and writes
- * `out` itself). Each part writes its rows' unnormalised fp32 output and
- * softmax state to `workspace`, and a merge kernel on the same stream combines
- * them into `out` (softmax's LSE identity, the same one split-K decode uses).
- * The result equals paged_attention_prefill's within rounding.
+ * paged_attention_prefill_split -- the same attention with the call's keys
+ * shared out evenly over the SMs (a split-K over the key range), for calls
+ * with few items over long contexts (one short chunk, few sequences). The key
+ * tiles (64 keys) of every (sequence, 2 * (128 / group) chunk tokens, kv
+ * head) item of the tcgen05 kernel, all items end to end, are cut into one
+ * contiguous range per SM of r tiles each: r at least the total over the SMs,
+ * at least min(16, the longest item's tiles), and long enough that no item
+ * meets more than key_parts ranges. An item inside one range writes `out`
+ * itself; an item cut by a range boundary writes, per piece, its rows'
+ * unnormalised fp32 output and softmax state to `workspace`, and a merge
+ * kernel on the same stream combines them into `out` (softmax's LSE identity,
+ * the same one split-K decode uses). The result equals
+ * paged_attention_prefill's within rounding.
  *
- *   key_parts        1 .. 16; 1 is paged_attention_prefill itself; 0 picks
- *                    the most parts whose items still fit one wave of the SMs
- *                    (the items counted from max_query_len), as many as the
- *                    workspace holds (1 without one)
+ *   key_parts        1 .. 32: most ranges one item meets; 1 is
+ *                    paged_attention_prefill itself. 0 splits when the items
+ *                    (counted from max_query_len) are fewer than the SMs and
+ *                    the workspace holds the split (32 ranges at most), else
+ *                    runs whole items. Calls of more than 500 items run whole
+ *                    items at any key_parts.
  *   workspace        device, 256-byte aligned, caller-owned, at least
- *                    paged_attention_prefill_workspace_bytes(num_tokens,
- *                    n_q_heads, head_dim, key_parts) bytes; its contents on
- *                    entry do not matter and are garbage afterwards
+ *                    paged_attention_prefill_workspace_bytes(head_dim) bytes
+ *                    (it depends on the device's SM count only); its contents
+ *                    on entry do not matter and are garbage afterwards
  *   other arguments  as for paged_attention_prefill
  *
- * Returns PAGEDKV_ERR_WORKSPACE when key_parts >= 2 and the workspace is
- * missing or too small, PAGEDKV_ERR_INVALID_ARG for key_parts outside 0 .. 16
- * or a misaligned workspace; otherwise as paged_attention_prefill (whose
- * device errors it sets the same way). With PAGEDKV_OPT_PREFILL_PATH = 1 (the
- * warp-level MMA kernel) the keys are not split. Asynchronous on `stream`;
- * allocates nothing.
+ * Returns PAGEDKV_ERR_WORKSPACE when the call splits (key_parts >= 2) and the
+ * workspace is missing or too small, PAGEDKV_ERR_INVALID_ARG for key_parts
+ * outside 0 .. 32 or a misaligned workspace; otherwise as
+ * paged_attention_prefill (whose device errors it sets the same way). With
+ * PAGEDKV_OPT_PREFILL_PATH = 1 (the warp-level MMA kernel) the keys are not
+ * split. Asynchronous on `stream`; allocates nothing. Calls that share a
+ * workspace must be ordered on one stream.
  */
 int paged_attention_prefill_split(const void *q, const void *k_cache, const void *v_cache,
                                   const int32_t *block_tables, const int32_t *query_start,
@@ -306,12 +312,11 @@ int paged_attention_prefill_split(const void *q, const void *k_cache, const void
                                   int max_blocks_per_seq, int dtype, int key_parts, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
-/* Workspace bytes of paged_attention_prefill_split for key_parts (2 .. 16;
- * 0 for anything else): fp32 outputs [key_parts][num_tokens * n_q_heads]
- * [head_dim], then two fp32 [key_parts][num_tokens * n_q_heads] arrays, each
- * on a 256-byte boundary. */
-size_t paged_attention_prefill_workspace_bytes(int num_tokens, int n_q_heads, int head_dim,
-                                               int key_parts);
+/* Workspace bytes of paged_attention_prefill_split on the current device
+ * (head_dim 64 or 128; 0 for any other, or without a device): an int per
+ * item (500), then fp32 outputs [2 * SMs][256 rows][head_dim], then two fp32
+ * [2 * SMs][256 rows] arrays, each on a 256-byte boundary. */
+size_t paged_attention_prefill_workspace_bytes(int head_dim);
 
 /*
  * paged_attention_decode -- fused paged-attention decode.

@@ -102,7 +102,7 @@ def load():
                                                   i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                                   vp, sz, vp]
     lib.paged_attention_prefill_split.restype = i32
-    lib.paged_attention_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.paged_attention_prefill_workspace_bytes.argtypes = [i32]
     lib.paged_attention_prefill_workspace_bytes.restype = sz
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
@@ -291,10 +291,11 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, cont
     [num_seqs + 1]; context_lens counts each sequence's cached tokens with its
     chunk (already appended) included. max_query_len bounds every chunk's
     length; by default it is read from query_start (a device-to-host copy).
-    With key_parts other than 1 the keys of each work item may be split over
-    key_parts items (0: as many as fill the SMs and the workspace), whose
-    states a merge kernel combines; the workspace (see prefill_workspace) is
-    taken from torch's allocator when none is given."""
+    With key_parts other than 1 the call's key tiles may be shared out in
+    equal ranges over the SMs, no item in more than key_parts of them (0: when
+    the items leave SMs idle and the workspace holds the split), and a merge
+    kernel combines the pieces' states; the workspace (see prefill_workspace)
+    is taken from torch's allocator when none is given."""
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise PagedKVError("q and out must be [num_tokens][n_q_heads][head_dim] of one type")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != q.dtype:
@@ -314,23 +315,24 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, query_start, cont
         _check(st, "paged_attention_prefill")
         return
     if workspace is None:
-        workspace = prefill_workspace(q, key_parts)
+        workspace = prefill_workspace(q)
     ws = _dev(workspace, "workspace")
     nbytes = workspace.numel() * workspace.element_size()
     st = load().paged_attention_prefill_split(*args, int(key_parts), ws, nbytes, _stream(stream))
     _check(st, "paged_attention_prefill_split")
 
 
-def prefill_workspace_bytes(num_tokens, n_q_heads, head_dim, key_parts):
-    """Workspace bytes of a prefill whose keys are split key_parts ways (0 below 2)."""
-    return load().paged_attention_prefill_workspace_bytes(int(num_tokens), int(n_q_heads), int(head_dim),
-                                                          int(key_parts))
+def prefill_workspace_bytes(head_dim):
+    """Workspace bytes of a prefill whose keys are split, on the current device
+    (it depends on the SM count alone; 0 without a device)."""
+    return load().paged_attention_prefill_workspace_bytes(int(head_dim))
 
 
-def prefill_workspace(q, key_parts):
+def prefill_workspace(q):
     """A device buffer for paged_attention_prefill(..., workspace=..., key_parts=...)
-    (key_parts 0 gets room for the largest split, 16)."""
-    n = prefill_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], key_parts if key_parts else 16)
+    on q's device."""
+    with torch.cuda.device(q.device):
+        n = prefill_workspace_bytes(q.shape[2])
     return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
 
 

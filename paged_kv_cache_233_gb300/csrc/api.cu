@@ -474,13 +474,15 @@ int paged_kv_swap_blocks(const void *src_k, const void *src_v, int src_num_block
 
 namespace {
 
-constexpr int kMaxKeyParts = 16;
+constexpr int kMaxKeyParts = pkv::kPfMaxSplitParts;
 
-// Bytes of the key split's workspace: fp32 O [parts][rows][head_dim], then m
-// and l [parts][rows], each on a 256-byte boundary (rows = tokens x query heads).
-size_t prefill_split_bytes(long long rows, int head_dim, int parts) {
-    return round256(size_t(parts) * size_t(rows) * size_t(head_dim) * 4) +
-           2 * round256(size_t(parts) * size_t(rows) * 4);
+// Bytes of the key split's workspace for a grid of `ctas` CTAs: the plan (an
+// int per item), then fp32 O [2 ctas][256 rows][head_dim], then m and l
+// [2 ctas][256 rows], each on a 256-byte boundary.
+size_t prefill_split_bytes(int head_dim, int ctas) {
+    const size_t rows = size_t(2) * size_t(ctas) * 256;
+    return round256(size_t(pkv::kPfMaxSplitItems) * 4) + round256(rows * size_t(head_dim) * 4) +
+           2 * round256(rows * 4);
 }
 
 int prefill_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -547,31 +549,33 @@ int prefill_impl(const void *q, const void *k_cache, const void *v_cache,
     // chunk tokens per item: the tcgen05 kernel's two Q tiles hold 128 / group
     // whole tokens each
     p.tile_tokens = tc ? 2 * (128 / group) : pkv::kPfRows / group;
-    // key split (tcgen05 kernel only): 0 picks the most parts whose items still
-    // fit one wave of the SMs, as far as the workspace holds them
+    // key split (tcgen05 kernel only): the call's key tiles in equal ranges,
+    // one per SM. 0 takes it when the items leave SMs idle and the workspace
+    // holds it (no item then in more than kMaxKeyParts ranges); an explicit
+    // count needs the workspace. Calls of more than kPfMaxSplitItems items,
+    // or whose key tiles could pass the plan's ints, run whole items.
     const long long tiles = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
-    const long long rows = (long long)num_tokens * n_q_heads;
-    int parts = tc ? key_parts : 1;
-    if (parts == 0) {
-        const long long items = tiles * n_kv_heads * num_seqs;
-        parts = int(items >= sms ? 1 : sms / items);
-        if (parts > kMaxKeyParts) parts = kMaxKeyParts;
-        while (parts > 1 && (!workspace || prefill_split_bytes(rows, head_dim, parts) > workspace_bytes))
-            --parts;
-    }
+    const long long items = tiles * n_kv_heads * num_seqs;
+    const long long tile_cap = (cap + 63) / 64;   // key tiles of one item at most
+    const bool splittable = tc && items <= pkv::kPfMaxSplitItems && items * tile_cap <= INT_MAX / 2;
+    const size_t split_bytes = prefill_split_bytes(head_dim, sms);
+    int parts = splittable ? key_parts : 1;
+    if (parts == 0)
+        parts = items < sms && workspace && split_bytes <= workspace_bytes ? kMaxKeyParts : 1;
     if (parts > 1) {
-        if (!workspace || prefill_split_bytes(rows, head_dim, parts) > workspace_bytes)
-            return PAGEDKV_ERR_WORKSPACE;
+        if (!workspace || split_bytes > workspace_bytes) return PAGEDKV_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return PAGEDKV_ERR_INVALID_ARG;
+        const size_t rows = size_t(2) * size_t(sms) * 256;
         uint8_t *ws = static_cast<uint8_t *>(workspace);
-        p.ws_o = reinterpret_cast<float *>(ws);
-        p.ws_m = reinterpret_cast<float *>(ws + round256(size_t(parts) * size_t(rows) * size_t(head_dim) * 4));
-        p.ws_l = p.ws_m + round256(size_t(parts) * size_t(rows) * 4) / 4;
+        p.ws_plan = reinterpret_cast<int *>(ws);
+        p.ws_o = reinterpret_cast<float *>(ws + round256(size_t(pkv::kPfMaxSplitItems) * 4));
+        p.ws_m = p.ws_o + round256(rows * size_t(head_dim) * 4) / 4;
+        p.ws_l = p.ws_m + round256(rows * 4) / 4;
     }
     p.key_parts = parts;
     if (tc) {
         // the persistent kernel counts its work items in ints
-        const long long per_seq = tiles * n_kv_heads * parts;
+        const long long per_seq = tiles * n_kv_heads;
         if (per_seq > (INT_MAX / 2) / num_seqs) return PAGEDKV_ERR_UNSUPPORTED;
     }
     p.num_blocks = num_blocks;
@@ -586,7 +590,8 @@ int prefill_impl(const void *q, const void *k_cache, const void *v_cache,
            : pkv::launch_prefill(dtype, head_dim, kmap, vmap, p, max_query_len,
                                  static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess && parts > 1)
-        e = pkv::launch_prefill_merge(dtype, head_dim, p, max_query_len, static_cast<cudaStream_t>(stream));
+        e = pkv::launch_prefill_merge(dtype, head_dim, p, max_query_len, sms,
+                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGEDKV_OK : PAGEDKV_ERR_CUDA;
 }
 
@@ -616,11 +621,12 @@ int paged_attention_prefill_split(const void *q, const void *k_cache, const void
                         workspace_bytes, stream);
 }
 
-size_t paged_attention_prefill_workspace_bytes(int num_tokens, int n_q_heads, int head_dim,
-                                               int key_parts) {
-    if (num_tokens < 1 || n_q_heads < 1 || head_dim < 1 || key_parts < 2 || key_parts > kMaxKeyParts)
-        return 0;
-    return prefill_split_bytes((long long)num_tokens * n_q_heads, head_dim, key_parts);
+size_t paged_attention_prefill_workspace_bytes(int head_dim) {
+    if (head_dim != 64 && head_dim != 128) return 0;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    if (device_state(&err, &sms) != PAGEDKV_OK) return 0;
+    return prefill_split_bytes(head_dim, sms);
 }
 
 size_t paged_attention_workspace_bytes(int num_seqs, int n_q_heads, int head_dim,

@@ -32,12 +32,17 @@ struct PrefillParams {
     int block_size;
     int log2_block;
     int max_blocks;
-    // tcgen05 kernel, key split: each item's key tiles are dealt to key_parts
-    // items of contiguous ranges, which write their rows' unnormalised fp32 O,
-    // reference maximum m (base 2, scaled) and sum l to ws_o [part][row][D],
-    // ws_m and ws_l [part][row] (row = token * n_q_heads + query head) for
-    // launch_prefill_merge; key_parts == 1 writes `out` itself
+    // tcgen05 kernel, key split (key_parts >= 2): one CTA per SM, each taking
+    // an equal contiguous range of the call's key tiles (all items' end to
+    // end; no item in more than key_parts ranges). An item cut by a range
+    // boundary writes, per piece, its rows' unnormalised fp32 O, reference
+    // maximum m (base 2, scaled) and sum l to ws_o [slot][row][D], ws_m and
+    // ws_l [slot][row] (2 slots per CTA, 256 row slots each), and CTA 0 writes
+    // each item's first CTA and range count to ws_plan [item], for
+    // launch_prefill_merge; an item within one range writes `out` itself.
+    // key_parts == 1: whole items
     int key_parts;
+    int *ws_plan;
     float *ws_o;
     float *ws_m;
     float *ws_l;
@@ -62,9 +67,15 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,
                               cudaStream_t stream);
 int prefill_tc_smem_bytes(int head_dim);
 
-// The key split's merge: per row of every item, the parts' states combined
-// into `out` (rows of a flagged sequence left unwritten, as the kernel does).
+// Key split limits: items per call (the plan lives in the kernel's shared
+// memory) and ranges per item (a merge lane each).
+constexpr int kPfMaxSplitItems = 500;
+constexpr int kPfMaxSplitParts = 32;
+
+// The key split's merge: per row of every item cut into pieces, the pieces'
+// states combined into `out` (rows of a flagged sequence left unwritten, as
+// the kernel does).
 cudaError_t launch_prefill_merge(int dtype, int head_dim, const PrefillParams &p, int max_query_len,
-                                 cudaStream_t stream);
+                                 int num_sms, cudaStream_t stream);
 
 }  // namespace pkv

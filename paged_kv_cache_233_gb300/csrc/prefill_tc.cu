@@ -104,11 +104,17 @@ constexpr int kDone = 2 * kTcStages + kPerTileBars * kTcTiles;
 // completes and both issuers have released it)
 constexpr int kTailV = kDone + 1;
 constexpr int kNumBars = kTailV + kTcStages;
-// key split: an item of N key tiles takes at most ceil(N / kMinPartTiles)
-// parts, so that a part holds 8 to 16 key tiles (N > 16) and an item of 16 or
-// fewer is not split (shorter parts save less key loop than the merge and the
-// fp32 states cost)
+// key split: the CTAs share the call's key tiles (all items' tiles end to end)
+// in equal contiguous ranges of r tiles, r at least min(kMinPartTiles, the
+// longest item) so that an item is not cut into pieces shorter than that
+// merely to reach every SM; a piece is an item's tiles within one range, and
+// an item cut into several pieces leaves per-row states for the merge
 constexpr int kMinPartTiles = 16;
+constexpr int kMaxSplitParts = kPfMaxSplitParts;   // pieces of one item (a merge lane each)
+// the split's plan in the item-order region: off[i] = key tiles of items
+// before i (i = 0 .. items), then this CTA's range
+constexpr int kMaxSplitItems = kPfMaxSplitItems;
+constexpr int kPlanRange = 504;        // r, start, end, first item, piece count, parts layout
 // sequences ranked by context length in shared memory (beyond this count the
 // items keep the sequences' own order)
 constexpr int kMaxRankedSeqs = 256;
@@ -134,6 +140,8 @@ struct TcLayout {
     static constexpr int kRefRow = kOutRow + 8 * kTcTiles * kTcRows;
     static constexpr int kTotal = kRefRow + 4 * kTcTiles * kTcRows;
     static_assert(2 * kTcKeys + D <= kTmemTile, "S buffers and O must fit a Q tile's columns");
+    static_assert(kMaxSplitItems < kPlanRange && 4 * (kPlanRange + 6) <= 8 * kMaxRankedSeqs,
+                  "the key split's plan must fit the item-order region");
 };
 
 // Whether the barrier's phase of this parity has completed, without waiting.
@@ -170,33 +178,29 @@ __device__ __forceinline__ void sts32(uint32_t addr, int v) {
 struct PfItem {
     int s, h;
     int q0, j0, ntok, pos0, L;   // ntok: chunk tokens of the item
-    int part, kb;       // key split: this item's part and its first key tile
+    int slot, kb;       // key split: the piece's state slot and its first key tile
     bool split;         // the item's keys are split (its rows leave states for the merge)
     int nk[kTcTiles];   // key tiles of Q tile t from kb: through the position of its last row
-    int nkt;            // key tiles of the item from kb (the part's range)
+    int nkt;            // key tiles of the item from kb (the piece's range)
     bool tail;          // the item's last key tile runs past the context
 };
 
 // Items in one order shared by every CTA: sequences by decreasing context
 // length (ranked, when there are few enough), within a sequence its query
-// tiles from the last (the most keys), then kv heads, then key parts, so that
-// the items that read a sequence's K/V run close together in time and share it
-// through L2. Item k of that order. Returns false for an item with no rows or
-// no key tiles (a part past the item's keys), or a sequence whose chunk or
-// length is invalid (reported once per sequence when `report`).
-template <bool kSplit>
-__device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked, int tiles, int k,
-                                        bool report, PfItem &it) {
-    const int parts = kSplit ? p.key_parts : 1;
-    const int per_tile = p.n_kv_heads * parts;
-    const int per_seq = tiles * per_tile;
+// tiles from the last (the most keys), then kv heads, so that the items that
+// read a sequence's K/V run close together in time and share it through L2.
+// Item k of that order: fills `it` but for its key range and returns its key
+// tiles N (through its last row's position), or 0 for an item with no rows or
+// a sequence whose chunk or length is invalid (reported once per sequence
+// when `report`).
+__device__ __forceinline__ int pf_decode(const PrefillParams &p, uint32_t ranked, int tiles, int k,
+                                         bool report, PfItem &it, int (&nk_all)[kTcTiles]) {
+    const int per_seq = tiles * p.n_kv_heads;
     const int r = k / per_seq;
     const int rem = k - r * per_seq;
     const int s = ranked ? lds32(ranked + 4u * uint32_t(r)) : r;
-    const int qt = tiles - 1 - rem / per_tile;
-    const int rem2 = rem - (rem / per_tile) * per_tile;
-    const int h = rem2 / parts;
-    const int part = rem2 - h * parts;
+    const int qt = tiles - 1 - rem / p.n_kv_heads;
+    const int h = rem - (rem / p.n_kv_heads) * p.n_kv_heads;
     const int q0 = __ldg(p.query_start + s);
     const int q1 = __ldg(p.query_start + s + 1);
     const int n = q1 - q0;
@@ -204,12 +208,12 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
     const bool rows_ok = q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens && n <= tiles * p.tile_tokens;
     const bool len_ok = L >= n && L <= p.max_blocks * p.block_size;
     if (!rows_ok || !len_ok) {
-        if (report && qt == tiles - 1 && h == 0 && part == 0)
+        if (report && qt == tiles - 1 && h == 0)
             atomicOr(p.err, rows_ok ? PAGEDKV_DEVERR_CONTEXT_LEN : PAGEDKV_DEVERR_POSITION);
-        return false;
+        return 0;
     }
     const int j0 = qt * p.tile_tokens;
-    if (j0 >= n) return false;
+    if (j0 >= n) return 0;
     it.s = s;
     it.h = h;
     it.q0 = q0;
@@ -220,36 +224,171 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t ranked,
     // Q tile t holds the item's tokens t*tq .. t*tq + tq - 1, tq = 128 / group
     // whole tokens (all of a token's heads in one tile)
     const int tq = kTcRows / p.group;
-    int nk_all[kTcTiles];
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) {
         const int nt = min(max(it.ntok - t * tq, 0), tq);
         nk_all[t] = nt > 0 ? (it.pos0 + t * tq + nt - 1) / kTcKeys + 1 : 0;
     }
-    // the part's key tiles: [kb, ke) of the item's N (a tile's own count ends
-    // at its last row's position), in at most ceil(N / kMinPartTiles) parts (a
-    // part past them is no item; an item of one part writes its rows itself)
-    const int N = nk_all[kTcTiles - 1] > 0 ? nk_all[kTcTiles - 1] : nk_all[0];
-    const int eff = min(parts, max(1, (N + kMinPartTiles - 1) / kMinPartTiles));
-    if (part >= eff) return false;
-    const int kb = int((long long)N * part / eff);
-    const int ke = int((long long)N * (part + 1) / eff);
-    it.part = part;
+    return nk_all[kTcTiles - 1] > 0 ? nk_all[kTcTiles - 1] : nk_all[0];
+}
+
+// This CTA's m-th piece of work. Whole items: item k of the shared order
+// (`order`: the ranked sequence ids, or 0). Key split: the m-th item that
+// meets this CTA's range of key tiles (`order`: the plan), restricted to the
+// range. Returns false for an item with no rows or no key tiles there.
+template <bool kSplit>
+__device__ __forceinline__ bool pf_item(const PrefillParams &p, uint32_t order, int tiles, int k,
+                                        bool report, PfItem &it) {
+    int nk_all[kTcTiles];
+    if (!kSplit) {
+        const int N = pf_decode(p, order, tiles, k, report, it, nk_all);
+        if (N == 0) return false;
+        it.slot = 0;
+        it.kb = 0;
+        it.split = false;
+#pragma unroll
+        for (int t = 0; t < kTcTiles; ++t) it.nk[t] = nk_all[t];
+        it.nkt = N;
+        it.tail = N * kTcKeys > it.L;
+        return true;
+    }
+    const int i = lds32(order + 4u * (kPlanRange + 3)) + k;
+    const int N = pf_decode(p, 0u, tiles, i, false, it, nk_all);
+    if (N == 0) return false;
+    const int off = lds32(order + 4u * uint32_t(i));
+    const int kb = max(lds32(order + 4u * (kPlanRange + 1)) - off, 0);
+    const int ke = min(lds32(order + 4u * (kPlanRange + 2)) - off, N);
+    if (ke <= kb) return false;
+    // a piece that starts inside the item is its CTA's first (slot 2c); one
+    // that starts the item is the CTA's last, or its only one (slot 2c + 1)
+    it.slot = 2 * int(blockIdx.x) + (kb > 0 ? 0 : 1);
     it.kb = kb;
-    it.split = eff > 1;
+    it.split = kb > 0 || ke < N;
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) it.nk[t] = max(min(nk_all[t], ke) - kb, 0);
     it.nkt = ke - kb;
-    it.tail = ke == N && N * kTcKeys > L;
+    it.tail = ke == N && N * kTcKeys > it.L;
     return true;
 }
 
-// This CTA's m-th item: bands of gridDim.x items, dealt forwards in even bands
-// and backwards in odd ones (so that every CTA gets a similar share of the
-// ranked work). The item count fits an int (the launcher checks).
+// This CTA's m-th item: whole items in bands of gridDim.x items, dealt
+// forwards in even bands and backwards in odd ones (so that every CTA gets a
+// similar share of the ranked work; the item count fits an int, the launcher
+// checks); under the key split the CTA's pieces in order.
+template <bool kSplit>
 __device__ __forceinline__ int pf_item_index(int m) {
+    if (kSplit) return m;
     const int G = int(gridDim.x), c = int(blockIdx.x);
     return m * G + ((m & 1) ? G - 1 - c : c);
+}
+
+// Key split: the plan, alike in every CTA, in one of two layouts. off[i]
+// (shared memory, i = 0 .. items) counts the key tiles of items before i
+// (T in all); a piece is an item's tiles within one CTA's range [start, end).
+// - Ranges: CTA c takes tiles [c r, min((c + 1) r, T)) of all items end to
+//   end, r at least ceil(T / grid), long enough that no item meets more than
+//   `parts` ranges (an item of N tiles meets at most ceil((N - 1) / r) + 1)
+//   and at least min(kMinPartTiles, the longest item). A range can hold the
+//   end of one item and the start of the next.
+// - Parts (at most grid / items CTAs per item and 16, p of them): CTA c takes part
+//   c % p of item c / p, whose N tiles go to min(p, ceil(N / kMinPartTiles))
+//   equal parts; every CTA holds one piece at most.
+// Either way an item's pieces sit in consecutive CTAs from c0. The plan takes
+// the layout whose longest CTA (key tiles, plus kPieceCost per piece) is the
+// shorter: parts, when the items are about equal and divide the SMs well.
+// Every thread of the CTA calls it.
+constexpr int kPieceCost = 4;   // a piece's fixed cost (Q copy, epilogue, merge) in key tiles
+constexpr int kMaxItemParts = 16;  // CTAs per item in the parts layout at most
+__device__ __forceinline__ void pf_split_plan(const PrefillParams &p, int tiles, int items, int *off,
+                                              bool report) {
+    for (int i = int(threadIdx.x); i < items; i += int(blockDim.x)) {
+        PfItem it;
+        int nk_all[kTcTiles];
+        off[i + 1] = pf_decode(p, 0u, tiles, i, report, it, nk_all);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = int(threadIdx.x);
+        const int G = int(gridDim.x);
+        // CTAs per item in the parts layout (0: it does not fit the grid; more
+        // than 16 parts cost the merge more than their shorter key loop saves)
+        const int pp = min(min(p.key_parts, kMaxItemParts), G / max(items, 1));
+        // a lane per run of items: the run's sum, maximum and longest part, then the prefix
+        const int per = (items + 31) / 32;
+        const int lo = min(lane * per, items), hi = min(lo + per, items);
+        int sum = 0, mx = 0, part_mx = 0;
+        for (int i = lo; i < hi; ++i) {
+            const int n = off[i + 1];
+            sum += n;
+            mx = max(mx, n);
+            if (pp > 0) {
+                const int eff = min(pp, max(1, (n + kMinPartTiles - 1) / kMinPartTiles));
+                part_mx = max(part_mx, (n + eff - 1) / eff);
+            }
+        }
+        int incl = sum;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(kAll, incl, d);
+            if (lane >= d) incl += y;
+        }
+        for (int d = 16; d >= 1; d >>= 1) {
+            mx = max(mx, __shfl_xor_sync(kAll, mx, d));
+            part_mx = max(part_mx, __shfl_xor_sync(kAll, part_mx, d));
+        }
+        int run = incl - sum;
+        for (int i = lo; i < hi; ++i) {
+            run += off[i + 1];
+            off[i + 1] = run;
+        }
+        const int T = __shfl_sync(kAll, incl, 31);
+        if (lane == 0) {
+            off[0] = 0;
+            int r = (T + G - 1) / G;
+            if (mx > 1) r = max(r, (mx - 2) / (p.key_parts - 1) + 1);
+            r = max(r, max(min(kMinPartTiles, mx), 1));
+            const int c = int(blockIdx.x);
+            long long start, end;
+            int first, count;
+            // the ranges' longest CTA: a range and two pieces (the end of one
+            // item, the start of the next) unless the items are shorter
+            const bool parts_layout = pp > 0 && part_mx + kPieceCost <= r + 2 * kPieceCost;
+            if (parts_layout) {
+                const int i = c / pp, q = c - i * pp;
+                const int n = i < items ? off[i + 1] - off[i] : 0;
+                const int eff = min(pp, max(1, (n + kMinPartTiles - 1) / kMinPartTiles));
+                first = i;
+                count = n > 0 && q < eff ? 1 : 0;
+                start = count ? off[i] + (long long)n * q / eff : 0;
+                end = count ? off[i] + (long long)n * (q + 1) / eff : 0;
+            } else {
+                start = min((long long)c * r, (long long)T);
+                end = min(start + r, (long long)T);
+                // the first item holding a tile at or past start, the last one
+                // holding a tile before end (off is non-decreasing)
+                int lo2 = 0, hi2 = items;
+                while (lo2 < hi2) {
+                    const int mid = (lo2 + hi2) >> 1;
+                    if (off[mid + 1] > start) hi2 = mid;
+                    else lo2 = mid + 1;
+                }
+                first = lo2;
+                lo2 = first;
+                hi2 = items;
+                while (lo2 < hi2) {
+                    const int mid = (lo2 + hi2) >> 1;
+                    if (off[mid + 1] >= end) hi2 = mid;
+                    else lo2 = mid + 1;
+                }
+                count = start < end ? lo2 - first + 1 : 0;
+            }
+            off[kPlanRange] = r;
+            off[kPlanRange + 1] = int(start);
+            off[kPlanRange + 2] = int(end);
+            off[kPlanRange + 3] = first;
+            off[kPlanRange + 4] = count;
+            off[kPlanRange + 5] = parts_layout ? pp : 0;
+        }
+    }
 }
 
 }  // namespace
@@ -273,7 +412,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int lane = threadIdx.x & 31;
     const int B = p.block_size;
     const int g = p.group;
-    const int num_items = p.num_seqs * tiles * p.n_kv_heads * (kSplit ? p.key_parts : 1);
+    const int all_items = p.num_seqs * tiles * p.n_kv_heads;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kTcStages; ++k) {
@@ -301,9 +440,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // sequences ranked by decreasing context length (ties by index), when some
     // CTA gets more than one item; the lengths are the caller's, read before
     // any grid dependency
-    uint32_t ranked = 0;   // shared address of the ranked sequence ids (0: natural order)
-    if (p.num_seqs > 1 && p.num_seqs <= kMaxRankedSeqs && num_items > int(gridDim.x)) {
-        ranked = base + Ly::kOrder;
+    // (whole items), or the key split's plan: the item order's shared address
+    uint32_t order = 0;    // 0: the sequences' own order
+    if (!kSplit && p.num_seqs > 1 && p.num_seqs <= kMaxRankedSeqs && all_items > int(gridDim.x)) {
+        order = base + Ly::kOrder;
         int *ids = reinterpret_cast<int *>(sm + Ly::kOrder);
         int *lens = ids + kMaxRankedSeqs;
         for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) lens[s] = __ldg(p.context_lens + s);
@@ -318,10 +458,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             ids[rank] = s;
         }
     }
+    if (kSplit) {
+        // (the launcher keeps the split to at most kMaxSplitItems items)
+        order = base + Ly::kOrder;
+        pf_split_plan(p, tiles, all_items, reinterpret_cast<int *>(sm + Ly::kOrder), blockIdx.x == 0);
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly::kTmemSlot);
+    // items (key split: this CTA's pieces) to work through
+    const int num_items = kSplit ? lds32(order + 4u * (kPlanRange + 4)) : all_items;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -338,6 +485,25 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         // the pools as the kernels before this one left them (launched as
         // the programmatic dependent of an append that may still be running)
         grid_dependency_wait();
+        if (kSplit && blockIdx.x == 0) {
+            // for the merge, per item: the CTA c0 of its first piece (bits 0-15)
+            // and its piece count (bits 16-31; fewer than 2: not split); written
+            // once the grids before this one are done with the workspace
+            const int *off = reinterpret_cast<const int *>(sm + Ly::kOrder);
+            const int r = off[kPlanRange], pp = off[kPlanRange + 5];
+            for (int i = lane; i < all_items; i += 32) {
+                const int o = off[i], n = off[i + 1] - o;
+                int c0 = 0, pieces = 0;
+                if (n > 0 && pp > 0) {
+                    c0 = i * pp;
+                    pieces = min(pp, max(1, (n + kMinPartTiles - 1) / kMinPartTiles));
+                } else if (n > 0) {
+                    c0 = o / r;
+                    pieces = (o + n - 1) / r - c0 + 1;
+                }
+                p.ws_plan[i] = c0 | (pieces << 16);
+            }
+        }
         const int rows_per_box = B >= 16 ? 16 : 8;
         // this lane's copy: box ci (rows_per_box keys), column block csl, operand cop
         constexpr int kCopies = 2 * Ly::kSlabs;              // per box
@@ -346,10 +512,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         int armed = 0;
         bool ok = true;
         for (int m = 0; ok; ++m) {
-            const int k = pf_item_index(m);
+            const int k = pf_item_index<kSplit>(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item<kSplit>(p, ranked, tiles, k, lane == 0, it)) continue;
+            if (!pf_item<kSplit>(p, order, tiles, k, lane == 0, it)) continue;
             const int32_t *table = p.block_tables + size_t(it.s) * p.max_blocks;
             for (int j = 0; j < it.nkt; ++j) {
                 const int gk = kt + j;
@@ -439,10 +605,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         uint32_t parity = 0;   // bit st: phase parity of stage st's tail barrier
         bool ok = true;
         for (int m = 0; ok; ++m) {
-            const int k = pf_item_index(m);
+            const int k = pf_item_index<kSplit>(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
+            if (!pf_item<kSplit>(p, order, tiles, k, false, it)) continue;
             {
                 bool got = true;
                 if (lane == 0) {
@@ -575,10 +741,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             int i = 0;    // items so far
             bool ok = true;
             for (int m = 0; ok; ++m) {
-                const int k = pf_item_index(m);
+                const int k = pf_item_index<kSplit>(m);
                 if (k >= num_items) break;
                 PfItem it;
-                if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
+                if (!pf_item<kSplit>(p, order, tiles, k, false, it)) continue;
                 const int nk = it.nk[t];
                 // the item's Q rows of this tile are in shared memory
                 ok = wait(bar_qfull(t), i);
@@ -674,10 +840,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             const bool prev_row = v_row != ~0ull;
             const unsigned long long prev_qrow = prev_row ? v_row & ((1ull << 48) - 1) : 0ull;
             const bool split = kSplit && prev_row && ((v_row >> 62) & 1ull);
-            // key split: every row of the item leaves its part's state, m = -inf
-            // when the part held none of its keys (its O is then not written)
-            const size_t wrow = size_t((v_row >> 48) & 0x3fffull) * (size_t(p.num_tokens) * size_t(p.n_q_heads)) +
-                                prev_qrow;
+            // key split: every row of the item leaves its piece's state in the
+            // piece's slot, m = -inf when the piece held none of its keys (its O
+            // is then not written)
+            const size_t wrow = size_t((v_row >> 48) & 0x3fffull) * size_t(kTcTiles * kTcRows) + size_t(R);
             if (split && prev_row) {
                 p.ws_m[wrow] = prev_nk > 0 ? __int_as_float(lds32(ref_row)) : -INFINITY;
                 p.ws_l[wrow] = prev_nk > 0 ? prev_l : 0.f;
@@ -718,10 +884,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         int jt = 0;   // key tiles of this Q tile before the item
         int i = 0;
         for (int m = 0; ok; ++m) {
-            const int k = pf_item_index(m);
+            const int k = pf_item_index<kSplit>(m);
             if (k >= num_items) break;
             PfItem it;
-            if (!pf_item<kSplit>(p, ranked, tiles, k, false, it)) continue;
+            if (!pf_item<kSplit>(p, order, tiles, k, false, it)) continue;
             const int nk = it.nk[t];
             // this thread's row: token tok of the item (t*tq + r/g), head r%g of the
             // group; none past the tile's tq*g rows or the item's tokens
@@ -737,9 +903,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 break;
             }
             {
-                // (an item of a split: its part in bits 48-61, bit 62 set)
+                // (a piece of a split item: its slot in bits 48-61, bit 62 set)
                 const unsigned long long v =
-                    row ? (kSplit ? qrow | ((unsigned long long)it.part << 48) | (it.split ? 1ull << 62 : 0ull) : qrow)
+                    row ? (kSplit ? qrow | ((unsigned long long)it.slot << 48) | (it.split ? 1ull << 62 : 0ull) : qrow)
                         : ~0ull;
                 sts32(out_row, int(unsigned(v)));
                 sts32(out_row + 4, int(unsigned(v >> 32)));
@@ -838,60 +1004,63 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 }
 
-// Key split: the merge. A warp per row of an item (a CTA per 8 row slots of
-// one (sequence, query tile, kv head)), so that every row is merged at once:
-// lane p loads part p's state, the warp reduces M = max m_p and
-// den = sum 2^(m_p - M) l_p (m_p in the kernel's base-2 units), and each lane
-// loads its columns of every part's O before it accumulates
-// out = sum 2^(m_p - M) O_p / den. A part that held none of the row's keys
-// left m_p = -inf and is skipped (its O was not written); a part past the
-// item's keys was no item at all. A flagged sequence's rows stay unwritten, as
-// the kernel leaves them.
-constexpr int kMergeRowsPerCta = 8;
-constexpr int kMaxMergeParts = 16;
+// Key split: the merge. A warp per row of an item (a CTA per 4 row slots of
+// one (sequence, query tile, kv head)): the item's pieces are its ranges'
+// CTAs c0 .. c0 + n - 1, the first in slot 2 c0 + 1, the others in slot 2c;
+// lane q loads piece q's (m, l), the warp reduces M = max m_q and
+// den = sum 2^(m_q - M) l_q (m_q in the kernel's base-2 units), and each lane
+// accumulates its columns of out = sum 2^(m_q - M) O_q / den, loading the
+// pieces' O kChunk at a time (the first kChunk in the same round trip as the
+// states). 8 at a time keeps 8 CTAs on an SM; 16 at a time holds more
+// registers and pays only where items have 9 or more pieces, which takes a
+// call of at most SMs / 9 items.
+// A piece that held none of the row's keys left m_q = -inf and is skipped
+// (its O was not written). An item not split, or of a flagged sequence, is
+// left as the kernel left it.
+constexpr int kMergeRowsPerCta = 4;
+static_assert(kMaxSplitParts <= 32, "a lane per piece");
 
-template <typename T, int D>
-__global__ void __launch_bounds__(32 * kMergeRowsPerCta)
+template <typename T, int D, int kChunk>
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta, kChunk > 8 ? 4 : 8)
 paged_prefill_merge_kernel(const PrefillParams p, int tiles) {
     constexpr int E = D / 32;
     constexpr int kSlices = kTcTiles * kTcRows / kMergeRowsPerCta;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int parts = p.key_parts;
     const int grp = blockIdx.x / kSlices;
     const int R = (blockIdx.x - grp * kSlices) * kMergeRowsPerCta + warp;   // row slot of the item
     PfItem it;
-    const bool valid = lane < parts && pf_item<true>(p, 0u, tiles, grp * parts + lane, false, it);
-    const unsigned present = __ballot_sync(kAll, valid);
-    // the states (and, for the stream's order, the kernel's end: this grid does
-    // not complete before it)
-    grid_dependency_wait();
-    // no item, or one whose keys were not split (it wrote its rows itself)
-    if (__popc(present) < 2) return;
-    const int src = __ffs(present) - 1;
-    const int q0 = __shfl_sync(kAll, it.q0, src), j0 = __shfl_sync(kAll, it.j0, src);
-    const int ntok = __shfl_sync(kAll, it.ntok, src), h = __shfl_sync(kAll, it.h, src);
+    int nk_all[kTcTiles];
+    const bool valid = pf_decode(p, 0u, tiles, grp, false, it, nk_all) > 0;
     const int g = p.group, tq = kTcRows / g;
     const int t = R / kTcRows, r = R - t * kTcRows;
     const int tok = t * tq + r / g;
-    if (r >= tq * g || tok >= ntok) return;
-    const size_t rows_total = size_t(p.num_tokens) * size_t(p.n_q_heads);
-    const size_t qrow = size_t(q0 + j0 + tok) * p.n_q_heads + size_t(h) * g + r % g;
-    // one round trip: lane p's (m, l) of part p, and every part's columns of
-    // this lane's O (a part's slot exists even where it holds nothing: the sums
-    // below take only the parts that hold something; the others may hold
-    // anything, NaN included)
+    // the plan and the states (and, for the stream's order, the kernel's end:
+    // this grid does not complete before it)
+    grid_dependency_wait();
+    if (!valid || r >= tq * g || tok >= it.ntok) return;
+    const int word = __ldcg(p.ws_plan + grp);
+    const int n = word >> 16, c0 = word & 0xffff;
+    if (n < 2) return;
+    const size_t qrow = size_t(it.q0 + it.j0 + tok) * p.n_q_heads + size_t(it.h) * g + r % g;
+    auto slot_row = [&](int q) {
+        return size_t(2 * (c0 + q) + (q == 0 ? 1 : 0)) * size_t(kTcTiles * kTcRows) + size_t(R);
+    };
     float mp = -INFINITY, lp = 0.f;
-    if ((present >> lane) & 1u) {
-        mp = __ldcg(p.ws_m + size_t(lane) * rows_total + qrow);
-        lp = __ldcg(p.ws_l + size_t(lane) * rows_total + qrow);
+    if (lane < n) {
+        mp = __ldcg(p.ws_m + slot_row(lane));
+        lp = __ldcg(p.ws_l + slot_row(lane));
     }
-    float x[kMaxMergeParts][E];
+    float x[kChunk][E];
+    auto load = [&](int q0) {
 #pragma unroll
-    for (int q = 0; q < kMaxMergeParts; ++q) {
-        const float *o = p.ws_o + (size_t(q < parts ? q : 0) * rows_total + qrow) * D + lane * E;
+        for (int q = 0; q < kChunk; ++q) {
+            const bool in = q0 + q < n;
+            const float *o = p.ws_o + slot_row(in ? q0 + q : 0) * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[q][e] = q < parts ? __ldcg(o + e) : 0.f;
-    }
+            for (int e = 0; e < E; ++e) x[q][e] = in ? __ldcg(o + e) : 0.f;
+        }
+    };
+    load(0);
     float M = mp;
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, mask));
@@ -902,11 +1071,15 @@ paged_prefill_merge_kernel(const PrefillParams p, int tiles) {
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int q0 = 0; q0 < n; q0 += kChunk) {
+        if (q0 > 0) load(q0);
 #pragma unroll
-    for (int q = 0; q < kMaxMergeParts; ++q) {
-        const float wq = __shfl_sync(kAll, w, q);
+        for (int q = 0; q < kChunk; ++q) {
+            const float wq = __shfl_sync(kAll, w, (q0 + q) & 31);
+            const bool use = q0 + q < n && wq != 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = wq != 0.f ? fmaf(wq, x[q][e], acc[e]) : acc[e];
+            for (int e = 0; e < E; ++e) acc[e] = use ? fmaf(wq, x[q][e], acc[e]) : acc[e];
+        }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     T *dst = reinterpret_cast<T *>(p.out) + qrow * D + lane * E;
@@ -936,11 +1109,14 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
     // items (and a CTA's band index, at most items + grid) must fit an int
     // (the API refuses larger calls)
     const long long tiles_ll = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
-    const long long per_seq = tiles_ll * p.n_kv_heads * (kSplit ? p.key_parts : 1);
+    const long long per_seq = tiles_ll * p.n_kv_heads;
     if (per_seq > (INT_MAX / 2) / p.num_seqs) return cudaErrorInvalidValue;
     const int tiles = int(tiles_ll);
     const long long items = per_seq * p.num_seqs;
-    const dim3 grid(unsigned(items < num_sms ? items : num_sms));
+    // (key split: every SM, each CTA a range of the call's key tiles)
+    if (kSplit && (items > kMaxSplitItems || p.key_parts < 2 || p.key_parts > kMaxSplitParts))
+        return cudaErrorInvalidValue;
+    const dim3 grid(unsigned(kSplit ? num_sms : items < num_sms ? items : num_sms));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -955,11 +1131,12 @@ static cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap
 }
 
 template <typename T, int D>
-static cudaError_t launch_merge_instance(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+static cudaError_t launch_merge_instance(const PrefillParams &p, int max_query_len, int num_sms,
+                                         cudaStream_t stream) {
     const long long tiles = ((long long)max_query_len + p.tile_tokens - 1) / p.tile_tokens;
     const long long groups = tiles * p.n_kv_heads * p.num_seqs;
     const long long ctas = groups * (kTcTiles * kTcRows / kMergeRowsPerCta);
-    if (ctas > INT_MAX || p.key_parts > kMaxMergeParts) return cudaErrorInvalidValue;
+    if (ctas > INT_MAX) return cudaErrorInvalidValue;
     // the programmatic dependent of the prefill kernel: its launch and its
     // items' set-up overlap the kernel's end
     cudaLaunchAttribute attr[1];
@@ -971,17 +1148,19 @@ static cudaError_t launch_merge_instance(const PrefillParams &p, int max_query_l
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D>, p, int(tiles));
+    // (items of 9 or more pieces need a call of at most SMs / 9 items)
+    if (groups * 9 <= num_sms) return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D, 16>, p, int(tiles));
+    return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D, 8>, p, int(tiles));
 }
 
 cudaError_t launch_prefill_merge(int dtype, int head_dim, const PrefillParams &p, int max_query_len,
-                                 cudaStream_t stream) {
+                                 int num_sms, cudaStream_t stream) {
     const bool bf16 = dtype == PAGEDKV_BF16;
     if (head_dim == 64)
-        return bf16 ? launch_merge_instance<__nv_bfloat16, 64>(p, max_query_len, stream)
-                    : launch_merge_instance<__half, 64>(p, max_query_len, stream);
-    return bf16 ? launch_merge_instance<__nv_bfloat16, 128>(p, max_query_len, stream)
-                : launch_merge_instance<__half, 128>(p, max_query_len, stream);
+        return bf16 ? launch_merge_instance<__nv_bfloat16, 64>(p, max_query_len, num_sms, stream)
+                    : launch_merge_instance<__half, 64>(p, max_query_len, num_sms, stream);
+    return bf16 ? launch_merge_instance<__nv_bfloat16, 128>(p, max_query_len, num_sms, stream)
+                : launch_merge_instance<__half, 128>(p, max_query_len, num_sms, stream);
 }
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const CUtensorMap &kmap,

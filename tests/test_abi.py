@@ -194,16 +194,8 @@ def test_prefill_key_split_host_checks(lib):
                                                  vp(16), 2, 64, 32, 32, 32, 128, 64, 16, 8, 1, parts,
                                                  None, 0, None)
 
-    assert call(17) == INVALID
+    assert call(33) == INVALID
     assert call(-1) == INVALID
-
-    def r256(x):
-        return (x + 255) // 256 * 256
-
-    rows = 100 * 32
-    for parts in (2, 4, 16):
-        assert lib.paged_attention_prefill_workspace_bytes(100, 32, 128, parts) == \
-            r256(parts * rows * 128 * 4) + 2 * r256(parts * rows * 4)
-    for parts in (-1, 0, 1, 17):
-        assert lib.paged_attention_prefill_workspace_bytes(100, 32, 128, parts) == 0
-    assert lib.paged_attention_prefill_workspace_bytes(0, 32, 128, 4) == 0
+    # the split's workspace depends on the device's SM count: none without a device
+    for d in (32, 64, 96, 128):
+        assert lib.paged_attention_prefill_workspace_bytes(d) == 0

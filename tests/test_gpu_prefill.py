@@ -263,7 +263,7 @@ def test_query_rows_past_every_chunk_stay_out(orc, g):
 def prefill_split(wl, qs, q, kc, vc, bt, parts, lens=None, workspace=None, out=None):
     out = torch.full_like(q, float("nan")) if out is None else out
     lens = wl.context_lens if lens is None else lens
-    ws = pk.prefill_workspace(q, parts) if workspace is None else workspace
+    ws = pk.prefill_workspace(q) if workspace is None else workspace
     pk.paged_attention_prefill(q, kc, vc, bt, torch.from_numpy(np.asarray(qs, np.int32)).cuda(),
                                torch.from_numpy(np.asarray(lens, np.int32)).cuda(), wl.scale, out,
                                workspace=ws, key_parts=parts)
@@ -276,14 +276,15 @@ SPLIT_CASES = [(0, 1), (1100, 1), (2500, 77), (1024, 50), (3000, 130), (37, 0), 
                (4300, 200)]
 
 
-@pytest.mark.parametrize("parts", [2, 3, 16])
+@pytest.mark.parametrize("parts", [2, 3, 32])
 @pytest.mark.parametrize("g", [1, 3, 8])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_key_split_matches_oracle(orc, dtype, D, g, parts):
-    """Each long item's keys split over up to 2, 3 or 16 parts (at most one per
-    16 of its key tiles; a part's range can lie past a Q tile's rows), short
-    items whole, the parts' states merged: every row against the oracle."""
+    """The call's key tiles in equal ranges over the SMs, no item in more than
+    2, 3 or 32 of them (a piece can lie past a Q tile's rows, a range can hold
+    the end of one item and the start of the next, short items whole), the
+    pieces' states merged: every row against the oracle."""
     wl, qs, tensors, q, kc, vc, bt = build(dtype, D, 16, g, seed=600 + D + g + parts, cases=SPLIT_CASES)
     pk.device_errors(reset=True)
     out = prefill_split(wl, qs, q, kc, vc, bt, parts)
@@ -324,23 +325,47 @@ def test_key_split_without_a_workspace_takes_one_from_torch(orc):
 
 
 def test_key_split_automatic_parts_and_a_short_workspace(orc, path):
-    """key_parts 0 picks enough parts to fill the SMs (as many as the workspace
-    holds); a workspace smaller than an explicit split needs is refused (on the
-    tcgen05 kernel: the warp-level MMA kernel does not split, and needs none)."""
+    """key_parts 0 splits a call of fewer items than SMs; a workspace smaller
+    than the split needs is refused (on the tcgen05 kernel: the warp-level MMA
+    kernel does not split, and needs none); the workspace's size follows the
+    SM count alone."""
     cases = [(1920, 128)]   # one sequence, one 128-token chunk after 1920 cached tokens
     wl, qs, tensors, q, kc, vc, bt = build("f16", 128, 16, 1, seed=640, cases=cases, n_kv=32)
     out = prefill_split(wl, qs, q, kc, vc, bt, 0)
     okc, ovc, _ = oracle_fill(orc, wl, tensors)
     ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "f16")
     assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
-    short = torch.empty(pk.prefill_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], 4) - 256,
-                        dtype=torch.uint8, device=q.device)
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+
+    def r256(x):
+        return (x + 255) // 256 * 256
+
+    rows = 2 * sms * 256
+    assert pk.prefill_workspace_bytes(128) == r256(500 * 4) + r256(rows * 128 * 4) + 2 * r256(rows * 4)
+    assert pk.prefill_workspace_bytes(96) == 0
+    short = torch.empty(pk.prefill_workspace_bytes(q.shape[2]) - 256, dtype=torch.uint8, device=q.device)
     if path == 2:
         with pytest.raises(pk.PagedKVError):
             prefill_split(wl, qs, q, kc, vc, bt, 4, workspace=short)
     else:
         out = prefill_split(wl, qs, q, kc, vc, bt, 4, workspace=short)
         assert float(np.abs(to_f64(out) - ref).max()) <= TOL["f16"]
+
+
+def test_key_split_of_many_items_and_past_its_item_limit(orc):
+    """Near the split's 500-item limit (ranges of short items end to end, a
+    long item cut) and past it (whole items at any key_parts): the oracle."""
+    rng = np.random.default_rng(680)
+    for n_seq, n_kv in ((60, 8), (62, 8), (63, 8)):   # 480 and 496 items split; 504 run whole
+        cases = [(int(b), int(c)) for b, c in zip(rng.integers(0, 300, n_seq), rng.integers(1, 200, n_seq))]
+        cases[0] = (5000, 200)
+        wl, qs, tensors, q, kc, vc, bt = build("bf16", 64, 16, 1, seed=680 + n_seq, cases=cases, n_kv=n_kv)
+        pk.device_errors(reset=True)
+        out = prefill_split(wl, qs, q, kc, vc, bt, 32)
+        assert pk.device_errors() == 0
+        okc, ovc, _ = oracle_fill(orc, wl, tensors)
+        ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+        assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"], (n_seq, n_kv)
 
 
 def test_key_split_leaves_flagged_and_padding_rows_alone(orc):

@@ -149,7 +149,7 @@ def test_prefill_key_split_on_a_side_stream_and_in_a_graph(orc):
         q = prefill_queries(wl, qs, "cuda")
         qs_d = torch.from_numpy(qs).cuda()
         lens_d = torch.from_numpy(wl.context_lens).cuda()
-        ws = pk.prefill_workspace(q, 4)
+        ws = pk.prefill_workspace(q)
         out = torch.full_like(q, float("nan"))
         pk.paged_attention_prefill(q, kc, vc, bt, qs_d, lens_d, wl.scale, out, 130, workspace=ws, key_parts=4)
     side.synchronize()

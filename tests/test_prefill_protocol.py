@@ -60,9 +60,101 @@ class Barrier:
         return (self.phase & 1) != (n & 1)
 
 
+def item_tiles(before, chunk, g, n_kv):
+    """Every item in the shared order without ranking (sequence, query tile
+    from the last, kv head): (L, pos0, ntok, nk per Q tile, N key tiles)."""
+    lens = [b + c for b, c in zip(before, chunk)]
+    tq = ROWS // g                  # whole tokens per Q tile
+    tile_tokens = 2 * tq
+    tiles = -(-max(chunk) // tile_tokens)
+    out = []
+    for s in range(len(chunk)):
+        for qt in range(tiles - 1, -1, -1):
+            for _ in range(n_kv):
+                n, L = chunk[s], lens[s]
+                j0 = qt * tile_tokens
+                if j0 >= n:
+                    out.append(None)
+                    continue
+                ntok = min(tile_tokens, n - j0)
+                pos0 = L - n + j0
+                nk = [(pos0 + t * tq + min(ntok - t * tq, tq) - 1) // KEYS + 1 if ntok > t * tq else 0
+                      for t in range(TILES)]
+                out.append((L, pos0, ntok, nk, nk[1] if nk[1] > 0 else nk[0]))
+    return out
+
+
+PIECE_COST = 4   # the plan's fixed cost of a piece, in key tiles
+MAX_ITEM_PARTS = 16  # parts per item in the parts layout at most
+
+
+def split_plan(Ns, grid, parts, min_part=MIN_PART_TILES):
+    """The key split's plan: (r, pp, off, T); pp > 0 picks the parts layout
+    (pp CTAs per item), else ranges of r tiles of all items end to end."""
+    off = np.concatenate([[0], np.cumsum(Ns)]).astype(int)
+    T, mx = int(off[-1]), max(Ns, default=0)
+    r = -(-T // grid)
+    if mx > 1:
+        r = max(r, (mx - 2) // (parts - 1) + 1)
+    r = max(r, max(min(min_part, mx), 1))
+    pp = min(parts, MAX_ITEM_PARTS, grid // max(len(Ns), 1))
+    if pp > 0:
+        part_mx = max((-(-n // part_count(n, pp, min_part)) for n in Ns), default=0)
+        if part_mx + PIECE_COST > r + 2 * PIECE_COST:
+            pp = 0
+    return r, pp, off, T
+
+
+def part_count(n, pp, min_part=MIN_PART_TILES):
+    return min(pp, max(1, -(-n // min_part)))
+
+
+def split_pieces(cta, plan, Ns, min_part=MIN_PART_TILES):
+    """The pieces of CTA `cta`, in order: (item, kb, ke, slot, split)."""
+    r, pp, off, T = plan
+    if pp > 0:
+        i, q = divmod(cta, pp)
+        if i >= len(Ns) or Ns[i] == 0 or q >= part_count(Ns[i], pp, min_part):
+            return []
+        e = part_count(Ns[i], pp, min_part)
+        start, end = off[i] + Ns[i] * q // e, off[i] + Ns[i] * (q + 1) // e
+    else:
+        start = min(cta * r, T)
+        end = min(start + r, T)
+    out = []
+    for i, N in enumerate(Ns):
+        kb, ke = max(start - off[i], 0), min(end - off[i], N)
+        if ke > kb:
+            out.append((i, kb, ke, 2 * cta + (0 if kb > 0 else 1), kb > 0 or ke < N))
+    return out
+
+
+def merge_word(i, plan, Ns, min_part=MIN_PART_TILES):
+    """The merge's (first CTA, piece count) of item i."""
+    r, pp, off, T = plan
+    N = Ns[i]
+    if N == 0:
+        return 0, 0
+    if pp > 0:
+        return i * pp, part_count(N, pp, min_part)
+    c0 = off[i] // r
+    return c0, (off[i] + N - 1) // r - c0 + 1
+
+
 def make_items(cta, grid, before, chunk, g, n_kv, parts=1, min_part=MIN_PART_TILES):
-    """The items of CTA `cta`, in the kernel's order (key parts innermost; an
-    item's keys in at most ceil(N / min_part) parts)."""
+    """The items of CTA `cta`, in the kernel's order. Whole items (parts 1):
+    sequences ranked by length, bands dealt in alternating directions. Key
+    split: the pieces of the CTA's range of the call's key tiles."""
+    if parts > 1:
+        its = item_tiles(before, chunk, g, n_kv)
+        Ns = [0 if x is None else x[4] for x in its]
+        plan = split_plan(Ns, grid, parts, min_part)
+        items = []
+        for i, kb, ke, _, _ in split_pieces(cta, plan, Ns, min_part):
+            L, _, _, nk, N = its[i]
+            items.append(dict(nk=[max(min(x, ke) - kb, 0) for x in nk], nkt=ke - kb,
+                              tail=ke == N and N * KEYS > L))
+        return items
     lens = [b + c for b, c in zip(before, chunk)]
     qs = np.concatenate([[0], np.cumsum(chunk)])
     tq = ROWS // g                  # whole tokens per Q tile
@@ -70,8 +162,7 @@ def make_items(cta, grid, before, chunk, g, n_kv, parts=1, min_part=MIN_PART_TIL
     tiles = -(-max(chunk) // tile_tokens)
     S = len(chunk)
     ranked = sorted(range(S), key=lambda s: (-lens[s], s)) if S > 1 else list(range(S))
-    per_tile = n_kv * parts
-    per_seq = tiles * per_tile
+    per_seq = tiles * n_kv
     num_items = S * per_seq
     items, m = [], 0
     while True:
@@ -81,8 +172,7 @@ def make_items(cta, grid, before, chunk, g, n_kv, parts=1, min_part=MIN_PART_TIL
             return items
         r, rem = divmod(k, per_seq)
         s = ranked[r]
-        qt = tiles - 1 - rem // per_tile
-        part = rem % per_tile % parts
+        qt = tiles - 1 - rem // n_kv
         n, L = int(qs[s + 1] - qs[s]), lens[s]
         j0 = qt * tile_tokens
         if j0 >= n:
@@ -92,12 +182,7 @@ def make_items(cta, grid, before, chunk, g, n_kv, parts=1, min_part=MIN_PART_TIL
         nk = [(pos0 + t * tq + min(ntok - t * tq, tq) - 1) // KEYS + 1 if ntok > t * tq else 0
               for t in range(TILES)]
         N = nk[1] if nk[1] > 0 else nk[0]
-        eff = min(parts, max(1, -(-N // min_part)))
-        if part >= eff:
-            continue
-        kb, ke = N * part // eff, N * (part + 1) // eff
-        items.append(dict(nk=[max(min(x, ke) - kb, 0) for x in nk], nkt=ke - kb,
-                          tail=ke == N and N * KEYS > L))
+        items.append(dict(nk=nk, nkt=N, tail=N * KEYS > L))
 
 
 def run_cta(items, rng, ofree=False):
@@ -246,15 +331,16 @@ def check(before, chunk, g, n_kv, grid, seeds, ofree=False, parts=1, min_part=MI
 
 
 @pytest.mark.parametrize("g,n_kv", [(1, 8), (3, 4), (8, 4), (64, 1)])
-@pytest.mark.parametrize("grid,parts", [(1, 1), (5, 1), (37, 1), (5, 3), (37, 3)])
+@pytest.mark.parametrize("grid,parts", [(1, 1), (5, 1), (37, 1), (5, 3), (37, 3), (152, 32)])
 def test_no_deadlock_or_phase_hazard(g, n_kv, grid, parts):
     """Chunks of one row to three query tiles, contexts on a 64-key boundary
     and ragged, second Q tiles empty: every interleaving tried ends, with no
     barrier two phases past a waiter or one behind it (groups that divide 128
-    and 3, whose Q tiles hold 42 whole tokens), whole items and items whose
-    keys are split in up to three parts (a part's first tile past a tile's
-    rows, a tail only in the last part; parts of one key tile or more, to split
-    far more items than the kernel's rule of one part per 16 key tiles would)."""
+    and 3, whose Q tiles hold 42 whole tokens), whole items and the key split's
+    pieces (a piece's first tile past a tile's rows, a tail only in an item's
+    last piece, a range holding the end of one item and the start of the next;
+    ranges of one key tile or more, to cut far more items than the kernel's
+    floor of 16 tiles would)."""
     before, chunk = many_items_workload()
     check(before, chunk, g, n_kv, grid, seeds=3, parts=parts, min_part=1 if parts > 1 else MIN_PART_TILES)
 
@@ -267,3 +353,76 @@ def test_model_finds_the_removed_o_free_hazard():
     before, chunk = many_items_workload()
     with pytest.raises(Hazard):
         check(before, chunk, 1, 8, 37, seeds=3, ofree=True)
+
+
+def kernel_and_merge_agree(Ns, grid, parts, min_part=MIN_PART_TILES):
+    plan = split_plan(Ns, grid, parts, min_part)
+    r, pp, off, T = plan
+    if pp == 0:
+        assert r * grid >= T
+    seen = {}                      # item -> [(cta, kb, ke, slot, split)] from the kernel's side
+    slots = set()
+    for c in range(grid):
+        ps = split_pieces(c, plan, Ns, min_part)
+        if pp > 0:
+            assert len(ps) <= 1
+        else:
+            # the CTA's first item and piece count as the kernel finds them (binary searches)
+            start = min(c * r, T)
+            end = min(start + r, T)
+            first = next((i for i in range(len(Ns)) if off[i + 1] > start), len(Ns))
+            last = next((i for i in range(first, len(Ns)) if off[i + 1] >= end), len(Ns))
+            count = last - first + 1 if start < end else 0
+            assert [i for i, *_ in ps] == [i for i in range(first, first + count) if Ns[i] > 0]
+        for i, kb, ke, slot, split in ps:
+            assert 0 <= slot < 2 * grid
+            if split:
+                assert slot not in slots, "two pieces in one slot"
+                slots.add(slot)
+            seen.setdefault(i, []).append((c, kb, ke, slot, split))
+    for i, N in enumerate(Ns):
+        got = seen.get(i, [])
+        # every key tile of the item exactly once, in order
+        assert sum(ke - kb for _, kb, ke, _, _ in got) == N
+        assert all(a[2] == b[1] for a, b in zip(got, got[1:]))
+        assert len(got) <= parts
+        c0, n = merge_word(i, plan, Ns, min_part)
+        assert n == len(got)
+        if N == 0:
+            continue
+        assert [g_[0] for g_ in got] == list(range(c0, c0 + n))
+        assert all(split == (n > 1) for *_, split in got)
+        if n > 1:
+            assert [slot for *_, slot, _ in got] == [2 * (c0 + q) + (1 if q == 0 else 0) for q in range(n)]
+    return pp
+
+
+@pytest.mark.parametrize("grid", [1, 7, 37, 152])
+@pytest.mark.parametrize("parts", [2, 3, 32])
+def test_key_split_plan(grid, parts):
+    """The key split's pieces, as the kernel cuts them (ranges or parts,
+    whichever the plan picks) and as the merge finds them: every key tile
+    once, no item in more than `parts` pieces, each piece of a cut item in a
+    slot of its own below 2 x grid, the merge's first CTA, piece count and
+    slots those of the kernel's pieces; items of no tiles, one long item among
+    short ones, and all-empty calls."""
+    rng = np.random.default_rng(grid * 100 + parts)
+    cases = [[258] * 32, [257] * 8, [34] * 32, [0] * 5, [1] * 40, [5000] + [3] * 60, [0, 16, 0, 17, 0],
+             list(rng.integers(0, 600, 500)), list(rng.integers(0, 3, 200)), [2] * 32,
+             [315] * 32 + [49] * 32, [130] * 128]
+    layouts = [kernel_and_merge_agree([int(x) for x in Ns], grid, parts) > 0 for Ns in cases]
+    if grid == 152 and parts == 32:
+        # equal items that divide the SMs take parts; one long item among short ones ranges
+        assert layouts[1] and layouts[2] and not layouts[0] and not layouts[5] and not layouts[10]
+
+
+@pytest.mark.parametrize("g,n_kv", [(1, 4), (3, 2), (8, 2)])
+def test_no_deadlock_in_the_parts_layout(g, n_kv):
+    """Few equal items over long contexts (the plan takes parts: one piece per
+    CTA, a part's first tile past the first Q tile's rows): every interleaving
+    tried ends without a phase hazard."""
+    before, chunk = [3000, 3000], [100, 37]
+    its = item_tiles(before, chunk, g, n_kv)
+    Ns = [0 if x is None else x[4] for x in its]
+    assert split_plan(Ns, 152, 32)[1] > 0
+    check(before, chunk, g, n_kv, 152, seeds=2, parts=32)
