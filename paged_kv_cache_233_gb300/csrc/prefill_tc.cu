@@ -1012,8 +1012,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 // accumulates its columns of out = sum 2^(m_q - M) O_q / den, loading the
 // pieces' O kChunk at a time (the first kChunk in the same round trip as the
 // states). 8 at a time keeps 8 CTAs on an SM; 16 at a time holds more
-// registers and pays only where items have 9 or more pieces, which takes a
-// call of at most SMs / 9 items.
+// registers and pays only where items have 9 or more pieces: the launcher
+// takes it for calls of at most SMs / 9 items, where every item may (a call
+// of more items with one long one among them takes 8 at a time, in more round
+// trips).
 // A piece that held none of the row's keys left m_q = -inf and is skipped
 // (its O was not written). An item not split, or of a flagged sequence, is
 // left as the kernel left it.
@@ -1148,7 +1150,7 @@ static cudaError_t launch_merge_instance(const PrefillParams &p, int max_query_l
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // (items of 9 or more pieces need a call of at most SMs / 9 items)
+    // (in calls of at most SMs / 9 items every item may have 9 or more pieces)
     if (groups * 9 <= num_sms) return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D, 16>, p, int(tiles));
     return cudaLaunchKernelEx(&cfg, paged_prefill_merge_kernel<T, D, 8>, p, int(tiles));
 }
