@@ -368,6 +368,23 @@ def test_key_split_of_many_items_and_past_its_item_limit(orc):
         assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"], (n_seq, n_kv)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_key_split_one_long_item_among_many_short(orc, D):
+    """20 items (more than SMs / 9: the merge loads 8 pieces at a time), two of
+    them over a 30,000-token context cut into about 30 ranges, so that the
+    merge takes several round trips per row; the short ones whole: the oracle."""
+    cases = [(30000, 40)] + [(0, 10)] * 9
+    wl, qs, tensors, q, kc, vc, bt = build("bf16", D, 16, 1, seed=690 + D, cases=cases, n_kv=2)
+    pk.device_errors(reset=True)
+    out = prefill_split(wl, qs, q, kc, vc, bt, 32)
+    assert pk.device_errors() == 0
+    okc, ovc, _ = oracle_fill(orc, wl, tensors)
+    ref = orc.prefill(to_np(q), okc, ovc, wl.block_tables, qs, wl.context_lens, wl.scale, "bf16")
+    got = to_f64(out)
+    assert not np.isnan(got).any()
+    assert float(np.abs(got - ref).max()) <= TOL["bf16"]
+
+
 def test_key_split_leaves_flagged_and_padding_rows_alone(orc):
     """Under a key split a sequence whose length is shorter than its chunk is
     flagged and its rows left unwritten, and output rows past the chunks keep
